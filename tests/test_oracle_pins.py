@@ -1,0 +1,477 @@
+"""Pins for the binary64 oracle: each check comes from something other than the oracle itself.
+
+* Philox4x32-10: the published known-answer vectors (tests/golden/philox4x32_10_kat.txt) and, where
+  Triton is installed, its interpreter's Philox as an independent library witness.
+* Canonical order and top-k: brute force over all k-subsets of tiny rows (the defining dominance
+  property, no sorting).
+* Top-p and min-p: exact rational arithmetic (fractions.Fraction) on tiny rows; closed forms for
+  uniform rows (ceil(p * V)), a forced single huge logit (exactly one token) and two-level rows.
+* LSE / log-probability: closed forms (uniform: -log V; two-value rows) and sum_v exp(logp_v) = 1.
+* Gumbel-max law: chi-square of many draws against the renormalised truncated distribution, and the
+  heavy-tailed Z-score construction of the Gumbel precision page.
+"""
+import itertools
+import math
+import os
+import subprocess
+import sys
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from oracle import philox as ph
+from oracle import sampler as sm
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ----------------------------------------------------------------------------------------------
+# Philox4x32-10
+# ----------------------------------------------------------------------------------------------
+def _kat_rows():
+    rows = []
+    with open(os.path.join(GOLDEN, "philox4x32_10_kat.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            v = [int(t, 16) for t in line.split()]
+            rows.append((tuple(v[0:4]), tuple(v[4:6]), tuple(v[6:10])))
+    return rows
+
+
+def test_philox_known_answer_vectors():
+    rows = _kat_rows()
+    assert len(rows) == 3
+    for ctr, key, out in rows:
+        assert ph.philox4x32_10(ctr, key) == out
+        vec = ph.philox4x32_10_np(*[np.array([c]) for c in ctr], *[np.array([k]) for k in key])
+        assert tuple(int(a[0]) for a in vec) == out
+
+
+def test_philox_vectorised_matches_scalar():
+    rng = np.random.default_rng(7)
+    ctr = rng.integers(0, 2**32, size=(64, 4), dtype=np.uint64)
+    key = rng.integers(0, 2**32, size=(64, 2), dtype=np.uint64)
+    vec = ph.philox4x32_10_np(ctr[:, 0], ctr[:, 1], ctr[:, 2], ctr[:, 3], key[:, 0], key[:, 1])
+    for i in range(64):
+        ref = ph.philox4x32_10(tuple(int(c) for c in ctr[i]), tuple(int(k) for k in key[i]))
+        assert tuple(int(v[i]) for v in vec) == ref
+
+
+def test_philox_token_word_layout():
+    # token v takes word v & 3 of Philox((v >> 2, row, step_lo, step_hi), (seed_lo, seed_hi))
+    seed, row, step = (0x1234_5678_9ABC_DEF0, 17, (5 << 32) | 9)
+    toks = np.arange(0, 23)
+    got = ph.token_words(toks, seed, row, step)
+    for v in toks:
+        ref = ph.philox4x32_10((v >> 2, row, step & 0xFFFFFFFF, step >> 32),
+                               (seed & 0xFFFFFFFF, seed >> 32))[v & 3]
+        assert int(got[v]) == ref
+
+
+_TRITON_WITNESS = r"""
+import sys, torch, triton, triton.language as tl
+@triton.jit
+def k(out_ptr, c_ptr, k0, k1, N: tl.constexpr):
+    o = tl.arange(0, N)
+    c0 = tl.load(c_ptr + 4 * o + 0); c1 = tl.load(c_ptr + 4 * o + 1)
+    c2 = tl.load(c_ptr + 4 * o + 2); c3 = tl.load(c_ptr + 4 * o + 3)
+    z = c0 * 0
+    a, b, c, d = triton.language.random.philox_impl(c0, c1, c2, c3, k0.to(tl.uint32) + z,
+                                                    k1.to(tl.uint32) + z, 10)
+    tl.store(out_ptr + 4 * o + 0, a); tl.store(out_ptr + 4 * o + 1, b)
+    tl.store(out_ptr + 4 * o + 2, c); tl.store(out_ptr + 4 * o + 3, d)
+vals = [int(t) for t in sys.argv[1:]]
+k0, k1, ctr = vals[0], vals[1], vals[2:]
+n = len(ctr) // 4
+c = torch.tensor(ctr, dtype=torch.int64).to(torch.uint32)
+out = torch.zeros(4 * n, dtype=torch.uint32)
+k[(1,)](out, c, k0, k1, N=n)
+print(" ".join(str(int(v) & 0xFFFFFFFF) for v in out.tolist()))
+"""
+
+
+def test_philox_matches_triton_interpreter_witness():
+    pytest.importorskip("triton")
+    rng = np.random.default_rng(11)
+    ctr = [int(v) for v in rng.integers(0, 2**32, size=32, dtype=np.uint64)]
+    k0, k1 = 0xDEADBEEF, 0x01234567
+    env = dict(os.environ, TRITON_INTERPRET="1")
+    try:
+        out = subprocess.run([sys.executable, "-c", _TRITON_WITNESS, str(k0), str(k1)] + [str(c) for c in ctr],
+                             capture_output=True, text=True, env=env, timeout=300)
+    except subprocess.TimeoutExpired:
+        pytest.skip("triton interpreter timed out")
+    if out.returncode != 0:
+        pytest.skip("triton interpreter unavailable: " + out.stderr.strip().splitlines()[-1][:200])
+    got = [int(t) for t in out.stdout.split()]
+    for i in range(8):
+        assert tuple(got[4 * i:4 * i + 4]) == ph.philox4x32_10(tuple(ctr[4 * i:4 * i + 4]), (k0, k1))
+
+
+# ----------------------------------------------------------------------------------------------
+# keys, widening, canonical order, top-k
+# ----------------------------------------------------------------------------------------------
+def test_widen_bf16_known_patterns():
+    bits = np.array([0x3F80, 0xC000, 0x461C, 0x0000, 0x8000, 0x7F80, 0x0001], dtype=np.uint16)
+    x = sm.widen(bits, "bf16")
+    assert x[0] == 1.0 and x[1] == -2.0 and x[2] == 9984.0
+    assert x[3] == 0.0 and x[4] == 0.0 and math.copysign(1.0, x[4]) < 0
+    assert math.isinf(x[5]) and x[6] == 2.0 ** -133
+
+
+def test_order_key_is_monotone_and_merges_signed_zero():
+    f = np.float32
+    vals = [-np.inf, -np.finfo(f).max, -1.5, -1.0, -np.finfo(f).tiny, -f(1e-45), -0.0, 0.0, f(1e-45),
+            np.finfo(f).tiny, 1.0, 1.5, np.finfo(f).max, np.inf]
+    keys = [sm.order_key(float(f(v))) for v in vals]
+    assert sm.order_key(-0.0) == sm.order_key(0.0) == 0x80000000
+    for a, b, ka, kb in zip(vals, vals[1:], keys, keys[1:]):
+        if float(a) == float(b):
+            assert ka == kb
+        else:
+            assert ka < kb
+    rng = np.random.default_rng(3)
+    x = (rng.standard_normal(4000) * np.exp(rng.uniform(-30, 30, 4000))).astype(np.float32)
+    k = np.array([sm.order_key(float(v)) for v in x], dtype=np.uint64)
+    assert np.array_equal(np.argsort(k, kind="stable"), np.argsort(x, kind="stable"))
+
+
+def _dominates(x, a, b):
+    return x[a] > x[b] or (x[a] == x[b] and a < b)
+
+
+def _brute_topk_set(x, k):
+    """The unique k-subset S with every member dominating every non-member (no sorting)."""
+    n = len(x)
+    found = [set(c) for c in itertools.combinations(range(n), k)
+             if all(_dominates(x, a, b) for a in c for b in range(n) if b not in c)]
+    assert len(found) == 1
+    return found[0]
+
+
+def _brute_order(x):
+    """pi from nested top-k sets: pi[k-1] = topk(k) minus topk(k-1)."""
+    prev, order = set(), []
+    for k in range(1, len(x) + 1):
+        cur = _brute_topk_set(x, k)
+        (new,) = cur - prev
+        order.append(new)
+        prev = cur
+    return order
+
+
+def test_canonical_order_and_topk_brute_force():
+    rng = np.random.default_rng(5)
+    for trial in range(60):
+        n = int(rng.integers(1, 9))
+        levels = np.array([-1.0, -0.0, 0.0, 0.5, 2.0, -3.25], dtype=np.float32)
+        x = levels[rng.integers(0, len(levels), n)] if trial % 2 else rng.standard_normal(n).astype(np.float32)
+        x64 = x.astype(np.float64)
+        order = _brute_order(list(x64))
+        assert list(sm.canonical_order(x64)) == order
+        for k in range(0, n + 2):
+            st, out = sm.topk_select_row(x, n, k, n + 2)
+            assert st == 0
+            want = sorted(_brute_topk_set(list(x64), min(k, n))) if k > 0 else []
+            assert list(out[:len(want)]) == want and all(v == -1 for v in out[len(want):])
+
+
+def test_topk_select_contract():
+    x = np.array([3, 1, 3, 3, 2, np.nan, np.nan], dtype=np.float32)
+    st, out = sm.topk_select_row(x, 5, 2, 4)
+    assert st == 0 and list(out) == [0, 2, -1, -1]         # lowest-index ties, ascending, -1 pad
+    st, out = sm.topk_select_row(x, 5, 9, 9)
+    assert st == 0 and list(out) == [0, 1, 2, 3, 4, -1, -1, -1, -1]   # short row: all, then pad
+    assert sm.topk_select_row(x, 6, 2, 4)[0] == sm.STATUS_NONFINITE     # NaN inside the length
+    assert sm.topk_select_row(x, 5, 5, 4)[0] == sm.STATUS_INVALID_ARG   # k > k_max
+    st, out = sm.topk_select_row(x, 5, 0, 3)
+    assert st == 0 and list(out) == [-1, -1, -1]
+    eq = np.zeros(100, dtype=np.float32)
+    assert list(sm.topk_select_row(eq, 100, 37, 37)[1]) == list(range(37))     # all_equal -> [0, k)
+    z = np.array([0.0, -0.0, 0.0, -0.0], dtype=np.float32)
+    assert list(sm.topk_select_row(z, 4, 3, 3)[1]) == [0, 1, 2]          # signed zeros tie
+    inf = np.array([-np.inf, 1.0, np.inf, -np.inf], dtype=np.float32)
+    assert list(sm.topk_select_row(inf, 4, 3, 3)[1]) == [0, 1, 2]
+
+
+def test_topk_matches_torch_set_on_distinct_values():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(9)
+    x = rng.permutation(5000).astype(np.float32) * 0.25
+    for k in (1, 50, 2048):
+        _, out = sm.topk_select_row(x, x.size, k, k)
+        ref = torch.topk(torch.from_numpy(x), k).indices.numpy()
+        assert set(out.tolist()) == set(ref.tolist())
+
+
+# ----------------------------------------------------------------------------------------------
+# top-p, min-p: exact rational brute force and closed forms
+# ----------------------------------------------------------------------------------------------
+def _exact_kept(x, T, k, p, mp):
+    """Kept count by exact rational prefix sums on the binary64 weights; None if within 1e-9 of a tie."""
+    x = [float(v) for v in x]
+    n = len(x)
+    order = _brute_order(x)
+    m = x[order[0]]
+    w = [Fraction(math.exp((x[v] - m) / T)) for v in order]
+    nk = k if 0 < k < n else n
+    kept = nk
+    if p < 1:
+        target = Fraction(float(np.float32(p))) * sum(w[:nk])
+        pref = Fraction(0)
+        cp = nk
+        for j in range(nk):
+            if abs(pref - target) <= target * Fraction(1, 10**9) and j > 0:
+                return None
+            if pref >= target:
+                cp = j
+                break
+            pref += w[j]
+        kept = min(kept, cp)
+    if mp > 0:
+        mpf = Fraction(float(np.float32(mp)))
+        kept = min(kept, sum(1 for wv in w if wv >= mpf))
+    return max(1, kept)
+
+
+def test_topp_minp_exact_rational_brute_force():
+    rng = np.random.default_rng(21)
+    checked = 0
+    for trial in range(400):
+        n = int(rng.integers(1, 11))
+        if trial % 3 == 0:
+            x = rng.integers(-3, 3, n).astype(np.float32) * np.float32(0.5)
+        else:
+            x = (rng.standard_normal(n) * 2).astype(np.float32)
+        T = float(np.float32(rng.choice([0.5, 1.0, 1.7])))
+        k = int(rng.integers(0, n + 2))
+        p = float(np.float32(rng.choice([1.0, rng.uniform(0.05, 1.0)])))
+        mp = float(np.float32(rng.choice([0.0, 0.0, rng.uniform(0.0, 1.0), 1.0])))
+        want = _exact_kept(x.astype(np.float64), T, k, p, mp)
+        if want is None:
+            continue
+        r = sm.sample_row(x, "f32", T, k, p, mp, seed=1, row_id=0, step=trial, keep_order=True)
+        assert r.status == 0
+        assert r.kept == want, (x, T, k, p, mp)
+        assert r.kept_lo <= r.kept <= r.kept_hi
+        assert list(r.order[:r.kept]) == _brute_order(list(x.astype(np.float64)))[:want]
+        checked += 1
+    assert checked > 300
+
+
+def test_uniform_rows_keep_ceil_p_times_V():
+    for n, p in [(1000, 0.9), (1000, 0.123), (4096, 0.5), (151936, 0.95)]:
+        x = np.full(n, 0.75, dtype=np.float32)
+        r = sm.sample_row(x, "f32", 1.0, 0, p, 0.0, seed=3, row_id=0, step=0)
+        want = math.ceil(Fraction(float(np.float32(p))) * n)
+        assert r.kept == want and r.idx_cut == want - 1
+        assert abs(r.row_logsum - math.log(n)) < 1e-12
+        assert abs(r.logprob + math.log(n)) < 1e-12
+        assert not r.ambiguous
+    # the bf16 +1e4 workload: every value rounds to 9984.0, kept = ceil(0.95f * 151936)
+    b = workloads.c4(B=2)
+    assert np.all(b.logits == 0x461C)
+    r = sm.sample_row(b.logits[0], "bf16", 1.0, 0, 0.95, 0.0, seed=3, row_id=0, step=0)
+    assert r.kept == 144340 and abs(r.logprob + math.log(151936)) < 1e-12
+
+
+def test_topk_then_topp_uses_topk_renormalised_mass():
+    x = np.zeros(100, dtype=np.float32)
+    r = sm.sample_row(x, "f32", 1.0, 10, 0.5, 0.0)
+    assert r.kept == 5                     # target = 0.5 * S_k = 5 (not 0.5 * S = 50 -> 10)
+    r = sm.sample_row(x, "f32", 1.0, 10, 1.0, 0.0)
+    assert r.kept == 10 and r.idx_cut == 9
+
+
+@pytest.mark.parametrize("big", [1.0e4, 1.0e30])
+def test_forced_single_huge_logit_keeps_exactly_one(big):
+    x = np.zeros(1000, dtype=np.float32)
+    x[377] = big
+    for p in (0.5, 0.9, 0.99999994):
+        for T in (0.5, 1.0, 1.5):
+            r = sm.sample_row(x, "f32", T, 0, p, 0.0, seed=5, row_id=2, step=1)
+            assert r.kept == 1 and r.token == 377 and r.logprob == 0.0 and not math.isnan(r.logprob)
+
+
+def test_two_level_rows_min_p_top_p_logprob():
+    x = np.array([0, -2, 0, -2, -2, 0, -2, -2], dtype=np.float32)      # 3 upper, 5 lower
+    S = 3 + 5 * math.exp(-2)
+    r = sm.sample_row(x, "f32", 1.0, 0, 1.0, 0.5)
+    assert r.kept == 3
+    assert sm.sample_row(x, "f32", 1.0, 0, 1.0, 0.1).kept == 8
+    assert sm.sample_row(x, "f32", 1.0, 0, 1.0, 1.0).kept == 3          # w >= min_p keeps the max ties
+    assert sm.sample_row(x, "f32", 1.0, 0, 0.5, 0.0).kept == math.ceil(0.5 * S)
+    assert abs(sm.logprob_row(x, "f32", 1.0, 0) + math.log(S)) < 1e-12
+    assert abs(sm.logprob_row(x, "f32", 1.0, 1) - (-2 - math.log(S))) < 1e-12
+    S2 = 3 + 5 * math.exp(-1)
+    assert abs(sm.logprob_row(x, "f32", 2.0, 1) - (-1 - math.log(S2))) < 1e-12
+    st, m, ls = sm.softmax_lse_row(x, "f32", 2.0)
+    assert st == 0 and m == 0.0 and abs(ls - math.log(S2)) < 1e-12
+
+
+def test_greedy_returns_lowest_index_argmax():
+    x = np.array([1, 5, 5, 2], dtype=np.float32)
+    for T in (0.0, -1.0):
+        r = sm.sample_row(x, "f32", T, 0, 0.3, 0.0, seed=9, row_id=0, step=4)
+        assert r.token == 1 and r.kept == 1
+        S = 2 + math.exp(-4) + math.exp(-3)
+        assert abs(r.logprob - min(0.0, -math.log(S))) < 1e-12
+
+
+def test_logprobs_normalise():
+    rng = np.random.default_rng(2)
+    x = (rng.standard_normal(300) * 3).astype(np.float32)
+    lp = [sm.logprob_row(x, "f32", 0.7, t) for t in range(300)]
+    assert abs(math.fsum(math.exp(v) for v in lp) - 1.0) < 1e-12
+
+
+def test_invalid_and_nonfinite_rows():
+    x = np.zeros(8, dtype=np.float32)
+    assert sm.sample_row(x, "f32", 1.0, 0, 0.0, 0.0).status == sm.STATUS_INVALID_ARG
+    assert sm.sample_row(x, "f32", 1.0, 0, float("nan"), 0.0).status == sm.STATUS_INVALID_ARG
+    assert sm.sample_row(x, "f32", 1.0, 0, 0.5, 1.5).status == sm.STATUS_INVALID_ARG
+    assert sm.sample_row(x, "f32", float("nan"), 0, 0.5, 0.0).status == sm.STATUS_INVALID_ARG
+    y = x.copy()
+    y[3] = np.inf
+    assert sm.sample_row(y, "f32", 1.0, 0, 0.5, 0.0).status == sm.STATUS_NONFINITE
+    y[3] = np.nan
+    assert sm.sample_row(y, "f32", 1.0, 0, 0.5, 0.0).status == sm.STATUS_NONFINITE
+
+
+def test_neumaier_scan_against_exact_prefix():
+    # sub-ulp increments: a plain running sum never moves off 1.0; the compensated scan finds the exact
+    # crossing (1 + 400 quarter-ulps == target), and the rounded fsum certificate cannot separate the
+    # last two prefixes, so the boundary is reported ambiguous ([TOPP] step 6).
+    tiny = 2.0 ** -54
+    w = np.array([1.0] + [tiny] * 1000)
+    target = 1.0 + 100 * 2.0 ** -52
+    acc, exact = Fraction(0), None
+    for i, v in enumerate(w):
+        acc += Fraction(float(v))
+        if acc >= Fraction(target):
+            exact = i + 1
+            break
+    assert exact == 401
+    naive = next((i + 1 for i, c in enumerate(np.cumsum(w)) if c >= target), len(w))
+    assert naive == len(w)
+    assert sm.neumaier_scan(w, target) == exact
+    c, amb = sm.nucleus_count(w, target)
+    assert c == exact and amb
+    # a boundary separated by more than an ulp certifies cleanly
+    w2 = np.array([0.5, 0.25, 0.125, 0.0625, 0.0625])
+    c2, amb2 = sm.nucleus_count(w2, 0.8)
+    assert c2 == 3 and not amb2
+
+
+def test_invariants_on_random_rows():
+    rng = np.random.default_rng(13)
+    for trial in range(40):
+        n = int(rng.integers(50, 3000))
+        x = (rng.standard_normal(n) * rng.uniform(0.1, 5)).astype(np.float32)
+        T = float(np.float32(rng.uniform(0.3, 2.0)))
+        k = int(rng.integers(0, n + 5))
+        p = float(np.float32(rng.uniform(0.1, 1.0)))
+        r = sm.sample_row(x, "f32", T, k, p, 0.0, seed=7, row_id=trial, step=0, keep_order=True)
+        x64 = x.astype(np.float64)
+        w = np.exp((x64 - x64.max()) / T)
+        order = r.order
+        assert np.all(np.diff(x64[order]) <= 0)
+        ties = np.diff(x64[order]) == 0
+        assert np.all(np.diff(order)[ties] > 0)
+        nk = k if 0 < k < n else n
+        Sk = math.fsum(w[order[:nk]].tolist())
+        target = p * Sk
+        kept_mass = math.fsum(w[order[:r.kept]].tolist())
+        less_one = math.fsum(w[order[:r.kept - 1]].tolist())
+        assert kept_mass >= target * (1 - 1e-12) or r.kept == nk
+        assert r.kept == 1 or less_one < target * (1 + 1e-12)
+        assert not r.ambiguous
+        assert r.token in set(order[:r.kept].tolist())
+        mask = sm.kept_mask(r, n)
+        assert mask.sum() == r.kept and np.all(mask[order[:r.kept]] == 1)
+
+
+def test_no_ambiguous_boundaries_on_the_workloads():
+    for b in (workloads.c1(), workloads.c2(B=4, V=20000), workloads.c4(B=2, V=5000),
+              workloads.c5(B=4, V=20000)):
+        for r in range(b.B):
+            res = sm.sample_row(b.logits[r], b.dtype, b.temperature[r], b.top_k[r], b.top_p[r],
+                                b.min_p[r], int(b.seed[r]), r, int(b.step[r]))
+            assert res.status == 0 and not res.ambiguous
+
+
+# ----------------------------------------------------------------------------------------------
+# Gumbel-max sampling law
+# ----------------------------------------------------------------------------------------------
+def _chi2(obs, probs, n):
+    exp = probs * n
+    return float(np.sum((obs - exp) ** 2 / exp))
+
+
+def test_gumbel_draws_follow_the_truncated_softmax():
+    x = np.array([0.0, -0.5, -1.0, -1.5, 0.3, -3.0], dtype=np.float32)
+    T = 0.8
+    s = (x.astype(np.float64) - 0.3) / np.float64(np.float32(T))
+    N = 200_000
+    steps = np.arange(N, dtype=np.uint64)
+    # full support
+    cand = sm.canonical_order(x.astype(np.float64))
+    tok = sm.draw_many(s, cand, seed=42, row_id=3, steps=steps)
+    w = np.exp(s)
+    obs = np.bincount(tok, minlength=6).astype(np.float64)
+    assert _chi2(obs, w / w.sum(), N) < 40.0            # 5 dof: p ~ 1e-7
+    # top-3 support, renormalised
+    cand3 = cand[:3]
+    tok3 = sm.draw_many(s, cand3, seed=42, row_id=3, steps=steps)
+    assert set(np.unique(tok3).tolist()) == set(cand3.tolist())
+    w3 = w[cand3]
+    obs3 = np.array([(tok3 == v).sum() for v in cand3], dtype=np.float64)
+    assert _chi2(obs3, w3 / w3.sum(), N) < 35.0         # 2 dof
+    # the per-step scalar draw agrees with the vectorised one
+    for st in range(5):
+        assert sm.draw(s, cand, 42, 3, st)[0] == tok[st]
+
+
+def test_heavy_tailed_z_scores():
+    # counts in {1,2,3}, one dominant count; logits = log(counts) (Gumbel precision page's test)
+    V = 64
+    counts = workloads.heavy_tail_counts(V, seed=1234, head_log_gap=6.0)
+    x = np.log(counts.astype(np.float64)).astype(np.float32)
+    s = x.astype(np.float64) - float(x.max())
+    N = 100_000
+    tok = sm.draw_many(s, np.arange(V), seed=1234, row_id=0, steps=np.arange(N, dtype=np.uint64))
+    total = counts.sum()
+    p0 = counts[0] / total
+
+    def z(obs, exp):
+        return (obs - exp) / math.sqrt(exp * (1 - exp / N))
+
+    assert abs(z((tok == 0).sum(), p0 * N)) < 10.0
+    assert abs(z((tok >= 1).sum(), (1 - p0) * N)) < 10.0
+
+
+def test_uniform_map_is_the_cell_midpoint():
+    top = 2**32 - 1
+    u0, u1 = sm.uniform_from_word(np.array([0, top]))
+    assert 0.0 < u0 < 1.0 and 0.0 < u1 < 1.0
+    b = np.random.default_rng(4).integers(0, 2**32, size=10000, dtype=np.uint64)
+    assert np.all(sm.uniform_from_word(b) + sm.uniform_from_word(np.uint64(top) - b) == 1.0)
+    assert np.all(np.isfinite(sm.gumbel_from_uniform(sm.uniform_from_word(np.array([0, 1, top - 1, top])))))
+
+
+def test_gumbel_noise_inverts_the_gumbel_cdf():
+    u = np.array([1e-9, 1e-4, 0.1, 0.5, 0.9, 0.999, 1 - 1e-9])
+    g = sm.gumbel_from_uniform(u)
+    assert np.all(np.diff(g) < 0)                       # larger u -> smaller noise
+    assert np.allclose(np.exp(-np.exp(-g)), 1.0 - u, rtol=1e-12, atol=0)
+
+
+def test_argmax_ties_go_to_the_lowest_index():
+    cand = np.array([7, 3, 9, 1])
+    assert sm.argmax_lowest(np.array([2.0, 5.0, 5.0, 1.0]), cand)[0] == 3
+    assert sm.argmax_lowest(np.array([5.0, 5.0, 5.0, 5.0]), cand)[0] == 1
+    assert list(sm.argmax_lowest(np.array([[1.0, 0.0, 1.0, 0.0], [0.0, 2.0, 0.0, 2.0]]), cand)) == [7, 1]

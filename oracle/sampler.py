@@ -307,11 +307,11 @@ def topk_select_row(scores, length: int, k: int, k_max: int):
     n = int(length)
     if n <= 0 or n > len(scores):
         return STATUS_INVALID_ARG, out
+    x = widen(np.asarray(scores)[:n], "f32")
+    if np.any(np.isnan(x)):                       # data errors are reported before parameter errors
+        return STATUS_NONFINITE, out
     if k > k_max:
         return STATUS_INVALID_ARG, out
-    x = widen(np.asarray(scores)[:n], "f32")
-    if np.any(np.isnan(x)):
-        return STATUS_NONFINITE, out
     if k <= 0:
         return STATUS_OK, out
     sel = np.sort(canonical_order(x)[:min(k, n)])

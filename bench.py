@@ -1,0 +1,372 @@
+"""Benchmark of the fused sampling stage (top-k / top-p / min-p + Gumbel-max draw + log-probability).
+
+Workload (one "step" = one call of vsamp_sample over one batch): B = 256 rows x V = 151,936 bf16 logits
+drawn from N(0, 2.5^2) + 1.0e4 (seed 3), top_p = 0.95, top_k off, min_p off, temperature 1, Philox key 3,
+step = the iteration number. Inputs live in HBM before the timed region; four copies of the batch
+(311 MB, more than twice the 135 MB L2) are used in rotation so every step reads its logits from HBM.
+
+Output: one JSON line (rank 0). `value` is rows/s over all ranks; `roofline` is measured live with CUDA
+events on the launch stream; `e2e` repeats the measurement through the same C-ABI call with the inputs in
+pinned host memory and the host<->device copies inside the timed region; `cpu_baseline` times the binary64
+oracle on a bounded sample of the same workload on the host's cores.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Multi-GPU (torchrun, one rank per GPU): every rank samples its own batch (rows are independent; the
+Philox row word is the global row index), no collective on the data path; `scaling` is "weak".
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import math
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "rows/s and logits-read GB/s (% of HBM peak), top-k+top-p sample, V=151936"
+B_ROWS, V_COLS, SEED = 256, 151936, 3
+TOP_P = 0.95
+N_COPIES = 4
+WORKLOAD = ("c4: B=256 x V=151936 bf16 logits N(0,2.5^2)+1e4 (seed 3), top_p=0.95, top_k off, "
+            "min_p off, T=1, Philox key 3, step = iteration")
+# algorithmic work per step
+BYTES_PER_STEP = B_ROWS * V_COLS * 2                      # one read of every logit
+KEPT_PER_ROW = 144340                                      # ceil(0.95f * 151936): every token ties
+PHILOX_MULS_PER_TOKEN = 10                                 # 10 rounds x 2 products x (lo, hi) / 4 tokens
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured", float(d.get("sm_max_mhz", 2070.0))
+    except Exception:
+        return 6800.0, "fallback", 2070.0
+
+
+# ------------------------------------------------------------------------------------------------
+# clocks
+# ------------------------------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int, out_path: str | None = None):
+        self.idx = device_index
+        self.proc = None
+        self.path = out_path or os.path.join("/tmp", f"vsamp_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.QUERY,
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() in ("active", "yes", "1"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples in the timed region"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU baseline: the binary64 oracle on a bounded sample of the workload
+# ------------------------------------------------------------------------------------------------
+_CACHE = {}
+
+
+def _oracle_rows(args):
+    """Worker: draw `rows` of the batch with the oracle (the batch itself is generated once, untimed)."""
+    rows, step = args
+    import workloads
+    from oracle import sampler as osm
+
+    need = max(rows) + 1
+    if _CACHE.get("B", 0) < need:
+        _CACHE["b"] = workloads.c4(B=max(need, 32))
+        _CACHE["B"] = max(need, 32)
+    b = _CACHE["b"]
+    out = []
+    for r in rows:
+        res = osm.sample_row(b.logits[r], b.dtype, b.temperature[r], b.top_k[r], b.top_p[r], b.min_p[r],
+                             int(b.seed[r]), r, step)
+        out.append(res.token)
+    return out
+
+
+def cpu_baseline(n_rows: int = 32, step: int = 0):
+    """Oracle rows/s on all host cores (spawned workers; no CUDA in them)."""
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    workers = max(1, min(cores, n_rows))
+    chunks = [list(range(i, n_rows, workers)) for i in range(workers)]
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(workers) as pool:
+        pool.map(_oracle_rows, [([n_rows - 1], 0)] * workers)   # warm the workers (imports, data)
+        t0 = time.perf_counter()
+        pool.map(_oracle_rows, [(c, step) for c in chunks])
+        dt = time.perf_counter() - t0
+    rows_s = n_rows / dt
+    return {"value": rows_s, "unit": "rows/s", "cores": workers, "kind": "oracle",
+            "sample": f"{n_rows} rows of the B=256 x V=151936 bf16 batch, {workers} worker processes",
+            "gbs": rows_s * V_COLS * 2 / 1e9, "seconds": dt}
+
+
+# ------------------------------------------------------------------------------------------------
+# GPU arm
+# ------------------------------------------------------------------------------------------------
+def run_gpu(args):
+    import torch
+
+    import top_sampling_gb300 as ts
+    import workloads
+    from top_sampling_gb300 import build as tb
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+
+        dist = dist_mod
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    tb.build()
+    lib = ts.load()
+
+    # cpu baseline first (spawned workers, before heavy GPU work)
+    cpu = cpu_baseline() if (rank == 0 and not args.no_cpu) else None
+
+    batch = workloads.c4(B=B_ROWS, V=V_COLS, seed=SEED)
+    host = np.ascontiguousarray(batch.logits).view(np.int16)
+    x0 = torch.from_numpy(host).to(dev).view(torch.bfloat16)
+    copies = [x0] + [x0.clone() for _ in range(N_COPIES - 1)]
+    f32 = lambda v: torch.full((B_ROWS,), v, dtype=torch.float32, device=dev)
+    temp, topp, minp = f32(1.0), f32(TOP_P), f32(0.0)
+    topk = torch.zeros(B_ROWS, dtype=torch.int32, device=dev)
+    seed = torch.full((B_ROWS,), SEED, dtype=torch.int64, device=dev)
+    row_id = (torch.arange(B_ROWS, dtype=torch.int32, device=dev) + rank * B_ROWS)
+    steps_dev = [torch.full((B_ROWS,), s, dtype=torch.int64, device=dev) for s in range(N_COPIES)]
+    token = torch.empty(B_ROWS, dtype=torch.int32, device=dev)
+    logprob = torch.empty(B_ROWS, dtype=torch.float32, device=dev)
+    status = torch.empty(B_ROWS, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+
+    def call(i, x_ptr=None, tok=None, lp=None):
+        rc = lib.vsamp_sample(x_ptr or copies[i % N_COPIES].data_ptr(), ts.VSAMP_BF16, B_ROWS, V_COLS, V_COLS,
+                              temp.data_ptr(), topk.data_ptr(), topp.data_ptr(), minp.data_ptr(), seed.data_ptr(),
+                              steps_dev[i % N_COPIES].data_ptr(), row_id.data_ptr(),
+                              (tok if tok is not None else token).data_ptr(),
+                              (lp if lp is not None else logprob).data_ptr(), status.data_ptr(), None, sh)
+        if rc != 0:
+            raise RuntimeError("vsamp_sample failed: " + ts.status_string(rc))
+
+    for i in range(args.warmup):
+        call(i)
+    torch.cuda.synchronize()
+    if int(status.ne(0).sum()) != 0:
+        raise RuntimeError("sampling rows reported errors")
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(args.steps):
+        call(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    dev_ms = ev0.elapsed_time(ev1)
+    if dist:
+        tt = torch.tensor([dev_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        dev_ms = float(tt.item())
+    ms_step = dev_ms / args.steps
+    launch_us = ms_step * 1e3                     # one kernel launch per step
+    rows_s = world * B_ROWS * args.steps / (dev_ms / 1e3)
+
+    # end to end through the same C-ABI call: pinned host logits in, token + logprob out, every step
+    hx = torch.from_numpy(host).view(torch.bfloat16).pin_memory()
+    htok = torch.empty(B_ROWS, dtype=torch.int32).pin_memory()
+    hlp = torch.empty(B_ROWS, dtype=torch.float32).pin_memory()
+    dbuf = torch.empty_like(x0)
+    e2e_steps = max(3, min(args.steps, 200))
+    for i in range(2):
+        dbuf.copy_(hx, non_blocking=True)
+        call(i, x_ptr=dbuf.data_ptr())
+        htok.copy_(token, non_blocking=True)
+        hlp.copy_(logprob, non_blocking=True)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(e2e_steps):
+        dbuf.copy_(hx, non_blocking=True)
+        call(i, x_ptr=dbuf.data_ptr())
+        htok.copy_(token, non_blocking=True)
+        hlp.copy_(logprob, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if dist:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e_rows_s = world * B_ROWS * e2e_steps / (e2e_ms / 1e3)
+
+    hbm_peak, peak_kind, sm_max_mhz = _peaks()
+    gbs = BYTES_PER_STEP / (launch_us * 1e-6) / 1e9
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "traffic_c4.json")
+    if os.path.exists(prof):
+        try:
+            traffic = json.load(open(prof)).get("dram_bytes_per_launch")
+        except Exception:
+            traffic = None
+    # integer-multiply roofline of the Philox draws: 64 lanes/clk/SM of 32-bit multiplies at the max clock
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    imul_peak = sms * 64 * sm_max_mhz * 1e6 / 1e12                     # T ops/s
+    imul_ach = B_ROWS * KEPT_PER_ROW * PHILOX_MULS_PER_TOKEN / (launch_us * 1e-6) / 1e12
+    out = {
+        "metric": METRIC,
+        "value": rows_s,
+        "unit": "rows/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B_ROWS, "V": V_COLS, "input_dtype": "bf16",
+                   "l2": f"rotating {N_COPIES} input copies ({N_COPIES * BYTES_PER_STEP / 1e6:.0f} MB > 2x L2)",
+                   "parallelism": f"rows sharded, {world} rank(s)"},
+        "logits_read_gbs": gbs * world,
+        "hbm_frac": gbs / hbm_peak,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
+                     "traffic": traffic, "peak_kind": peak_kind, "kernel": "row_kernel<bf16,256,SAMPLE>",
+                     "launch_us": launch_us},
+        "roofline_alu": {"bound": "alu", "achieved": imul_ach, "peak": imul_peak, "unit": "Tops/s (32-bit imul)",
+                         "frac": imul_ach / imul_peak},
+        "e2e": {"value": e2e_rows_s, "unit": "rows/s", "h2d_bytes_per_step": BYTES_PER_STEP,
+                "d2h_bytes_per_step": B_ROWS * 8, "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    if cpu is not None:
+        out["cpu_baseline"] = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    if dist:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def run_reference(args):
+    """The oracle as the reference arm: rank 0 only, a bounded sample of the workload per step."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    rows_per_step = 16
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    workers = max(1, min(cores, rows_per_step))
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(workers) as pool:
+        pool.map(_oracle_rows, [([rows_per_step - 1], 0)] * workers)
+        for s in range(args.warmup):
+            pool.map(_oracle_rows, [([r], s) for r in range(min(workers, rows_per_step))])
+        t0 = time.perf_counter()
+        for s in range(args.steps):
+            chunks = [list(range(i, rows_per_step, workers)) for i in range(workers)]
+            pool.map(_oracle_rows, [(c, s) for c in chunks])
+        dt = time.perf_counter() - t0
+    rows_s = rows_per_step * args.steps / dt
+    sample = f"{rows_per_step} rows of the B=256 x V=151936 bf16 batch per step, {workers} worker processes"
+    out = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": rows_s,
+        "unit": "rows/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B_ROWS, "V": V_COLS, "input_dtype": "bf16"},
+        "cpu_baseline": {"value": rows_s, "unit": "rows/s", "cores": workers, "kind": "oracle", "sample": sample},
+        "e2e": {"value": rows_s, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="vsamp", choices=["vsamp", "reference"])
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        if args.steps > 20:          # each step is a bounded sample; report the steps actually run
+            args.steps = 20
+        args.warmup = min(args.warmup, 3)
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,162 @@
+/*
+ * vsamp.h -- C ABI of libvsamp.so, the GB300 (sm_103a) per-row vocabulary sampling stage.
+ *
+ * For each row of a [B, V] logits batch the stage computes an online max / log-sum-exp, an exact
+ * top-k select with index-ordered ties, a top-p nucleus cut (probability-space predicate, row maximum
+ * always kept), a min-p filter, a Philox4x32-10 Gumbel-max draw and the selected token's
+ * log-probability.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Pointers: every array argument is a DEVICE pointer unless its comment says otherwise. The caller
+ *   allocates and owns every buffer; the library keeps no pointer after a call returns and allocates
+ *   no device memory.
+ * Layout: logits / scores are row-major [B, ld] with ld >= V (elements, not bytes); row r starts at
+ *   element r * ld. Only the first V (or lengths[r]) elements of a row are read.
+ * Streams: `stream` is a cudaStream_t (NULL = the legacy default stream). Every call only enqueues
+ *   work on `stream` and returns without synchronising; outputs are valid once the stream reaches
+ *   that point.
+ * Errors: the return value reports problems the host can see before launch (NULL pointers, sizes,
+ *   dtype, a device that cannot hold the row) and launch failures (VSAMP_ERR_CUDA). Nothing is
+ *   enqueued when the return value is not VSAMP_OK. Data-dependent problems are reported per row in
+ *   `row_status[r]` (when the caller passes it) with the row's outputs set to sentinels (token -1,
+ *   logprob NaN, indices -1); the device never traps or asserts.
+ * Keys: `pivot_key` values are the order-preserving 32-bit key of the fp32 value (bf16 values are
+ *   widened exactly): positive floats get the sign bit set, negative floats are bit-inverted, and
+ *   -0.0 is read as +0.0 ("[Kernel] Make persistent_topk deterministic", Changes: signed zeros are
+ *   one key).
+ *
+ * Per-row parameters (arrays of length B; NULL selects the default in brackets):
+ *   temperature [1.0]  T > 0 scales scores as (x - max) / T; T <= 0 is greedy (the lowest-index
+ *                      maximum, all filters keep one token) and log-probabilities then use T = 1.
+ *   top_k [off]        0 < k < V keeps the k largest by (value desc, index asc); k <= 0 or k >= V: off.
+ *   top_p [off]        0 < p < 1 keeps the shortest prefix of that order whose mass reaches p * S_k,
+ *                      S_k the mass kept by top-k; p >= 1: off; p <= 0 or NaN: row error.
+ *   min_p [off]        0 < q <= 1 keeps tokens with exp((x - max)/T) >= q; q <= 0: off; q > 1 or NaN:
+ *                      row error.
+ *   seed, step [0]     Philox4x32-10 key = (seed mod 2^32, seed >> 32); token v of a row uses output
+ *                      word v & 3 of the counter (v >> 2, row_id, step mod 2^32, step >> 32).
+ *   row_id [r]         32-bit counter word identifying the row (use the global row index when a batch
+ *                      is split across devices, or a per-request id for batch-invariant draws).
+ * Transform order: temperature -> top-k -> top-p -> min-p ("[WS2][Logprob] Deterministic SM90
+ * linear_logp ...", Integration). The kept set is always a prefix of the order (value desc, index
+ * asc) and holds at least the row maximum ("Split top-p numerical reference and conservative gate",
+ * Source basis).
+ */
+#ifndef VSAMP_H_
+#define VSAMP_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum vsamp_status {
+  VSAMP_OK = 0,
+  VSAMP_ERR_INVALID_ARG = 1,   /* bad pointer / size / parameter */
+  VSAMP_ERR_UNSUPPORTED = 2,   /* this device cannot hold the row (shared memory, cluster size) */
+  VSAMP_ERR_CUDA = 3,          /* a CUDA runtime call failed (launch, attribute) */
+  VSAMP_ERR_NONFINITE = 4,     /* per row: NaN or +-inf in the row */
+  VSAMP_ERR_TIMEOUT = 5        /* per row: a bounded device-side wait gave up */
+} vsamp_status;
+
+typedef enum vsamp_dtype {
+  VSAMP_F32 = 0,
+  VSAMP_BF16 = 1
+} vsamp_dtype;
+
+/* Cut descriptor of one row: token v is kept iff key(x_v) > pivot_key, or key(x_v) == pivot_key and
+ * v <= idx_cut. (pivot_key, idx_cut) are the key and index of the last kept token in the order
+ * (value desc, index asc); kept is the number of kept tokens. */
+typedef struct vsamp_cut {
+  uint32_t pivot_key;
+  int32_t idx_cut;
+  int32_t kept;
+  int32_t status;      /* vsamp_status of the row */
+} vsamp_cut;
+
+/* Device limits the library works with (filled by vsamp_device_info). */
+typedef struct vsamp_limits {
+  int32_t sm_count;
+  int32_t smem_optin_bytes;       /* cudaDevAttrMaxSharedMemoryPerBlockOptin */
+  int32_t max_cluster;            /* largest cluster size the row kernels may use on this device */
+  int64_t max_row_f32;            /* longest fp32 row a cluster can hold in shared memory */
+  int64_t max_row_bf16;           /* longest bf16 row */
+} vsamp_limits;
+
+/* Online max / log-sum-exp ("[WS2][Logprob] Deterministic SM90 linear_logp ...", Design: the numeric
+ * contract: m = max_v x_v, S = sum_v exp(x_v - m), lse = m + log S; temperature applied to the
+ * statistics, stored logits left unscaled).
+ *   row_max[r]    = max_v x[r, v] (fp32)
+ *   row_logsum[r] = log sum_v exp((x[r, v] - row_max[r]) / T_r), T_r <= 0 read as 1.
+ * The sum is accumulated in 64-bit fixed point (2^-40 units), so it does not depend on scheduling,
+ * batch size or neighbouring rows. Either output may be NULL. */
+vsamp_status vsamp_softmax_lse(const void* logits, vsamp_dtype dt, int64_t B, int64_t V, int64_t ld,
+                               const float* temperature, float* row_max, float* row_logsum,
+                               int32_t* row_status, void* stream);
+
+/* Deterministic exact top-k select ("[Kernel] Make persistent_topk deterministic", Changes: a radix
+ * select whose pivot is exact, then an index-ordered emission of everything above the pivot and the
+ * lowest-index elements equal to it; output in ascending index order, identical across calls).
+ *   scores   [B, ld] fp32 or bf16; row r has lengths[r] valid elements (NULL: max_len for all rows).
+ *            +-inf are ordinary keys; NaN inside the length is a row error.
+ *   k        [B] per-row k (NULL: k_max for every row); k <= 0 selects nothing; k > k_max is a row
+ *            error.
+ *   out_idx  [B, k_max] int32: the first min(k, len) slots hold the selected indices in ascending
+ *            order, the remaining slots -1 (also on error). */
+vsamp_status vsamp_topk_select(const void* scores, vsamp_dtype dt, int64_t B, int64_t max_len,
+                               int64_t ld, const int32_t* lengths, const int32_t* k, int32_t k_max,
+                               int32_t* out_idx, int32_t* row_status, void* stream);
+
+/* Top-p / min-p cut after top-k ("Split top-p numerical reference and conservative gate", Source
+ * basis: mask with the probability-space predicate and always keep the row maximum; Independent
+ * binary64 numerical reference: the smallest prefix of (value desc, index asc) whose mass reaches
+ * p * normaliser; "Sorting-free top-k/top-p/min-p sampling ... #901", Background: min-p pivot =
+ * max * p). No logit-space threshold is ever rebuilt.
+ *   cut   [B] descriptor of the kept prefix (required).
+ *   mask  [B, V] uint8, 1 = kept (NULL: not written).
+ *   stats [B, 4] int32 or NULL: {full passes over the row, radix rounds, kept, path flags}. */
+vsamp_status vsamp_topp_minp_mask(const void* logits, vsamp_dtype dt, int64_t B, int64_t V, int64_t ld,
+                                  const float* temperature, const int32_t* top_k, const float* top_p,
+                                  const float* min_p, vsamp_cut* cut, uint8_t* mask, int32_t* stats,
+                                  void* stream);
+
+/* The fused stage: LSE, top-k, top-p, min-p, then a Gumbel-max draw over the kept tokens and the
+ * drawn token's log-probability ("[vLLM PR #45996] use log1p(-u) to improve FP32 Gumbel sampling
+ * precision": noise -log(-log1p(-u)), masked arg-max over logits + noise with the lowest index among
+ * equal maxima; temperature 0 returns the arg-max).
+ *   u = (b + 0.5) * 2^-32 for the token's 32-bit Philox word b; score = (x - max)/T + noise.
+ *   token   [B] int32 (required): the drawn token, -1 on a row error.
+ *   logprob [B] fp32 or NULL: min((x_t - max)/T - log S, 0) over the full row ("[WS2][Logprob]
+ *           ...", Design: logp = min(z_t - lse, 0)).
+ *   stats   [B, 4] int32 or NULL: as for vsamp_topp_minp_mask. */
+vsamp_status vsamp_sample(const void* logits, vsamp_dtype dt, int64_t B, int64_t V, int64_t ld,
+                          const float* temperature, const int32_t* top_k, const float* top_p,
+                          const float* min_p, const uint64_t* seed, const uint64_t* step,
+                          const uint32_t* row_id, int32_t* token, float* logprob,
+                          int32_t* row_status, int32_t* stats, void* stream);
+
+/* Selected-token log-probability ("[WS2][Logprob] ...", Design: logp = min(z_t - lse, 0), temperature
+ * applied to the statistics):
+ *   out[r] = min((x[r, t] - row_max[r]) / T_r - row_logsum[r], 0), t = token[r], T_r <= 0 read as 1.
+ * row_max and row_logsum must both be given (from vsamp_softmax_lse at the same temperature) or both
+ * be NULL, in which case they are recomputed from the row. token[r] outside [0, V) is a row error. */
+vsamp_status vsamp_logprob(const void* logits, vsamp_dtype dt, int64_t B, int64_t V, int64_t ld,
+                           const float* temperature, const int32_t* token, const float* row_max,
+                           const float* row_logsum, float* out, int32_t* row_status, void* stream);
+
+/* Static description of a status code. */
+const char* vsamp_status_string(vsamp_status s);
+
+/* Limits on `device` (queried once per device and cached; thread-safe). Host pointer `out`. */
+vsamp_status vsamp_device_info(int device, vsamp_limits* out);
+
+/* ABI version: (major << 16) | minor. */
+int32_t vsamp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VSAMP_H_ */

@@ -1,0 +1,87 @@
+"""C-ABI checks that need no GPU: the library builds for sm_103a, loads, exports every function that
+include/vsamp.h declares, and its host-only calls answer."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "vsamp.h")
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(vsamp_[a-z_]+)\s*\(", src)))
+
+
+def _header_enum(name):
+    src = open(HEADER).read()
+    m = re.search(r"\b" + name + r"\s*=\s*(\d+)", src)
+    return int(m.group(1))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from top_sampling_gb300 import build as b
+
+    path = b.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_five_stage_calls():
+    fns = _declared_functions()
+    for f in ("vsamp_softmax_lse", "vsamp_topk_select", "vsamp_topp_minp_mask", "vsamp_sample", "vsamp_logprob",
+              "vsamp_status_string", "vsamp_device_info", "vsamp_version"):
+        assert f in fns
+
+
+def test_library_exports_every_declared_function(lib):
+    for f in _declared_functions():
+        assert hasattr(lib, f), f"libvsamp.so does not export {f}"
+
+
+def test_status_strings_and_version(lib):
+    lib.vsamp_status_string.restype = ctypes.c_char_p
+    lib.vsamp_status_string.argtypes = [ctypes.c_int]
+    for code in range(6):
+        s = lib.vsamp_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert lib.vsamp_status_string(99).decode() == "unknown status"
+    lib.vsamp_version.restype = ctypes.c_int32
+    assert lib.vsamp_version() >> 16 == 1
+
+
+def test_status_codes_agree_across_header_binding_and_oracle():
+    import top_sampling_gb300 as ts
+    from oracle import sampler as osm
+
+    assert _header_enum("VSAMP_OK") == ts.VSAMP_OK == osm.STATUS_OK
+    assert _header_enum("VSAMP_ERR_INVALID_ARG") == ts.VSAMP_ERR_INVALID_ARG == osm.STATUS_INVALID_ARG
+    assert _header_enum("VSAMP_ERR_NONFINITE") == ts.VSAMP_ERR_NONFINITE == osm.STATUS_NONFINITE
+    assert _header_enum("VSAMP_ERR_UNSUPPORTED") == ts.VSAMP_ERR_UNSUPPORTED
+    assert _header_enum("VSAMP_ERR_TIMEOUT") == ts.VSAMP_ERR_TIMEOUT
+    assert _header_enum("VSAMP_BF16") == ts.VSAMP_BF16
+
+
+def test_binding_declares_argument_types(lib):
+    import top_sampling_gb300 as ts
+
+    l2 = ts.load()
+    assert set(ts.EXPORTED) == set(_declared_functions())
+    for f in ts.EXPORTED:
+        assert getattr(l2, f).restype is not None
+
+
+def test_host_argument_checks_reject_before_any_device_work(lib):
+    # NULL logits / bad sizes are rejected on the host; no CUDA call is made, so no GPU is needed
+    vp = ctypes.c_void_p
+    lib.vsamp_sample.restype = ctypes.c_int
+    lib.vsamp_sample.argtypes = [vp, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64] + [vp] * 12
+    assert lib.vsamp_sample(None, 0, 4, 100, 100, *([None] * 12)) == 1
+    dummy = ctypes.c_void_p(16)
+    assert lib.vsamp_sample(dummy, 7, 4, 100, 100, *([None] * 12)) == 1        # bad dtype
+    assert lib.vsamp_sample(dummy, 0, 4, 100, 50, *([None] * 12)) == 1         # ld < V
+    assert lib.vsamp_sample(dummy, 0, 0, 100, 100, *([None] * 12)) == 1        # B = 0
+    assert lib.vsamp_sample(dummy, 0, 4, 100, 100, *([None] * 7), None, *([None] * 4)) == 1   # token NULL

@@ -1,0 +1,263 @@
+"""Thin Python binding of libvsamp.so, the GB300 per-row vocabulary sampling stage.
+
+The functions carry the C-ABI names (include/vsamp.h) and only marshal arguments: torch tensors are
+passed as device pointers, missing outputs are allocated with torch on the input's device, and the
+call is enqueued on the current torch stream. Every step of the stage runs in the library's CUDA
+kernels; there is no CPU or PyTorch fallback. If the library is missing the import still works, but
+every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libvsamp.so")
+
+VSAMP_OK = 0
+VSAMP_ERR_INVALID_ARG = 1
+VSAMP_ERR_UNSUPPORTED = 2
+VSAMP_ERR_CUDA = 3
+VSAMP_ERR_NONFINITE = 4
+VSAMP_ERR_TIMEOUT = 5
+VSAMP_F32 = 0
+VSAMP_BF16 = 1
+
+EXPORTED = ("vsamp_softmax_lse", "vsamp_topk_select", "vsamp_topp_minp_mask", "vsamp_sample",
+            "vsamp_logprob", "vsamp_status_string", "vsamp_device_info", "vsamp_version")
+
+
+class VsampError(RuntimeError):
+    def __init__(self, status: int, fn: str):
+        self.status = status
+        super().__init__(f"{fn}: {status_string(status)} (status {status})")
+
+
+class vsamp_cut(ctypes.Structure):
+    _fields_ = [("pivot_key", ctypes.c_uint32), ("idx_cut", ctypes.c_int32), ("kept", ctypes.c_int32),
+                ("status", ctypes.c_int32)]
+
+
+class vsamp_limits(ctypes.Structure):
+    _fields_ = [("sm_count", ctypes.c_int32), ("smem_optin_bytes", ctypes.c_int32),
+                ("max_cluster", ctypes.c_int32), ("max_row_f32", ctypes.c_int64),
+                ("max_row_bf16", ctypes.c_int64)]
+
+
+_lib = None
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libvsamp.so (once) and declare the C signatures."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} is not built: run `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(p)
+    vp, i64, i32, st = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int
+    lib.vsamp_softmax_lse.argtypes = [vp, st, i64, i64, i64, vp, vp, vp, vp, vp]
+    lib.vsamp_topk_select.argtypes = [vp, st, i64, i64, i64, vp, vp, i32, vp, vp, vp]
+    lib.vsamp_topp_minp_mask.argtypes = [vp, st, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.vsamp_sample.argtypes = [vp, st, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.vsamp_logprob.argtypes = [vp, st, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp]
+    for f in ("vsamp_softmax_lse", "vsamp_topk_select", "vsamp_topp_minp_mask", "vsamp_sample", "vsamp_logprob"):
+        getattr(lib, f).restype = st
+    lib.vsamp_status_string.argtypes = [st]
+    lib.vsamp_status_string.restype = ctypes.c_char_p
+    lib.vsamp_device_info.argtypes = [ctypes.c_int, ctypes.POINTER(vsamp_limits)]
+    lib.vsamp_device_info.restype = st
+    lib.vsamp_version.argtypes = []
+    lib.vsamp_version.restype = i32
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().vsamp_status_string(int(status)).decode()
+
+
+def version() -> int:
+    return int(load().vsamp_version())
+
+
+def device_info(device: int = 0) -> vsamp_limits:
+    out = vsamp_limits()
+    _check(load().vsamp_device_info(int(device), ctypes.byref(out)), "vsamp_device_info")
+    return out
+
+
+# ------------------------------------------------------------------------------------------------
+# marshalling helpers
+# ------------------------------------------------------------------------------------------------
+def _check(status: int, fn: str):
+    if status != VSAMP_OK:
+        raise VsampError(status, fn)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return VSAMP_F32
+    if t.dtype == torch.bfloat16:
+        return VSAMP_BF16
+    raise TypeError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+def _rows(x: torch.Tensor, V: Optional[int]):
+    if x.dim() != 2 or not x.is_cuda:
+        raise ValueError("logits must be a 2-D CUDA tensor [B, >= V]")
+    if x.stride(1) != 1:
+        raise ValueError("logits rows must be contiguous (stride(1) == 1)")
+    B = x.shape[0]
+    V = x.shape[1] if V is None else int(V)
+    return B, V, x.stride(0) if B > 1 else max(x.stride(0), V)
+
+
+def _ptr(t: Optional[torch.Tensor], dtype=None, dev=None, B=None, name="") -> int:
+    if t is None:
+        return 0
+    if not t.is_cuda or (dev is not None and t.device != dev):
+        raise ValueError(f"{name} must be on {dev}")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if B is not None and t.numel() < B:
+        raise ValueError(f"{name} needs at least {B} elements")
+    return t.data_ptr()
+
+
+def _param(v, B: int, dtype, dev, name):
+    """Per-row parameter: None, a scalar (broadcast) or a [B] device tensor."""
+    if v is None:
+        return None
+    if isinstance(v, torch.Tensor):
+        return v.to(device=dev, dtype=dtype).contiguous()
+    return torch.full((B,), v, dtype=dtype, device=dev)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+# ------------------------------------------------------------------------------------------------
+# entry points (same names as the C ABI)
+# ------------------------------------------------------------------------------------------------
+def vsamp_softmax_lse(logits, temperature=None, V=None, row_max=None, row_logsum=None, row_status=None,
+                      stream=None):
+    """Row maximum and log-sum-exp of (x - max)/T. Returns (row_max, row_logsum, row_status)."""
+    B, V, ld = _rows(logits, V)
+    dev = logits.device
+    temperature = _param(temperature, B, torch.float32, dev, "temperature")
+    row_max = torch.empty(B, dtype=torch.float32, device=dev) if row_max is None else row_max
+    row_logsum = torch.empty(B, dtype=torch.float32, device=dev) if row_logsum is None else row_logsum
+    row_status = torch.empty(B, dtype=torch.int32, device=dev) if row_status is None else row_status
+    st = load().vsamp_softmax_lse(
+        logits.data_ptr(), _dtype_code(logits), B, V, ld, _ptr(temperature, torch.float32, dev, B, "temperature"),
+        _ptr(row_max, torch.float32, dev, B, "row_max"), _ptr(row_logsum, torch.float32, dev, B, "row_logsum"),
+        _ptr(row_status, torch.int32, dev, B, "row_status"), _stream(stream))
+    _check(st, "vsamp_softmax_lse")
+    return row_max, row_logsum, row_status
+
+
+def vsamp_topk_select(scores, k, k_max=None, lengths=None, max_len=None, out_idx=None, row_status=None,
+                      stream=None):
+    """Top-k indices per row in ascending index order, -1 padded. Returns (out_idx [B, k_max], row_status)."""
+    B, max_len, ld = _rows(scores, max_len)
+    dev = scores.device
+    if isinstance(k, int) and k_max is None:
+        k_max = k
+    if k_max is None:
+        raise ValueError("k_max is required when k is a tensor")
+    k = _param(k, B, torch.int32, dev, "k")
+    lengths = _param(lengths, B, torch.int32, dev, "lengths")
+    out_idx = torch.empty((B, int(k_max)), dtype=torch.int32, device=dev) if out_idx is None else out_idx
+    row_status = torch.empty(B, dtype=torch.int32, device=dev) if row_status is None else row_status
+    st = load().vsamp_topk_select(
+        scores.data_ptr(), _dtype_code(scores), B, max_len, ld, _ptr(lengths, torch.int32, dev, B, "lengths"),
+        _ptr(k, torch.int32, dev, B, "k"), int(k_max), _ptr(out_idx, torch.int32, dev, B * int(k_max), "out_idx"),
+        _ptr(row_status, torch.int32, dev, B, "row_status"), _stream(stream))
+    _check(st, "vsamp_topk_select")
+    return out_idx, row_status
+
+
+def vsamp_topp_minp_mask(logits, temperature=None, top_k=None, top_p=None, min_p=None, V=None,
+                         want_mask=True, cut=None, mask=None, stats=None, stream=None):
+    """Cut descriptors [B, 4] int32 (pivot_key as int32 bits, idx_cut, kept, status), mask [B, V] uint8
+    (or None) and stats [B, 4]."""
+    B, V, ld = _rows(logits, V)
+    dev = logits.device
+    temperature = _param(temperature, B, torch.float32, dev, "temperature")
+    top_k = _param(top_k, B, torch.int32, dev, "top_k")
+    top_p = _param(top_p, B, torch.float32, dev, "top_p")
+    min_p = _param(min_p, B, torch.float32, dev, "min_p")
+    cut = torch.empty((B, 4), dtype=torch.int32, device=dev) if cut is None else cut
+    if want_mask and mask is None:
+        mask = torch.empty((B, V), dtype=torch.uint8, device=dev)
+    stats = torch.empty((B, 4), dtype=torch.int32, device=dev) if stats is None else stats
+    st = load().vsamp_topp_minp_mask(
+        logits.data_ptr(), _dtype_code(logits), B, V, ld, _ptr(temperature, torch.float32, dev, B, "temperature"),
+        _ptr(top_k, torch.int32, dev, B, "top_k"), _ptr(top_p, torch.float32, dev, B, "top_p"),
+        _ptr(min_p, torch.float32, dev, B, "min_p"), _ptr(cut, torch.int32, dev, 4 * B, "cut"),
+        _ptr(mask, torch.uint8, dev, B * V, "mask"), _ptr(stats, torch.int32, dev, 4 * B, "stats"),
+        _stream(stream))
+    _check(st, "vsamp_topp_minp_mask")
+    return cut, mask, stats
+
+
+def vsamp_sample(logits, temperature=None, top_k=None, top_p=None, min_p=None, seed=None, step=None,
+                 row_id=None, V=None, token=None, logprob=None, row_status=None, stats=None,
+                 want_logprob=True, want_stats=False, stream=None):
+    """The fused stage. Returns (token [B] int32, logprob [B] fp32 or None, row_status [B], stats or None)."""
+    B, V, ld = _rows(logits, V)
+    dev = logits.device
+    temperature = _param(temperature, B, torch.float32, dev, "temperature")
+    top_k = _param(top_k, B, torch.int32, dev, "top_k")
+    top_p = _param(top_p, B, torch.float32, dev, "top_p")
+    min_p = _param(min_p, B, torch.float32, dev, "min_p")
+    seed = _param(seed, B, torch.int64, dev, "seed")
+    step = _param(step, B, torch.int64, dev, "step")
+    row_id = _param(row_id, B, torch.int32, dev, "row_id")
+    token = torch.empty(B, dtype=torch.int32, device=dev) if token is None else token
+    if want_logprob and logprob is None:
+        logprob = torch.empty(B, dtype=torch.float32, device=dev)
+    row_status = torch.empty(B, dtype=torch.int32, device=dev) if row_status is None else row_status
+    if want_stats and stats is None:
+        stats = torch.empty((B, 4), dtype=torch.int32, device=dev)
+    st = load().vsamp_sample(
+        logits.data_ptr(), _dtype_code(logits), B, V, ld, _ptr(temperature, torch.float32, dev, B, "temperature"),
+        _ptr(top_k, torch.int32, dev, B, "top_k"), _ptr(top_p, torch.float32, dev, B, "top_p"),
+        _ptr(min_p, torch.float32, dev, B, "min_p"), _ptr(seed, torch.int64, dev, B, "seed"),
+        _ptr(step, torch.int64, dev, B, "step"), _ptr(row_id, torch.int32, dev, B, "row_id"),
+        _ptr(token, torch.int32, dev, B, "token"), _ptr(logprob, torch.float32, dev, B, "logprob"),
+        _ptr(row_status, torch.int32, dev, B, "row_status"), _ptr(stats, torch.int32, dev, 4 * B, "stats"),
+        _stream(stream))
+    _check(st, "vsamp_sample")
+    return token, logprob, row_status, stats
+
+
+def vsamp_logprob(logits, token, temperature=None, row_max=None, row_logsum=None, V=None, out=None,
+                  row_status=None, stream=None):
+    """min((x_t - max)/T - log S, 0) per row. Returns (logprob, row_status)."""
+    B, V, ld = _rows(logits, V)
+    dev = logits.device
+    temperature = _param(temperature, B, torch.float32, dev, "temperature")
+    token = _param(token, B, torch.int32, dev, "token")
+    out = torch.empty(B, dtype=torch.float32, device=dev) if out is None else out
+    row_status = torch.empty(B, dtype=torch.int32, device=dev) if row_status is None else row_status
+    st = load().vsamp_logprob(
+        logits.data_ptr(), _dtype_code(logits), B, V, ld, _ptr(temperature, torch.float32, dev, B, "temperature"),
+        _ptr(token, torch.int32, dev, B, "token"), _ptr(row_max, torch.float32, dev, B, "row_max"),
+        _ptr(row_logsum, torch.float32, dev, B, "row_logsum"), _ptr(out, torch.float32, dev, B, "out"),
+        _ptr(row_status, torch.int32, dev, B, "row_status"), _stream(stream))
+    _check(st, "vsamp_logprob")
+    return out, row_status

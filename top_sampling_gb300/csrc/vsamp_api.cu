@@ -1,0 +1,292 @@
+// Host side of libvsamp.so: argument checks, per-device limits, launch geometry (cluster size, vectors
+// per thread) and the extern "C" entry points declared in include/vsamp.h.
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "vsamp_host.h"
+
+namespace vsamp {
+
+constexpr int kMaxDevices = 64;
+
+static DeviceInfo g_dev[kMaxDevices];
+static std::mutex g_mu;
+
+int env_int(const char* name, int dflt) {
+  const char* v = std::getenv(name);
+  if (!v || !*v) return dflt;
+  return std::atoi(v);
+}
+
+vsamp_status device_info(int dev, DeviceInfo& out) {
+  if (dev < 0 || dev >= kMaxDevices) return VSAMP_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return VSAMP_ERR_CUDA;
+    }
+    cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    int cl = 0;
+    cudaDeviceGetAttribute(&cl, cudaDevAttrClusterLaunch, dev);
+    cudaGetLastError();
+    d.max_cluster = cl ? 16 : 1;
+    // a smaller opt-in can be simulated for tests of the capacity checks
+    const int ov = env_int("VSAMP_SMEM_OPTIN_OVERRIDE", 0);
+    if (ov > 0 && ov < d.optin) d.optin = ov;
+    d.ready = 1;
+  }
+  out = d;
+  return VSAMP_OK;
+}
+
+// Launch geometry. A row spans C CTAs (one cluster); each CTA holds NT * q 16-byte vectors of it in
+// shared memory. The per-CTA budget keeps `per_sm` CTAs resident on an SM. Among the
+// cluster sizes whose slices fit, the one with the least padding is taken (q odd when that costs at
+// most an eighth: conflict-free 16-byte shared-memory loads); small batches spread rows over more CTAs.
+vsamp_status choose_geometry(int64_t V, int esize, int64_t B, const DeviceInfo& d, Geometry& g) {
+  const int64_t VE = 16 / esize;
+  const int64_t nvec = (V + VE - 1) / VE;
+  const int NT = env_int("VSAMP_THREADS", 256) == 128 ? kThreadsSmall : kThreadsLarge;
+  const int head = NT == kThreadsSmall ? slice_offset<kThreadsSmall>() : slice_offset<kThreadsLarge>();
+  const int per_sm = env_int("VSAMP_CTAS_PER_SM", NT == kThreadsSmall ? 5 : 3);
+  const int smem_sm = d.smem_per_sm > 0 ? d.smem_per_sm : d.optin;
+  const int odd = env_int("VSAMP_ODD_Q", 1);
+  const int forced = env_int("VSAMP_CLUSTER", 0);
+  auto q_for = [&](int C) {
+    int64_t q = (nvec + (int64_t)C * NT - 1) / ((int64_t)C * NT);
+    if (q < 1) q = 1;
+    if (odd && (q & 1) == 0 && (q + 1) * 8 <= q * 9) ++q;
+    return q;
+  };
+  const int64_t cap1 = (int64_t)d.optin - head;                       // one buffer, one CTA per SM
+  for (int nbuf = 1; nbuf >= 1; --nbuf) {
+    int64_t budget = ((int64_t)smem_sm / (per_sm > 0 ? per_sm : 1) - 1024 - head) / nbuf;
+    if (budget * nbuf > cap1) budget = cap1 / nbuf;
+    int C = 0;
+    if (forced > 0) {
+      if (forced <= d.max_cluster && (int64_t)NT * q_for(forced) * 16 * nbuf <= cap1) C = forced;
+    } else {
+      int cmin = 0;
+      for (int c = 1; c <= d.max_cluster; ++c)
+        if ((int64_t)NT * q_for(c) * 16 <= budget) { cmin = c; break; }
+      if (!cmin && nbuf == 1) {
+        for (int c = 1; c <= d.max_cluster; ++c)
+          if ((int64_t)NT * q_for(c) * 16 <= cap1) { cmin = c; break; }
+      }
+      if (cmin) {
+        C = cmin;
+        int64_t best = (int64_t)cmin * q_for(cmin);
+        for (int c = cmin + 1; c <= cmin + 3 && c <= d.max_cluster; ++c)
+          if ((int64_t)c * q_for(c) < best) { best = (int64_t)c * q_for(c); C = c; }
+        // small batches: more CTAs per row while slices stay >= 8 KB
+        while (C < d.max_cluster && B * C < 2LL * d.sm_count && (int64_t)NT * q_for(C + 1) * 16 >= 8192) ++C;
+      }
+    }
+    if (!C) continue;
+    g.NT = NT;
+    g.C = C;
+    g.q = (int)q_for(C);
+    g.nbuf = nbuf;
+    g.smem = head + nbuf * NT * g.q * 16;
+    return VSAMP_OK;
+  }
+  return VSAMP_ERR_UNSUPPORTED;
+}
+
+template <int MODE>
+static vsamp_status dispatch(Params p, vsamp_dtype dt, int64_t B, cudaStream_t s) {
+  if (dt == VSAMP_F32) return launch<float, MODE>(p, B, 4, s);
+  if (dt == VSAMP_BF16) return launch<__nv_bfloat16, MODE>(p, B, 2, s);
+  return VSAMP_ERR_INVALID_ARG;
+}
+
+static bool aligned16(const void* ptr, int64_t ld, int esize) {
+  return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0 && ((ld * esize) & 15) == 0;
+}
+
+static vsamp_status check_common(const void* x, vsamp_dtype dt, int64_t B, int64_t V, int64_t ld) {
+  if (!x) return VSAMP_ERR_INVALID_ARG;
+  if (dt != VSAMP_F32 && dt != VSAMP_BF16) return VSAMP_ERR_INVALID_ARG;
+  if (B <= 0 || V <= 0 || ld < V) return VSAMP_ERR_INVALID_ARG;
+  if (V > 0x7FFFFFF0LL) return VSAMP_ERR_UNSUPPORTED;
+  return VSAMP_OK;
+}
+
+static Params base_params(const void* x, vsamp_dtype dt, int64_t B, int64_t V, int64_t ld) {
+  Params p;
+  std::memset(&p, 0, sizeof(p));
+  p.x = static_cast<const unsigned char*>(x);
+  p.B = B;
+  p.V = V;
+  p.ld = ld;
+  const int es = dt == VSAMP_F32 ? 4 : 2;
+  p.tma = aligned16(x, ld, es) && env_int("VSAMP_NO_TMA", 0) == 0;
+  return p;
+}
+
+// Log-probability from given statistics: one thread per row.
+template <typename T>
+__global__ void logprob_from_stats_kernel(const unsigned char* x, int64_t B, int64_t V, int64_t ld,
+                                          const float* temperature, const int32_t* token, const float* row_max,
+                                          const float* row_logsum, float* out, int32_t* row_status) {
+  const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= B) return;
+  const int32_t tk = token[r];
+  const float temp = temperature ? temperature[r] : 1.f;
+  int st = VSAMP_OK;
+  float lp = __int_as_float(0x7FC00000);
+  if (tk < 0 || (int64_t)tk >= V || isnan(temp) || isinf(temp)) {
+    st = VSAMP_ERR_INVALID_ARG;
+  } else {
+    const float Teff = temp > 0.f ? temp : 1.f;
+    const float xt = Traits<T>::load_global(x, r * ld + tk);
+    const float m = row_max[r], ls = row_logsum[r];
+    if (!isfinite(xt) || !isfinite(m) || !isfinite(ls)) {
+      st = VSAMP_ERR_NONFINITE;
+    } else {
+      const double s = (double)((xt - m) * (1.f / Teff));
+      lp = (float)fmin(s - (double)ls, 0.0);
+    }
+  }
+  out[r] = lp;
+  if (row_status) row_status[r] = st;
+}
+
+}  // namespace vsamp
+
+using namespace vsamp;
+
+extern "C" {
+
+vsamp_status vsamp_softmax_lse(const void* logits, vsamp_dtype dt, int64_t B, int64_t V, int64_t ld,
+                               const float* temperature, float* row_max, float* row_logsum,
+                               int32_t* row_status, void* stream) {
+  vsamp_status st = check_common(logits, dt, B, V, ld);
+  if (st != VSAMP_OK) return st;
+  Params p = base_params(logits, dt, B, V, ld);
+  p.temperature = temperature;
+  p.row_max = row_max;
+  p.row_logsum = row_logsum;
+  p.row_status = row_status;
+  return dispatch<MODE_LSE>(p, dt, B, static_cast<cudaStream_t>(stream));
+}
+
+vsamp_status vsamp_topk_select(const void* scores, vsamp_dtype dt, int64_t B, int64_t max_len, int64_t ld,
+                               const int32_t* lengths, const int32_t* k, int32_t k_max, int32_t* out_idx,
+                               int32_t* row_status, void* stream) {
+  vsamp_status st = check_common(scores, dt, B, max_len, ld);
+  if (st != VSAMP_OK) return st;
+  if (!out_idx || k_max <= 0) return VSAMP_ERR_INVALID_ARG;
+  Params p = base_params(scores, dt, B, max_len, ld);
+  p.lengths = lengths;
+  p.k_sel = k;
+  p.k_max = k_max;
+  p.out_idx = out_idx;
+  p.row_status = row_status;
+  return dispatch<MODE_SELECT>(p, dt, B, static_cast<cudaStream_t>(stream));
+}
+
+vsamp_status vsamp_topp_minp_mask(const void* logits, vsamp_dtype dt, int64_t B, int64_t V, int64_t ld,
+                                  const float* temperature, const int32_t* top_k, const float* top_p,
+                                  const float* min_p, vsamp_cut* cut, uint8_t* mask, int32_t* stats,
+                                  void* stream) {
+  vsamp_status st = check_common(logits, dt, B, V, ld);
+  if (st != VSAMP_OK) return st;
+  if (!cut) return VSAMP_ERR_INVALID_ARG;
+  Params p = base_params(logits, dt, B, V, ld);
+  p.temperature = temperature;
+  p.top_k = top_k;
+  p.top_p = top_p;
+  p.min_p = min_p;
+  p.cut = cut;
+  p.mask = mask;
+  p.stats = stats;
+  if (mask) return dispatch<MODE_CUT | MODE_MASK>(p, dt, B, static_cast<cudaStream_t>(stream));
+  return dispatch<MODE_CUT>(p, dt, B, static_cast<cudaStream_t>(stream));
+}
+
+vsamp_status vsamp_sample(const void* logits, vsamp_dtype dt, int64_t B, int64_t V, int64_t ld,
+                          const float* temperature, const int32_t* top_k, const float* top_p, const float* min_p,
+                          const uint64_t* seed, const uint64_t* step, const uint32_t* row_id, int32_t* token,
+                          float* logprob, int32_t* row_status, int32_t* stats, void* stream) {
+  vsamp_status st = check_common(logits, dt, B, V, ld);
+  if (st != VSAMP_OK) return st;
+  if (!token) return VSAMP_ERR_INVALID_ARG;
+  Params p = base_params(logits, dt, B, V, ld);
+  p.temperature = temperature;
+  p.top_k = top_k;
+  p.top_p = top_p;
+  p.min_p = min_p;
+  p.seed = seed;
+  p.step = step;
+  p.row_id = row_id;
+  p.token = token;
+  p.logprob = logprob;
+  p.row_status = row_status;
+  p.stats = stats;
+  return dispatch<MODE_SAMPLE>(p, dt, B, static_cast<cudaStream_t>(stream));
+}
+
+vsamp_status vsamp_logprob(const void* logits, vsamp_dtype dt, int64_t B, int64_t V, int64_t ld,
+                           const float* temperature, const int32_t* token, const float* row_max,
+                           const float* row_logsum, float* out, int32_t* row_status, void* stream) {
+  vsamp_status st = check_common(logits, dt, B, V, ld);
+  if (st != VSAMP_OK) return st;
+  if (!token || !out) return VSAMP_ERR_INVALID_ARG;
+  if ((row_max == nullptr) != (row_logsum == nullptr)) return VSAMP_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (row_max) {
+    const int threads = 256;
+    const unsigned blocks = (unsigned)((B + threads - 1) / threads);
+    const unsigned char* x = static_cast<const unsigned char*>(logits);
+    if (dt == VSAMP_F32)
+      logprob_from_stats_kernel<float><<<blocks, threads, 0, s>>>(x, B, V, ld, temperature, token, row_max,
+                                                                  row_logsum, out, row_status);
+    else
+      logprob_from_stats_kernel<__nv_bfloat16><<<blocks, threads, 0, s>>>(x, B, V, ld, temperature, token,
+                                                                          row_max, row_logsum, out, row_status);
+    if (cudaGetLastError() != cudaSuccess) return VSAMP_ERR_CUDA;
+    return VSAMP_OK;
+  }
+  Params p = base_params(logits, dt, B, V, ld);
+  p.temperature = temperature;
+  p.token_in = token;
+  p.logprob = out;
+  p.row_status = row_status;
+  return dispatch<MODE_LOGPROB>(p, dt, B, s);
+}
+
+const char* vsamp_status_string(vsamp_status s) {
+  switch (s) {
+    case VSAMP_OK: return "ok";
+    case VSAMP_ERR_INVALID_ARG: return "invalid argument";
+    case VSAMP_ERR_UNSUPPORTED: return "unsupported on this device (shared memory or cluster size)";
+    case VSAMP_ERR_CUDA: return "CUDA runtime error";
+    case VSAMP_ERR_NONFINITE: return "non-finite value in the row";
+    case VSAMP_ERR_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+vsamp_status vsamp_device_info(int device, vsamp_limits* out) {
+  if (!out) return VSAMP_ERR_INVALID_ARG;
+  DeviceInfo d;
+  vsamp_status st = device_info(device, d);
+  if (st != VSAMP_OK) return st;
+  out->sm_count = d.sm_count;
+  out->smem_optin_bytes = d.optin;
+  out->max_cluster = d.max_cluster;
+  const int64_t per_cta = ((int64_t)d.optin - slice_offset<kThreadsLarge>()) / 16 * 16;
+  out->max_row_f32 = per_cta / 4 * d.max_cluster;
+  out->max_row_bf16 = per_cta / 2 * d.max_cluster;
+  return VSAMP_OK;
+}
+
+int32_t vsamp_version(void) { return (1 << 16) | 0; }
+
+}  // extern "C"

@@ -1,0 +1,255 @@
+// Device helpers for the sampling-stage kernels (sm_103a): bulk-copy / mbarrier / cluster PTX
+// wrappers, Philox4x32-10, order-preserving keys, fixed-point mass and reductions.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cooperative_groups.h>
+
+namespace vsamp {
+namespace cg = cooperative_groups;
+
+constexpr uint32_t kFullMask = 0xFFFFFFFFu;
+// Fixed-point scale of probability mass: w in (0, 1] is stored as round(w * 2^40) in a uint64.
+// A 2^21-token row sums to < 2^61, so row totals never overflow.
+constexpr int kMassShift = 40;
+constexpr float kMassScale = 1099511627776.0f;   // 2^40
+
+// ------------------------------------------------------------------------------------------------
+// Shared-memory addressing, bulk copies and mbarriers (PTX ISA: cp.async.bulk, mbarrier).
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(void* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(void* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+
+// Global -> own shared memory bulk copy; completion is signalled on `bar` as transaction bytes.
+// dst, src and bytes must all be multiples of 16.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, void* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Orders this thread's earlier generic-proxy accesses to shared memory before later async-proxy
+// (bulk copy) writes to it.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(void* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase: gives up after ~`max_cycles` SM clock cycles and returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(void* bar, uint32_t parity, long long max_cycles) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (clock64() - t0 > max_cycles) return false;
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// Distributed shared memory: a CTA's shared address mapped into the address window of CTA `rank` of
+// the cluster, stores and an acquire-release atomic add there.
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t dsmem_map(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void dsmem_store_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+__device__ __forceinline__ uint4 dsmem_load_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ void dsmem_store_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+// Atomic add at cluster scope with acquire-release ordering; returns the previous value.
+__device__ __forceinline__ uint32_t dsmem_atomic_add_acq_rel(uint32_t addr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.cluster.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
+  return old;
+}
+
+// ------------------------------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3", SC'11).
+// Round: (c0,c1,c2,c3) -> (hi(M1*c2)^c1^k0, lo(M1*c2), hi(M0*c0)^c3^k1, lo(M0*c0)); the key advances by
+// the Weyl constants between rounds.
+// ------------------------------------------------------------------------------------------------
+struct PhiloxKey {
+  uint32_t k0, k1;
+};
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, PhiloxKey key) {
+  constexpr uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
+  constexpr uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+  uint32_t k0 = key.k0, k1 = key.k1;
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    // one 32x32 -> 64-bit product per multiplier, split into its high and low words
+    unsigned long long p0, p1;
+    asm("mul.wide.u32 %0, %1, %2;" : "=l"(p0) : "r"(c.x), "r"(M0));
+    asm("mul.wide.u32 %0, %1, %2;" : "=l"(p1) : "r"(c.z), "r"(M1));
+    const uint32_t lo0 = (uint32_t)p0, hi0 = (uint32_t)(p0 >> 32);
+    const uint32_t lo1 = (uint32_t)p1, hi1 = (uint32_t)(p1 >> 32);
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    k0 += W0;
+    k1 += W1;
+  }
+  return c;
+}
+
+__device__ __forceinline__ uint32_t philox_word(uint4 w, int lane) {
+  return lane == 0 ? w.x : lane == 1 ? w.y : lane == 2 ? w.z : w.w;
+}
+
+// ------------------------------------------------------------------------------------------------
+// Order-preserving keys. fp32: positive -> bits | 0x80000000, negative -> ~bits; -0.0 reads as +0.0.
+// bf16 uses the same map on 16 bits. key32_of_key16 widens a bf16 key to the fp32 key of the same value.
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t key_f32_bits(uint32_t b) {
+  b = (b == 0x80000000u) ? 0u : b;
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ uint32_t key_bf16_bits(uint32_t h) {
+  h &= 0xFFFFu;
+  h = (h == 0x8000u) ? 0u : h;
+  return (h & 0x8000u) ? (~h & 0xFFFFu) : (h | 0x8000u);
+}
+__device__ __forceinline__ uint32_t key32_of_key16(uint32_t k16) {
+  return (k16 << 16) | ((k16 & 0x8000u) ? 0u : 0xFFFFu);
+}
+__device__ __forceinline__ float value_of_key32(uint32_t k) {
+  const uint32_t b = (k & 0x80000000u) ? (k ^ 0x80000000u) : ~k;
+  return __uint_as_float(b);
+}
+
+// ------------------------------------------------------------------------------------------------
+// exp as 2^(s * log2 e) with the hardware ex2 approximation (no flush to zero; relative error of a
+// few ulp, tested against expf in the GPU test suite).
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ uint64_t mass_fx(float w) { return __float2ull_rn(w * kMassScale); }
+
+// ceil(p * S) for an fp32 p in [0, 1] and a fixed-point mass S < 2^63, exactly, in integer arithmetic:
+// p = m * 2^(e - 150) with a 24-bit m, and the 88-bit product m * S is shifted right with rounding up.
+__host__ __device__ __forceinline__ unsigned long long ceil_mul_frac(float p, unsigned long long S) {
+  if (!(p > 0.f)) return 0ull;
+  if (p >= 1.f) return S;
+#ifdef __CUDA_ARCH__
+  const uint32_t bits = __float_as_uint(p);
+#else
+  uint32_t bits;
+  __builtin_memcpy(&bits, &p, 4);
+#endif
+  uint32_t e = (bits >> 23) & 0xFFu;
+  unsigned long long m = bits & 0x7FFFFFu;
+  if (e) m |= 0x800000u; else e = 1;
+  const int sh = 150 - (int)e;                      // >= 24 because p < 1
+  const unsigned long long lo = m * S;
+#ifdef __CUDA_ARCH__
+  const unsigned long long hi = __umul64hi(m, S);
+#else
+  const unsigned long long hi = (unsigned long long)(((unsigned __int128)m * S) >> 64);
+#endif
+  unsigned long long qv;
+  bool rem;
+  if (sh < 64) {
+    qv = (lo >> sh) | (hi << (64 - sh));
+    rem = (lo & ((1ull << sh) - 1ull)) != 0ull;
+  } else if (sh == 64) {
+    qv = hi;
+    rem = lo != 0ull;
+  } else if (sh < 128) {
+    qv = hi >> (sh - 64);
+    rem = lo != 0ull || (hi & ((1ull << (sh - 64)) - 1ull)) != 0ull;
+  } else {
+    qv = 0ull;
+    rem = (lo | hi) != 0ull;
+  }
+  return qv + (rem ? 1ull : 0ull);
+}
+
+// A 64-bit count or fixed-point mass as fp32 (two exact 32-bit conversions, relative error ~1e-7).
+__device__ __forceinline__ float u64_to_float(unsigned long long v) {
+  return fmaf((float)(uint32_t)(v >> 32), 4294967296.0f, (float)(uint32_t)v);
+}
+
+// ------------------------------------------------------------------------------------------------
+// Warp reductions.
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ float warp_max_f(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFullMask, v, o));
+  return v;
+}
+__device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFullMask, v, o);
+  return v;
+}
+__device__ __forceinline__ uint32_t warp_sum_u32(uint32_t v) { return __reduce_add_sync(kFullMask, v); }
+__device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) { return __reduce_max_sync(kFullMask, v); }
+__device__ __forceinline__ uint32_t warp_min_u32(uint32_t v) { return __reduce_min_sync(kFullMask, v); }
+
+// (score, index) arg-max with ties to the lower index.
+struct ArgMax {
+  float score;
+  int32_t idx;
+  float s;        // max-subtracted, temperature-scaled logit of idx
+};
+__device__ __forceinline__ bool argmax_better(float a, int32_t ia, float b, int32_t ib) {
+  return a > b || (a == b && ia < ib);
+}
+__device__ __forceinline__ ArgMax warp_argmax(ArgMax v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    ArgMax w;
+    w.score = __shfl_xor_sync(kFullMask, v.score, o);
+    w.idx = __shfl_xor_sync(kFullMask, v.idx, o);
+    w.s = __shfl_xor_sync(kFullMask, v.s, o);
+    if (argmax_better(w.score, w.idx, v.score, v.idx)) v = w;
+  }
+  return v;
+}
+
+}  // namespace vsamp

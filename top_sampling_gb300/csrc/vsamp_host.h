@@ -1,0 +1,39 @@
+// Host-side pieces shared by the translation units of libvsamp.so: device limits, launch geometry and
+// the kernel launcher.
+#pragma once
+
+#include <cstdint>
+#include <cstdlib>
+
+#include "vsamp.h"
+#include "vsamp_row.cuh"
+
+namespace vsamp {
+
+constexpr int kThreadsSmall = 128;   // threads per CTA (two instantiations of every kernel)
+constexpr int kThreadsLarge = 256;
+
+struct DeviceInfo {
+  int ready = 0;
+  int sm_count = 0;
+  int optin = 0;           // max shared memory per block (opt-in)
+  int smem_per_sm = 0;     // shared memory per multiprocessor
+  int max_cluster = 0;     // largest cluster size the kernels request
+};
+
+struct Geometry {
+  int NT = 256;    // threads per CTA
+  int C = 1;       // CTAs per row (cluster size)
+  int q = 1;       // 16-byte vectors per thread
+  int nbuf = 2;    // slice buffers per CTA
+  int smem = 0;    // dynamic shared memory bytes
+};
+
+int env_int(const char* name, int dflt);
+vsamp_status device_info(int dev, DeviceInfo& out);
+vsamp_status choose_geometry(int64_t V, int esize, int64_t B, const DeviceInfo& d, Geometry& g);
+
+template <typename T, int MODE>
+vsamp_status launch(Params p, int64_t B, int esize, cudaStream_t stream);
+
+}  // namespace vsamp

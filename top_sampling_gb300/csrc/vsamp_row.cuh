@@ -1,0 +1,1346 @@
+// The per-row sampling engine: one thread-block cluster of C CTAs owns one row; each CTA holds a slice
+// of the row in shared memory (bulk-copied from HBM once) and every later pass reads shared memory.
+//
+// Passes (each thread owns q consecutive 16-byte vectors of its CTA's slice, in index order):
+//   load   -- cp.async.bulk of the slice in four chunks, each on its own mbarrier;
+//   P1     -- row maximum M and a non-finite check;
+//   P2     -- S = sum exp((x - M)/T) in 64-bit fixed point, each thread's count of maxima and, when
+//             min-p is on, the min-p statistics;
+//   select -- top-k / top-p cut: directly inside the maximum's tie group when it holds the cut,
+//             otherwise by cluster-wide radix rounds over the order-preserving keys with count and
+//             fixed-point mass histograms exchanged through distributed shared memory;
+//   ties   -- the cut takes the lowest-index elements of its key group: from per-thread counts and an
+//             index-ordered prefix over threads and CTAs, every thread derives its own last kept index
+//             (only the thread holding the boundary rescans its chunk);
+//   P4     -- Philox4x32-10 per group of four tokens, Gumbel-max over the kept prefix with a prune
+//             bound from the kept mass, cluster arg-max, log-probability.
+// Per-row scalar decisions (in binary64 where needed) are taken by thread 0 and broadcast through
+// shared memory. Every branch that decides which cluster barriers run depends only on cluster-reduced
+// values, so all CTAs of a cluster execute the same barrier sequence.
+#pragma once
+
+#include "vsamp_device.cuh"
+#include "vsamp.h"
+
+namespace vsamp {
+
+enum Mode : int {
+  MODE_LSE = 1,       // row_max / row_logsum
+  MODE_SELECT = 2,    // stand-alone top-k select (out_idx)
+  MODE_CUT = 4,       // cut descriptor
+  MODE_MASK = 8,      // uint8 mask of the cut
+  MODE_SAMPLE = 16,   // Gumbel-max draw + log-probability
+  MODE_LOGPROB = 32,  // log-probability of given tokens (statistics recomputed)
+};
+
+// Path flags reported in stats[r][3].
+enum PathFlag : int {
+  PATH_MAXGROUP = 1,    // the cut lies in the maximum's tie group (no radix rounds)
+  PATH_RADIX_K = 2,     // top-k radix rounds ran
+  PATH_RADIX_P = 4,     // top-p radix rounds ran
+  PATH_MINP = 8,        // min-p gave the shortest prefix
+  PATH_FALLBACK = 16,   // the prune bound did not certify the draw; all kept tokens were evaluated
+  PATH_NOTMA = 32,      // rows were loaded with plain loads (unaligned)
+};
+
+struct Params {
+  const unsigned char* x;   // [B, ld] elements
+  int64_t B, V, ld;         // V: row length (max length when `lengths` is given)
+  const int32_t* lengths;
+  const float* temperature;
+  const int32_t* top_k;
+  const float* top_p;
+  const float* min_p;
+  const uint64_t* seed;
+  const uint64_t* step;
+  const uint32_t* row_id;
+  const int32_t* token_in;
+  const int32_t* k_sel;
+  int32_t k_max;
+  float* row_max;
+  float* row_logsum;
+  int32_t* out_idx;
+  vsamp_cut* cut;
+  uint8_t* mask;
+  int32_t* token;
+  float* logprob;
+  int32_t* row_status;
+  int32_t* stats;
+  int64_t row0;             // first row of this launch
+  int32_t q;                // 16-byte vectors per thread
+  int32_t tma;              // rows are 16-byte aligned: bulk copies
+  long long wait_cycles;    // bound of every device-side wait
+};
+
+constexpr int32_t kNoIndex = -1;
+constexpr int32_t kAllIndex = 0x7FFFFFFF;
+constexpr float kTwoM32 = 2.3283064365386963e-10f;   // 2^-32
+constexpr float kTwoM33 = 1.1641532182693481e-10f;   // 2^-33
+
+// ------------------------------------------------------------------------------------------------
+// Element traits: fp32 (4 per vector, 32-bit radix keys) and bf16 (8 per vector, 16-bit radix keys).
+// ------------------------------------------------------------------------------------------------
+template <typename T>
+struct Traits;
+
+template <>
+struct Traits<float> {
+  static constexpr int VE = 4;
+  static constexpr int KB = 32;
+  static constexpr int ESIZE = 4;
+  __device__ static __forceinline__ void values(const uint4& v, float (&x)[4]) {
+    x[0] = __uint_as_float(v.x); x[1] = __uint_as_float(v.y);
+    x[2] = __uint_as_float(v.z); x[3] = __uint_as_float(v.w);
+  }
+  __device__ static __forceinline__ uint32_t rkey_of_value(float x) { return key_f32_bits(__float_as_uint(x)); }
+  // every element of the vector is >= xv
+  __device__ static __forceinline__ bool all_ge(const uint4& v, float xv) {
+    return fminf(fminf(__uint_as_float(v.x), __uint_as_float(v.y)), fminf(__uint_as_float(v.z), __uint_as_float(v.w))) >= xv;
+  }
+  __device__ static __forceinline__ uint32_t key32(uint32_t rk) { return rk; }
+  __device__ static __forceinline__ float value_of_rkey(uint32_t rk) { return value_of_key32(rk); }
+  __device__ static __forceinline__ float load_global(const unsigned char* p, int64_t e) {
+    return reinterpret_cast<const float*>(p)[e];
+  }
+};
+
+template <>
+struct Traits<__nv_bfloat16> {
+  static constexpr int VE = 8;
+  static constexpr int KB = 16;
+  static constexpr int ESIZE = 2;
+  __device__ static __forceinline__ void values(const uint4& v, float (&x)[8]) {
+    x[0] = __uint_as_float(v.x << 16); x[1] = __uint_as_float(v.x & 0xFFFF0000u);
+    x[2] = __uint_as_float(v.y << 16); x[3] = __uint_as_float(v.y & 0xFFFF0000u);
+    x[4] = __uint_as_float(v.z << 16); x[5] = __uint_as_float(v.z & 0xFFFF0000u);
+    x[6] = __uint_as_float(v.w << 16); x[7] = __uint_as_float(v.w & 0xFFFF0000u);
+  }
+  __device__ static __forceinline__ uint32_t rkey_of_value(float x) { return key_bf16_bits(__float_as_uint(x) >> 16); }
+  __device__ static __forceinline__ __nv_bfloat162 pair(uint32_t w) {
+    __nv_bfloat162 r;
+    __builtin_memcpy(&r, &w, 4);
+    return r;
+  }
+  // every element of the vector is >= xv (packed minimum of the eight values)
+  __device__ static __forceinline__ bool all_ge(const uint4& v, float xv) {
+    const __nv_bfloat162 m = __hmin2(__hmin2(pair(v.x), pair(v.y)), __hmin2(pair(v.z), pair(v.w)));
+    return fminf(__low2float(m), __high2float(m)) >= xv;
+  }
+  __device__ static __forceinline__ uint32_t key32(uint32_t rk) { return key32_of_key16(rk); }
+  __device__ static __forceinline__ float value_of_rkey(uint32_t rk) { return value_of_key32(key32_of_key16(rk)); }
+  __device__ static __forceinline__ float load_global(const unsigned char* p, int64_t e) {
+    const uint32_t h = reinterpret_cast<const uint16_t*>(p)[e];
+    return __uint_as_float(h << 16);
+  }
+};
+
+// ------------------------------------------------------------------------------------------------
+// Shared memory.
+// ------------------------------------------------------------------------------------------------
+struct Mail {             // one CTA's contribution to a cluster exchange (read by peers via DSMEM)
+  float f[4];
+  uint32_t u[8];
+  unsigned long long q[4];
+  int32_t i[4];
+};
+
+// A cut: the kept prefix ends inside the key group `rk` after `need` of its elements (index order).
+struct Cut {
+  uint32_t rk;
+  unsigned long long above;     // elements with a larger key
+  unsigned long long need;      // elements taken from the group
+  unsigned long long cnt_eq;    // group size (0 if unknown)
+  unsigned long long mass;      // fixed-point mass of the kept prefix
+  int whole;                    // every element of the group is kept
+  __host__ __device__ unsigned long long kept() const { return above + need; }
+};
+
+// Per-row scalar decisions; every thread derives the same values from cluster-reduced statistics.
+struct Plan {
+  int status;
+  int ck_mode;                  // top-k: 0 off, 1 inside the maximum's group, 2 radix
+  int cp_mode;                  // top-p: 0 off, 1 inside the maximum's group, 2 radix
+  int path;
+  float goal_p;                 // top-p radix goal as a fraction of the row mass (< 0: use cp_goal)
+  unsigned long long cp_goal;
+  Cut ck, cp, fin;
+  uint32_t kmin32;              // min-p: keep keys >= kmin32 (fp32 key space)
+  int all_cand;                 // P4: evaluate every kept token
+  uint32_t bk;                  // P4: a token is a candidate only if its Philox word is < bk
+  float kappa;                  // P4: e^3 / kept mass
+  float b0;                     // P4: prune bound -log(kappa)
+  float logS;                   // log of the row mass (fixed-point units removed)
+};
+
+template <int NT>
+struct Smem {
+  static constexpr int NW = NT / 32;
+  unsigned long long bar[NT / 32];   // one mbarrier per warp: its region of the slice has landed
+  Mail mail[2];
+  // P4 partial arg-max of every CTA of the cluster (used in CTA 0's copy), per row parity, and the
+  // number of CTAs that have published theirs
+  uint4 aslot[2][16];
+  uint32_t acnt[2];
+  uint32_t hcnt[2][256];
+  uint32_t hlo[2][256];
+  uint32_t hhi[2][256];
+  uint32_t gcnt[256];
+  unsigned long long gmass[256];
+  uint32_t tcount[NT];
+  uint32_t tpre[NT];
+  float wf[NW][3];
+  uint32_t wu[NW][4];
+  unsigned long long wq[NW][3];
+  int32_t wi[NW][2];
+  uint32_t bu[8];
+  unsigned long long bq[4];
+  int32_t bi[4];
+  float bf[4];
+};
+
+template <int NT>
+__host__ __device__ constexpr int slice_offset() {
+  return (int)((sizeof(Smem<NT>) + 127) / 128 * 128);
+}
+
+// Result of a cluster-wide radix search.
+struct RadixOut {
+  uint32_t rk;                  // the group's radix key
+  unsigned long long cnt_above; // elements with a larger key
+  unsigned long long mass_above;
+  unsigned long long cnt_eq;    // elements with exactly this key
+  unsigned long long mass_eq;
+  unsigned long long goal;      // the goal left inside the group (top-p: target mass minus mass above)
+  int ok;
+};
+
+template <typename T, int NT, int MODE>
+struct RowEngine {
+  using Tr = Traits<T>;
+  static constexpr int VE = Tr::VE;
+  static constexpr int NW = NT / 32;
+
+  const Params& p;
+  Smem<NT>& sh;
+  const uint4* mine;       // this thread's vectors in shared memory
+  cg::cluster_group cluster;
+  int C, crank, row, t, lane, warp, q;
+  int64_t n;               // valid elements in the row
+  int64_t thr_e0;          // global index of this thread's first element
+  int thr_n;               // valid elements in this thread's chunk
+  int xc;                  // cluster exchange counter (ping-pong parity)
+  int passes, rounds;
+
+  __device__ RowEngine(const Params& p_, Smem<NT>& sh_)
+      : p(p_), sh(sh_), cluster(cg::this_cluster()) {
+    C = gridDim.x;
+    crank = blockIdx.x;
+    row = 0;
+    t = threadIdx.x;
+    lane = t & 31;
+    warp = t >> 5;
+    q = p.q;
+    mine = nullptr;
+    xc = 0;
+    passes = 0;
+    rounds = 0;
+  }
+  __device__ void set_slice(const unsigned char* slice) { mine = reinterpret_cast<const uint4*>(slice) + (size_t)t * q; }
+
+  // ---------------- cluster exchange primitives ----------------
+  __device__ __forceinline__ Mail& my_mail() { return sh.mail[xc & 1]; }
+  // All threads, after this CTA's mail is written (by thread 0): publishes it and waits for the peers.
+  __device__ __forceinline__ void exchange() {
+    __syncthreads();
+    cluster.sync();
+  }
+  __device__ __forceinline__ const Mail* peer_mail(int rank) {
+    return cluster.map_shared_rank(&sh.mail[xc & 1], rank);
+  }
+  __device__ __forceinline__ void exchange_done() { ++xc; }
+
+  // Exclusive scan of tcount[] over threads (index order) into tpre[]; returns the block total.
+  __device__ uint32_t block_scan_tcount() {
+    __syncthreads();
+    const uint32_t v = sh.tcount[t];
+    uint32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFullMask, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) sh.wu[warp][1] = incl;
+    __syncthreads();
+    uint32_t wbase = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const uint32_t s = sh.wu[w][1];
+      if (w < warp) wbase += s;
+      total += s;
+    }
+    sh.tpre[t] = wbase + incl - v;
+    __syncthreads();
+    return total;
+  }
+
+  // Calls f(global index, value) for every valid element of this thread's chunk, in index order.
+  template <class F>
+  __device__ __forceinline__ void for_each(F&& f) {
+    const int nfull = thr_n / VE;
+    for (int j = 0; j < nfull; ++j) {
+      float x[VE];
+      Tr::values(mine[j], x);
+#pragma unroll
+      for (int i = 0; i < VE; ++i) f(thr_e0 + (int64_t)j * VE + i, x[i]);
+    }
+    const int tail = thr_n - nfull * VE;
+    if (tail) {
+      float x[VE];
+      Tr::values(mine[nfull], x);
+#pragma unroll
+      for (int i = 0; i < VE; ++i)
+        if (i < tail) f(thr_e0 + (int64_t)nfull * VE + i, x[i]);
+    }
+  }
+
+  // Cluster exclusive prefix of a per-CTA value: returns (sum over lower ranks, total) to every thread.
+  __device__ void cluster_prefix_u32(uint32_t mine_val, int slot, uint32_t& pre, uint32_t& total) {
+    if (t == 0) my_mail().u[slot] = mine_val;
+    exchange();
+    if (warp == 0) {
+      const uint32_t v = lane < C ? peer_mail(lane)->u[slot] : 0u;
+      uint32_t incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFullMask, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const uint32_t tot = __shfl_sync(kFullMask, incl, 31);
+      const uint32_t mypre = __shfl_sync(kFullMask, incl - v, crank);
+      if (lane == 0) { sh.bu[0] = mypre; sh.bu[1] = tot; }
+    }
+    exchange_done();
+    __syncthreads();
+    pre = sh.bu[0];
+    total = sh.bu[1];
+    __syncthreads();
+  }
+
+  // Per-thread count of elements equal to xv, into tcount[].
+  __device__ void count_equal_pass(float xv) {
+    uint32_t c = 0;
+    for_each([&](int64_t, float x) { c += (x == xv) ? 1u : 0u; });
+    sh.tcount[t] = c;
+    ++passes;
+  }
+
+  // The group of value xv keeps its `need` lowest-index elements. tcount[]/tpre[] hold each thread's
+  // count of the group and its exclusive prefix in the CTA; cpre is the count over lower CTA ranks.
+  // Returns this thread's last kept index (kAllIndex: every element of the group in its chunk is kept;
+  // kNoIndex: none). The thread holding the need-th element gets it in `boundary`; its warp finds it
+  // together (one 16-byte vector of that thread's chunk per lane, then a warp prefix of the counts).
+  __device__ int32_t local_cut_index(float xv, unsigned long long need, uint32_t cpre, int32_t& boundary) {
+    const unsigned long long start = (unsigned long long)cpre + sh.tpre[t];
+    const unsigned long long cnt = sh.tcount[t];
+    boundary = kNoIndex;
+    const bool holds = start < need && need <= start + cnt;
+    const uint32_t bal = __ballot_sync(kFullMask, holds);
+    if (bal) {
+      const int src = __ffs(bal) - 1;
+      uint32_t remaining = __shfl_sync(kFullMask, (uint32_t)(need - start), src);
+      const int src_n = __shfl_sync(kFullMask, thr_n, src);
+      const long long src_e0 = __shfl_sync(kFullMask, (long long)thr_e0, src);
+      const uint4* src_vec = mine + (src - lane) * q;
+      int32_t found = kNoIndex;
+      for (int j0 = 0; j0 * VE < src_n; j0 += 32) {
+        const int j = j0 + lane;
+        const bool okv = j * VE < src_n;
+        float x[VE];
+        uint32_t c = 0;
+        if (okv) {
+          Tr::values(src_vec[j], x);
+#pragma unroll
+          for (int i = 0; i < VE; ++i) c += (j * VE + i < src_n && x[i] == xv) ? 1u : 0u;
+        }
+        uint32_t incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(kFullMask, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const uint32_t excl = incl - c;
+        const bool here = okv && excl < remaining && remaining <= incl;
+        int32_t idx = kNoIndex;
+        if (here) {
+          uint32_t seen = excl;
+#pragma unroll
+          for (int i = 0; i < VE; ++i) {
+            if (idx < 0 && j * VE + i < src_n && x[i] == xv && ++seen == remaining)
+              idx = (int32_t)(src_e0 + (long long)j * VE + i);
+          }
+        }
+        const uint32_t hb = __ballot_sync(kFullMask, here);
+        if (hb) {
+          found = __shfl_sync(kFullMask, idx, __ffs(hb) - 1);
+          break;
+        }
+        remaining -= __shfl_sync(kFullMask, incl, 31);
+      }
+      if (lane == src) {
+        boundary = found;
+        return found;
+      }
+    }
+    if (start >= need) return kNoIndex;
+    return kAllIndex;
+  }
+
+  // ---------------- radix search ----------------
+  // COUNT (mass_mode == false): the group holding the goal-th largest element (1-based).
+  // MASS: the group where the cumulative mass (from the largest key down) first reaches the goal;
+  //       if goal_p >= 0 the goal is ceil(goal_p * total mass of the row) taken in the first round.
+  // want_mass: also histogram masses (mass_above / mass_eq are valid).
+  __device__ RadixOut radix_search(bool mass_mode, unsigned long long goal, float goal_p, bool want_mass, float M,
+                                   float c1) {
+    RadixOut out{};
+    out.ok = 1;
+    uint32_t prefix = 0;
+    unsigned long long cnt_above = 0, mass_above = 0;
+    const bool hist_mass = want_mass || mass_mode;
+    for (int shift = Tr::KB - 8; shift >= 0; shift -= 8) {
+      const int par = xc & 1;
+      uint32_t* hc = sh.hcnt[par];
+      uint32_t* hl = sh.hlo[par];
+      uint32_t* hh = sh.hhi[par];
+      for (int b = t; b < 256; b += NT) { hc[b] = 0; hl[b] = 0; hh[b] = 0; }
+      __syncthreads();
+      const int hi_shift = shift + 8;
+      const uint32_t hmask = hi_shift >= 32 ? 0u : (0xFFFFFFFFu << hi_shift);
+      uint32_t run_bin = 0xFFFFFFFFu, run_cnt = 0;
+      unsigned long long run_mass = 0;
+      auto flush = [&]() {
+        if (run_cnt) {
+          atomicAdd(&hc[run_bin], run_cnt);
+          if (hist_mass) {
+            const uint32_t lo = (uint32_t)run_mass, hi = (uint32_t)(run_mass >> 32);
+            const uint32_t old = atomicAdd(&hl[run_bin], lo);
+            const uint32_t carry = (old + lo < old) ? 1u : 0u;
+            if (hi + carry) atomicAdd(&hh[run_bin], hi + carry);
+          }
+        }
+      };
+      for_each([&](int64_t, float x) {
+        const uint32_t rk = Tr::rkey_of_value(x);
+        if ((rk & hmask) == (prefix & hmask)) {
+          const uint32_t bin = (rk >> shift) & 255u;
+          if (bin != run_bin) {
+            flush();
+            run_bin = bin;
+            run_cnt = 0;
+            run_mass = 0;
+          }
+          ++run_cnt;
+          if (hist_mass) run_mass += mass_fx(ex2_approx((x - M) * c1));
+        }
+      });
+      flush();
+      ++passes;
+      ++rounds;
+      exchange();
+      // cluster-sum the histograms
+      for (int b = t; b < 256; b += NT) {
+        uint32_t cs = 0;
+        unsigned long long ms = 0;
+        for (int r = 0; r < C; ++r) {
+          cs += cluster.map_shared_rank(&sh.hcnt[par][b], r)[0];
+          if (hist_mass) {
+            const unsigned long long lo = cluster.map_shared_rank(&sh.hlo[par][b], r)[0];
+            const unsigned long long hi = cluster.map_shared_rank(&sh.hhi[par][b], r)[0];
+            ms += lo + (hi << 32);
+          }
+        }
+        sh.gcnt[b] = cs;
+        sh.gmass[b] = ms;
+      }
+      exchange_done();
+      __syncthreads();
+      if (mass_mode && goal_p >= 0.f && shift == Tr::KB - 8) {
+        if (warp == 0) {
+          unsigned long long tot = 0;
+          for (int b = lane; b < 256; b += 32) tot += sh.gmass[b];
+          tot = warp_sum_u64(tot);
+          if (lane == 0) sh.bq[3] = ceil_mul_frac(goal_p, tot);
+        }
+        __syncthreads();
+        goal = sh.bq[3];
+      }
+      // warp 0: suffix scan from the top bin; lane l covers bins 255-8l .. 248-8l
+      if (warp == 0) {
+        uint32_t lc = 0;
+        unsigned long long lm = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int b = 255 - 8 * lane - i;
+          lc += sh.gcnt[b];
+          lm += sh.gmass[b];
+        }
+        uint32_t ic = lc;
+        unsigned long long im = lm;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t yc = __shfl_up_sync(kFullMask, ic, o);
+          const unsigned long long ym = __shfl_up_sync(kFullMask, im, o);
+          if (lane >= o) { ic += yc; im += ym; }
+        }
+        const unsigned long long ec = ic - lc, em = im - lm;   // bins above this lane's
+        const unsigned long long g = goal;
+        const bool mine_has = mass_mode ? (em < g && g <= im) : (ec < g && g <= (unsigned long long)ic);
+        const uint32_t ballot = __ballot_sync(kFullMask, mine_has);
+        if (ballot == 0) {
+          if (lane == 0) sh.bu[2] = 0xFFFFFFFFu;
+        } else if (lane == __ffs(ballot) - 1) {
+          unsigned long long ac = ec, am = em;
+          int sel = -1;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int b = 255 - 8 * lane - i;
+            const unsigned long long c = sh.gcnt[b], m = sh.gmass[b];
+            const bool hit = mass_mode ? (am < g && g <= am + m) : (ac < g && g <= ac + c);
+            if (hit && sel < 0) sel = b;
+            if (sel < 0) { ac += c; am += m; }
+          }
+          sh.bu[2] = (uint32_t)sel;
+          sh.bq[0] = ac;
+          sh.bq[1] = am;
+        }
+      }
+      __syncthreads();
+      const uint32_t sel = sh.bu[2];
+      if (sel > 255u) {   // cannot happen with consistent histograms; reported as an error
+        out.ok = 0;
+        __syncthreads();
+        return out;
+      }
+      const unsigned long long ac = sh.bq[0], am = sh.bq[1];
+      out.cnt_eq = sh.gcnt[sel];
+      out.mass_eq = sh.gmass[sel];
+      __syncthreads();
+      prefix |= sel << shift;
+      cnt_above += ac;
+      mass_above += am;
+      if (mass_mode) goal -= am; else goal -= ac;
+    }
+    out.rk = prefix;
+    out.cnt_above = cnt_above;
+    out.mass_above = mass_above;
+    out.goal = goal;
+    return out;
+  }
+};
+
+// ------------------------------------------------------------------------------------------------
+// Perturbed score of one candidate token: E = -log1p(-u) = -log(1 - u), evaluated on the exact side of
+// 1/2 (1 - u is itself a cell midpoint of the complementary word ~b), score = s - log(E).
+// ------------------------------------------------------------------------------------------------
+static __device__ __noinline__ float gumbel_score(float s, uint32_t b) {
+  float E;
+  if (b < 0x80000000u) {
+    const float u = fmaf((float)b, kTwoM32, kTwoM33);
+    E = -log1pf(-u);
+  } else {
+    const float um = fmaf((float)(~b), kTwoM32, kTwoM33);
+    E = -logf(um);
+  }
+  return s - logf(E);
+}
+
+// ------------------------------------------------------------------------------------------------
+// The kernel: persistent clusters. Cluster y handles rows y, y + G, y + 2G, ... (G = gridDim.y); every
+// warp bulk-copies its own region of the slice; right after its last pass over row r it copies its region
+// of row r + G (the P4 fallback pass, which is rare, then reads the row from global memory), so HBM
+// streams while the row's reductions and the other CTAs on the SM finish.
+// ------------------------------------------------------------------------------------------------
+template <typename T, int NT, int MODE>
+__global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Params p) {
+  using Tr = Traits<T>;
+  using Eng = RowEngine<T, NT, MODE>;
+  constexpr int VE = Tr::VE;
+  constexpr int ES = Tr::ESIZE;
+  constexpr bool kSel = (MODE & MODE_SELECT) != 0;
+  constexpr bool kCutLike = (MODE & (MODE_CUT | MODE_SAMPLE)) != 0;
+  extern __shared__ __align__(128) unsigned char dyn[];
+  Smem<NT>& sh = *reinterpret_cast<Smem<NT>*>(dyn);
+  unsigned char* slice = dyn + slice_offset<NT>();
+  Eng E(p, sh);
+  Plan plan{};          // per-row decisions, computed identically by every thread
+  const int t = E.t, lane = E.lane, warp = E.warp, q = E.q, C = E.C, crank = E.crank;
+  const int64_t G = gridDim.y;
+  const int64_t first = blockIdx.y;
+  const int64_t elems_cta = (int64_t)NT * q * VE;
+  const int64_t cta_e0 = (int64_t)crank * elems_cta;
+  const int64_t warp_bytes = (int64_t)32 * q * 16;     // each warp's region of the slice
+
+  auto row_len = [&](int64_t r) -> int64_t {
+    int64_t n = p.V;
+    if (p.lengths) n = p.lengths[r];
+    return (n > 0 && n <= p.V) ? n : 0;
+  };
+  auto cta_count = [&](int64_t n) -> int64_t {
+    const int64_t c = n - cta_e0;
+    return c < 0 ? 0 : (c > elems_cta ? elems_cta : c);
+  };
+  // lane 0 of each warp: bulk copy of the warp's region of row r (its 16-byte-aligned part)
+  auto issue_warp = [&](int64_t r) {
+    const int64_t b16 = (cta_count(row_len(r)) * ES) & ~(int64_t)15;
+    const int64_t lo = (int64_t)warp * warp_bytes;
+    int64_t nb = b16 - lo;
+    nb = nb < 0 ? 0 : (nb > warp_bytes ? warp_bytes : nb);
+    mbar_arrive_expect_tx(&sh.bar[warp], (uint32_t)nb);
+    if (nb) bulk_copy_g2s(slice + lo, p.x + ((int64_t)r * p.ld + cta_e0) * ES + lo, (uint32_t)nb, &sh.bar[warp]);
+  };
+  if (t == 0) { sh.acnt[0] = 0u; sh.acnt[1] = 0u; }
+  int uses = 0;          // completed phases of this warp's mbarrier
+  bool pending = false;  // a copy into this warp's region is in flight
+  if (p.tma) {
+    if (lane == 0) {
+      mbar_init(&sh.bar[warp], 1);
+      fence_mbar_init();
+    }
+    __syncthreads();
+    if (first < p.B) {
+      if (lane == 0) issue_warp(first);
+      pending = true;
+    }
+  }
+  bool dead = false;   // a load timed out: later rows are reported as timed out, not computed
+
+  for (int64_t k = 0;; ++k) {
+    const int64_t row = first + k * G;
+    if (row >= p.B) break;
+    E.set_slice(slice);
+    E.row = (int)row;
+    E.passes = 0;
+    E.rounds = 0;
+
+  // ---------------- row geometry ----------------
+  int64_t n = p.V;
+  if (p.lengths) n = p.lengths[row];
+  const bool bad_len = !(n > 0 && n <= p.V);
+  if (bad_len) n = 0;
+  E.n = n;
+  const int64_t cta_n = n - cta_e0 < 0 ? 0 : (n - cta_e0 > elems_cta ? elems_cta : n - cta_e0);
+  E.thr_e0 = cta_e0 + (int64_t)t * q * VE;
+  {
+    const int64_t r = n - E.thr_e0;
+    E.thr_n = r < 0 ? 0 : (r > (int64_t)q * VE ? q * VE : (int)r);
+  }
+  const unsigned char* grow = p.x + ((int64_t)row * p.ld + cta_e0) * ES;
+
+  // ---------------- wait for this row's slice ----------------
+    bool timeout = dead;
+    if (p.tma) {
+      if (pending) {
+        if (!mbar_wait_bounded(&sh.bar[warp], (uint32_t)(uses & 1), p.wait_cycles)) timeout = true;
+        ++uses;
+        pending = false;
+      }
+      // the (< 16 byte) tail of the slice, by its owner thread with plain loads
+      const int64_t b16 = (cta_n * ES) & ~(int64_t)15;
+      const int64_t tail_e0 = b16 / ES;
+      if (!timeout && tail_e0 < cta_n && t == (int)(tail_e0 / ((int64_t)q * VE))) {
+        for (int64_t e = tail_e0; e < cta_n; ++e) {
+          if (ES == 4) reinterpret_cast<uint32_t*>(slice)[e] = reinterpret_cast<const uint32_t*>(grow)[e];
+          else reinterpret_cast<uint16_t*>(slice)[e] = reinterpret_cast<const uint16_t*>(grow)[e];
+        }
+      }
+    } else {
+      for (int64_t e = 0; e < E.thr_n; ++e) {
+        const int64_t le = (int64_t)t * q * VE + e;
+        if (ES == 4) reinterpret_cast<uint32_t*>(slice)[le] = reinterpret_cast<const uint32_t*>(grow)[le];
+        else reinterpret_cast<uint16_t*>(slice)[le] = reinterpret_cast<const uint16_t*>(grow)[le];
+      }
+    }
+    __syncthreads();
+    // This warp is done reading its region of the slice for this row: copy the cluster's next row
+    // into it (first thing after the last pass over the row, so HBM streams while the row finishes).
+    bool refilled = false;
+    auto refill = [&]() {
+      if (refilled) return;
+      refilled = true;
+      const int64_t nr = row + G;
+      if (!p.tma || dead || nr >= p.B) return;
+      __syncwarp();
+      if (lane == 0) {
+        fence_proxy_async_shared();
+        issue_warp(nr);
+      }
+      pending = true;
+    };
+
+  // ---------------- P1: maximum (minimum for cut descriptors), non-finite check ----------------
+  float mx = -INFINITY, mn = INFINITY, nf = 0.f;
+  {
+    const int nfull = E.thr_n / VE;
+    if constexpr (VE == 8) {
+      // bf16: packed maximum / minimum; x * 0 (or x != x for the top-k select) flags non-finite values
+      const __nv_bfloat162 zero2 = __float2bfloat162_rn(0.f);
+      __nv_bfloat162 mx2 = __float2bfloat162_rn(-INFINITY), mn2 = __float2bfloat162_rn(INFINITY), nf2 = zero2;
+      for (int j = 0; j < nfull; ++j) {
+        const uint4 v = E.mine[j];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const __nv_bfloat162 a = Tr::pair(w[h]);
+          mx2 = __hmax2(mx2, a);
+          if (MODE & MODE_CUT) mn2 = __hmin2(mn2, a);
+          nf2 = kSel ? __hmax2(nf2, __hneu2(a, a)) : __hfma2(a, zero2, nf2);
+        }
+      }
+      mx = fmaxf(__low2float(mx2), __high2float(mx2));
+      mn = fminf(__low2float(mn2), __high2float(mn2));
+      const float n0 = __low2float(nf2), n1 = __high2float(nf2);
+      nf = (n0 != 0.f || n1 != 0.f) ? 1.f : 0.f;     // NaN compares unequal as well
+    } else {
+      for (int j = 0; j < nfull; ++j) {
+        float x[VE];
+        Tr::values(E.mine[j], x);
+#pragma unroll
+        for (int i = 0; i < VE; ++i) {
+          mx = fmaxf(mx, x[i]);
+          if (MODE & MODE_CUT) mn = fminf(mn, x[i]);
+          // x * 0 is NaN for +-inf and NaN; the top-k select only rejects NaN
+          nf = kSel ? (x[i] != x[i] ? 1.f : nf) : fmaf(x[i], 0.f, nf);
+        }
+      }
+    }
+    const int tail = E.thr_n - nfull * VE;
+    if (tail) {
+      float x[VE];
+      Tr::values(E.mine[nfull], x);
+#pragma unroll
+      for (int i = 0; i < VE; ++i) {
+        if (i < tail) {
+          mx = fmaxf(mx, x[i]);
+          if (MODE & MODE_CUT) mn = fminf(mn, x[i]);
+          nf = kSel ? (x[i] != x[i] ? 1.f : nf) : fmaf(x[i], 0.f, nf);
+        }
+      }
+    }
+  }
+  E.passes = 1;
+  {
+    const uint32_t bad = (nf != 0.f) ? 1u : 0u;    // NaN compares unequal as well
+    mx = warp_max_f(mx);
+    mn = -warp_max_f(-mn);
+    const uint32_t flags = __reduce_or_sync(kFullMask, bad | (timeout ? 2u : 0u));
+    if (lane == 0) { sh.wf[warp][0] = mx; sh.wf[warp][1] = mn; sh.wu[warp][3] = flags; }
+    __syncthreads();
+    if (t == 0) {
+      float m = -INFINITY, m2 = INFINITY;
+      uint32_t fl = 0;
+      for (int w = 0; w < Eng::NW; ++w) { m = fmaxf(m, sh.wf[w][0]); m2 = fminf(m2, sh.wf[w][1]); fl |= sh.wu[w][3]; }
+      Mail& ml = E.my_mail();
+      ml.f[0] = m;
+      ml.f[1] = m2;
+      ml.u[1] = fl;
+    }
+    E.exchange();
+    if (warp == 0) {
+      float m = -INFINITY, m2 = INFINITY;
+      uint32_t fl = 0;
+      if (lane < C) {
+        const Mail* pm = E.peer_mail(lane);
+        m = pm->f[0];
+        m2 = pm->f[1];
+        fl = pm->u[1];
+      }
+      m = warp_max_f(m);
+      m2 = -warp_max_f(-m2);
+      fl = __reduce_or_sync(kFullMask, fl);
+      if (lane == 0) { sh.bf[0] = m; sh.bf[3] = m2; sh.bu[5] = fl; }
+    }
+    E.exchange_done();
+    __syncthreads();
+  }
+  const float M = sh.bf[0];
+  const float Mmin = sh.bf[3];
+  const uint32_t gflags = sh.bu[5];
+  if (gflags & 2u) dead = true;
+
+  // ---------------- row status and parameters (uniform over the cluster) ----------------
+  float temp = 1.f, topp = 1.f, minp = 0.f;
+  int32_t topk = 0;
+  if (p.temperature) temp = p.temperature[row];
+  if (p.top_k) topk = p.top_k[row];
+  if (p.top_p) topp = p.top_p[row];
+  if (p.min_p) minp = p.min_p[row];
+  int32_t ksel = p.k_max;
+  if (kSel && p.k_sel) ksel = p.k_sel[row];
+  int status = VSAMP_OK;
+  if (bad_len) status = VSAMP_ERR_INVALID_ARG;
+  else if (gflags & 2u) status = VSAMP_ERR_TIMEOUT;
+  else if (gflags & 1u) status = VSAMP_ERR_NONFINITE;
+  else if (kSel && ksel > p.k_max) status = VSAMP_ERR_INVALID_ARG;
+  else if (kCutLike && (isnan(temp) || isinf(temp) || isnan(topp) || !(topp > 0.f) || isnan(minp) || minp > 1.f))
+    status = VSAMP_ERR_INVALID_ARG;
+  else if ((MODE & (MODE_LSE | MODE_LOGPROB)) && (isnan(temp) || isinf(temp)))
+    status = VSAMP_ERR_INVALID_ARG;
+  int32_t tok_in = 0;
+  if ((MODE & MODE_LOGPROB) && status == VSAMP_OK) {
+    tok_in = p.token_in[row];
+    if (tok_in < 0 || (int64_t)tok_in >= n) status = VSAMP_ERR_INVALID_ARG;
+  }
+  const bool greedy = !(temp > 0.f);
+  const float Teff = greedy ? 1.f : temp;
+  const float invT = 1.f / Teff;
+  const float c1 = kLog2e * invT;
+  const bool minp_on = kCutLike && !greedy && minp > 0.f;
+  const unsigned long long one = 1ull << kMassShift;     // fixed-point mass of a maximum token
+
+  // min-p keeps w >= minp  <=>  x >= x* = M + T ln(minp). x* is formed as an unevaluated sum hi + lo
+  // (exact product and sum corrections), and the threshold is the smallest fp32 value >= x*.
+  if (minp_on && status == VSAMP_OK) {
+    const float L = logf(minp);
+    const float ph = Teff * L, pl = fmaf(Teff, L, -ph);        // T*L = ph + pl exactly
+    const float sh_ = M + ph;                                   // M + ph = sh_ + sl exactly
+    const float bb = sh_ - M;
+    const float sl = (M - (sh_ - bb)) + (ph - bb);
+    const float lo = sl + pl;
+    const float xf = lo > 0.f ? nextafterf(sh_, INFINITY) : sh_;
+    plan.kmin32 = key_f32_bits(__float_as_uint(xf));
+  }
+
+  unsigned long long Sfx = 0, cM = 0;
+  uint32_t cpreM = 0;
+  float xP = -INFINITY;          // kept: x > xP, or x == xP and index <= It
+  int32_t It = kAllIndex;
+  int32_t boundary = kNoIndex;   // global index of the last kept token, if this thread holds it
+  bool fin_valid = false;
+  Cut fin{};
+
+  if (status == VSAMP_OK) {
+    if (!kSel) {
+      // ---------------- P2: fixed-point sum, maxima per thread, min-p statistics ----------------
+      unsigned long long s_loc = 0, mge = 0;
+      uint32_t cm_loc = 0, cge = 0, minkey = 0xFFFFFFFFu, cmin = 0;
+      const uint32_t kmin32 = minp_on ? plan.kmin32 : 0u;
+      const int nfull = E.thr_n / VE;
+      for (int j = 0; j <= nfull; ++j) {
+        const int cnt = j < nfull ? VE : (E.thr_n - nfull * VE);
+        if (cnt <= 0) break;
+        float x[VE], w[VE];
+        Tr::values(E.mine[j], x);
+#pragma unroll
+        for (int i = 0; i < VE; ++i) {
+          const bool ok = i < cnt;
+          const float d = x[i] - M;
+          w[i] = ok ? ex2_approx(d * c1) : 0.f;
+          cm_loc += (ok && d == 0.f) ? 1u : 0u;
+        }
+        if (minp_on) {
+#pragma unroll
+          for (int i = 0; i < VE; ++i) {
+            const uint32_t k32 = key_f32_bits(__float_as_uint(x[i]));
+            if (i < cnt && k32 >= kmin32) {
+              ++cge;
+              mge += mass_fx(w[i]);
+              if (k32 < minkey) { minkey = k32; cmin = 1; }
+              else if (k32 == minkey) ++cmin;
+            }
+          }
+        }
+        // pairwise sum of the vector, then one fixed-point conversion
+#pragma unroll
+        for (int h = VE / 2; h >= 1; h >>= 1)
+#pragma unroll
+          for (int i = 0; i < h; ++i) w[i] += w[i + h];
+        s_loc += mass_fx(w[0]);
+      }
+      E.passes += 1;
+      sh.tcount[t] = cm_loc;
+      s_loc = warp_sum_u64(s_loc);
+      cm_loc = warp_sum_u32(cm_loc);
+      if (minp_on) {
+        mge = warp_sum_u64(mge);
+        cge = warp_sum_u32(cge);
+        const uint32_t mk = warp_min_u32(minkey);
+        cmin = warp_sum_u32(minkey == mk ? cmin : 0u);
+        minkey = mk;
+      }
+      if (lane == 0) {
+        sh.wq[warp][0] = s_loc; sh.wq[warp][1] = mge;
+        sh.wu[warp][0] = cm_loc; sh.wu[warp][1] = cge; sh.wu[warp][2] = minkey; sh.wu[warp][3] = cmin;
+      }
+      __syncthreads();
+      if (t == 0) {
+        unsigned long long a = 0, b = 0;
+        uint32_t c = 0, d = 0, mk = 0xFFFFFFFFu, cc = 0;
+        for (int w = 0; w < Eng::NW; ++w) {
+          a += sh.wq[w][0]; b += sh.wq[w][1]; c += sh.wu[w][0]; d += sh.wu[w][1];
+          if (sh.wu[w][2] < mk) { mk = sh.wu[w][2]; cc = sh.wu[w][3]; }
+          else if (sh.wu[w][2] == mk) cc += sh.wu[w][3];
+        }
+        Mail& ml = E.my_mail();
+        ml.q[0] = a; ml.q[1] = b; ml.u[0] = c; ml.u[1] = d; ml.u[2] = mk; ml.u[3] = cc;
+      }
+      E.exchange();
+      if (warp == 0) {
+        unsigned long long a = 0, b = 0;
+        uint32_t c = 0, d = 0, mk = 0xFFFFFFFFu, cc = 0;
+        if (lane < C) {
+          const Mail* pm = E.peer_mail(lane);
+          a = pm->q[0]; b = pm->q[1]; c = pm->u[0]; d = pm->u[1]; mk = pm->u[2]; cc = pm->u[3];
+        }
+        uint32_t incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(kFullMask, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const uint32_t cpre = __shfl_sync(kFullMask, incl - c, crank);   // maxima in lower ranks
+        a = warp_sum_u64(a);
+        b = warp_sum_u64(b);
+        c = warp_sum_u32(c);
+        d = warp_sum_u32(d);
+        const uint32_t gmk = warp_min_u32(mk);
+        cc = warp_sum_u32(mk == gmk ? cc : 0u);
+        if (lane == 0) {
+          sh.bq[0] = a; sh.bq[1] = b; sh.bu[0] = c; sh.bu[1] = d; sh.bu[2] = gmk; sh.bu[3] = cc; sh.bu[6] = cpre;
+        }
+      }
+      E.exchange_done();
+      __syncthreads();
+      Sfx = sh.bq[0];
+      cM = sh.bu[0];
+      cpreM = sh.bu[6];
+      // ---------------- per-row plan ----------------
+      {
+        plan.status = VSAMP_OK;
+        plan.path = p.tma ? 0 : PATH_NOTMA;
+        plan.logS = logf(u64_to_float(Sfx) * 9.094947017729282379e-13f);   // 2^-40
+        plan.ck_mode = 0;
+        plan.cp_mode = 0;
+        plan.goal_p = -1.f;
+        plan.cp_goal = 0;
+        const unsigned long long mass_ge = sh.bq[1];
+        const uint32_t cnt_ge = sh.bu[1], minkey_ge = sh.bu[2], cnt_minkey = sh.bu[3];
+        if (kCutLike) {
+          const uint32_t rkM = Tr::rkey_of_value(M);
+          if (greedy) {
+            plan.fin = Cut{rkM, 0, 1, cM, one, 0};
+            plan.path |= PATH_MAXGROUP;
+          } else {
+            const bool topk_on = topk > 0 && (int64_t)topk < n;
+            const bool topp_on = topp < 1.f;
+            const unsigned long long keff = topk_on ? (unsigned long long)topk : (unsigned long long)n;
+            if (topk_on) {
+              if (keff <= cM) {
+                plan.ck = Cut{rkM, 0, keff, cM, keff * one, 0};
+                plan.ck_mode = 1;
+              } else {
+                plan.ck = Cut{0, 0, keff, 0, 0, 0};
+                plan.ck_mode = 2;
+              }
+            }
+            if (topp_on) {
+              if (plan.ck_mode != 2) {
+                const unsigned long long Sk = topk_on ? plan.ck.mass : Sfx;
+                const unsigned long long target = ceil_mul_frac(topp, Sk);
+                if (target <= cM * one) {
+                  unsigned long long need = (target + one - 1) >> kMassShift;
+                  need = need < 1 ? 1 : need;
+                  plan.cp = Cut{rkM, 0, need, cM, need * one, 0};
+                  plan.cp_mode = 1;
+                } else {
+                  plan.cp_mode = 2;
+                  if (topk_on) plan.cp_goal = target;
+                  else plan.goal_p = topp;
+                }
+              } else if (ceil_mul_frac(topp, Sfx) <= one) {
+                // target <= p * S <= one maximum's mass: the first maximum alone reaches it
+                plan.cp = Cut{rkM, 0, 1, cM, one, 0};
+                plan.cp_mode = 1;
+              } else {
+                plan.cp_mode = 2;   // goal from the top-k mass, after the top-k rounds
+              }
+            }
+            if (plan.ck_mode == 1 || plan.cp_mode == 1) plan.path |= PATH_MAXGROUP;
+            if (minp_on) {
+              // min-p keeps the whole group of the smallest key at or above its threshold
+              const uint32_t rkm = (Tr::KB == 32) ? minkey_ge : (minkey_ge >> 16);
+              plan.fin = Cut{rkm, (unsigned long long)(cnt_ge - cnt_minkey), cnt_minkey, cnt_minkey, mass_ge, 1};
+            } else {
+              // no filter binds: every token. The prefix ends with the row minimum's group; only the cut
+              // descriptor needs that group (a one-token row's minimum is its maximum).
+              const uint32_t rk_last = (MODE & MODE_CUT) ? Tr::rkey_of_value(Mmin) : rkM;
+              plan.fin = Cut{rk_last, 0, (unsigned long long)n, 0, Sfx, 1};
+            }
+          }
+        }
+      }
+      if (kCutLike && !greedy) {
+        // ---------------- radix rounds where the cut leaves the maximum's group ----------------
+        if (plan.ck_mode == 2) {
+          const RadixOut r = E.radix_search(false, plan.ck.need, -1.f, plan.cp_mode == 2, M, c1);
+          {
+            if (!r.ok) plan.status = VSAMP_ERR_INVALID_ARG;
+            const unsigned long long need = plan.ck.need - r.cnt_above;
+            const unsigned long long wP = mass_fx(ex2_approx((Tr::value_of_rkey(r.rk) - M) * c1));
+            plan.ck = Cut{r.rk, r.cnt_above, need, r.cnt_eq, r.mass_above + need * wP, 0};
+            plan.path |= PATH_RADIX_K;
+            if (plan.cp_mode == 2) plan.cp_goal = ceil_mul_frac(topp, plan.ck.mass);
+          }
+        }
+        if (plan.cp_mode == 2 && plan.status == VSAMP_OK) {
+          const RadixOut r = E.radix_search(true, plan.cp_goal, plan.goal_p, true, M, c1);
+          {
+            if (!r.ok) plan.status = VSAMP_ERR_INVALID_ARG;
+            const unsigned long long wP = mass_fx(ex2_approx((Tr::value_of_rkey(r.rk) - M) * c1));
+            // a group element is kept while the mass before it is below the target
+            unsigned long long need = wP ? (r.goal + wP - 1) / wP : 1;
+            need = need < 1 ? 1 : (need > r.cnt_eq ? r.cnt_eq : need);
+            plan.cp = Cut{r.rk, r.cnt_above, need, r.cnt_eq, r.mass_above + need * wP, 0};
+            plan.path |= PATH_RADIX_P;
+          }
+        }
+        // ---------------- the shortest prefix wins ----------------
+        {
+          Cut best = plan.fin;   // the min-p cut, or every token
+          if (plan.ck_mode && plan.ck.kept() < best.kept()) best = plan.ck;
+          if (plan.cp_mode && plan.cp.kept() < best.kept()) best = plan.cp;
+          if (minp_on && best.whole) plan.path |= PATH_MINP;
+          plan.fin = best;
+        }
+      }
+      status = plan.status;
+      fin = plan.fin;
+      fin_valid = kCutLike && status == VSAMP_OK;
+    } else {
+      // ---------------- stand-alone top-k select ----------------
+      if (ksel <= 0) {
+        fin = Cut{0u, 0, 0, 0, 0, 0};
+      } else if (ksel >= n) {
+        fin = Cut{0u, 0, (unsigned long long)n, 0, 0, 1};
+      } else {
+        const RadixOut r = E.radix_search(false, (unsigned long long)ksel, -1.f, false, M, c1);
+        if (!r.ok) status = VSAMP_ERR_INVALID_ARG;
+        fin = Cut{r.rk, r.cnt_above, (unsigned long long)ksel - r.cnt_above, r.cnt_eq, 0, 0};
+      }
+      fin_valid = status == VSAMP_OK;
+    }
+  }
+
+  // ---------------- the cut's last kept index, per thread ----------------
+  bool select_none = false;
+  if (fin_valid) {
+    const bool need_boundary = !fin.whole || (MODE & MODE_CUT) || ((MODE & MODE_SAMPLE) && fin.kept() == 1);
+    if (kSel && fin.need == 0 && fin.above == 0) {
+      select_none = true;
+      xP = INFINITY;
+      It = kNoIndex;
+    } else if (!need_boundary) {
+      // every element of the group is kept and no output needs the boundary index
+      const bool every_token = fin.above == 0 && fin.cnt_eq == 0;
+      xP = every_token ? -INFINITY : Tr::value_of_rkey(fin.rk);
+      It = kAllIndex;
+    } else {
+      xP = Tr::value_of_rkey(fin.rk);
+      uint32_t cpre;
+      unsigned long long need = fin.need;
+      if (!kSel && fin.rk == Tr::rkey_of_value(M)) {
+        // tcount[] still holds the P2 counts of maxima; cpreM is the count over lower ranks
+        E.block_scan_tcount();
+        cpre = cpreM;
+        if (fin.whole) need = cM;
+      } else {
+        E.count_equal_pass(xP);
+        const uint32_t ctot = E.block_scan_tcount();
+        uint32_t total;
+        E.cluster_prefix_u32(ctot, 0, cpre, total);
+        if (fin.whole) need = total;     // the last element of the group
+      }
+      It = E.local_cut_index(xP, need, cpre, boundary);
+    }
+  }
+
+  // ---------------- P4: Gumbel-max draw over the kept prefix ----------------
+  int32_t out_token = -1;
+  bool last_cta = false;     // this CTA reduced the row's arg-max and writes the draw's outputs
+  if ((MODE & MODE_SAMPLE) && fin_valid) {
+    const unsigned long long kept = fin.kept();
+    if (greedy || kept == 1) {
+      // the first maximum: written by the thread that holds it
+      if (boundary >= 0) {
+        const float xt = Tr::load_global(p.x, (int64_t)row * p.ld + boundary);
+        p.token[row] = boundary;
+        if (p.logprob) p.logprob[row] = fminf((xt - M) * invT - plan.logS, 0.f);
+      }
+    } else {
+      {
+        // prune bound: a token can beat B0 = ln(S_kept) - 3 only if u < w * kappa, kappa = e^3 / S_kept
+        const float skept = fmaxf(u64_to_float(fin.mass) * 9.094947017729282379e-13f, 1.f);   // 2^-40
+        const float kappa = 20.085536923187668f / skept;
+        plan.kappa = kappa;
+        plan.all_cand = kappa >= 0.99f;
+        plan.bk = plan.all_cand ? 0xFFFFFFFFu : __float2uint_ru(kappa * 1.00001f * 4294967296.0f);
+        plan.b0 = -logf(kappa);
+      }
+      const uint64_t sd = p.seed ? p.seed[row] : 0ull;
+      const uint64_t st = p.step ? p.step[row] : 0ull;
+      const uint32_t rid = p.row_id ? p.row_id[row] : (uint32_t)row;
+      const PhiloxKey key{(uint32_t)sd, (uint32_t)(sd >> 32)};
+      const uint32_t st_lo = (uint32_t)st, st_hi = (uint32_t)(st >> 32);
+      const float kappa = plan.kappa;
+      const uint32_t bk = plan.bk;
+      const float B0 = plan.b0;
+      {
+        const bool all_cand = plan.all_cand;
+        float bscore = -INFINITY, bs = 0.f;
+        int32_t bidx = 0x7FFFFFFF;
+        const int nfull = E.thr_n / VE;
+        for (int j = 0; j <= nfull; ++j) {
+          const int cnt = j < nfull ? VE : (E.thr_n - nfull * VE);
+          if (cnt <= 0) break;
+          const int64_t e0 = E.thr_e0 + (int64_t)j * VE;
+          const uint4 v = E.mine[j];
+          // evaluates the kept candidates (mask c) of this vector exactly
+          auto candidates = [&](const bool (&c)[VE], const uint32_t (&b)[VE]) {
+            float x[VE];
+            Tr::values(v, x);
+#pragma unroll
+            for (int i = 0; i < VE; ++i) {
+              if (!c[i]) continue;
+              const float d = x[i] - M;
+              const float s = d * invT;
+              if (!all_cand) {
+                const float w = ex2_approx(d * c1);
+                const float u = fmaf((float)b[i], kTwoM32, kTwoM33);
+                if (!(u < w * kappa * 1.00001f)) continue;
+              }
+              const float score = gumbel_score(s, b[i]);
+              const int32_t idx = (int32_t)(e0 + i);
+              if (argmax_better(score, idx, bscore, bidx)) { bscore = score; bidx = idx; bs = s; }
+            }
+          };
+          uint32_t b[VE];
+          if (cnt == VE && e0 + VE - 1 <= (int64_t)It && Tr::all_ge(v, xP)) {
+            // every token of the vector is kept
+#pragma unroll
+            for (int g = 0; g < VE / 4; ++g) {
+              const uint4 w4 = philox4x32_10(make_uint4((uint32_t)((e0 >> 2) + g), rid, st_lo, st_hi), key);
+              b[4 * g + 0] = w4.x; b[4 * g + 1] = w4.y; b[4 * g + 2] = w4.z; b[4 * g + 3] = w4.w;
+            }
+            bool c[VE];
+            bool anyc = false;
+#pragma unroll
+            for (int i = 0; i < VE; ++i) {
+              c[i] = all_cand || b[i] < bk;
+              anyc |= c[i];
+            }
+            if (__builtin_expect(anyc, 0)) candidates(c, b);
+            continue;
+          }
+          float x[VE];
+          Tr::values(v, x);
+          bool k[VE];
+          bool any = false;
+#pragma unroll
+          for (int i = 0; i < VE; ++i) {
+            k[i] = i < cnt && (x[i] > xP || (x[i] == xP && e0 + i <= (int64_t)It));
+            any |= k[i];
+          }
+          if (!any) continue;
+#pragma unroll
+          for (int g = 0; g < VE / 4; ++g) {
+            const uint4 w4 = philox4x32_10(make_uint4((uint32_t)((e0 >> 2) + g), rid, st_lo, st_hi), key);
+            b[4 * g + 0] = w4.x; b[4 * g + 1] = w4.y; b[4 * g + 2] = w4.z; b[4 * g + 3] = w4.w;
+          }
+          bool c[VE];
+          bool anyc = false;
+#pragma unroll
+          for (int i = 0; i < VE; ++i) {
+            c[i] = k[i] && (all_cand || b[i] < bk);
+            anyc |= c[i];
+          }
+          if (__builtin_expect(anyc, 0)) candidates(c, b);
+        }
+        E.passes += 1;
+        refill();    // this warp has finished reading its region of the slice
+        // ---------------- lock-free cluster arg-max ----------------
+        // Each CTA publishes its partial into CTA 0's slot for this row and counts itself in with an
+        // acquire-release atomic; the last CTA to arrive reduces the slots and writes the row's outputs,
+        // the others go straight on to their next row.
+        const ArgMax best = warp_argmax(ArgMax{bscore, bidx, bs});
+        int32_t wcut = boundary;  // the cut's boundary index, if this warp holds it (else -1)
+#pragma unroll
+        for (int o = 16; o; o >>= 1) wcut = max(wcut, __shfl_xor_sync(kFullMask, wcut, o));
+        if (lane == 0) { sh.wf[warp][1] = best.score; sh.wf[warp][2] = best.s; sh.wi[warp][0] = best.idx; sh.wi[warp][1] = wcut; }
+        __syncthreads();
+        const int par = (int)(k & 1);
+        if (t == 0) {
+          ArgMax b2{-INFINITY, 0x7FFFFFFF, 0.f};
+          for (int w = 0; w < Eng::NW; ++w)
+            if (argmax_better(sh.wf[w][1], sh.wi[w][0], b2.score, b2.idx)) b2 = ArgMax{sh.wf[w][1], sh.wi[w][0], sh.wf[w][2]};
+          int32_t my_cut = -1;
+          for (int w = 0; w < Eng::NW; ++w) my_cut = max(my_cut, sh.wi[w][1]);
+          dsmem_store_v4(dsmem_map(&sh.aslot[par][crank], 0), __float_as_uint(b2.score), (uint32_t)b2.idx,
+                         __float_as_uint(b2.s), (uint32_t)my_cut);
+          const uint32_t old = dsmem_atomic_add_acq_rel(dsmem_map(&sh.acnt[par], 0), 1u);
+          sh.bu[7] = (old == (uint32_t)(C - 1)) ? 1u : 0u;
+        }
+        __syncthreads();
+        last_cta = sh.bu[7] != 0;
+        if (last_cta) {
+          if (t == 0) {
+            ArgMax g{-INFINITY, 0x7FFFFFFF, 0.f};
+            int32_t cut = -1;
+            for (int r = 0; r < C; ++r) {
+              const uint4 v = dsmem_load_v4(dsmem_map(&sh.aslot[par][r], 0));
+              const ArgMax a2{__uint_as_float(v.x), (int32_t)v.y, __uint_as_float(v.z)};
+              if (argmax_better(a2.score, a2.idx, g.score, g.idx)) g = a2;
+              cut = max(cut, (int32_t)v.w);
+            }
+            dsmem_store_u32(dsmem_map(&sh.acnt[par], 0), 0u);
+            sh.bf[1] = g.score;
+            sh.bi[2] = g.idx;
+            sh.bi[1] = cut < 0 ? kAllIndex : cut;
+          }
+          __syncthreads();
+          const float gscore = sh.bf[1];
+          const int32_t gidx = sh.bi[2];
+          const bool certified = all_cand || (gscore > B0 + 1e-4f * fmaxf(1.f, fabsf(B0)));
+          if (certified) {
+            out_token = gidx;
+          } else {
+            // the prune bound did not certify the draw (probability ~1e-9): this CTA evaluates every kept
+            // token of the row from global memory
+            plan.path |= PATH_FALLBACK;
+            const int32_t Ig = sh.bi[1];
+            float fs = -INFINITY, fsv = 0.f;
+            int32_t fi = 0x7FFFFFFF;
+            for (int64_t e = t; e < n; e += NT) {
+              const float xv = Tr::load_global(p.x, (int64_t)row * p.ld + e);
+              if (!(xv > xP || (xv == xP && e <= (int64_t)Ig))) continue;
+              const uint4 w4 = philox4x32_10(make_uint4((uint32_t)(e >> 2), rid, st_lo, st_hi), key);
+              const uint32_t bw = philox_word(w4, (int)(e & 3));
+              const float sv = (xv - M) * invT;
+              const float score = gumbel_score(sv, bw);
+              if (argmax_better(score, (int32_t)e, fs, fi)) { fs = score; fi = (int32_t)e; fsv = sv; }
+            }
+            const ArgMax fb = warp_argmax(ArgMax{fs, fi, fsv});
+            __syncthreads();
+            if (lane == 0) { sh.wf[warp][1] = fb.score; sh.wi[warp][0] = fb.idx; }
+            __syncthreads();
+            if (t == 0) {
+              ArgMax b4{-INFINITY, 0x7FFFFFFF, 0.f};
+              for (int w = 0; w < Eng::NW; ++w)
+                if (argmax_better(sh.wf[w][1], sh.wi[w][0], b4.score, b4.idx)) b4 = ArgMax{sh.wf[w][1], sh.wi[w][0], 0.f};
+              sh.bi[2] = b4.idx;
+            }
+            __syncthreads();
+            out_token = sh.bi[2];
+          }
+        }
+      }
+    }
+  }
+
+  // ---------------- top-k select emission (ascending index order) ----------------
+  if (kSel) {
+    int32_t* orow = p.out_idx + (int64_t)row * p.k_max;
+    uint32_t total = 0;
+    if (fin_valid && !select_none) {
+      uint32_t c = 0;
+      E.for_each([&](int64_t e, float x) { c += (x > xP || (x == xP && e <= (int64_t)It)) ? 1u : 0u; });
+      sh.tcount[t] = c;
+      const uint32_t ctot = E.block_scan_tcount();
+      uint32_t cpre;
+      E.cluster_prefix_u32(ctot, 1, cpre, total);
+      uint32_t pos = cpre + sh.tpre[t];
+      E.for_each([&](int64_t e, float x) {
+        if (x > xP || (x == xP && e <= (int64_t)It)) {
+          if (pos < (uint32_t)p.k_max) orow[pos] = (int32_t)e;
+          ++pos;
+        }
+      });
+      E.passes += 2;
+    }
+    if (crank == 0)
+      for (int64_t j = (int64_t)total + t; j < p.k_max; j += NT) orow[j] = -1;
+  }
+
+  // ---------------- mask ----------------
+  if (MODE & MODE_MASK) {
+    uint8_t* mrow = p.mask + (int64_t)row * p.V;
+    E.for_each([&](int64_t e, float x) {
+      const bool k = fin_valid && (x > xP || (x == xP && e <= (int64_t)It));
+      mrow[e] = k ? 1 : 0;
+    });
+  }
+
+  // ---------------- finalisation ----------------
+  if ((MODE & MODE_CUT) && fin_valid && boundary >= 0) p.cut[row].idx_cut = boundary;
+  // the row's outputs come from CTA 0, except a Gumbel draw's, which come from the CTA that reduced it
+  const bool p4_path = (MODE & MODE_SAMPLE) && fin_valid && !(greedy || fin.kept() == 1);
+  const bool writer = p4_path ? last_cta : (crank == 0);
+  if (writer && t == 0) {
+    if (MODE & MODE_LSE) {
+      if (p.row_max) p.row_max[row] = status == VSAMP_OK ? M : __int_as_float(0x7FC00000);
+      if (p.row_logsum) p.row_logsum[row] = status == VSAMP_OK ? (float)plan.logS : __int_as_float(0x7FC00000);
+    }
+    if (MODE & MODE_LOGPROB) {
+      float lp = __int_as_float(0x7FC00000);
+      if (status == VSAMP_OK) {
+        const float xt = Tr::load_global(p.x, (int64_t)row * p.ld + tok_in);
+        lp = fminf((xt - M) * invT - plan.logS, 0.f);
+      }
+      if (p.logprob) p.logprob[row] = lp;
+    }
+    if (MODE & MODE_SAMPLE) {
+      const bool one_token = fin_valid && (greedy || fin.kept() == 1);
+      if (!fin_valid) {
+        p.token[row] = -1;
+        if (p.logprob) p.logprob[row] = __int_as_float(0x7FC00000);
+      } else if (!one_token) {
+        if (out_token >= 0) {
+          const float xt = Tr::load_global(p.x, (int64_t)row * p.ld + out_token);
+          p.token[row] = out_token;
+          if (p.logprob) p.logprob[row] = fminf((xt - M) * invT - plan.logS, 0.f);
+        } else {
+          status = VSAMP_ERR_INVALID_ARG;
+          p.token[row] = -1;
+          if (p.logprob) p.logprob[row] = __int_as_float(0x7FC00000);
+        }
+      }
+    }
+    if (MODE & MODE_CUT) {
+      vsamp_cut& c = p.cut[row];
+      c.status = status;
+      if (fin_valid) {
+        c.pivot_key = Tr::key32(fin.rk);
+        c.kept = (int32_t)fin.kept();
+      } else {
+        c.pivot_key = 0;
+        c.idx_cut = -1;
+        c.kept = 0;
+      }
+    }
+    if (p.row_status) p.row_status[row] = status;
+    if (p.stats) {
+      p.stats[row * 4 + 0] = E.passes;
+      p.stats[row * 4 + 1] = E.rounds;
+      p.stats[row * 4 + 2] = fin_valid ? (int32_t)fin.kept() : 0;
+      p.stats[row * 4 + 3] = (kSel || !fin_valid) ? (p.tma ? 0 : PATH_NOTMA) : plan.path;
+    }
+  }
+    refill();
+    __syncthreads();
+  }
+  // after a timed-out load, wait (again bounded) for this CTA's outstanding bulk copies before leaving
+  if (p.tma && pending && lane == 0) (void)mbar_wait_bounded(&sh.bar[warp], (uint32_t)(uses & 1), p.wait_cycles);
+  // no CTA may leave while a peer can still read its shared memory
+  E.cluster.sync();
+  (void)q;
+}
+
+}  // namespace vsamp

@@ -18,6 +18,8 @@ from __future__ import annotations
 
 import argparse
 import ctypes
+import glob
+import hashlib
 import json
 import math
 import multiprocessing as mp
@@ -37,7 +39,7 @@ B_ROWS, V_COLS, SEED = 256, 151936, 3
 TOP_P = 0.95
 N_COPIES = 4
 WORKLOAD = ("c4: B=256 x V=151936 bf16 logits N(0,2.5^2)+1e4 (seed 3), top_p=0.95, top_k off, "
-            "min_p off, T=1, Philox key 3, step = iteration")
+            "min_p off, T=1, Philox key 3, step = iteration mod 4")
 # algorithmic work per step
 BYTES_PER_STEP = B_ROWS * V_COLS * 2                      # one read of every logit
 KEPT_PER_ROW = 144340                                      # ceil(0.95f * 151936): every token ties
@@ -51,6 +53,59 @@ def _peaks():
         return float(d["hbm_gbs"]), "measured", float(d.get("sm_max_mhz", 2070.0))
     except Exception:
         return 6800.0, "fallback", 2070.0
+
+
+PROFILE = os.path.join(ROOT, "profiles", "row_kernel_c4_sample.md")
+
+
+def _csrc_digest() -> str:
+    """SHA-256 (first 16 hex digits) over the kernel sources, file names and contents in name order."""
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "top_sampling_gb300", "csrc", "*"))):
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic():
+    """DRAM bytes per launch from the committed ncu summary, or None once the kernel sources changed."""
+    try:
+        fields = {}
+        with open(PROFILE) as f:
+            for line in f:
+                k, _, v = line.partition(":")
+                if k in ("source_digest", "dram_bytes_per_launch"):
+                    fields[k] = v.strip()
+        if fields.get("source_digest") != _csrc_digest():
+            return None
+        return int(fields["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------------------------------------
+# multi-rank helpers (rows are independent: each rank samples its own rows, no data-path collective)
+# ------------------------------------------------------------------------------------------------
+def shard_row_ids(rank: int, rows_per_rank: int) -> np.ndarray:
+    """Global row indices of a rank's rows: the Philox row word, so draws do not depend on the sharding."""
+    return np.arange(rows_per_rank, dtype=np.int64) + int(rank) * int(rows_per_rank)
+
+
+def max_over_ranks(value: float, dist=None, device=None) -> float:
+    """The slowest rank's time (a MAX all-reduce of one scalar; the identity on one rank)."""
+    if dist is None:
+        return float(value)
+    import torch
+
+    tt = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_rows_per_s(world: int, rows_per_rank: int, steps: int, ms: float) -> float:
+    """Whole-job throughput: the rows every rank processed over the slowest rank's time."""
+    return world * rows_per_rank * steps / (ms / 1e3)
 
 
 # ------------------------------------------------------------------------------------------------
@@ -111,17 +166,20 @@ class ClockSampler:
 _CACHE = {}
 
 
+def _batch():
+    import workloads
+
+    if "b" not in _CACHE:
+        _CACHE["b"] = workloads.c4(B=B_ROWS, V=V_COLS, seed=SEED)
+    return _CACHE["b"]
+
+
 def _oracle_rows(args):
     """Worker: draw `rows` of the batch with the oracle (the batch itself is generated once, untimed)."""
     rows, step = args
-    import workloads
     from oracle import sampler as osm
 
-    need = max(rows) + 1
-    if _CACHE.get("B", 0) < need:
-        _CACHE["b"] = workloads.c4(B=max(need, 32))
-        _CACHE["B"] = max(need, 32)
-    b = _CACHE["b"]
+    b = _batch()
     out = []
     for r in rows:
         res = osm.sample_row(b.logits[r], b.dtype, b.temperature[r], b.top_k[r], b.top_p[r], b.min_p[r],
@@ -130,7 +188,15 @@ def _oracle_rows(args):
     return out
 
 
-def cpu_baseline(n_rows: int = 32, step: int = 0):
+def _oracle_row_seconds(_):
+    """Worker: seconds the oracle takes for one row (after a warm-up row)."""
+    _oracle_rows(([0], 0))
+    t0 = time.perf_counter()
+    _oracle_rows(([1], 0))
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(n_rows: int = B_ROWS, step: int = 0):
     """Oracle rows/s on all host cores (spawned workers; no CUDA in them)."""
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     workers = max(1, min(cores, n_rows))
@@ -172,7 +238,7 @@ def run_gpu(args):
     lib = ts.load()
 
     # cpu baseline first (spawned workers, before heavy GPU work)
-    cpu = cpu_baseline() if (rank == 0 and not args.no_cpu) else None
+    cpu = cpu_baseline() if (world == 1 and not args.no_cpu) else None
 
     batch = workloads.c4(B=B_ROWS, V=V_COLS, seed=SEED)
     host = np.ascontiguousarray(batch.logits).view(np.int16)
@@ -182,7 +248,7 @@ def run_gpu(args):
     temp, topp, minp = f32(1.0), f32(TOP_P), f32(0.0)
     topk = torch.zeros(B_ROWS, dtype=torch.int32, device=dev)
     seed = torch.full((B_ROWS,), SEED, dtype=torch.int64, device=dev)
-    row_id = (torch.arange(B_ROWS, dtype=torch.int32, device=dev) + rank * B_ROWS)
+    row_id = torch.from_numpy(shard_row_ids(rank, B_ROWS).astype(np.int32)).to(dev)
     steps_dev = [torch.full((B_ROWS,), s, dtype=torch.int64, device=dev) for s in range(N_COPIES)]
     token = torch.empty(B_ROWS, dtype=torch.int32, device=dev)
     logprob = torch.empty(B_ROWS, dtype=torch.float32, device=dev)
@@ -220,14 +286,10 @@ def run_gpu(args):
     if dist:
         dist.barrier()
     clk = clocks.stop()
-    dev_ms = ev0.elapsed_time(ev1)
-    if dist:
-        tt = torch.tensor([dev_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        dev_ms = float(tt.item())
+    dev_ms = max_over_ranks(ev0.elapsed_time(ev1), dist, dev)
     ms_step = dev_ms / args.steps
     launch_us = ms_step * 1e3                     # one kernel launch per step
-    rows_s = world * B_ROWS * args.steps / (dev_ms / 1e3)
+    rows_s = job_rows_per_s(world, B_ROWS, args.steps, dev_ms)
 
     # end to end through the same C-ABI call: pinned host logits in, token + logprob out, every step
     hx = torch.from_numpy(host).view(torch.bfloat16).pin_memory()
@@ -252,22 +314,12 @@ def run_gpu(args):
         hlp.copy_(logprob, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if dist:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    e2e_rows_s = world * B_ROWS * e2e_steps / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
+    e2e_rows_s = job_rows_per_s(world, B_ROWS, e2e_steps, e2e_ms)
 
     hbm_peak, peak_kind, sm_max_mhz = _peaks()
     gbs = BYTES_PER_STEP / (launch_us * 1e-6) / 1e9
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", "traffic_c4.json")
-    if os.path.exists(prof):
-        try:
-            traffic = json.load(open(prof)).get("dram_bytes_per_launch")
-        except Exception:
-            traffic = None
+    traffic = _traffic()
     # integer-multiply roofline of the Philox draws: 64 lanes/clk/SM of 32-bit multiplies at the max clock
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     imul_peak = sms * 64 * sm_max_mhz * 1e6 / 1e12                     # T ops/s
@@ -313,30 +365,37 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    rows_per_step = 16
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    workers = max(1, min(cores, rows_per_step))
+    workers = max(1, cores)
+    steps = max(1, args.steps)
+    budget_s = 60.0                      # wall-clock target of the timed steps
     ctx = mp.get_context("spawn")
     with ctx.Pool(workers) as pool:
-        pool.map(_oracle_rows, [([rows_per_step - 1], 0)] * workers)
-        for s in range(args.warmup):
-            pool.map(_oracle_rows, [([r], s) for r in range(min(workers, rows_per_step))])
+        t_row = max(pool.map(_oracle_row_seconds, range(workers)))
+        # each step is a bounded sample of the batch: as many rows as fit the budget, 1..B
+        rows_per_step = int(max(1, min(B_ROWS, budget_s * workers / (steps * t_row))))
+
+        def items(s):
+            rows = [(s * rows_per_step + j) % B_ROWS for j in range(rows_per_step)]
+            per = max(1, -(-rows_per_step // workers))
+            return [(rows[i:i + per], s) for i in range(0, rows_per_step, per)]
+
+        pool.map(_oracle_rows, [it for s in range(args.warmup) for it in items(s)])
         t0 = time.perf_counter()
-        for s in range(args.steps):
-            chunks = [list(range(i, rows_per_step, workers)) for i in range(workers)]
-            pool.map(_oracle_rows, [(c, s) for c in chunks])
+        pool.map(_oracle_rows, [it for s in range(steps) for it in items(s)])
         dt = time.perf_counter() - t0
-    rows_s = rows_per_step * args.steps / dt
-    sample = f"{rows_per_step} rows of the B=256 x V=151936 bf16 batch per step, {workers} worker processes"
+    rows_s = rows_per_step * steps / dt
+    sample = (f"{rows_per_step} of the 256 rows of the B=256 x V=151936 bf16 batch per step "
+              f"(steps run concurrently), {workers} worker processes")
     out = {
         "impl": "reference",
         "metric": METRIC,
         "value": rows_s,
         "unit": "rows/s",
         "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
-        "steps": args.steps,
+        "steps": steps,
         "warmup": args.warmup,
-        "ms_per_step": dt / args.steps * 1e3,
+        "ms_per_step": dt / steps * 1e3,
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -360,9 +419,6 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
-        if args.steps > 20:          # each step is a bounded sample; report the steps actually run
-            args.steps = 20
-        args.warmup = min(args.warmup, 3)
         run_reference(args)
     else:
         run_gpu(args)

@@ -20,6 +20,12 @@ int env_int(const char* name, int dflt) {
   return std::atoi(v);
 }
 
+long long env_ll(const char* name, long long dflt) {
+  const char* v = std::getenv(name);
+  if (!v || !*v) return dflt;
+  return std::strtoll(v, nullptr, 10);
+}
+
 vsamp_status device_info(int dev, DeviceInfo& out) {
   if (dev < 0 || dev >= kMaxDevices) return VSAMP_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lk(g_mu);

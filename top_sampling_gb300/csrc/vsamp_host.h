@@ -30,6 +30,7 @@ struct Geometry {
 };
 
 int env_int(const char* name, int dflt);
+long long env_ll(const char* name, long long dflt);
 vsamp_status device_info(int dev, DeviceInfo& out);
 vsamp_status choose_geometry(int64_t V, int esize, int64_t B, const DeviceInfo& d, Geometry& g);
 

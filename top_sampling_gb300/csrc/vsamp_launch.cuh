@@ -60,7 +60,10 @@ vsamp_status launch(Params p, int64_t B, int esize, cudaStream_t stream) {
   st = choose_geometry(p.V, esize, B, d, g);
   if (st != VSAMP_OK) return st;
   p.q = g.q;
-  p.wait_cycles = 4000000000LL;   // ~2 s at the maximum SM clock
+  // bound of a load wait: ~2 s at the maximum SM clock unless VSAMP_WAIT_CYCLES sets another
+  const long long wc = env_ll("VSAMP_WAIT_CYCLES", 0);
+  p.wait_cycles = wc > 0 ? wc : 4000000000LL;
+  p.drop_loads = env_int("VSAMP_TEST_DROP_LOADS", 0) != 0 ? 1 : 0;
   if (g.NT == kThreadsSmall) return launch_nt<T, kThreadsSmall, MODE>(p, B, g, stream);
   return launch_nt<T, kThreadsLarge, MODE>(p, B, g, stream);
 }

@@ -2,7 +2,8 @@
 // of the row in shared memory (bulk-copied from HBM once) and every later pass reads shared memory.
 //
 // Passes (each thread owns q consecutive 16-byte vectors of its CTA's slice, in index order):
-//   load   -- cp.async.bulk of the slice in four chunks, each on its own mbarrier;
+//   load   -- cp.async.bulk of each warp's region of the slice on the warp's own mbarrier; a warp
+//             re-arms its region with the cluster's next row as soon as its last pass is done;
 //   P1     -- row maximum M and a non-finite check;
 //   P2     -- S = sum exp((x - M)/T) in 64-bit fixed point, each thread's count of maxima and, when
 //             min-p is on, the min-p statistics;
@@ -13,10 +14,12 @@
 //             index-ordered prefix over threads and CTAs, every thread derives its own last kept index
 //             (only the thread holding the boundary rescans its chunk);
 //   P4     -- Philox4x32-10 per group of four tokens, Gumbel-max over the kept prefix with a prune
-//             bound from the kept mass, cluster arg-max, log-probability.
-// Per-row scalar decisions (in binary64 where needed) are taken by thread 0 and broadcast through
-// shared memory. Every branch that decides which cluster barriers run depends only on cluster-reduced
-// values, so all CTAs of a cluster execute the same barrier sequence.
+//             bound from the kept mass; the CTAs' partial arg-maxes meet in CTA 0's shared memory and
+//             the last CTA to arrive reduces them and writes the row's outputs.
+// Per-row scalar decisions are computed redundantly, in the same order, by every thread from
+// cluster-reduced values (a per-thread `Plan`), so no broadcast barrier is needed for them. Every
+// branch that decides which cluster barriers run depends only on cluster-reduced values, so all CTAs
+// of a cluster execute the same barrier sequence.
 #pragma once
 
 #include "vsamp_device.cuh"
@@ -69,7 +72,9 @@ struct Params {
   int64_t row0;             // first row of this launch
   int32_t q;                // 16-byte vectors per thread
   int32_t tma;              // rows are 16-byte aligned: bulk copies
-  long long wait_cycles;    // bound of every device-side wait
+  long long wait_cycles;    // bound of every device-side wait on a row's load
+  int32_t drop_loads;       // failure-detection test hook: loads are armed but never issued, so every
+                            // load wait runs out and the rows report VSAMP_ERR_TIMEOUT
 };
 
 constexpr int32_t kNoIndex = -1;
@@ -589,18 +594,24 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
     const int64_t c = n - cta_e0;
     return c < 0 ? 0 : (c > elems_cta ? elems_cta : c);
   };
-  // lane 0 of each warp: bulk copy of the warp's region of row r (its 16-byte-aligned part)
-  auto issue_warp = [&](int64_t r) {
+  // lane 0 of each warp: bulk copy of the warp's region of row r (its 16-byte-aligned part); returns
+  // whether a copy is in flight
+  auto issue_warp = [&](int64_t r) -> bool {
     const int64_t b16 = (cta_count(row_len(r)) * ES) & ~(int64_t)15;
     const int64_t lo = (int64_t)warp * warp_bytes;
     int64_t nb = b16 - lo;
     nb = nb < 0 ? 0 : (nb > warp_bytes ? warp_bytes : nb);
     mbar_arrive_expect_tx(&sh.bar[warp], (uint32_t)nb);
-    if (nb) bulk_copy_g2s(slice + lo, p.x + ((int64_t)r * p.ld + cta_e0) * ES + lo, (uint32_t)nb, &sh.bar[warp]);
+    if (nb && !p.drop_loads) {
+      bulk_copy_g2s(slice + lo, p.x + ((int64_t)r * p.ld + cta_e0) * ES + lo, (uint32_t)nb, &sh.bar[warp]);
+      return true;
+    }
+    return false;
   };
   if (t == 0) { sh.acnt[0] = 0u; sh.acnt[1] = 0u; }
-  int uses = 0;          // completed phases of this warp's mbarrier
-  bool pending = false;  // a copy into this warp's region is in flight
+  int uses = 0;            // completed phases of this warp's mbarrier
+  bool pending = false;    // this warp's mbarrier has an armed phase that has not completed
+  bool inflight = false;   // lane 0: a bulk copy into this warp's region may still be landing
   if (p.tma) {
     if (lane == 0) {
       mbar_init(&sh.bar[warp], 1);
@@ -608,7 +619,7 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
     }
     __syncthreads();
     if (first < p.B) {
-      if (lane == 0) issue_warp(first);
+      if (lane == 0) inflight = issue_warp(first);
       pending = true;
     }
   }
@@ -639,10 +650,14 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
   // ---------------- wait for this row's slice ----------------
     bool timeout = dead;
     if (p.tma) {
-      if (pending) {
-        if (!mbar_wait_bounded(&sh.bar[warp], (uint32_t)(uses & 1), p.wait_cycles)) timeout = true;
-        ++uses;
-        pending = false;
+      if (pending && !dead) {
+        if (mbar_wait_bounded(&sh.bar[warp], (uint32_t)(uses & 1), p.wait_cycles)) {
+          ++uses;
+          pending = false;
+          inflight = false;
+        } else {
+          timeout = true;   // the phase stays armed; no further copies are issued (the cluster is dead)
+        }
       }
       // the (< 16 byte) tail of the slice, by its owner thread with plain loads
       const int64_t b16 = (cta_n * ES) & ~(int64_t)15;
@@ -672,7 +687,7 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
       __syncwarp();
       if (lane == 0) {
         fence_proxy_async_shared();
-        issue_warp(nr);
+        inflight = issue_warp(nr);
       }
       pending = true;
     };
@@ -1336,8 +1351,9 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
     refill();
     __syncthreads();
   }
-  // after a timed-out load, wait (again bounded) for this CTA's outstanding bulk copies before leaving
-  if (p.tma && pending && lane == 0) (void)mbar_wait_bounded(&sh.bar[warp], (uint32_t)(uses & 1), p.wait_cycles);
+  // after a timed-out load, wait (again bounded, ~2 s) for a bulk copy of this warp that may still be
+  // landing in shared memory before the CTA leaves
+  if (p.tma && inflight) (void)mbar_wait_bounded(&sh.bar[warp], (uint32_t)(uses & 1), 4000000000LL);
   // no CTA may leave while a peer can still read its shared memory
   E.cluster.sync();
   (void)q;

@@ -75,10 +75,26 @@ __device__ __forceinline__ bool mbar_wait_bounded(void* bar, uint32_t parity, lo
   }
 }
 
+// Cluster-wide barrier of all threads that publishes this thread's earlier shared-memory writes to the
+// peers (a release restricted to shared memory, so stores to global memory still in flight are not
+// waited for) and acquires theirs. It also synchronises the threads of this CTA.
+__device__ __forceinline__ void cluster_barrier_shared() {
+  asm volatile("fence.release.sync_restrict::shared::cta.cluster;" ::: "memory");
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
 // ------------------------------------------------------------------------------------------------
 // Distributed shared memory: a CTA's shared address mapped into the address window of CTA `rank` of
 // the cluster, stores and an acquire-release atomic add there.
 // ------------------------------------------------------------------------------------------------
+// Acquire-release add on a word of this CTA's shared memory, at CTA scope; returns the old value.
+__device__ __forceinline__ uint32_t smem_atomic_add_acq_rel_cta(void* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(smem_addr(p)), "r"(v) : "memory");
+  return old;
+}
+
 __device__ __forceinline__ uint32_t dsmem_map(const void* p, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
@@ -158,12 +174,13 @@ __device__ __forceinline__ float value_of_key32(uint32_t k) {
 }
 
 // ------------------------------------------------------------------------------------------------
-// exp as 2^(s * log2 e) with the hardware ex2 approximation (no flush to zero; relative error of a
-// few ulp, tested against expf in the GPU test suite).
+// exp as 2^(s * log2 e) with the hardware ex2 approximation (relative error of a few ulp). Results
+// below 2^-126 flush to zero: every caller either rounds them to zero anyway (2^-40 fixed-point masses)
+// or uses them in a prune test where a token that small can never be drawn.
 // ------------------------------------------------------------------------------------------------
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
-  asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 constexpr float kLog2e = 1.4426950408889634f;

@@ -129,7 +129,7 @@ struct Traits<__nv_bfloat16> {
   // every element of the vector is >= xv (packed minimum of the eight values)
   __device__ static __forceinline__ bool all_ge(const uint4& v, float xv) {
     const __nv_bfloat162 m = __hmin2(__hmin2(pair(v.x), pair(v.y)), __hmin2(pair(v.z), pair(v.w)));
-    return fminf(__low2float(m), __high2float(m)) >= xv;
+    return __hbge2(m, __float2bfloat162_rn(xv));      // xv is a bf16 value: the conversion is exact
   }
   __device__ static __forceinline__ uint32_t key32(uint32_t rk) { return key32_of_key16(rk); }
   __device__ static __forceinline__ float value_of_rkey(uint32_t rk) { return value_of_key32(key32_of_key16(rk)); }
@@ -182,9 +182,14 @@ struct Smem {
   static constexpr int NW = NT / 32;
   unsigned long long bar[NT / 32];   // one mbarrier per warp: its region of the slice has landed
   Mail mail[2];
-  // P4 partial arg-max of every CTA of the cluster (used in CTA 0's copy), per row parity, and the
-  // number of CTAs that have published theirs
+  // per-warp exchange slots (P1: max, min, flags; P2: mass, counts), double-buffered by exchange parity;
+  // every warp of the cluster reads every slot after the cluster barrier
+  uint4 ws[2][NT / 32][2];
+  // P4 arg-max, per row parity: each warp's partial (its CTA's last warp reduces them), each CTA's
+  // partial in CTA 0's copy (the cluster's last warp reduces them), and the two arrival counters
+  uint4 apart[2][NT / 32];
   uint4 aslot[2][16];
+  uint32_t lcnt[2];
   uint32_t acnt[2];
   uint32_t hcnt[2][256];
   uint32_t hlo[2][256];
@@ -254,15 +259,22 @@ struct RowEngine {
 
   // ---------------- cluster exchange primitives ----------------
   __device__ __forceinline__ Mail& my_mail() { return sh.mail[xc & 1]; }
-  // All threads, after this CTA's mail is written (by thread 0): publishes it and waits for the peers.
+  // All threads, after this CTA's mail is written (by thread 0): publishes it and waits for the peers
+  // (for a one-CTA cluster, a block barrier). Mail is double-buffered by the exchange parity, so the
+  // peers' copies may be read until the next exchange.
   __device__ __forceinline__ void exchange() {
-    __syncthreads();
-    cluster.sync();
+    if (C == 1) __syncthreads();
+    else cluster_barrier_shared();
   }
   __device__ __forceinline__ const Mail* peer_mail(int rank) {
     return cluster.map_shared_rank(&sh.mail[xc & 1], rank);
   }
   __device__ __forceinline__ void exchange_done() { ++xc; }
+  // slot k of warp w of CTA r in the current exchange's slots (after exchange())
+  __device__ __forceinline__ uint4 wslot(int r, int w, int k) {
+    const uint4* a = &sh.ws[xc & 1][w][k];
+    return C == 1 ? *a : dsmem_load_v4(dsmem_map(a, (uint32_t)r));
+  }
 
   // Exclusive scan of tcount[] over threads (index order) into tpre[]; returns the block total.
   __device__ uint32_t block_scan_tcount() {
@@ -312,23 +324,17 @@ struct RowEngine {
   __device__ void cluster_prefix_u32(uint32_t mine_val, int slot, uint32_t& pre, uint32_t& total) {
     if (t == 0) my_mail().u[slot] = mine_val;
     exchange();
-    if (warp == 0) {
-      const uint32_t v = lane < C ? peer_mail(lane)->u[slot] : 0u;
-      uint32_t incl = v;
+    // every warp reads the peers' values (no broadcast barrier)
+    const uint32_t v = lane < C ? peer_mail(lane)->u[slot] : 0u;
+    uint32_t incl = v;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(kFullMask, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const uint32_t tot = __shfl_sync(kFullMask, incl, 31);
-      const uint32_t mypre = __shfl_sync(kFullMask, incl - v, crank);
-      if (lane == 0) { sh.bu[0] = mypre; sh.bu[1] = tot; }
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFullMask, incl, o);
+      if (lane >= o) incl += y;
     }
+    total = __shfl_sync(kFullMask, incl, 31);
+    pre = __shfl_sync(kFullMask, incl - v, crank);
     exchange_done();
-    __syncthreads();
-    pre = sh.bu[0];
-    total = sh.bu[1];
-    __syncthreads();
   }
 
   // Per-thread count of elements equal to xv, into tcount[].
@@ -344,9 +350,9 @@ struct RowEngine {
   // Returns this thread's last kept index (kAllIndex: every element of the group in its chunk is kept;
   // kNoIndex: none). The thread holding the need-th element gets it in `boundary`; its warp finds it
   // together (one 16-byte vector of that thread's chunk per lane, then a warp prefix of the counts).
-  __device__ int32_t local_cut_index(float xv, unsigned long long need, uint32_t cpre, int32_t& boundary) {
-    const unsigned long long start = (unsigned long long)cpre + sh.tpre[t];
-    const unsigned long long cnt = sh.tcount[t];
+  // start: elements equal to xv before this thread's chunk (index order); cnt: those in its chunk
+  __device__ int32_t local_cut_index(float xv, unsigned long long need, unsigned long long start,
+                                     unsigned long long cnt, int32_t& boundary) {
     boundary = kNoIndex;
     const bool holds = start < need && need <= start + cnt;
     const uint32_t bal = __ballot_sync(kFullMask, holds);
@@ -560,6 +566,161 @@ static __device__ __noinline__ float gumbel_score(float s, uint32_t b) {
 }
 
 // ------------------------------------------------------------------------------------------------
+// The two streaming passes over a thread's chunk, kept out of line: the kernel's per-row state is saved
+// once around each call and the loop gets the registers (the Philox rounds, their keys) to itself.
+// ------------------------------------------------------------------------------------------------
+struct MassPart {
+  unsigned long long s;     // fixed-point mass of the chunk
+  unsigned long long mge;   // min-p: mass of the elements at or above the threshold
+  uint32_t cm;              // elements equal to the row maximum
+  uint32_t cge;             // min-p: elements at or above the threshold
+  uint32_t minkey;          // min-p: smallest such key (fp32 key space)
+  uint32_t cmin;            // min-p: its count
+};
+
+// P2: sum of 2^((x - M) * c1) in 2^-40 fixed point (each 16-byte vector summed pairwise in a fixed
+// order, then converted), the count of maxima and, with MINP, the min-p statistics.
+template <typename T, bool MINP>
+static __device__ __noinline__ MassPart mass_pass(const uint4* mine, int thr_n, float M, float c1, uint32_t kmin32) {
+  using Tr = Traits<T>;
+  constexpr int VE = Tr::VE;
+  MassPart o{0ull, 0ull, 0u, 0u, 0xFFFFFFFFu, 0u};
+  const int nfull = thr_n / VE;
+  const float2 mM = make_float2(-M, -M), cc = make_float2(c1, c1);
+  uint32_t cm2 = 0;   // bf16: maxima counts in two 16-bit lanes
+  auto minp_stats = [&](const float (&x)[VE], const float (&w)[VE], int cnt) {
+#pragma unroll
+    for (int i = 0; i < VE; ++i) {
+      const uint32_t k32 = key_f32_bits(__float_as_uint(x[i]));
+      if (i < cnt && k32 >= kmin32) {
+        ++o.cge;
+        o.mge += mass_fx(w[i]);
+        if (k32 < o.minkey) { o.minkey = k32; o.cmin = 1; }
+        else if (k32 == o.minkey) ++o.cmin;
+      }
+    }
+  };
+  for (int j = 0; j < nfull; ++j) {
+    const uint4 v = mine[j];
+    float x[VE];
+    Tr::values(v, x);
+    float2 w2[VE / 2];
+#pragma unroll
+    for (int h = 0; h < VE / 2; ++h) {
+      const float2 e = __fmul2_rn(__fadd2_rn(make_float2(x[2 * h], x[2 * h + 1]), mM), cc);
+      w2[h] = make_float2(ex2_approx(e.x), ex2_approx(e.y));
+    }
+    if constexpr (VE == 8) {
+      const __nv_bfloat162 M2 = __float2bfloat162_rn(M);   // M is a bf16 value: exact
+      cm2 += __heq2_mask(Tr::pair(v.x), M2) & 0x00010001u;
+      cm2 += __heq2_mask(Tr::pair(v.y), M2) & 0x00010001u;
+      cm2 += __heq2_mask(Tr::pair(v.z), M2) & 0x00010001u;
+      cm2 += __heq2_mask(Tr::pair(v.w), M2) & 0x00010001u;
+    } else {
+#pragma unroll
+      for (int i = 0; i < VE; ++i) o.cm += x[i] == M ? 1u : 0u;
+    }
+    if (MINP) {
+      float w[VE];
+#pragma unroll
+      for (int h = 0; h < VE / 2; ++h) { w[2 * h] = w2[h].x; w[2 * h + 1] = w2[h].y; }
+      minp_stats(x, w, VE);
+    }
+    // (w0 + w4) + (w2 + w6) and (w1 + w5) + (w3 + w7) for eight, (w0 + w2) and (w1 + w3) for four
+    float2 a;
+    if constexpr (VE == 8) a = __fadd2_rn(__fadd2_rn(w2[0], w2[2]), __fadd2_rn(w2[1], w2[3]));
+    else a = __fadd2_rn(w2[0], w2[1]);
+    o.s += mass_fx(a.x + a.y);
+  }
+  const int cnt = thr_n - nfull * VE;
+  if (cnt > 0) {
+    float x[VE], w[VE];
+    Tr::values(mine[nfull], x);
+#pragma unroll
+    for (int i = 0; i < VE; ++i) {
+      const bool ok = i < cnt;
+      const float d = x[i] - M;
+      w[i] = ok ? ex2_approx(d * c1) : 0.f;
+      o.cm += (ok && d == 0.f) ? 1u : 0u;
+    }
+    if (MINP) minp_stats(x, w, cnt);
+#pragma unroll
+    for (int h = VE / 2; h >= 1; h >>= 1)
+#pragma unroll
+      for (int i = 0; i < h; ++i) w[i] += w[i + h];
+    o.s += mass_fx(w[0]);
+  }
+  o.cm += (cm2 & 0xFFFFu) + (cm2 >> 16);
+  return o;
+}
+
+// The vectors of a thread's chunk that hold a kept token (no Philox words: used when every kept token
+// is a candidate, i.e. the kept mass is below e^3).
+template <typename T>
+static __device__ __noinline__ unsigned long long kept_vectors(const uint4* mine, int thr_n, int64_t thr_e0, float xP,
+                                                              int32_t It) {
+  using Tr = Traits<T>;
+  constexpr int VE = Tr::VE;
+  const int nfull = thr_n / VE;
+  const int nvec = (thr_n + VE - 1) / VE;
+  unsigned long long m = 0ull;
+  for (int j = 0; j < nvec; ++j) {
+    float x[VE];
+    Tr::values(mine[j], x);
+    const int cnt = j < nfull ? VE : thr_n - nfull * VE;
+    const int64_t e0 = thr_e0 + (int64_t)j * VE;
+    bool any = false;
+#pragma unroll
+    for (int i = 0; i < VE; ++i) any |= i < cnt && (x[i] > xP || (x[i] == xP && e0 + i <= (int64_t)It));
+    if (any) m |= 1ull << j;
+  }
+  return m;
+}
+
+// P4 main pass: one Philox4x32-10 word per kept token (x > xP, or x == xP and index <= It); returns the
+// mask of vectors holding a kept token whose word is below bk. Vectors j < jfull whose every element is
+// >= xP are kept whole (their indices are <= It).
+template <typename T>
+static __device__ __noinline__ unsigned long long draw_pass(const uint4* mine, int thr_n, int64_t thr_e0, int jfull,
+                                                          float xP, int32_t It, uint32_t g0, uint32_t rid,
+                                                          uint32_t st_lo, uint32_t st_hi, PhiloxKey key, uint32_t bk) {
+  using Tr = Traits<T>;
+  constexpr int VE = Tr::VE;
+  const int nfull = thr_n / VE;
+  const int nvec = (thr_n + VE - 1) / VE;
+  unsigned long long flagged = 0ull;
+  for (int j = 0; j < nvec; ++j) {
+    const uint4 v = mine[j];
+    uint32_t bmin = 0xFFFFFFFFu;
+    if (j < jfull && Tr::all_ge(v, xP)) {
+#pragma unroll
+      for (int g = 0; g < VE / 4; ++g) {
+        const uint4 w4 = philox4x32_10(make_uint4(g0 + (uint32_t)(j * (VE / 4) + g), rid, st_lo, st_hi), key);
+        bmin = min(bmin, min(min(w4.x, w4.y), min(w4.z, w4.w)));
+      }
+    } else {
+      float x[VE];
+      Tr::values(v, x);
+      const int cnt = j < nfull ? VE : thr_n - nfull * VE;
+      const int64_t e0 = thr_e0 + (int64_t)j * VE;
+      uint32_t gmask = 0u;   // groups of four tokens holding a kept token
+#pragma unroll
+      for (int i = 0; i < VE; ++i)
+        if (i < cnt && (x[i] > xP || (x[i] == xP && e0 + i <= (int64_t)It))) gmask |= 1u << (i >> 2);
+      if (!gmask) continue;
+#pragma unroll
+      for (int g = 0; g < VE / 4; ++g) {
+        if (!((gmask >> g) & 1u)) continue;
+        const uint4 w4 = philox4x32_10(make_uint4(g0 + (uint32_t)(j * (VE / 4) + g), rid, st_lo, st_hi), key);
+        bmin = min(bmin, min(min(w4.x, w4.y), min(w4.z, w4.w)));
+      }
+    }
+    if (bmin < bk) flagged |= 1ull << j;
+  }
+  return flagged;
+}
+
+// ------------------------------------------------------------------------------------------------
 // The kernel: persistent clusters. Cluster y handles rows y, y + G, y + 2G, ... (G = gridDim.y); every
 // warp bulk-copies its own region of the slice; right after its last pass over row r it copies its region
 // of row r + G (the P4 fallback pass, which is rare, then reads the row from global memory), so HBM
@@ -608,7 +769,7 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
     }
     return false;
   };
-  if (t == 0) { sh.acnt[0] = 0u; sh.acnt[1] = 0u; }
+  if (t == 0) { sh.acnt[0] = 0u; sh.acnt[1] = 0u; sh.lcnt[0] = 0u; sh.lcnt[1] = 0u; }
   int uses = 0;            // completed phases of this warp's mbarrier
   bool pending = false;    // this warp's mbarrier has an armed phase that has not completed
   bool inflight = false;   // lane 0: a bulk copy into this warp's region may still be landing
@@ -646,6 +807,23 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
     E.thr_n = r < 0 ? 0 : (r > (int64_t)q * VE ? q * VE : (int)r);
   }
   const unsigned char* grow = p.x + ((int64_t)row * p.ld + cta_e0) * ES;
+
+  // ---------------- the row's parameters (loads issued before the wait, so their latency overlaps it) ----
+  float temp = 1.f, topp = 1.f, minp = 0.f;
+  int32_t topk = 0;
+  if (p.temperature) temp = p.temperature[row];
+  if (p.top_k) topk = p.top_k[row];
+  if (p.top_p) topp = p.top_p[row];
+  if (p.min_p) minp = p.min_p[row];
+  int32_t ksel = p.k_max;
+  if (kSel && p.k_sel) ksel = p.k_sel[row];
+  uint64_t sd = 0ull, st = 0ull;
+  uint32_t rid = (uint32_t)row;
+  if (MODE & MODE_SAMPLE) {
+    if (p.seed) sd = p.seed[row];
+    if (p.step) st = p.step[row];
+    if (p.row_id) rid = p.row_id[row];
+  }
 
   // ---------------- wait for this row's slice ----------------
     bool timeout = dead;
@@ -743,54 +921,32 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
     }
   }
   E.passes = 1;
+  float M, Mmin;
+  uint32_t gflags;
   {
     const uint32_t bad = (nf != 0.f) ? 1u : 0u;    // NaN compares unequal as well
     mx = warp_max_f(mx);
     mn = -warp_max_f(-mn);
     const uint32_t flags = __reduce_or_sync(kFullMask, bad | (timeout ? 2u : 0u));
-    if (lane == 0) { sh.wf[warp][0] = mx; sh.wf[warp][1] = mn; sh.wu[warp][3] = flags; }
-    __syncthreads();
-    if (t == 0) {
-      float m = -INFINITY, m2 = INFINITY;
-      uint32_t fl = 0;
-      for (int w = 0; w < Eng::NW; ++w) { m = fmaxf(m, sh.wf[w][0]); m2 = fminf(m2, sh.wf[w][1]); fl |= sh.wu[w][3]; }
-      Mail& ml = E.my_mail();
-      ml.f[0] = m;
-      ml.f[1] = m2;
-      ml.u[1] = fl;
-    }
+    if (lane == 0) sh.ws[E.xc & 1][warp][0] = make_uint4(__float_as_uint(mx), __float_as_uint(mn), flags, 0u);
     E.exchange();
-    if (warp == 0) {
-      float m = -INFINITY, m2 = INFINITY;
-      uint32_t fl = 0;
-      if (lane < C) {
-        const Mail* pm = E.peer_mail(lane);
-        m = pm->f[0];
-        m2 = pm->f[1];
-        fl = pm->u[1];
-      }
-      m = warp_max_f(m);
-      m2 = -warp_max_f(-m2);
-      fl = __reduce_or_sync(kFullMask, fl);
-      if (lane == 0) { sh.bf[0] = m; sh.bf[3] = m2; sh.bu[5] = fl; }
+    // every warp reduces every warp's slot (no broadcast barrier)
+    float m = -INFINITY, m2 = INFINITY;
+    uint32_t fl = 0;
+    for (int i = lane; i < C * Eng::NW; i += 32) {
+      const uint4 v = E.wslot(i / Eng::NW, i % Eng::NW, 0);
+      m = fmaxf(m, __uint_as_float(v.x));
+      m2 = fminf(m2, __uint_as_float(v.y));
+      fl |= v.z;
     }
+    M = warp_max_f(m);
+    Mmin = -warp_max_f(-m2);
+    gflags = __reduce_or_sync(kFullMask, fl);
     E.exchange_done();
-    __syncthreads();
   }
-  const float M = sh.bf[0];
-  const float Mmin = sh.bf[3];
-  const uint32_t gflags = sh.bu[5];
   if (gflags & 2u) dead = true;
 
   // ---------------- row status and parameters (uniform over the cluster) ----------------
-  float temp = 1.f, topp = 1.f, minp = 0.f;
-  int32_t topk = 0;
-  if (p.temperature) temp = p.temperature[row];
-  if (p.top_k) topk = p.top_k[row];
-  if (p.top_p) topp = p.top_p[row];
-  if (p.min_p) minp = p.min_p[row];
-  int32_t ksel = p.k_max;
-  if (kSel && p.k_sel) ksel = p.k_sel[row];
   int status = VSAMP_OK;
   if (bad_len) status = VSAMP_ERR_INVALID_ARG;
   else if (gflags & 2u) status = VSAMP_ERR_TIMEOUT;
@@ -826,7 +982,7 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
   }
 
   unsigned long long Sfx = 0, cM = 0;
-  uint32_t cpreM = 0;
+  uint32_t cm_thr = 0, cm_pre = 0;   // this thread's maxima, and the maxima before its chunk (index order)
   float xP = -INFINITY;          // kept: x > xP, or x == xP and index <= It
   int32_t It = kAllIndex;
   int32_t boundary = kNoIndex;   // global index of the last kept token, if this thread holds it
@@ -836,45 +992,20 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
   if (status == VSAMP_OK) {
     if (!kSel) {
       // ---------------- P2: fixed-point sum, maxima per thread, min-p statistics ----------------
-      unsigned long long s_loc = 0, mge = 0;
-      uint32_t cm_loc = 0, cge = 0, minkey = 0xFFFFFFFFu, cmin = 0;
-      const uint32_t kmin32 = minp_on ? plan.kmin32 : 0u;
-      const int nfull = E.thr_n / VE;
-      for (int j = 0; j <= nfull; ++j) {
-        const int cnt = j < nfull ? VE : (E.thr_n - nfull * VE);
-        if (cnt <= 0) break;
-        float x[VE], w[VE];
-        Tr::values(E.mine[j], x);
-#pragma unroll
-        for (int i = 0; i < VE; ++i) {
-          const bool ok = i < cnt;
-          const float d = x[i] - M;
-          w[i] = ok ? ex2_approx(d * c1) : 0.f;
-          cm_loc += (ok && d == 0.f) ? 1u : 0u;
-        }
-        if (minp_on) {
-#pragma unroll
-          for (int i = 0; i < VE; ++i) {
-            const uint32_t k32 = key_f32_bits(__float_as_uint(x[i]));
-            if (i < cnt && k32 >= kmin32) {
-              ++cge;
-              mge += mass_fx(w[i]);
-              if (k32 < minkey) { minkey = k32; cmin = 1; }
-              else if (k32 == minkey) ++cmin;
-            }
-          }
-        }
-        // pairwise sum of the vector, then one fixed-point conversion
-#pragma unroll
-        for (int h = VE / 2; h >= 1; h >>= 1)
-#pragma unroll
-          for (int i = 0; i < h; ++i) w[i] += w[i + h];
-        s_loc += mass_fx(w[0]);
-      }
+      const MassPart mp = minp_on ? mass_pass<T, true>(E.mine, E.thr_n, M, c1, plan.kmin32)
+                                  : mass_pass<T, false>(E.mine, E.thr_n, M, c1, 0u);
+      unsigned long long s_loc = mp.s, mge = mp.mge;
+      uint32_t cm_loc = mp.cm, cge = mp.cge, minkey = mp.minkey, cmin = mp.cmin;
       E.passes += 1;
-      sh.tcount[t] = cm_loc;
+      uint32_t cm_incl = cm_loc;      // inclusive prefix of the maxima counts within the warp
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFullMask, cm_incl, o);
+        if (lane >= o) cm_incl += y;
+      }
+      cm_thr = cm_loc;
       s_loc = warp_sum_u64(s_loc);
-      cm_loc = warp_sum_u32(cm_loc);
+      cm_loc = __shfl_sync(kFullMask, cm_incl, 31);
       if (minp_on) {
         mge = warp_sum_u64(mge);
         cge = warp_sum_u32(cge);
@@ -883,51 +1014,43 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
         minkey = mk;
       }
       if (lane == 0) {
-        sh.wq[warp][0] = s_loc; sh.wq[warp][1] = mge;
-        sh.wu[warp][0] = cm_loc; sh.wu[warp][1] = cge; sh.wu[warp][2] = minkey; sh.wu[warp][3] = cmin;
-      }
-      __syncthreads();
-      if (t == 0) {
-        unsigned long long a = 0, b = 0;
-        uint32_t c = 0, d = 0, mk = 0xFFFFFFFFu, cc = 0;
-        for (int w = 0; w < Eng::NW; ++w) {
-          a += sh.wq[w][0]; b += sh.wq[w][1]; c += sh.wu[w][0]; d += sh.wu[w][1];
-          if (sh.wu[w][2] < mk) { mk = sh.wu[w][2]; cc = sh.wu[w][3]; }
-          else if (sh.wu[w][2] == mk) cc += sh.wu[w][3];
-        }
-        Mail& ml = E.my_mail();
-        ml.q[0] = a; ml.q[1] = b; ml.u[0] = c; ml.u[1] = d; ml.u[2] = mk; ml.u[3] = cc;
+        uint4* ws = sh.ws[E.xc & 1][warp];
+        ws[0] = make_uint4((uint32_t)s_loc, (uint32_t)(s_loc >> 32), cm_loc, cge);
+        ws[1] = make_uint4((uint32_t)mge, (uint32_t)(mge >> 32), minkey, cmin);
       }
       E.exchange();
-      if (warp == 0) {
+      // every warp reduces every warp's slot (no broadcast barrier); the slots are in index order
+      // (CTA rank, then warp), so the maxima of the slots before this warp's give its prefix
+      unsigned long long mass_ge = 0ull;
+      uint32_t cnt_ge = 0, minkey_ge = 0xFFFFFFFFu, cnt_minkey = 0;
+      {
+        const int mine_slot = crank * Eng::NW + warp;
         unsigned long long a = 0, b = 0;
-        uint32_t c = 0, d = 0, mk = 0xFFFFFFFFu, cc = 0;
-        if (lane < C) {
-          const Mail* pm = E.peer_mail(lane);
-          a = pm->q[0]; b = pm->q[1]; c = pm->u[0]; d = pm->u[1]; mk = pm->u[2]; cc = pm->u[3];
+        uint32_t c = 0, cb = 0, d = 0, mk = 0xFFFFFFFFu, cc = 0;
+        for (int i = lane; i < C * Eng::NW; i += 32) {
+          const uint4 v0 = E.wslot(i / Eng::NW, i % Eng::NW, 0);
+          a += ((unsigned long long)v0.y << 32) | v0.x;
+          c += v0.z;
+          if (i < mine_slot) cb += v0.z;
+          if (minp_on) {
+            const uint4 v1 = E.wslot(i / Eng::NW, i % Eng::NW, 1);
+            d += v0.w;
+            b += ((unsigned long long)v1.y << 32) | v1.x;
+            if (v1.z < mk) { mk = v1.z; cc = v1.w; }
+            else if (v1.z == mk) cc += v1.w;
+          }
         }
-        uint32_t incl = c;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t y = __shfl_up_sync(kFullMask, incl, o);
-          if (lane >= o) incl += y;
-        }
-        const uint32_t cpre = __shfl_sync(kFullMask, incl - c, crank);   // maxima in lower ranks
-        a = warp_sum_u64(a);
-        b = warp_sum_u64(b);
-        c = warp_sum_u32(c);
-        d = warp_sum_u32(d);
-        const uint32_t gmk = warp_min_u32(mk);
-        cc = warp_sum_u32(mk == gmk ? cc : 0u);
-        if (lane == 0) {
-          sh.bq[0] = a; sh.bq[1] = b; sh.bu[0] = c; sh.bu[1] = d; sh.bu[2] = gmk; sh.bu[3] = cc; sh.bu[6] = cpre;
+        Sfx = warp_sum_u64(a);
+        cM = warp_sum_u32(c);
+        cm_pre = warp_sum_u32(cb) + (cm_incl - cm_thr);   // maxima before this thread's chunk
+        if (minp_on) {
+          mass_ge = warp_sum_u64(b);
+          cnt_ge = warp_sum_u32(d);
+          minkey_ge = warp_min_u32(mk);
+          cnt_minkey = warp_sum_u32(mk == minkey_ge ? cc : 0u);
         }
       }
       E.exchange_done();
-      __syncthreads();
-      Sfx = sh.bq[0];
-      cM = sh.bu[0];
-      cpreM = sh.bu[6];
       // ---------------- per-row plan ----------------
       {
         plan.status = VSAMP_OK;
@@ -937,8 +1060,6 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
         plan.cp_mode = 0;
         plan.goal_p = -1.f;
         plan.cp_goal = 0;
-        const unsigned long long mass_ge = sh.bq[1];
-        const uint32_t cnt_ge = sh.bu[1], minkey_ge = sh.bu[2], cnt_minkey = sh.bu[3];
         if (kCutLike) {
           const uint32_t rkM = Tr::rkey_of_value(M);
           if (greedy) {
@@ -1060,35 +1181,36 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
       It = kAllIndex;
     } else {
       xP = Tr::value_of_rkey(fin.rk);
-      uint32_t cpre;
-      unsigned long long need = fin.need;
+      unsigned long long need = fin.need, start, cnt;
       if (!kSel && fin.rk == Tr::rkey_of_value(M)) {
-        // tcount[] still holds the P2 counts of maxima; cpreM is the count over lower ranks
-        E.block_scan_tcount();
-        cpre = cpreM;
+        // the group of maxima: P2 counted them per thread and prefixed them over the cluster
+        start = cm_pre;
+        cnt = cm_thr;
         if (fin.whole) need = cM;
       } else {
         E.count_equal_pass(xP);
         const uint32_t ctot = E.block_scan_tcount();
-        uint32_t total;
+        uint32_t cpre, total;
         E.cluster_prefix_u32(ctot, 0, cpre, total);
+        start = (unsigned long long)cpre + sh.tpre[t];
+        cnt = sh.tcount[t];
         if (fin.whole) need = total;     // the last element of the group
       }
-      It = E.local_cut_index(xP, need, cpre, boundary);
+      It = E.local_cut_index(xP, need, start, cnt, boundary);
     }
   }
 
   // ---------------- P4: Gumbel-max draw over the kept prefix ----------------
   int32_t out_token = -1;
-  bool last_cta = false;     // this CTA reduced the row's arg-max and writes the draw's outputs
+  float out_s = 0.f;         // (x - M) / T of the drawn token
+  bool last_cta = false;     // this warp reduced the row's arg-max and writes the draw's outputs
   if ((MODE & MODE_SAMPLE) && fin_valid) {
     const unsigned long long kept = fin.kept();
     if (greedy || kept == 1) {
       // the first maximum: written by the thread that holds it
       if (boundary >= 0) {
-        const float xt = Tr::load_global(p.x, (int64_t)row * p.ld + boundary);
-        p.token[row] = boundary;
-        if (p.logprob) p.logprob[row] = fminf((xt - M) * invT - plan.logS, 0.f);
+        p.token[row] = boundary;                                  // a maximum: (x - M) / T = 0
+        if (p.logprob) p.logprob[row] = fminf(-plan.logS, 0.f);
       }
     } else {
       {
@@ -1100,9 +1222,6 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
         plan.bk = plan.all_cand ? 0xFFFFFFFFu : __float2uint_ru(kappa * 1.00001f * 4294967296.0f);
         plan.b0 = -logf(kappa);
       }
-      const uint64_t sd = p.seed ? p.seed[row] : 0ull;
-      const uint64_t st = p.step ? p.step[row] : 0ull;
-      const uint32_t rid = p.row_id ? p.row_id[row] : (uint32_t)row;
       const PhiloxKey key{(uint32_t)sd, (uint32_t)(sd >> 32)};
       const uint32_t st_lo = (uint32_t)st, st_hi = (uint32_t)(st >> 32);
       const float kappa = plan.kappa;
@@ -1110,150 +1229,139 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
       const float B0 = plan.b0;
       {
         const bool all_cand = plan.all_cand;
+        const int nfull = E.thr_n / VE;
+        // leading full vectors whose tokens equal to the pivot value are all kept: e0 + VE - 1 <= It
+        int jfull = 0;
+        {
+          const int64_t lim = (int64_t)It - E.thr_e0 - (VE - 1);
+          if (lim >= 0) jfull = (int)(lim / VE + 1 < (int64_t)nfull ? lim / VE + 1 : (int64_t)nfull);
+        }
+        const uint32_t g0 = (uint32_t)(E.thr_e0 >> 2);      // Philox counter of the thread's first 4 tokens
+        // Main pass: a vector is flagged when one of its kept tokens' words is below the prune bound bk
+        // (about e^3 tokens per row); flagged vectors are evaluated exactly below. When every kept token
+        // is a candidate, every vector holding a kept token is flagged.
+        unsigned long long flagged =
+            all_cand ? kept_vectors<T>(E.mine, E.thr_n, E.thr_e0, xP, It)
+                     : draw_pass<T>(E.mine, E.thr_n, E.thr_e0, jfull, xP, It, g0, rid, st_lo, st_hi, key, bk);
+        // Flagged vectors: the kept tokens whose word passes the bound get the exact perturbed score.
         float bscore = -INFINITY, bs = 0.f;
         int32_t bidx = 0x7FFFFFFF;
-        const int nfull = E.thr_n / VE;
-        for (int j = 0; j <= nfull; ++j) {
-          const int cnt = j < nfull ? VE : (E.thr_n - nfull * VE);
-          if (cnt <= 0) break;
-          const int64_t e0 = E.thr_e0 + (int64_t)j * VE;
+        while (flagged) {
+          const int j = __ffsll((long long)flagged) - 1;
+          flagged &= flagged - 1ull;
           const uint4 v = E.mine[j];
-          // evaluates the kept candidates (mask c) of this vector exactly
-          auto candidates = [&](const bool (&c)[VE], const uint32_t (&b)[VE]) {
-            float x[VE];
-            Tr::values(v, x);
-#pragma unroll
-            for (int i = 0; i < VE; ++i) {
-              if (!c[i]) continue;
-              const float d = x[i] - M;
-              const float s = d * invT;
-              if (!all_cand) {
-                const float w = ex2_approx(d * c1);
-                const float u = fmaf((float)b[i], kTwoM32, kTwoM33);
-                if (!(u < w * kappa * 1.00001f)) continue;
-              }
-              const float score = gumbel_score(s, b[i]);
-              const int32_t idx = (int32_t)(e0 + i);
-              if (argmax_better(score, idx, bscore, bidx)) { bscore = score; bidx = idx; bs = s; }
-            }
-          };
-          uint32_t b[VE];
-          if (cnt == VE && e0 + VE - 1 <= (int64_t)It && Tr::all_ge(v, xP)) {
-            // every token of the vector is kept
-#pragma unroll
-            for (int g = 0; g < VE / 4; ++g) {
-              const uint4 w4 = philox4x32_10(make_uint4((uint32_t)((e0 >> 2) + g), rid, st_lo, st_hi), key);
-              b[4 * g + 0] = w4.x; b[4 * g + 1] = w4.y; b[4 * g + 2] = w4.z; b[4 * g + 3] = w4.w;
-            }
-            bool c[VE];
-            bool anyc = false;
-#pragma unroll
-            for (int i = 0; i < VE; ++i) {
-              c[i] = all_cand || b[i] < bk;
-              anyc |= c[i];
-            }
-            if (__builtin_expect(anyc, 0)) candidates(c, b);
-            continue;
-          }
           float x[VE];
           Tr::values(v, x);
-          bool k[VE];
-          bool any = false;
-#pragma unroll
-          for (int i = 0; i < VE; ++i) {
-            k[i] = i < cnt && (x[i] > xP || (x[i] == xP && e0 + i <= (int64_t)It));
-            any |= k[i];
-          }
-          if (!any) continue;
+          const int cnt = j < nfull ? VE : E.thr_n - nfull * VE;
+          const int64_t e0 = E.thr_e0 + (int64_t)j * VE;
+          uint32_t b[VE];
 #pragma unroll
           for (int g = 0; g < VE / 4; ++g) {
-            const uint4 w4 = philox4x32_10(make_uint4((uint32_t)((e0 >> 2) + g), rid, st_lo, st_hi), key);
+            const uint4 w4 = philox4x32_10(make_uint4(g0 + (uint32_t)(j * (VE / 4) + g), rid, st_lo, st_hi), key);
             b[4 * g + 0] = w4.x; b[4 * g + 1] = w4.y; b[4 * g + 2] = w4.z; b[4 * g + 3] = w4.w;
           }
-          bool c[VE];
-          bool anyc = false;
 #pragma unroll
           for (int i = 0; i < VE; ++i) {
-            c[i] = k[i] && (all_cand || b[i] < bk);
-            anyc |= c[i];
+            if (!(i < cnt && (x[i] > xP || (x[i] == xP && e0 + i <= (int64_t)It)))) continue;
+            if (!all_cand && b[i] >= bk) continue;
+            const float d = x[i] - M;
+            const float s = d * invT;
+            if (!all_cand) {
+              const float w = ex2_approx(d * c1);
+              const float u = fmaf((float)b[i], kTwoM32, kTwoM33);
+              if (!(u < w * kappa * 1.00001f)) continue;
+            }
+            const float score = gumbel_score(s, b[i]);
+            const int32_t idx = (int32_t)(e0 + i);
+            if (argmax_better(score, idx, bscore, bidx)) { bscore = score; bidx = idx; bs = s; }
           }
-          if (__builtin_expect(anyc, 0)) candidates(c, b);
         }
         E.passes += 1;
         refill();    // this warp has finished reading its region of the slice
         // ---------------- lock-free cluster arg-max ----------------
-        // Each CTA publishes its partial into CTA 0's slot for this row and counts itself in with an
-        // acquire-release atomic; the last CTA to arrive reduces the slots and writes the row's outputs,
-        // the others go straight on to their next row.
+        // Two levels, no barrier: each warp publishes its partial and counts itself in with an
+        // acquire-release atomic; the last warp of each CTA reduces its CTA's partials and publishes them
+        // in CTA 0; the last of those reduces the cluster's and writes the row's outputs. Every other warp
+        // goes straight on to its next row.
         const ArgMax best = warp_argmax(ArgMax{bscore, bidx, bs});
         int32_t wcut = boundary;  // the cut's boundary index, if this warp holds it (else -1)
 #pragma unroll
         for (int o = 16; o; o >>= 1) wcut = max(wcut, __shfl_xor_sync(kFullMask, wcut, o));
-        if (lane == 0) { sh.wf[warp][1] = best.score; sh.wf[warp][2] = best.s; sh.wi[warp][0] = best.idx; sh.wi[warp][1] = wcut; }
-        __syncthreads();
         const int par = (int)(k & 1);
-        if (t == 0) {
-          ArgMax b2{-INFINITY, 0x7FFFFFFF, 0.f};
-          for (int w = 0; w < Eng::NW; ++w)
-            if (argmax_better(sh.wf[w][1], sh.wi[w][0], b2.score, b2.idx)) b2 = ArgMax{sh.wf[w][1], sh.wi[w][0], sh.wf[w][2]};
-          int32_t my_cut = -1;
-          for (int w = 0; w < Eng::NW; ++w) my_cut = max(my_cut, sh.wi[w][1]);
-          dsmem_store_v4(dsmem_map(&sh.aslot[par][crank], 0), __float_as_uint(b2.score), (uint32_t)b2.idx,
-                         __float_as_uint(b2.s), (uint32_t)my_cut);
-          const uint32_t old = dsmem_atomic_add_acq_rel(dsmem_map(&sh.acnt[par], 0), 1u);
-          sh.bu[7] = (old == (uint32_t)(C - 1)) ? 1u : 0u;
+        // level 1: each warp publishes its partial in its CTA and counts itself in; the CTA's last warp
+        // reduces the CTA's partials
+        uint32_t old = 0;
+        if (lane == 0) {
+          sh.apart[par][warp] = make_uint4(__float_as_uint(best.score), (uint32_t)best.idx, __float_as_uint(best.s),
+                                           (uint32_t)wcut);
+          old = smem_atomic_add_acq_rel_cta(&sh.lcnt[par], 1u);
         }
-        __syncthreads();
-        last_cta = sh.bu[7] != 0;
-        if (last_cta) {
-          if (t == 0) {
-            ArgMax g{-INFINITY, 0x7FFFFFFF, 0.f};
-            int32_t cut = -1;
-            for (int r = 0; r < C; ++r) {
-              const uint4 v = dsmem_load_v4(dsmem_map(&sh.aslot[par][r], 0));
-              const ArgMax a2{__uint_as_float(v.x), (int32_t)v.y, __uint_as_float(v.z)};
-              if (argmax_better(a2.score, a2.idx, g.score, g.idx)) g = a2;
-              cut = max(cut, (int32_t)v.w);
-            }
-            dsmem_store_u32(dsmem_map(&sh.acnt[par], 0), 0u);
-            sh.bf[1] = g.score;
-            sh.bi[2] = g.idx;
-            sh.bi[1] = cut < 0 ? kAllIndex : cut;
+        old = __shfl_sync(kFullMask, old, 0);
+        if (old == (uint32_t)(Eng::NW - 1)) {
+          __syncwarp();
+          ArgMax c2{-INFINITY, 0x7FFFFFFF, 0.f};
+          int32_t ccut = -1;
+          if (lane < Eng::NW) {
+            const uint4 v = sh.apart[par][lane];
+            c2 = ArgMax{__uint_as_float(v.x), (int32_t)v.y, __uint_as_float(v.z)};
+            ccut = (int32_t)v.w;
           }
-          __syncthreads();
-          const float gscore = sh.bf[1];
-          const int32_t gidx = sh.bi[2];
-          const bool certified = all_cand || (gscore > B0 + 1e-4f * fmaxf(1.f, fabsf(B0)));
-          if (certified) {
-            out_token = gidx;
-          } else {
-            // the prune bound did not certify the draw (probability ~1e-9): this CTA evaluates every kept
-            // token of the row from global memory
-            plan.path |= PATH_FALLBACK;
-            const int32_t Ig = sh.bi[1];
-            float fs = -INFINITY, fsv = 0.f;
-            int32_t fi = 0x7FFFFFFF;
-            for (int64_t e = t; e < n; e += NT) {
-              const float xv = Tr::load_global(p.x, (int64_t)row * p.ld + e);
-              if (!(xv > xP || (xv == xP && e <= (int64_t)Ig))) continue;
-              const uint4 w4 = philox4x32_10(make_uint4((uint32_t)(e >> 2), rid, st_lo, st_hi), key);
-              const uint32_t bw = philox_word(w4, (int)(e & 3));
-              const float sv = (xv - M) * invT;
-              const float score = gumbel_score(sv, bw);
-              if (argmax_better(score, (int32_t)e, fs, fi)) { fs = score; fi = (int32_t)e; fsv = sv; }
+          c2 = warp_argmax(c2);
+#pragma unroll
+          for (int o = 16; o; o >>= 1) ccut = max(ccut, __shfl_xor_sync(kFullMask, ccut, o));
+          // level 2: the CTA's partial goes to CTA 0; the cluster's last warp reduces the C partials
+          uint32_t old2 = 0;
+          if (lane == 0) {
+            sh.lcnt[par] = 0u;
+            if (C > 1) {
+              dsmem_store_v4(dsmem_map(&sh.aslot[par][crank], 0), __float_as_uint(c2.score), (uint32_t)c2.idx,
+                             __float_as_uint(c2.s), (uint32_t)ccut);
+              old2 = dsmem_atomic_add_acq_rel(dsmem_map(&sh.acnt[par], 0), 1u);
             }
-            const ArgMax fb = warp_argmax(ArgMax{fs, fi, fsv});
-            __syncthreads();
-            if (lane == 0) { sh.wf[warp][1] = fb.score; sh.wi[warp][0] = fb.idx; }
-            __syncthreads();
-            if (t == 0) {
-              ArgMax b4{-INFINITY, 0x7FFFFFFF, 0.f};
-              for (int w = 0; w < Eng::NW; ++w)
-                if (argmax_better(sh.wf[w][1], sh.wi[w][0], b4.score, b4.idx)) b4 = ArgMax{sh.wf[w][1], sh.wi[w][0], 0.f};
-              sh.bi[2] = b4.idx;
+          }
+          old2 = __shfl_sync(kFullMask, old2, 0);
+          if (C == 1 || old2 == (uint32_t)(C - 1)) {
+            __syncwarp();
+            last_cta = true;        // this warp writes the row's outputs
+            ArgMax g = c2;
+            int32_t cut = ccut;
+            if (C > 1) {
+              g = ArgMax{-INFINITY, 0x7FFFFFFF, 0.f};
+              cut = -1;
+              if (lane < C) {
+                const uint4 v = dsmem_load_v4(dsmem_map(&sh.aslot[par][lane], 0));
+                g = ArgMax{__uint_as_float(v.x), (int32_t)v.y, __uint_as_float(v.z)};
+                cut = (int32_t)v.w;
+              }
+              g = warp_argmax(g);
+#pragma unroll
+              for (int o = 16; o; o >>= 1) cut = max(cut, __shfl_xor_sync(kFullMask, cut, o));
+              if (lane == 0) dsmem_store_u32(dsmem_map(&sh.acnt[par], 0), 0u);
             }
-            __syncthreads();
-            out_token = sh.bi[2];
+            const bool certified = all_cand || (g.score > B0 + 1e-4f * fmaxf(1.f, fabsf(B0)));
+            if (certified) {
+              out_token = g.idx;
+              out_s = g.s;
+            } else {
+              // the prune bound did not certify the draw (probability ~1e-9): this warp evaluates every
+              // kept token of the row from global memory
+              plan.path |= PATH_FALLBACK;
+              const int32_t Ig = cut < 0 ? kAllIndex : cut;
+              float fs = -INFINITY, fsv = 0.f;
+              int32_t fi = 0x7FFFFFFF;
+              for (int64_t e = lane; e < n; e += 32) {
+                const float xv = Tr::load_global(p.x, (int64_t)row * p.ld + e);
+                if (!(xv > xP || (xv == xP && e <= (int64_t)Ig))) continue;
+                const uint4 w4 = philox4x32_10(make_uint4((uint32_t)(e >> 2), rid, st_lo, st_hi), key);
+                const uint32_t bw = philox_word(w4, (int)(e & 3));
+                const float sv = (xv - M) * invT;
+                const float score = gumbel_score(sv, bw);
+                if (argmax_better(score, (int32_t)e, fs, fi)) { fs = score; fi = (int32_t)e; fsv = sv; }
+              }
+              const ArgMax fb = warp_argmax(ArgMax{fs, fi, fsv});
+              out_token = fb.idx;
+              out_s = fb.s;
+            }
           }
         }
       }
@@ -1295,10 +1403,11 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
 
   // ---------------- finalisation ----------------
   if ((MODE & MODE_CUT) && fin_valid && boundary >= 0) p.cut[row].idx_cut = boundary;
-  // the row's outputs come from CTA 0, except a Gumbel draw's, which come from the CTA that reduced it
+  // the row's outputs come from thread 0, except a Gumbel draw's, which come from lane 0 of the warp
+  // that reduced it
   const bool p4_path = (MODE & MODE_SAMPLE) && fin_valid && !(greedy || fin.kept() == 1);
-  const bool writer = p4_path ? last_cta : (crank == 0);
-  if (writer && t == 0) {
+  const bool writer = p4_path ? last_cta : (crank == 0 && warp == 0);
+  if (writer && lane == 0) {
     if (MODE & MODE_LSE) {
       if (p.row_max) p.row_max[row] = status == VSAMP_OK ? M : __int_as_float(0x7FC00000);
       if (p.row_logsum) p.row_logsum[row] = status == VSAMP_OK ? (float)plan.logS : __int_as_float(0x7FC00000);
@@ -1317,10 +1426,9 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
         p.token[row] = -1;
         if (p.logprob) p.logprob[row] = __int_as_float(0x7FC00000);
       } else if (!one_token) {
-        if (out_token >= 0) {
-          const float xt = Tr::load_global(p.x, (int64_t)row * p.ld + out_token);
+        if (out_token >= 0 && (int64_t)out_token < n) {
           p.token[row] = out_token;
-          if (p.logprob) p.logprob[row] = fminf((xt - M) * invT - plan.logS, 0.f);
+          if (p.logprob) p.logprob[row] = fminf(out_s - plan.logS, 0.f);
         } else {
           status = VSAMP_ERR_INVALID_ARG;
           p.token[row] = -1;

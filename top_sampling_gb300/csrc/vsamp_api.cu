@@ -55,11 +55,16 @@ vsamp_status device_info(int dev, DeviceInfo& out) {
 // cluster sizes whose slices fit, the one with the least padding is taken (q odd when that costs at
 // most an eighth: conflict-free 16-byte shared-memory loads); small batches spread rows over more CTAs.
 vsamp_status choose_geometry(int64_t V, int esize, int64_t B, const DeviceInfo& d, Geometry& g) {
-  const int64_t VE = 16 / esize;
-  const int64_t nvec = (V + VE - 1) / VE;
   const int NT = env_int("VSAMP_THREADS", 256) == 128 ? kThreadsSmall : kThreadsLarge;
   const int head = NT == kThreadsSmall ? slice_offset<kThreadsSmall>() : slice_offset<kThreadsLarge>();
   const int per_sm = env_int("VSAMP_CTAS_PER_SM", NT == kThreadsSmall ? 5 : 3);
+  return choose_geometry_for(V, esize, B, d, NT, head, per_sm, g);
+}
+
+vsamp_status choose_geometry_for(int64_t V, int esize, int64_t B, const DeviceInfo& d, int NT, int head, int per_sm,
+                                 Geometry& g) {
+  const int64_t VE = 16 / esize;
+  const int64_t nvec = (V + VE - 1) / VE;
   const int smem_sm = d.smem_per_sm > 0 ? d.smem_per_sm : d.optin;
   const int odd = env_int("VSAMP_ODD_Q", 1);
   const int forced = env_int("VSAMP_CLUSTER", 0);
@@ -235,7 +240,8 @@ vsamp_status vsamp_sample(const void* logits, vsamp_dtype dt, int64_t B, int64_t
   p.logprob = logprob;
   p.row_status = row_status;
   p.stats = stats;
-  return dispatch<MODE_SAMPLE>(p, dt, B, static_cast<cudaStream_t>(stream));
+  if (dt == VSAMP_F32) return launch_sample<float>(p, B, 4, static_cast<cudaStream_t>(stream));
+  return launch_sample<__nv_bfloat16>(p, B, 2, static_cast<cudaStream_t>(stream));
 }
 
 vsamp_status vsamp_logprob(const void* logits, vsamp_dtype dt, int64_t B, int64_t V, int64_t ld,

@@ -64,6 +64,36 @@ __device__ __forceinline__ bool mbar_try_wait(void* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Arrival on an mbarrier of another CTA of the cluster (a shared::cluster address from mapa), with
+// release semantics at cluster scope: this thread's earlier writes to that CTA's shared memory are
+// visible to whoever observes the completed phase.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// Test of an mbarrier phase with acquire semantics at cluster scope (pairs with mbar_arrive_remote).
+__device__ __forceinline__ bool mbar_try_wait_cluster(void* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(void* bar, uint32_t parity, long long max_cycles) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (clock64() - t0 > max_cycles) return false;
+  }
+}
+
 // Bounded wait on an mbarrier phase: gives up after ~`max_cycles` SM clock cycles and returns false.
 __device__ __forceinline__ bool mbar_wait_bounded(void* bar, uint32_t parity, long long max_cycles) {
   if (mbar_try_wait(bar, parity)) return true;

@@ -33,6 +33,13 @@ int env_int(const char* name, int dflt);
 long long env_ll(const char* name, long long dflt);
 vsamp_status device_info(int dev, DeviceInfo& out);
 vsamp_status choose_geometry(int64_t V, int esize, int64_t B, const DeviceInfo& d, Geometry& g);
+// NT data threads per CTA, head bytes of shared memory before the slice, per_sm CTAs resident per SM
+vsamp_status choose_geometry_for(int64_t V, int esize, int64_t B, const DeviceInfo& d, int NT, int head, int per_sm,
+                                 Geometry& g);
+
+// vsamp_sample's kernel (specialised warps), in its own translation units
+template <typename T>
+vsamp_status launch_sample(Params p, int64_t B, int esize, cudaStream_t stream);
 
 template <typename T, int MODE>
 vsamp_status launch(Params p, int64_t B, int esize, cudaStream_t stream);

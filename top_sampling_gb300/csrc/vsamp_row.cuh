@@ -581,7 +581,7 @@ struct MassPart {
 // P2: sum of 2^((x - M) * c1) in 2^-40 fixed point (each 16-byte vector summed pairwise in a fixed
 // order, then converted), the count of maxima and, with MINP, the min-p statistics.
 template <typename T, bool MINP>
-static __device__ __noinline__ MassPart mass_pass(const uint4* mine, int thr_n, float M, float c1, uint32_t kmin32) {
+__device__ __forceinline__ MassPart mass_pass_body(const uint4* mine, int thr_n, float M, float c1, uint32_t kmin32) {
   using Tr = Traits<T>;
   constexpr int VE = Tr::VE;
   MassPart o{0ull, 0ull, 0u, 0u, 0xFFFFFFFFu, 0u};
@@ -652,6 +652,11 @@ static __device__ __noinline__ MassPart mass_pass(const uint4* mine, int thr_n, 
   }
   o.cm += (cm2 & 0xFFFFu) + (cm2 >> 16);
   return o;
+}
+
+template <typename T, bool MINP>
+static __device__ __noinline__ MassPart mass_pass(const uint4* mine, int thr_n, float M, float c1, uint32_t kmin32) {
+  return mass_pass_body<T, MINP>(mine, thr_n, M, c1, kmin32);
 }
 
 // The vectors of a thread's chunk that hold a kept token (no Philox words: used when every kept token

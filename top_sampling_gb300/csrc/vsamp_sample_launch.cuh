@@ -1,0 +1,76 @@
+// Launcher of the specialised-warp sampling kernel: cluster launch over (C, G) blocks of kSampleThreads
+// threads, persistent over rows.
+#pragma once
+
+#include "vsamp_host.h"
+#include "vsamp_sample.cuh"
+
+namespace vsamp {
+
+template <typename T, int NDW, int PER_SM>
+static vsamp_status launch_sample_cfg(Params p, int64_t B, int esize, const DeviceInfo& d, cudaStream_t stream) {
+  constexpr int kDataThreads = NDW * 32;
+  constexpr int kSampleThreads = kDataThreads + 32;
+  Geometry g;
+  vsamp_status st = choose_geometry_for(p.V, esize, B, d, kDataThreads, sample_slice_offset(), PER_SM, g);
+  if (st != VSAMP_OK) return st;
+  p.q = g.q;
+  const long long wc = env_ll("VSAMP_WAIT_CYCLES", 0);
+  p.wait_cycles = wc > 0 ? wc : 4000000000LL;   // ~2 s at the maximum SM clock
+  p.drop_loads = env_int("VSAMP_TEST_DROP_LOADS", 0) != 0 ? 1 : 0;
+  auto kern = sample_kernel<T, NDW, PER_SM>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem) != cudaSuccess) {
+    cudaGetLastError();
+    return VSAMP_ERR_UNSUPPORTED;
+  }
+  if (g.C > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+    cudaGetLastError();
+    return VSAMP_ERR_UNSUPPORTED;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kSampleThreads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)g.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)g.C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3((unsigned)g.C, 1, 1);
+  int nclusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&nclusters, kern, &cfg) != cudaSuccess || nclusters < 1) {
+    cudaGetLastError();
+    return VSAMP_ERR_UNSUPPORTED;
+  }
+  const int fit = env_int("VSAMP_GRID_CLUSTERS", 0) > 0 ? env_int("VSAMP_GRID_CLUSTERS", 0) : nclusters;
+  int64_t G = B < fit ? B : fit;
+  const int64_t rounds = (B + G - 1) / G;   // every cluster gets the same number of rows (+-1)
+  G = (B + rounds - 1) / rounds;
+  if (G > 65535) G = 65535;
+  p.row0 = 0;
+  cfg.gridDim = dim3((unsigned)g.C, (unsigned)G, 1);
+  if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) {
+    cudaGetLastError();
+    return VSAMP_ERR_CUDA;
+  }
+  return VSAMP_OK;
+}
+
+template <typename T>
+vsamp_status launch_sample(Params p, int64_t B, int esize, cudaStream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return VSAMP_ERR_CUDA; }
+  DeviceInfo d;
+  vsamp_status st = device_info(dev, d);
+  if (st != VSAMP_OK) return st;
+  switch (env_int("VSAMP_SAMPLE_CFG", 0)) {
+    case 1: return launch_sample_cfg<T, 4, 6>(p, B, esize, d, stream);
+    case 2: return launch_sample_cfg<T, 4, 5>(p, B, esize, d, stream);
+    case 3: return launch_sample_cfg<T, 8, 4>(p, B, esize, d, stream);
+    default: return launch_sample_cfg<T, 8, 3>(p, B, esize, d, stream);
+  }
+}
+
+}  // namespace vsamp

@@ -46,6 +46,7 @@
 #ifndef VSAMP_H_
 #define VSAMP_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -136,6 +137,28 @@ vsamp_status vsamp_sample(const void* logits, vsamp_dtype dt, int64_t B, int64_t
                           const float* min_p, const uint64_t* seed, const uint64_t* step,
                           const uint32_t* row_id, int32_t* token, float* logprob,
                           int32_t* row_status, int32_t* stats, void* stream);
+
+/* vsamp_sample with a workspace. The same draw, computed by two streaming kernels over fixed 16 KB
+ * chunks of every row instead of one thread-block cluster per row, so rows need no cross-CTA
+ * synchronisation; faster on large batches. Results are deterministic and do not depend on the batch;
+ * they agree with vsamp_sample except for the last bits of the row mass (chunk masses are rescaled to
+ * the row maximum in binary64), which moves a top-p cut only inside the 1e-6 tolerance band.
+ *   workspace        device buffer of at least vsamp_sample_workspace_size(dt, B, V) bytes, 16-byte
+ *                    aligned, zero-filled before its first use. Every completed call leaves its counters
+ *                    and chunk statistics zero again (whatever B and V the next call uses), so it can be
+ *                    reused without clearing. Calls sharing a workspace must not run at the same time (use
+ *                    one workspace per stream).
+ *   workspace_bytes  its size in bytes; too small, unaligned or NULL is VSAMP_ERR_INVALID_ARG.
+ * Every other argument is as for vsamp_sample. */
+vsamp_status vsamp_sample_ws(const void* logits, vsamp_dtype dt, int64_t B, int64_t V, int64_t ld,
+                             const float* temperature, const int32_t* top_k, const float* top_p,
+                             const float* min_p, const uint64_t* seed, const uint64_t* step,
+                             const uint32_t* row_id, int32_t* token, float* logprob,
+                             int32_t* row_status, int32_t* stats, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/* Workspace bytes vsamp_sample_ws needs for B rows of V logits of type dt (0 for invalid arguments). */
+size_t vsamp_sample_workspace_size(vsamp_dtype dt, int64_t B, int64_t V);
 
 /* Selected-token log-probability ("[WS2][Logprob] ...", Design: logp = min(z_t - lse, 0), temperature
  * applied to the statistics):

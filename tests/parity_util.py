@@ -19,6 +19,13 @@ import torch
 from oracle import sampler as osm
 
 LOGP_TOL = 1e-5
+# the entry point the sampling checks call: "vsamp_sample" (one cluster per row) or "vsamp_sample_ws"
+# (split vocabulary, workspace)
+SAMPLE_FN = "vsamp_sample"
+
+
+def sample_fn(ts):
+    return getattr(ts, SAMPLE_FN)
 
 
 def to_device(batch_logits: np.ndarray, dtype: str, dev) -> torch.Tensor:
@@ -39,7 +46,7 @@ def t(arr, dev, dtype=None):
 
 def run_sample(ts, batch, dev, V=None, row_id=None, x=None):
     x = to_device(batch.logits, batch.dtype, dev) if x is None else x
-    tok, lp, st, stats = ts.vsamp_sample(
+    tok, lp, st, stats = sample_fn(ts)(
         x, temperature=t(batch.temperature, dev), top_k=t(batch.top_k, dev), top_p=t(batch.top_p, dev),
         min_p=t(batch.min_p, dev), seed=t(batch.seed, dev), step=t(batch.step, dev),
         row_id=None if row_id is None else t(row_id, dev), V=V if V is not None else batch.V, want_stats=True)

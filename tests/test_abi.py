@@ -85,3 +85,19 @@ def test_host_argument_checks_reject_before_any_device_work(lib):
     assert lib.vsamp_sample(dummy, 0, 4, 100, 50, *([None] * 12)) == 1         # ld < V
     assert lib.vsamp_sample(dummy, 0, 0, 100, 100, *([None] * 12)) == 1        # B = 0
     assert lib.vsamp_sample(dummy, 0, 4, 100, 100, *([None] * 7), None, *([None] * 4)) == 1   # token NULL
+
+
+def test_workspace_size_and_host_checks_of_the_workspace_entry_point(lib):
+    import top_sampling_gb300 as ts
+
+    l2 = ts.load()
+    # 128 bytes per row plus 16 per 64 KB chunk of the row
+    assert l2.vsamp_sample_workspace_size(ts.VSAMP_BF16, 256, 151936) == 256 * 128 + 256 * 5 * 16
+    assert l2.vsamp_sample_workspace_size(ts.VSAMP_F32, 4, 32000) == 4 * 128 + 4 * 2 * 16
+    assert l2.vsamp_sample_workspace_size(7, 4, 100) == 0
+    assert l2.vsamp_sample_workspace_size(ts.VSAMP_F32, 0, 100) == 0
+    dummy = ctypes.c_void_p(16)
+    args = [dummy, ts.VSAMP_F32, 4, 100, 100] + [None] * 7 + [dummy] + [None] * 3
+    assert l2.vsamp_sample_ws(*args, None, 4096, None) == ts.VSAMP_ERR_INVALID_ARG          # no workspace
+    assert l2.vsamp_sample_ws(*args, ctypes.c_void_p(4096 + 8), 4096, None) == ts.VSAMP_ERR_INVALID_ARG   # unaligned
+    assert l2.vsamp_sample_ws(*args, ctypes.c_void_p(4096), 16, None) == ts.VSAMP_ERR_INVALID_ARG  # too small

@@ -12,6 +12,7 @@ from oracle import sampler as osm
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
+import parity_util  # noqa: E402
 from parity_util import (LOGP_TOL, TieCounter, check_cut, check_sample, oracle_row, run_cut, run_sample, t,  # noqa: E402
                          to_device)
 
@@ -280,7 +281,7 @@ def test_heavy_tailed_z_scores_one_million_draws(ts, dev):
     hits0 = tail = 0
     first = None
     for s in range(steps):
-        tok, _, st, _ = ts.vsamp_sample(x, seed=seeds, step=torch.full((B,), s, dtype=torch.int64, device=dev),
+        tok, _, st, _ = parity_util.sample_fn(ts)(x, seed=seeds, step=torch.full((B,), s, dtype=torch.int64, device=dev),
                                         row_id=rid, want_logprob=False)
         if first is None:
             first = tok.cpu().numpy()
@@ -308,7 +309,7 @@ def test_small_vocab_chi_square(ts, dev):
     temp = torch.full((B,), T, dtype=torch.float32, device=dev)
     counts = np.zeros(8)
     for s in range(steps):
-        tok, _, _, _ = ts.vsamp_sample(xt, temperature=temp, seed=torch.full((B,), 99, dtype=torch.int64, device=dev),
+        tok, _, _, _ = parity_util.sample_fn(ts)(xt, temperature=temp, seed=torch.full((B,), 99, dtype=torch.int64, device=dev),
                                        step=torch.full((B,), s, dtype=torch.int64, device=dev), want_logprob=False)
         counts += np.bincount(tok.cpu().numpy(), minlength=8)
     s = (x.astype(np.float64) - 0.3) / np.float64(np.float32(T))

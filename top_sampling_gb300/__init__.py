@@ -27,7 +27,8 @@ VSAMP_F32 = 0
 VSAMP_BF16 = 1
 
 EXPORTED = ("vsamp_softmax_lse", "vsamp_topk_select", "vsamp_topp_minp_mask", "vsamp_sample",
-            "vsamp_logprob", "vsamp_status_string", "vsamp_device_info", "vsamp_version")
+            "vsamp_sample_ws", "vsamp_sample_workspace_size", "vsamp_logprob", "vsamp_status_string",
+            "vsamp_device_info", "vsamp_version")
 
 
 class VsampError(RuntimeError):
@@ -65,7 +66,12 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.vsamp_topp_minp_mask.argtypes = [vp, st, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.vsamp_sample.argtypes = [vp, st, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.vsamp_logprob.argtypes = [vp, st, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp]
-    for f in ("vsamp_softmax_lse", "vsamp_topk_select", "vsamp_topp_minp_mask", "vsamp_sample", "vsamp_logprob"):
+    lib.vsamp_sample_ws.argtypes = [vp, st, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                    ctypes.c_size_t, vp]
+    lib.vsamp_sample_workspace_size.argtypes = [st, i64, i64]
+    lib.vsamp_sample_workspace_size.restype = ctypes.c_size_t
+    for f in ("vsamp_softmax_lse", "vsamp_topk_select", "vsamp_topp_minp_mask", "vsamp_sample", "vsamp_logprob",
+              "vsamp_sample_ws"):
         getattr(lib, f).restype = st
     lib.vsamp_status_string.argtypes = [st]
     lib.vsamp_status_string.restype = ctypes.c_char_p
@@ -242,6 +248,59 @@ def vsamp_sample(logits, temperature=None, top_k=None, top_p=None, min_p=None, s
         _ptr(row_status, torch.int32, dev, B, "row_status"), _ptr(stats, torch.int32, dev, 4 * B, "stats"),
         _stream(stream))
     _check(st, "vsamp_sample")
+    return token, logprob, row_status, stats
+
+
+_WORKSPACES = {}
+
+
+def sample_workspace(device, nbytes: int, stream=None) -> torch.Tensor:
+    """A zero-filled workspace of at least nbytes for vsamp_sample_ws, cached per (device, stream).
+
+    The library leaves a workspace zero-filled after every completed call, so it is reused as is; calls
+    on one stream never overlap, so a workspace per stream is enough."""
+    dev = torch.device(device)
+    key = (dev.index if dev.index is not None else torch.cuda.current_device(), _stream(stream))
+    ws = _WORKSPACES.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=dev)
+        _WORKSPACES[key] = ws
+    return ws
+
+
+def vsamp_sample_ws(logits, temperature=None, top_k=None, top_p=None, min_p=None, seed=None, step=None,
+                    row_id=None, V=None, token=None, logprob=None, row_status=None, stats=None,
+                    want_logprob=True, want_stats=False, stream=None, workspace=None):
+    """vsamp_sample through the split-vocabulary kernels and a workspace (cached per device and stream
+    unless given). Returns (token, logprob or None, row_status, stats or None)."""
+    B, V, ld = _rows(logits, V)
+    dev = logits.device
+    temperature = _param(temperature, B, torch.float32, dev, "temperature")
+    top_k = _param(top_k, B, torch.int32, dev, "top_k")
+    top_p = _param(top_p, B, torch.float32, dev, "top_p")
+    min_p = _param(min_p, B, torch.float32, dev, "min_p")
+    seed = _param(seed, B, torch.int64, dev, "seed")
+    step = _param(step, B, torch.int64, dev, "step")
+    row_id = _param(row_id, B, torch.int32, dev, "row_id")
+    token = torch.empty(B, dtype=torch.int32, device=dev) if token is None else token
+    if want_logprob and logprob is None:
+        logprob = torch.empty(B, dtype=torch.float32, device=dev)
+    row_status = torch.empty(B, dtype=torch.int32, device=dev) if row_status is None else row_status
+    if want_stats and stats is None:
+        stats = torch.empty((B, 4), dtype=torch.int32, device=dev)
+    lib = load()
+    need = int(lib.vsamp_sample_workspace_size(_dtype_code(logits), B, V))
+    if workspace is None:
+        workspace = sample_workspace(dev, need, stream)
+    st = lib.vsamp_sample_ws(
+        logits.data_ptr(), _dtype_code(logits), B, V, ld, _ptr(temperature, torch.float32, dev, B, "temperature"),
+        _ptr(top_k, torch.int32, dev, B, "top_k"), _ptr(top_p, torch.float32, dev, B, "top_p"),
+        _ptr(min_p, torch.float32, dev, B, "min_p"), _ptr(seed, torch.int64, dev, B, "seed"),
+        _ptr(step, torch.int64, dev, B, "step"), _ptr(row_id, torch.int32, dev, B, "row_id"),
+        _ptr(token, torch.int32, dev, B, "token"), _ptr(logprob, torch.float32, dev, B, "logprob"),
+        _ptr(row_status, torch.int32, dev, B, "row_status"), _ptr(stats, torch.int32, dev, 4 * B, "stats"),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "vsamp_sample_ws")
     return token, logprob, row_status, stats
 
 

@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libvsamp.so")
 
-SOURCES = ["vsamp_api.cu", "vsamp_inst_f32.cu", "vsamp_inst_bf16.cu", "vsamp_sample_f32.cu", "vsamp_sample_bf16.cu"]
+SOURCES = ["vsamp_api.cu", "vsamp_inst_f32.cu", "vsamp_inst_bf16.cu", "vsamp_sample_f32.cu", "vsamp_sample_bf16.cu", "vsamp_split_f32.cu", "vsamp_split_bf16.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 

@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "vsamp_host.h"
+#include "vsamp_split.cuh"
 
 namespace vsamp {
 
@@ -242,6 +243,39 @@ vsamp_status vsamp_sample(const void* logits, vsamp_dtype dt, int64_t B, int64_t
   p.stats = stats;
   if (dt == VSAMP_F32) return launch_sample<float>(p, B, 4, static_cast<cudaStream_t>(stream));
   return launch_sample<__nv_bfloat16>(p, B, 2, static_cast<cudaStream_t>(stream));
+}
+
+size_t vsamp_sample_workspace_size(vsamp_dtype dt, int64_t B, int64_t V) {
+  if ((dt != VSAMP_F32 && dt != VSAMP_BF16) || B <= 0 || V <= 0) return 0;
+  const int es = dt == VSAMP_F32 ? 4 : 2;
+  return (size_t)B * sizeof(RowPlan) + (size_t)B * (size_t)split_nchunks(V, es) * sizeof(ChunkStat);
+}
+
+vsamp_status vsamp_sample_ws(const void* logits, vsamp_dtype dt, int64_t B, int64_t V, int64_t ld,
+                             const float* temperature, const int32_t* top_k, const float* top_p,
+                             const float* min_p, const uint64_t* seed, const uint64_t* step,
+                             const uint32_t* row_id, int32_t* token, float* logprob, int32_t* row_status,
+                             int32_t* stats, void* workspace, size_t workspace_bytes, void* stream) {
+  vsamp_status st = check_common(logits, dt, B, V, ld);
+  if (st != VSAMP_OK) return st;
+  if (!token || !workspace || (reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return VSAMP_ERR_INVALID_ARG;
+  if (workspace_bytes < vsamp_sample_workspace_size(dt, B, V)) return VSAMP_ERR_INVALID_ARG;
+  if (V > 0x7FFEFFFFLL) return VSAMP_ERR_UNSUPPORTED;   // 32-bit element indices, chunk ends included
+  Params p = base_params(logits, dt, B, V, ld);
+  p.temperature = temperature;
+  p.top_k = top_k;
+  p.top_p = top_p;
+  p.min_p = min_p;
+  p.seed = seed;
+  p.step = step;
+  p.row_id = row_id;
+  p.token = token;
+  p.logprob = logprob;
+  p.row_status = row_status;
+  p.stats = stats;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dt == VSAMP_F32) return launch_sample_split<float>(p, B, 4, workspace, s);
+  return launch_sample_split<__nv_bfloat16>(p, B, 2, workspace, s);
 }
 
 vsamp_status vsamp_logprob(const void* logits, vsamp_dtype dt, int64_t B, int64_t V, int64_t ld,

@@ -178,6 +178,33 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, PhiloxKey key) {
   return c;
 }
 
+// The ten round keys of a Philox4x32-10 key, computed once for many calls.
+struct PhiloxRoundKeys {
+  uint32_t k0[10], k1[10];
+  __device__ __forceinline__ explicit PhiloxRoundKeys(PhiloxKey key) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+      k0[r] = key.k0 + (uint32_t)r * 0x9E3779B9u;
+      k1[r] = key.k1 + (uint32_t)r * 0xBB67AE85u;
+    }
+  }
+};
+
+// Philox4x32-10 with precomputed round keys (same output as philox4x32_10).
+__device__ __forceinline__ uint4 philox4x32_10_rk(uint4 c, const PhiloxRoundKeys& K) {
+  constexpr uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    unsigned long long p0, p1;
+    asm("mul.wide.u32 %0, %1, %2;" : "=l"(p0) : "r"(c.x), "r"(M0));
+    asm("mul.wide.u32 %0, %1, %2;" : "=l"(p1) : "r"(c.z), "r"(M1));
+    const uint32_t lo0 = (uint32_t)p0, hi0 = (uint32_t)(p0 >> 32);
+    const uint32_t lo1 = (uint32_t)p1, hi1 = (uint32_t)(p1 >> 32);
+    c = make_uint4(hi1 ^ c.y ^ K.k0[r], lo1, hi0 ^ c.w ^ K.k1[r], lo0);
+  }
+  return c;
+}
+
 __device__ __forceinline__ uint32_t philox_word(uint4 w, int lane) {
   return lane == 0 ? w.x : lane == 1 ? w.y : lane == 2 ? w.z : w.w;
 }

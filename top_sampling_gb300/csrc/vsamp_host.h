@@ -41,6 +41,10 @@ vsamp_status choose_geometry_for(int64_t V, int esize, int64_t B, const DeviceIn
 template <typename T>
 vsamp_status launch_sample(Params p, int64_t B, int esize, cudaStream_t stream);
 
+// vsamp_sample_ws's kernels (split vocabulary, caller's workspace)
+template <typename T>
+vsamp_status launch_sample_split(Params p, int64_t B, int esize, void* workspace, cudaStream_t stream);
+
 template <typename T, int MODE>
 vsamp_status launch(Params p, int64_t B, int esize, cudaStream_t stream);
 

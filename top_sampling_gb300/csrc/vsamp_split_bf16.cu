@@ -1,0 +1,6 @@
+// bf16 instantiation of the split-vocabulary sampling kernels and their launcher.
+#include "vsamp_split_launch.cuh"
+
+namespace vsamp {
+template vsamp_status launch_sample_split<__nv_bfloat16>(Params, int64_t, int, void*, cudaStream_t);
+}  // namespace vsamp

@@ -138,7 +138,7 @@ vsamp_status vsamp_sample(const void* logits, vsamp_dtype dt, int64_t B, int64_t
                           const uint32_t* row_id, int32_t* token, float* logprob,
                           int32_t* row_status, int32_t* stats, void* stream);
 
-/* vsamp_sample with a workspace. The same draw, computed by two streaming kernels over fixed 16 KB
+/* vsamp_sample with a workspace. The same draw, computed by two streaming kernels over fixed 64 KB
  * chunks of every row instead of one thread-block cluster per row, so rows need no cross-CTA
  * synchronisation; faster on large batches. Results are deterministic and do not depend on the batch;
  * they agree with vsamp_sample except for the last bits of the row mass (chunk masses are rescaled to

@@ -59,7 +59,8 @@ typedef enum vsamp_status {
   VSAMP_ERR_UNSUPPORTED = 2,   /* this device cannot hold the row (shared memory, cluster size) */
   VSAMP_ERR_CUDA = 3,          /* a CUDA runtime call failed (launch, attribute) */
   VSAMP_ERR_NONFINITE = 4,     /* per row: NaN or +-inf in the row */
-  VSAMP_ERR_TIMEOUT = 5        /* per row: a bounded device-side wait gave up */
+  VSAMP_ERR_TIMEOUT = 5,       /* per row: a bounded device-side wait gave up */
+  VSAMP_ERR_SCRATCH_LIMIT = 6  /* vsamp_sample_static: the batch needs more than its fixed scratch array */
 } vsamp_status;
 
 typedef enum vsamp_dtype {
@@ -159,6 +160,27 @@ vsamp_status vsamp_sample_ws(const void* logits, vsamp_dtype dt, int64_t B, int6
 
 /* Workspace bytes vsamp_sample_ws needs for B rows of V logits of type dt (0 for invalid arguments). */
 size_t vsamp_sample_workspace_size(vsamp_dtype dt, int64_t B, int64_t V);
+
+/* Bytes of the fixed device array that vsamp_sample_static uses as its workspace. */
+#define VSAMP_STATIC_SCRATCH_BYTES 1048576
+
+/* vsamp_sample_ws on a fixed scratch array of VSAMP_STATIC_SCRATCH_BYTES bytes that the library holds in
+ * device memory (a file-scope __device__ array of its module), so the call allocates nothing: no device
+ * allocation by the library or by the caller. The sampling method has no counterpart of this call; it
+ * exists for callers that must not allocate (for instance while a memory pool is frozen).
+ *   Size limit: vsamp_sample_workspace_size(dt, B, V) must not exceed VSAMP_STATIC_SCRATCH_BYTES, else
+ *     the call returns VSAMP_ERR_SCRATCH_LIMIT and enqueues nothing.
+ *   Set-up: the first call on each device (with that device current) looks up the array's address once.
+ *   Zeroing: every call first enqueues a clear, on `stream`, of the bytes it uses, then the two kernels.
+ *   Races: one array per device is shared by every caller of this function, so calls whose kernels
+ *     overlap on one device (from two streams or two host threads) race on it and give wrong results;
+ *     serialise them, or use vsamp_sample_ws with a workspace per stream.
+ * Every other argument, the results and the errors are as for vsamp_sample_ws. */
+vsamp_status vsamp_sample_static(const void* logits, vsamp_dtype dt, int64_t B, int64_t V, int64_t ld,
+                                 const float* temperature, const int32_t* top_k, const float* top_p,
+                                 const float* min_p, const uint64_t* seed, const uint64_t* step,
+                                 const uint32_t* row_id, int32_t* token, float* logprob,
+                                 int32_t* row_status, int32_t* stats, void* stream);
 
 /* Selected-token log-probability ("[WS2][Logprob] ...", Design: logp = min(z_t - lse, 0), temperature
  * applied to the statistics):

@@ -171,6 +171,35 @@ __global__ void logprob_from_stats_kernel(const unsigned char* x, int64_t B, int
 
 }  // namespace vsamp
 
+namespace vsamp {
+
+// vsamp_sample_static's workspace: a fixed array in this module's device memory, so that call allocates
+// nothing. Its address on each device is looked up once, with that device current.
+static __device__ __align__(256) unsigned char g_static_scratch[VSAMP_STATIC_SCRATCH_BYTES];
+static void* g_static_ptr[kMaxDevices];   // guarded by g_mu
+
+static vsamp_status static_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return VSAMP_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return VSAMP_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_static_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress((void**)&ptr, g_static_scratch) != cudaSuccess || !ptr) {
+      cudaGetLastError();
+      return VSAMP_ERR_CUDA;
+    }
+    g_static_ptr[dev] = ptr;
+  }
+  *out = g_static_ptr[dev];
+  return VSAMP_OK;
+}
+
+}  // namespace vsamp
+
 using namespace vsamp;
 
 extern "C" {
@@ -278,6 +307,26 @@ vsamp_status vsamp_sample_ws(const void* logits, vsamp_dtype dt, int64_t B, int6
   return launch_sample_split<__nv_bfloat16>(p, B, 2, workspace, s);
 }
 
+vsamp_status vsamp_sample_static(const void* logits, vsamp_dtype dt, int64_t B, int64_t V, int64_t ld,
+                                 const float* temperature, const int32_t* top_k, const float* top_p,
+                                 const float* min_p, const uint64_t* seed, const uint64_t* step,
+                                 const uint32_t* row_id, int32_t* token, float* logprob, int32_t* row_status,
+                                 int32_t* stats, void* stream) {
+  vsamp_status st = check_common(logits, dt, B, V, ld);
+  if (st != VSAMP_OK) return st;
+  if (!token) return VSAMP_ERR_INVALID_ARG;
+  if (V > 0x7FFEFFFFLL) return VSAMP_ERR_UNSUPPORTED;
+  const size_t need = vsamp_sample_workspace_size(dt, B, V);
+  if (need > (size_t)VSAMP_STATIC_SCRATCH_BYTES) return VSAMP_ERR_SCRATCH_LIMIT;
+  void* scratch = nullptr;
+  st = static_scratch(&scratch);
+  if (st != VSAMP_OK) return st;
+  // the row counters and chunk statistics the kernels accumulate into start at zero
+  if (cudaMemsetAsync(scratch, 0, need, static_cast<cudaStream_t>(stream)) != cudaSuccess) return VSAMP_ERR_CUDA;
+  return vsamp_sample_ws(logits, dt, B, V, ld, temperature, top_k, top_p, min_p, seed, step, row_id, token,
+                         logprob, row_status, stats, scratch, (size_t)VSAMP_STATIC_SCRATCH_BYTES, stream);
+}
+
 vsamp_status vsamp_logprob(const void* logits, vsamp_dtype dt, int64_t B, int64_t V, int64_t ld,
                            const float* temperature, const int32_t* token, const float* row_max,
                            const float* row_logsum, float* out, int32_t* row_status, void* stream) {
@@ -315,6 +364,7 @@ const char* vsamp_status_string(vsamp_status s) {
     case VSAMP_ERR_CUDA: return "CUDA runtime error";
     case VSAMP_ERR_NONFINITE: return "non-finite value in the row";
     case VSAMP_ERR_TIMEOUT: return "device-side wait timed out";
+    case VSAMP_ERR_SCRATCH_LIMIT: return "batch needs more than the fixed scratch array of vsamp_sample_static";
   }
   return "unknown status";
 }

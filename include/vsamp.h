@@ -139,16 +139,15 @@ vsamp_status vsamp_sample(const void* logits, vsamp_dtype dt, int64_t B, int64_t
                           const uint32_t* row_id, int32_t* token, float* logprob,
                           int32_t* row_status, int32_t* stats, void* stream);
 
-/* vsamp_sample with a workspace. The same draw, computed by two streaming kernels over fixed 64 KB
- * chunks of every row instead of one thread-block cluster per row, so rows need no cross-CTA
- * synchronisation; faster on large batches. Results are deterministic and do not depend on the batch;
- * they agree with vsamp_sample except for the last bits of the row mass (chunk masses are rescaled to
- * the row maximum in binary64), which moves a top-p cut only inside the 1e-6 tolerance band.
- *   workspace        device buffer of at least vsamp_sample_workspace_size(dt, B, V) bytes, 16-byte
- *                    aligned, zero-filled before its first use. Every completed call leaves its counters
- *                    and chunk statistics zero again (whatever B and V the next call uses), so it can be
- *                    reused without clearing. Calls sharing a workspace must not run at the same time (use
- *                    one workspace per stream).
+/* vsamp_sample with a workspace. The same draw, computed by streaming kernels over fixed 32 KB chunks of
+ * every row instead of one thread-block cluster per row: chunk statistics (one HBM read), a plan per row, the
+ * draw over the chunks (read again, mostly from L2) and the outputs, in four launches on `stream`. Results are
+ * deterministic and do not depend on the batch; they agree with vsamp_sample except for the last bits of the
+ * row mass (chunk masses are rescaled to the row maximum in binary64), which moves a top-p cut only inside
+ * the 1e-6 tolerance band.
+ *   workspace        device buffer of at least vsamp_sample_workspace_size(dt, B, V) bytes, 16-byte aligned.
+ *                    It needs no initialisation: every call writes what it reads. Calls sharing a workspace
+ *                    must not run at the same time (use one workspace per stream).
  *   workspace_bytes  its size in bytes; too small, unaligned or NULL is VSAMP_ERR_INVALID_ARG.
  * Every other argument is as for vsamp_sample. */
 vsamp_status vsamp_sample_ws(const void* logits, vsamp_dtype dt, int64_t B, int64_t V, int64_t ld,
@@ -171,7 +170,7 @@ size_t vsamp_sample_workspace_size(vsamp_dtype dt, int64_t B, int64_t V);
  *   Size limit: vsamp_sample_workspace_size(dt, B, V) must not exceed VSAMP_STATIC_SCRATCH_BYTES, else
  *     the call returns VSAMP_ERR_SCRATCH_LIMIT and enqueues nothing.
  *   Set-up: the first call on each device (with that device current) looks up the array's address once.
- *   Zeroing: every call first enqueues a clear, on `stream`, of the bytes it uses, then the two kernels.
+ *   Zeroing: every call first enqueues a clear, on `stream`, of the bytes it uses, then the kernels.
  *   Races: one array per device is shared by every caller of this function, so calls whose kernels
  *     overlap on one device (from two streams or two host threads) race on it and give wrong results;
  *     serialise them, or use vsamp_sample_ws with a workspace per stream.

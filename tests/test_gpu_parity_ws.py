@@ -32,9 +32,10 @@ def test_workspace_is_left_zero_filled(ts, dev):
                                            seed=parity_util.t(b.seed, dev), workspace=ws)
         torch.cuda.synchronize()
         assert int(st.ne(0).sum()) == 0
-        # the per-row counters and draw slots are back to zero (the chunk statistics may stay)
-        plans = ws[: 128 * b.logits.shape[0]].view(-1, 128)[:, :16]
-        assert int(plans.ne(0).sum()) == 0
+        # the reserved header and the per-row counters and draw slots are back to zero
+        assert int(ws[:256].ne(0).sum()) == 0
+        plans = ws[256: 256 + 128 * b.logits.shape[0]].view(-1, 128)
+        assert int(plans[:, :16].ne(0).sum()) == 0
 
 
 def test_workspace_too_small_or_unaligned_is_refused(ts, dev):

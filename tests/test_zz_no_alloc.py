@@ -73,9 +73,10 @@ def test_static_scratch_matches_the_workspace_entry_point_on_two_calls_in_a_row(
 def test_static_scratch_refuses_a_batch_beyond_its_size(ts, dev):
     lib = ts.load()
     V = 151936
-    per_row = int(lib.vsamp_sample_workspace_size(ts.VSAMP_BF16, 1, V))
-    B = ts.VSAMP_STATIC_SCRATCH_BYTES // per_row + 1
-    assert int(lib.vsamp_sample_workspace_size(ts.VSAMP_BF16, B, V)) > ts.VSAMP_STATIC_SCRATCH_BYTES
+    size = lambda b: int(lib.vsamp_sample_workspace_size(ts.VSAMP_BF16, b, V))
+    per_row, fixed = size(2) - size(1), 2 * size(1) - size(2)   # the size is fixed + per_row * B
+    B = (ts.VSAMP_STATIC_SCRATCH_BYTES - fixed) // per_row + 1
+    assert size(B) > ts.VSAMP_STATIC_SCRATCH_BYTES >= size(B - 1)
     # full-size buffers although the call is refused on the host before any launch
     x = torch.empty((B, V), dtype=torch.bfloat16, device=dev)
     token = torch.full((B,), -7, dtype=torch.int32, device=dev)
@@ -85,7 +86,7 @@ def test_static_scratch_refuses_a_batch_beyond_its_size(ts, dev):
     torch.cuda.synchronize()
     assert int(token.ne(-7).sum()) == 0
     # one row fewer than the limit allows is accepted
-    B_ok = ts.VSAMP_STATIC_SCRATCH_BYTES // per_row
+    B_ok = B - 1
     tok, _, st, _ = ts.vsamp_sample_static(x[:B_ok].zero_(), want_logprob=False)
     torch.cuda.synchronize()
     assert int(st.ne(0).sum()) == 0

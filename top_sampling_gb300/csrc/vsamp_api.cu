@@ -63,7 +63,7 @@ vsamp_status choose_geometry(int64_t V, int esize, int64_t B, const DeviceInfo& 
 }
 
 vsamp_status choose_geometry_for(int64_t V, int esize, int64_t B, const DeviceInfo& d, int NT, int head, int per_sm,
-                                 Geometry& g) {
+                                 Geometry& g, int max_nbuf) {
   const int64_t VE = 16 / esize;
   const int64_t nvec = (V + VE - 1) / VE;
   const int smem_sm = d.smem_per_sm > 0 ? d.smem_per_sm : d.optin;
@@ -76,7 +76,7 @@ vsamp_status choose_geometry_for(int64_t V, int esize, int64_t B, const DeviceIn
     return q;
   };
   const int64_t cap1 = (int64_t)d.optin - head;                       // one buffer, one CTA per SM
-  for (int nbuf = 1; nbuf >= 1; --nbuf) {
+  for (int nbuf = max_nbuf; nbuf >= 1; --nbuf) {
     int64_t budget = ((int64_t)smem_sm / (per_sm > 0 ? per_sm : 1) - 1024 - head) / nbuf;
     if (budget * nbuf > cap1) budget = cap1 / nbuf;
     int C = 0;
@@ -100,6 +100,8 @@ vsamp_status choose_geometry_for(int64_t V, int esize, int64_t B, const DeviceIn
       }
     }
     if (!C) continue;
+    // a second buffer only pays when clusters have more than one row to stream
+    if (nbuf > 1 && forced <= 0 && B * C < 3LL * d.sm_count * (per_sm > 0 ? per_sm : 1) / 2) continue;
     g.NT = NT;
     g.C = C;
     g.q = (int)q_for(C);
@@ -277,7 +279,7 @@ vsamp_status vsamp_sample(const void* logits, vsamp_dtype dt, int64_t B, int64_t
 size_t vsamp_sample_workspace_size(vsamp_dtype dt, int64_t B, int64_t V) {
   if ((dt != VSAMP_F32 && dt != VSAMP_BF16) || B <= 0 || V <= 0) return 0;
   const int es = dt == VSAMP_F32 ? 4 : 2;
-  return (size_t)B * sizeof(RowPlan) + (size_t)B * (size_t)split_nchunks(V, es) * sizeof(ChunkStat);
+  return sizeof(StreamHeader) + (size_t)B * sizeof(RowPlan) + (size_t)B * (size_t)split_nchunks(V, es) * sizeof(ChunkStat);
 }
 
 vsamp_status vsamp_sample_ws(const void* logits, vsamp_dtype dt, int64_t B, int64_t V, int64_t ld,

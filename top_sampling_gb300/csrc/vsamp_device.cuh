@@ -205,6 +205,50 @@ __device__ __forceinline__ uint4 philox4x32_10_rk(uint4 c, const PhiloxRoundKeys
   return c;
 }
 
+// Philox4x32-10 along one row: the counters (c0, c1, c2, c3) of a row differ only in c0, so the first
+// round's product M1 * c2 and the second round's product M0 * x1 (x1, y1: the first round's output words
+// that do not depend on c0) are formed once. Each counter then costs 18 wide multiplies instead of 20.
+// Same output as philox4x32_10.
+struct PhiloxRow {
+  uint32_t k0[10], k1[10];   // round keys
+  uint32_t y1, z1k;          // first round: y1 = lo(M1 c2); z1k = c3 ^ k1[0]
+  uint32_t x2k, hi2, w2;     // second round: x2k = y1 ^ k0[1]; hi2 ^ ..., w2 = hi / lo of M0 * x1
+  __device__ __forceinline__ PhiloxRow(PhiloxKey key, uint32_t c1, uint32_t c2, uint32_t c3) {
+    constexpr uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+      k0[r] = key.k0 + (uint32_t)r * 0x9E3779B9u;
+      k1[r] = key.k1 + (uint32_t)r * 0xBB67AE85u;
+    }
+    const unsigned long long p1 = (unsigned long long)M1 * c2;
+    const uint32_t x1 = (uint32_t)(p1 >> 32) ^ c1 ^ k0[0];
+    y1 = (uint32_t)p1;
+    z1k = c3 ^ k1[0];
+    const unsigned long long p2 = (unsigned long long)M0 * x1;
+    x2k = y1 ^ k0[1];
+    hi2 = (uint32_t)(p2 >> 32) ^ k1[1];
+    w2 = (uint32_t)p2;
+  }
+  __device__ __forceinline__ uint4 operator()(uint32_t c0) const {
+    constexpr uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
+    unsigned long long p0, p1;
+    asm("mul.wide.u32 %0, %1, %2;" : "=l"(p0) : "r"(c0), "r"(M0));
+    const uint32_t z1 = (uint32_t)(p0 >> 32) ^ z1k, w1 = (uint32_t)p0;
+    asm("mul.wide.u32 %0, %1, %2;" : "=l"(p1) : "r"(z1), "r"(M1));
+    uint4 c = make_uint4((uint32_t)(p1 >> 32) ^ x2k, (uint32_t)p1, hi2 ^ w1, w2);
+#pragma unroll
+    for (int r = 2; r < 10; ++r) {
+      asm("mul.wide.u32 %0, %1, %2;" : "=l"(p0) : "r"(c.x), "r"(M0));
+      asm("mul.wide.u32 %0, %1, %2;" : "=l"(p1) : "r"(c.z), "r"(M1));
+      c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k0[r], (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ k1[r],
+                     (uint32_t)p0);
+    }
+    return c;
+  }
+};
+
+__device__ __forceinline__ uint32_t min4_u32(uint4 w) { return min(__vimin3_u32(w.x, w.y, w.z), w.w); }
+
 __device__ __forceinline__ uint32_t philox_word(uint4 w, int lane) {
   return lane == 0 ? w.x : lane == 1 ? w.y : lane == 2 ? w.z : w.w;
 }

@@ -35,7 +35,7 @@ vsamp_status device_info(int dev, DeviceInfo& out);
 vsamp_status choose_geometry(int64_t V, int esize, int64_t B, const DeviceInfo& d, Geometry& g);
 // NT data threads per CTA, head bytes of shared memory before the slice, per_sm CTAs resident per SM
 vsamp_status choose_geometry_for(int64_t V, int esize, int64_t B, const DeviceInfo& d, int NT, int head, int per_sm,
-                                 Geometry& g);
+                                 Geometry& g, int max_nbuf = 1);
 
 // vsamp_sample's kernel (specialised warps), in its own translation units
 template <typename T>

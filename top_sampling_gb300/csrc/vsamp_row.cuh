@@ -75,6 +75,7 @@ struct Params {
   long long wait_cycles;    // bound of every device-side wait on a row's load
   int32_t drop_loads;       // failure-detection test hook: loads are armed but never issued, so every
                             // load wait runs out and the rows report VSAMP_ERR_TIMEOUT
+  int32_t nbuf;             // slice buffers per CTA (vsamp_sample: 2 streams the next row during this one)
 };
 
 constexpr int32_t kNoIndex = -1;

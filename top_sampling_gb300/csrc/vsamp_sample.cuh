@@ -71,7 +71,7 @@ struct SampleCtl {
 };
 
 struct SampleSmem {
-  unsigned long long lbar[kMaxDataWarps];   // per data warp: its region of the slice has landed
+  unsigned long long lbar[2][kMaxDataWarps];   // per slice buffer and data warp: its region has landed
   unsigned long long xbar[2];            // cluster exchange: one arrival per CTA, per exchange parity
   uint4 xm[2][16][2];                    // cluster exchange mailboxes: each CTA's 32-byte message
   uint4 dp[kMaxDataWarps][2];            // data -> control partials (P1, P2, tie counts)
@@ -127,6 +127,120 @@ __device__ __forceinline__ unsigned long long u64_of(uint32_t lo, uint32_t hi) {
 }
 
 // ------------------------------------------------------------------------------------------------
+// P1 over one thread's vectors: the maximum, and nf != 0 when a value is NaN or +-inf (x * 0 is NaN
+// exactly for those). bf16 pairs are handled packed.
+// ------------------------------------------------------------------------------------------------
+template <typename T>
+static __device__ __noinline__ float max_pass(const uint4* mine, int thr_n, float& nf_out) {
+  using Tr = Traits<T>;
+  constexpr int VE = Tr::VE;
+  const int nfull = thr_n / VE;
+  float mx = -INFINITY, nf = 0.f;
+  if constexpr (VE == 8) {
+    const __nv_bfloat162 zero2 = __float2bfloat162_rn(0.f);
+    __nv_bfloat162 mxa = __float2bfloat162_rn(-INFINITY), mxb = mxa, nfa = zero2, nfb = zero2;
+    for (int j = 0; j < nfull; ++j) {
+      const uint4 v = mine[j];
+      mxa = __hmax2(mxa, __hmax2(Tr::pair(v.x), Tr::pair(v.y)));
+      mxb = __hmax2(mxb, __hmax2(Tr::pair(v.z), Tr::pair(v.w)));
+      nfa = __hfma2(Tr::pair(v.x), zero2, __hfma2(Tr::pair(v.y), zero2, nfa));
+      nfb = __hfma2(Tr::pair(v.z), zero2, __hfma2(Tr::pair(v.w), zero2, nfb));
+    }
+    mxa = __hmax2(mxa, mxb);
+    nfa = __hadd2(nfa, nfb);
+    mx = fmaxf(__low2float(mxa), __high2float(mxa));
+    nf = (__low2float(nfa) != 0.f || __high2float(nfa) != 0.f) ? 1.f : 0.f;
+  } else {
+    float mb = -INFINITY, nb = 0.f;
+    for (int j = 0; j < nfull; ++j) {
+      float x[VE];
+      Tr::values(mine[j], x);
+      mx = fmaxf(mx, fmaxf(x[0], x[1]));
+      mb = fmaxf(mb, fmaxf(x[2], x[3]));
+      nf = fmaf(x[0], 0.f, fmaf(x[1], 0.f, nf));
+      nb = fmaf(x[2], 0.f, fmaf(x[3], 0.f, nb));
+    }
+    mx = fmaxf(mx, mb);
+    nf += nb;
+  }
+  const int tail = thr_n - nfull * VE;
+  if (tail) {
+    float x[VE];
+    Tr::values(mine[nfull], x);
+#pragma unroll
+    for (int i = 0; i < VE; ++i)
+      if (i < tail) { mx = fmaxf(mx, x[i]); nf = fmaf(x[i], 0.f, nf); }
+  }
+  nf_out = nf;
+  return mx;
+}
+
+// ------------------------------------------------------------------------------------------------
+// P4 main pass over one thread's vectors: one Philox4x32-10 word per kept token (x > xP, or x == xP and
+// index <= It); returns the mask of vectors holding a kept token whose word is below bk. Vectors j < jfull
+// lie at indices <= It, so only their values decide; in that range the pass draws four counters at a time
+// (two bf16 vectors, four fp32 vectors) whenever every element of the group of vectors is kept.
+// ------------------------------------------------------------------------------------------------
+template <typename T>
+static __device__ __noinline__ unsigned long long draw_scan(const uint4* mine, int thr_n, int64_t thr_e0, int jfull,
+                                                           float xP, int32_t It, uint32_t g0, uint32_t rid,
+                                                           uint32_t st_lo, uint32_t st_hi, uint32_t k0, uint32_t k1,
+                                                           uint32_t bk) {
+  using Tr = Traits<T>;
+  constexpr int VE = Tr::VE;
+  constexpr int G = VE / 4;            // counters per vector
+  constexpr int U = 4 / G;             // vectors per step: four counters
+  const PhiloxRow ph(PhiloxKey{k0, k1}, rid, st_lo, st_hi);
+  const int nfull = thr_n / VE;
+  const int nvec = (thr_n + VE - 1) / VE;
+  unsigned long long flagged = 0ull;
+  // one vector, any position: the groups of four tokens holding a kept token
+  auto one = [&](int j) {
+    float x[VE];
+    Tr::values(mine[j], x);
+    const int cnt = j < nfull ? VE : thr_n - nfull * VE;
+    const int64_t e0 = thr_e0 + (int64_t)j * VE;
+    uint32_t gmask = 0u;
+#pragma unroll
+    for (int i = 0; i < VE; ++i)
+      if (i < cnt && (x[i] > xP || (x[i] == xP && e0 + i <= (int64_t)It))) gmask |= 1u << (i >> 2);
+    if (!gmask) return;
+    uint32_t bmin = 0xFFFFFFFFu;
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+      if ((gmask >> g) & 1u) bmin = min(bmin, min4_u32(ph(g0 + (uint32_t)(j * G + g))));
+    if (bmin < bk) flagged |= 1ull << j;
+  };
+  int j = 0;
+  for (; j + U <= jfull; j += U) {
+    uint4 v[U];
+    bool all = true;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      v[u] = mine[j + u];
+      all = all && Tr::all_ge(v[u], xP);
+    }
+    if (all) {
+      const uint32_t c0 = g0 + (uint32_t)(j * G);
+      const uint4 w0 = ph(c0), w1 = ph(c0 + 1u), w2 = ph(c0 + 2u), w3 = ph(c0 + 3u);
+      uint32_t m[4] = {min4_u32(w0), min4_u32(w1), min4_u32(w2), min4_u32(w3)};
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        uint32_t mu = m[u * G];
+#pragma unroll
+        for (int g = 1; g < G; ++g) mu = min(mu, m[u * G + g]);
+        if (mu < bk) flagged |= 1ull << (j + u);
+      }
+    } else {
+#pragma unroll 1
+      for (int u = 0; u < U; ++u) one(j + u);
+    }
+  }
+  for (; j < nvec; ++j) one(j);
+  return flagged;
+}
+
+// ------------------------------------------------------------------------------------------------
 // The kernel.
 // ------------------------------------------------------------------------------------------------
 // NDW data warps and one control warp per CTA; PER_SM CTAs resident per SM (the register budget).
@@ -140,7 +254,7 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
   constexpr int ES = Tr::ESIZE;
   extern __shared__ __align__(128) unsigned char dyn[];
   SampleSmem& sh = *reinterpret_cast<SampleSmem*>(dyn);
-  unsigned char* slice = dyn + sample_slice_offset();
+  unsigned char* slices = dyn + sample_slice_offset();   // p.nbuf buffers of one slice each
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int C = gridDim.x, crank = blockIdx.x;
   const int q = p.q;
@@ -151,7 +265,10 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
   const int64_t warp_bytes = (int64_t)32 * q * 16;
 
   if (t == 0) {
-    for (int w = 0; w < kDataWarps; ++w) mbar_init(&sh.lbar[w], 1);
+    for (int w = 0; w < kDataWarps; ++w) {
+      mbar_init(&sh.lbar[0][w], 1);
+      mbar_init(&sh.lbar[1][w], 1);
+    }
     mbar_init(&sh.xbar[0], (uint32_t)C);
     mbar_init(&sh.xbar[1], (uint32_t)C);
     sh.acnt[0] = 0u;
@@ -169,28 +286,36 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
   if (warp < kDataWarps) {
     // =============================== data warps ===============================
     const int td = t;
-    const uint4* mine = reinterpret_cast<const uint4*>(slice) + (size_t)td * q;
+    const int nbuf = p.nbuf > 1 ? 2 : 1;
+    const int64_t slice_bytes = (int64_t)kDataThreads * q * 16;
     auto cta_count = [&](int64_t n) -> int64_t {
       const int64_t c = n - cta_e0;
       return c < 0 ? 0 : (c > elems_cta ? elems_cta : c);
     };
-    auto issue_warp = [&](int64_t r) -> bool {
+    // this warp's region of row r's slice into buffer b
+    auto issue_warp = [&](int64_t r, int b) -> bool {
       const int64_t b16 = (cta_count(row_len(r)) * ES) & ~(int64_t)15;
       const int64_t lo = (int64_t)warp * warp_bytes;
       int64_t nb = b16 - lo;
       nb = nb < 0 ? 0 : (nb > warp_bytes ? warp_bytes : nb);
-      mbar_arrive_expect_tx(&sh.lbar[warp], (uint32_t)nb);
+      mbar_arrive_expect_tx(&sh.lbar[b][warp], (uint32_t)nb);
       if (nb && !p.drop_loads) {
-        bulk_copy_g2s(slice + lo, p.x + ((int64_t)r * p.ld + cta_e0) * ES + lo, (uint32_t)nb, &sh.lbar[warp]);
+        bulk_copy_g2s(slices + b * slice_bytes + lo, p.x + ((int64_t)r * p.ld + cta_e0) * ES + lo, (uint32_t)nb,
+                      &sh.lbar[b][warp]);
         return true;
       }
       return false;
     };
-    int uses = 0;
-    bool pending = false, inflight = false, dead = false;
-    if (p.tma && first < p.B) {
-      if (lane == 0) inflight = issue_warp(first);
-      pending = true;
+    // per buffer: completed phases, a copy armed and not yet waited for, a copy in flight
+    int uses[2] = {0, 0};
+    bool pending[2] = {false, false}, inflight[2] = {false, false};
+    bool dead = false;
+    if (p.tma) {
+      for (int b = 0; b < nbuf; ++b) {
+        if (first + b * G >= p.B) break;
+        if (lane == 0) inflight[b] = issue_warp(first + b * G, b);
+        pending[b] = true;
+      }
     }
 
     for (int64_t k = 0;; ++k) {
@@ -205,15 +330,18 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
       }
       const int nfull = thr_n / VE;
       const unsigned char* grow = p.x + ((int64_t)row * p.ld + cta_e0) * ES;
+      const int buf = (int)(k % nbuf);
+      unsigned char* slice = slices + buf * slice_bytes;
+      const uint4* mine = reinterpret_cast<const uint4*>(slice) + (size_t)td * q;
 
       // ---- the slice ----
       bool timeout = dead;
       if (p.tma) {
-        if (pending && !dead) {
-          if (mbar_wait_bounded(&sh.lbar[warp], (uint32_t)(uses & 1), p.wait_cycles)) {
-            ++uses;
-            pending = false;
-            inflight = false;
+        if (pending[buf] && !dead) {
+          if (mbar_wait_bounded(&sh.lbar[buf][warp], (uint32_t)(uses[buf] & 1), p.wait_cycles)) {
+            ++uses[buf];
+            pending[buf] = false;
+            inflight[buf] = false;
           } else {
             timeout = true;
           }
@@ -236,56 +364,24 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
       }
       __syncwarp();   // the boundary search reads the chunks of the warp's other threads
       bool refilled = false;
+      // after its last pass over this row the warp re-arms its region of this buffer with the row nbuf rows on
       auto refill = [&]() {
         if (refilled) return;
         refilled = true;
-        const int64_t nr = row + G;
+        const int64_t nr = row + nbuf * G;
         if (!p.tma || dead || nr >= p.B) return;
         __syncwarp();
         if (lane == 0) {
           fence_proxy_async_shared();
-          inflight = issue_warp(nr);
+          inflight[buf] = issue_warp(nr, buf);
         }
-        pending = true;
+        pending[buf] = true;
       };
 
       // ---- P1: maximum and non-finite check ----
       {
-        float mx = -INFINITY, nf = 0.f;
-        if constexpr (VE == 8) {
-          const __nv_bfloat162 zero2 = __float2bfloat162_rn(0.f);
-          __nv_bfloat162 mx2 = __float2bfloat162_rn(-INFINITY), nf2 = zero2;
-          for (int j = 0; j < nfull; ++j) {
-            const uint4 v = mine[j];
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              const __nv_bfloat162 a = Tr::pair(w[h]);
-              mx2 = __hmax2(mx2, a);
-              nf2 = __hfma2(a, zero2, nf2);   // x * 0 is NaN for +-inf and NaN
-            }
-          }
-          mx = fmaxf(__low2float(mx2), __high2float(mx2));
-          nf = (__low2float(nf2) != 0.f || __high2float(nf2) != 0.f) ? 1.f : 0.f;
-        } else {
-          for (int j = 0; j < nfull; ++j) {
-            float x[VE];
-            Tr::values(mine[j], x);
-#pragma unroll
-            for (int i = 0; i < VE; ++i) {
-              mx = fmaxf(mx, x[i]);
-              nf = fmaf(x[i], 0.f, nf);
-            }
-          }
-        }
-        const int tail = thr_n - nfull * VE;
-        if (tail) {
-          float x[VE];
-          Tr::values(mine[nfull], x);
-#pragma unroll
-          for (int i = 0; i < VE; ++i)
-            if (i < tail) { mx = fmaxf(mx, x[i]); nf = fmaf(x[i], 0.f, nf); }
-        }
+        float nf;
+        float mx = max_pass<T>(mine, thr_n, nf);
         const uint32_t flags = __reduce_or_sync(kFullMask, ((nf != 0.f) ? 1u : 0u) | (timeout ? 2u : 0u));
         mx = warp_max_f(mx);
         if (lane == 0) sh.dp[warp][0] = make_uint4(__float_as_uint(mx), flags, 0u, 0u);
@@ -304,8 +400,8 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
       uint32_t cm_thr, cm_pre;
       {
         const float c1 = sh.ctl.c1;
-        const MassPart mp = sh.ctl.minp_on ? mass_pass_body<T, true>(mine, thr_n, M, c1, sh.ctl.kmin32)
-                                           : mass_pass_body<T, false>(mine, thr_n, M, c1, 0u);
+        const MassPart mp = sh.ctl.minp_on ? mass_pass<T, true>(mine, thr_n, M, c1, sh.ctl.kmin32)
+                                           : mass_pass<T, false>(mine, thr_n, M, c1, 0u);
         uint32_t incl = mp.cm;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -494,47 +590,9 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
           if (lim >= 0) jfull = (int)(lim / VE + 1 < (int64_t)nfull ? lim / VE + 1 : (int64_t)nfull);
         }
         const uint32_t g0 = (uint32_t)(thr_e0 >> 2);
-        const int nvec = (thr_n + VE - 1) / VE;
-        unsigned long long flagged = 0ull;
-        for (int j = 0; j < nvec; ++j) {
-          const uint4 v = mine[j];
-          if (all_cand) {
-            float x[VE];
-            Tr::values(v, x);
-            const int cnt = j < nfull ? VE : thr_n - nfull * VE;
-            const int64_t e0 = thr_e0 + (int64_t)j * VE;
-            bool any = false;
-#pragma unroll
-            for (int i = 0; i < VE; ++i) any |= i < cnt && (x[i] > xP || (x[i] == xP && e0 + i <= (int64_t)It));
-            if (any) flagged |= 1ull << j;
-            continue;
-          }
-          uint32_t bmin = 0xFFFFFFFFu;
-          if (j < jfull && Tr::all_ge(v, xP)) {
-#pragma unroll
-            for (int g = 0; g < VE / 4; ++g) {
-              const uint4 w4 = philox4x32_10(make_uint4(g0 + (uint32_t)(j * (VE / 4) + g), rid, st_lo, st_hi), key);
-              bmin = min(bmin, min(min(w4.x, w4.y), min(w4.z, w4.w)));
-            }
-          } else {
-            float x[VE];
-            Tr::values(v, x);
-            const int cnt = j < nfull ? VE : thr_n - nfull * VE;
-            const int64_t e0 = thr_e0 + (int64_t)j * VE;
-            uint32_t gmask = 0u;
-#pragma unroll
-            for (int i = 0; i < VE; ++i)
-              if (i < cnt && (x[i] > xP || (x[i] == xP && e0 + i <= (int64_t)It))) gmask |= 1u << (i >> 2);
-            if (!gmask) continue;
-#pragma unroll
-            for (int g = 0; g < VE / 4; ++g) {
-              if (!((gmask >> g) & 1u)) continue;
-              const uint4 w4 = philox4x32_10(make_uint4(g0 + (uint32_t)(j * (VE / 4) + g), rid, st_lo, st_hi), key);
-              bmin = min(bmin, min(min(w4.x, w4.y), min(w4.z, w4.w)));
-            }
-          }
-          if (bmin < bk) flagged |= 1ull << j;
-        }
+        unsigned long long flagged =
+            all_cand ? kept_vectors<T>(mine, thr_n, thr_e0, xP, It)
+                     : draw_scan<T>(mine, thr_n, thr_e0, jfull, xP, It, g0, rid, st_lo, st_hi, key.k0, key.k1, bk);
         // flagged vectors: the kept tokens whose word passes the bound get the exact perturbed score
         float bscore = -INFINITY, bs = 0.f;
         int32_t bidx = 0x7FFFFFFF;
@@ -581,7 +639,8 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
       refill();
     }
     // a bulk copy of this warp that may still be landing in shared memory (after a timed-out load)
-    if (p.tma && inflight) (void)mbar_wait_bounded(&sh.lbar[warp], (uint32_t)(uses & 1), 4000000000LL);
+    for (int b = 0; b < nbuf; ++b)
+      if (p.tma && inflight[b]) (void)mbar_wait_bounded(&sh.lbar[b][warp], (uint32_t)(uses[b] & 1), 4000000000LL);
   } else {
     // =============================== control warp ===============================
     ClusterXchg X;
@@ -916,6 +975,8 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
             cp_mode = 2;
           }
         }
+        // top-p keeping the first maximum alone is the shortest cut: no radix search for top-k
+        if (cp_mode == 1 && cp.kept() == 1 && ck_mode == 2) ck_mode = 0;
         if (ck_mode == 1 || cp_mode == 1) path |= PATH_MAXGROUP;
         if (minp_on) {
           const uint32_t rkm = (Tr::KB == 32) ? minkey_ge : (minkey_ge >> 16);

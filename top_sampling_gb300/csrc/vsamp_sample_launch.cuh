@@ -12,9 +12,11 @@ static vsamp_status launch_sample_cfg(Params p, int64_t B, int esize, const Devi
   constexpr int kDataThreads = NDW * 32;
   constexpr int kSampleThreads = kDataThreads + 32;
   Geometry g;
-  vsamp_status st = choose_geometry_for(p.V, esize, B, d, kDataThreads, sample_slice_offset(), PER_SM, g);
+  vsamp_status st = choose_geometry_for(p.V, esize, B, d, kDataThreads, sample_slice_offset(), PER_SM, g,
+                                        env_int("VSAMP_NBUF", 1) == 2 ? 2 : 1);
   if (st != VSAMP_OK) return st;
   p.q = g.q;
+  p.nbuf = g.nbuf;
   const long long wc = env_ll("VSAMP_WAIT_CYCLES", 0);
   p.wait_cycles = wc > 0 ? wc : 4000000000LL;   // ~2 s at the maximum SM clock
   p.drop_loads = env_int("VSAMP_TEST_DROP_LOADS", 0) != 0 ? 1 : 0;

@@ -1,21 +1,6 @@
-// The split-vocabulary sampling path: vsamp_sample with a caller-provided workspace.
-//
-// Every row is cut into fixed 64 KB chunks (32768 bf16 / 16384 fp32 logits); two streaming kernels sweep all
-// (row, chunk) pairs of the batch with no per-row synchronisation inside a kernel:
-//   split_stats_kernel  reads each chunk once from HBM and computes, in one pass, its maximum, its count of
-//                       maxima and its mass sum(2^((x - m_c) * log2e / T)): every thread keeps a running
-//                       maximum and a binary32 sum relative to it (rescaled when the maximum grows), and the
-//                       threads' sums are rescaled to the chunk maximum m_c and added in 2^-40 fixed point.
-//                       The last chunk of a row to finish (an atomic ticket) plans
-//                       the row with the whole CTA: M = max m_c, S = sum of the chunk masses rescaled to M,
-//                       the top-k / top-p / min-p cut (radix rounds and min-p statistics scan the row from
-//                       L2 when the cut leaves the maximum's tie group), the cut's last kept index, and the
-//                       draw's prune bound. Rows that keep one token get their outputs here.
-//   split_draw_kernel   reads each chunk again (from L2) and draws: one Philox4x32-10 word per kept token, the
-//                       prune bound, the exact perturbed score of the few candidates, and a 64-bit atomic
-//                       maximum of (score, index) per row, published by every warp. The last warp of a row
-//                       certifies the draw and writes the row's outputs.
-// Chunking depends only on V, so results are deterministic and do not depend on the batch.
+// The split-vocabulary sampling path (vsamp_sample_ws): every row is cut into fixed 32 KB chunks and two
+// persistent streaming kernels sweep all (row, chunk) pairs of the batch (see the section "The streaming
+// sampler" below). Chunking depends only on V, so results are deterministic and do not depend on the batch.
 #pragma once
 
 #include "vsamp_row.cuh"
@@ -23,8 +8,8 @@
 namespace vsamp {
 
 constexpr int kSplitThreads = 256;
-constexpr int kChunkBytes = 65536;   // 256 threads x 16 vectors of 16 bytes
-constexpr int kSplitVec = 16;        // vectors per thread
+constexpr int kStreamVec = 8;        // 16-byte vectors per thread per chunk
+constexpr int kChunkBytes = kSplitThreads * kStreamVec * 16;   // 32 KB
 
 struct ChunkStat {                   // 16 bytes per (row, chunk)
   float m;                           // chunk maximum (NaN flags a non-finite value)
@@ -32,8 +17,10 @@ struct ChunkStat {                   // 16 bytes per (row, chunk)
   unsigned long long s;              // sum of 2^((x - m) * c1), 2^-40 fixed point
 };
 
+constexpr int32_t kDeferIndex = -2;   // RowPlan::It: the draw kernel finds the cut's last kept index
+
 struct RowPlan {                     // 128 bytes per row
-  uint32_t done1, done2;             // chunks finished in each kernel (the last chunk resets its counter)
+  uint32_t done1, done2;             // reserved (zero)
   unsigned long long best;           // draw: (orderable score << 32) | (0xFFFFFFFF - index); 0 = none
   int32_t status;                    // the row's status; the draw kernel skips rows that are not VSAMP_OK
   int32_t draw;                      // 1: the draw kernel draws the token; 0: the outputs are written
@@ -44,7 +31,10 @@ struct RowPlan {                     // 128 bytes per row
   uint32_t rid, st_lo, st_hi, k0, k1;
   int32_t passes, rounds, path;
   uint32_t kept;
-  uint32_t pad[7];
+  int32_t cb;                        // It == kDeferIndex: the chunk holding the cut's last kept maximum,
+  uint32_t cneed;                    //   which is the cneed-th maximum of that chunk (the draw finds it)
+  int32_t one;                       // the cut keeps one token (the first maximum): no draw
+  uint32_t pad[4];
 };
 static_assert(sizeof(RowPlan) == 128, "RowPlan layout");
 static_assert(sizeof(ChunkStat) == 16, "ChunkStat layout");
@@ -99,6 +89,16 @@ __device__ __forceinline__ int load_vec(const Params& p, const unsigned char* xr
     v = make_uint4(w[0], w[1], w[2], w[3]);
   }
   return cnt;
+}
+
+// A chunk statistic written by another CTA of the same launch: read through L2 (L1 is not coherent).
+__device__ __forceinline__ ChunkStat load_stat(const ChunkStat* a) {
+  const uint4 v = __ldcg(reinterpret_cast<const uint4*>(a));
+  ChunkStat cs;
+  cs.m = __uint_as_float(v.x);
+  cs.cnt = v.y;
+  cs.s = ((unsigned long long)v.w << 32) | v.z;
+  return cs;
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -185,7 +185,7 @@ __device__ __forceinline__ uint32_t block_scan_u32(uint32_t v, uint32_t& total, 
 }
 
 // ------------------------------------------------------------------------------------------------
-// The row planner: the last chunk's CTA of split_stats_kernel, once every chunk of the row is done.
+// The row planner: the CTA whose chunk completes the row in stream_stats_kernel.
 // ------------------------------------------------------------------------------------------------
 template <typename T>
 struct RowPlanner {
@@ -209,8 +209,12 @@ struct RowPlanner {
       if (vi < nvec) {
         const int64_t e = vi * VE;
         cnt = n - e >= VE ? VE : (int)(n - e);
+        if (cnt == VE && p.tma) {
+          Tr::values(reinterpret_cast<const uint4*>(xr)[vi], x);
+        } else {
 #pragma unroll
-        for (int i = 0; i < VE; ++i) x[i] = i < cnt ? Tr::load_global(xr, e + i) : -INFINITY;
+          for (int i = 0; i < VE; ++i) x[i] = i < cnt ? Tr::load_global(xr, e + i) : -INFINITY;
+        }
       } else {
 #pragma unroll
         for (int i = 0; i < VE; ++i) x[i] = -INFINITY;
@@ -357,30 +361,49 @@ struct RowPlanner {
   }
 
   // the index of the need-th element (1-based, index order) equal to xv, visiting vectors from begin_vec;
-  // -1 if there are fewer
+  // -1 if there are fewer. Tiles of 256 threads x 4 consecutive vectors, one block scan per tile.
   __device__ int32_t nth_equal(float xv, unsigned long long need, int64_t begin_vec) {
+    constexpr int PV = 4;
+    const unsigned char* xr = p.x + (int64_t)row * p.ld * Tr::ESIZE;
+    const int64_t nvec = (n + VE - 1) / VE;
+    const int t = threadIdx.x;
     int32_t found = -1;
     unsigned long long before = 0;
-    for_each_tile(begin_vec, [&](int64_t, int64_t e, const float (&x)[VE], int cnt) {
+    for (int64_t v0 = begin_vec; v0 < nvec; v0 += (int64_t)kSplitThreads * PV) {
+      float x[PV][VE];
+      int cnt[PV];
       uint32_t c = 0;
 #pragma unroll
-      for (int i = 0; i < VE; ++i) c += (i < cnt && x[i] == xv) ? 1u : 0u;
+      for (int q = 0; q < PV; ++q) {
+        const int64_t vi = v0 + (int64_t)t * PV + q;
+        const int64_t e = vi * VE;
+        cnt[q] = vi < nvec ? (n - e >= VE ? VE : (int)(n - e)) : 0;
+        if (cnt[q] == VE && p.tma) {
+          Tr::values(reinterpret_cast<const uint4*>(xr)[vi], x[q]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < VE; ++i) x[q][i] = i < cnt[q] ? Tr::load_global(xr, e + i) : -INFINITY;
+        }
+#pragma unroll
+        for (int i = 0; i < VE; ++i) c += (i < cnt[q] && x[q][i] == xv) ? 1u : 0u;
+      }
       uint32_t tot;
       const uint32_t pre = block_scan_u32(c, tot, sh);
-      const bool here = before + pre < need && need <= before + pre + c;
-      if (here) {
+      if (before + pre < need && need <= before + pre + c) {
         unsigned long long seen = before + pre;
 #pragma unroll
-        for (int i = 0; i < VE; ++i)
-          if (i < cnt && x[i] == xv && ++seen == need) sh.i[0] = (int32_t)(e + i);
+        for (int q = 0; q < PV; ++q)
+#pragma unroll
+          for (int i = 0; i < VE; ++i)
+            if (i < cnt[q] && x[q][i] == xv && ++seen == need) sh.i[0] = (int32_t)((v0 + (int64_t)t * PV + q) * VE + i);
       }
       const bool done = before + tot >= need;
       before += tot;
       __syncthreads();
       if (done) found = sh.i[0];
       __syncthreads();
-      return !done;
-    });
+      if (done) break;
+    }
     ++passes;
     return found;
   }
@@ -403,7 +426,7 @@ static __device__ __noinline__ void plan_row(const Params p, RowPlan* plans, con
   float m = -INFINITY;
   uint32_t nonfin = 0;
   for (int k = t; k < nchunks; k += kSplitThreads) {
-    const float mk = stats[row * nchunks + k].m;
+    const float mk = load_stat(stats + row * nchunks + k).m;
     if (mk != mk) nonfin = 1;
     else m = fmaxf(m, mk);
   }
@@ -412,7 +435,7 @@ static __device__ __noinline__ void plan_row(const Params p, RowPlan* plans, con
   unsigned long long Sp = 0;
   uint32_t cMp = 0;
   for (int k = t; k < nchunks; k += kSplitThreads) {
-    const ChunkStat cs = stats[row * nchunks + k];
+    const ChunkStat cs = load_stat(stats + row * nchunks + k);
     if (cs.m == M) {
       Sp += cs.s;
       cMp += cs.cnt;
@@ -451,15 +474,15 @@ static __device__ __noinline__ void plan_row(const Params p, RowPlan* plans, con
       }
     }
   };
-  // the row's chunk statistics are zeroed once used and its counter reset, so that every completed call
-  // leaves the workspace's counters and statistics zero whatever the next call's B and V
+  // the row's status, whether the draw kernel draws it, and its draw slot (the atomic maximum) cleared
   auto finish = [&](int st, int draw) {
     __syncthreads();
-    for (int k = t; k < nchunks; k += kSplitThreads) stats[row * nchunks + k] = ChunkStat{0.f, 0u, 0ull};
     if (t == 0) {
       pl.status = st;
       pl.draw = draw;
       pl.done1 = 0u;
+      pl.done2 = 0u;
+      pl.best = 0ull;
     }
   };
   if (status != VSAMP_OK) {
@@ -511,8 +534,11 @@ static __device__ __noinline__ void plan_row(const Params p, RowPlan* plans, con
         cp_mode = 2;
       }
     }
+    // top-p keeping the first maximum alone is the shortest cut: no radix search for top-k, no min-p pass
+    const bool cp_one = cp_mode == 1 && cp.kept() == 1;
+    if (cp_one && ck_mode == 2) ck_mode = 0;
     if (ck_mode == 1 || cp_mode == 1) path |= PATH_MAXGROUP;
-    if (minp_on) {
+    if (minp_on && !cp_one) {
       // min-p keeps w >= minp <=> x >= x* = M + T ln(minp) (an unevaluated sum; the threshold is the
       // smallest fp32 value >= x*): the kept group ends with the smallest key at or above it
       const float L = logf(minp);
@@ -565,6 +591,8 @@ static __device__ __noinline__ void plan_row(const Params p, RowPlan* plans, con
   const bool one_token = greedy || kept == 1;
   float xP = Tr::value_of_rkey(fin.rk);
   int32_t It = kAllIndex;
+  int32_t cb_def = -1;
+  uint32_t cneed_def = 0u;
   if (fin.whole && !one_token) {
     if (fin.above == 0 && fin.cnt_eq == 0) xP = -INFINITY;   // every element
   } else if (fin.rk == rkM) {
@@ -576,7 +604,7 @@ static __device__ __noinline__ void plan_row(const Params p, RowPlan* plans, con
       const int64_t k = k0 + t;
       uint32_t ck = 0;
       if (k < nchunks) {
-        const ChunkStat cs = stats[row * nchunks + k];
+        const ChunkStat cs = load_stat(stats + row * nchunks + k);
         ck = cs.m == M ? cs.cnt : 0u;
       }
       uint32_t tot;
@@ -591,19 +619,20 @@ static __device__ __noinline__ void plan_row(const Params p, RowPlan* plans, con
       if (done) cb = (int64_t)sh.bq[2];
       __syncthreads();
     }
-    const unsigned long long skip = sh.bq[3];
-    const int64_t begin_vec = cb * (split_chunk_elems(Tr::ESIZE) / VE);
-    It = P.nth_equal(M, need - skip, begin_vec);
+    // the draw kernel finds it in chunk cb, which it holds in shared memory anyway
+    cb_def = (int32_t)cb;
+    cneed_def = (uint32_t)(need - sh.bq[3]);
+    It = kDeferIndex;
   } else {
     const unsigned long long need = fin.whole ? fin.cnt_eq : fin.need;
     It = P.nth_equal(xP, need, 0);
   }
-  if (It < 0) {   // cannot happen with consistent counts; reported as an error
+  if (It < 0 && It != kDeferIndex) {   // cannot happen with consistent counts; reported as an error
     write_outputs(-1, __int_as_float(0x7FC00000), VSAMP_ERR_INVALID_ARG, 0u);
     finish(VSAMP_ERR_INVALID_ARG, 0);
     return;
   }
-  if (one_token) {
+  if (one_token && It != kDeferIndex) {
     // the first maximum; (x - M) / T = 0
     write_outputs(It, fminf(-logS, 0.f), VSAMP_OK, (uint32_t)kept);
     finish(VSAMP_OK, 0);
@@ -635,310 +664,670 @@ static __device__ __noinline__ void plan_row(const Params p, RowPlan* plans, con
     pl.rounds = P.rounds;
     pl.path = path;
     pl.kept = (uint32_t)kept;
+    pl.cb = cb_def;
+    pl.cneed = cneed_def;
+    pl.one = one_token ? 1 : 0;
   }
   finish(VSAMP_OK, 1);
 }
 
 // ------------------------------------------------------------------------------------------------
-// Kernel 1: chunk statistics in one pass; the last chunk of each row plans the row.
+// The streaming sampler: four kernels, ordered by the stream.
+//   stream_stats_kernel  persistent, over (row, chunk) items in a static schedule (CTA b takes items b, b + G,
+//                        b + 2G, ...; item i is chunk i mod nc of row i / nc): each chunk read once from HBM,
+//                        its maximum m_c, count of maxima and mass relative to m_c in 2^-40 fixed point summed
+//                        per 16-byte vector.
+//   stream_plan_kernel   one CTA per row: the row's plan from its chunk statistics (radix rounds over the row
+//                        only when the cut leaves the maximum's tie group).
+//   stream_draw_kernel   persistent, the same schedule: each chunk read again (mostly from L2) with the row's
+//                        128-byte plan copied beside it; one Philox4x32-10 word per kept token, the prune bound,
+//                        exact scores of the few candidates; each CTA's best meets the row's in a 64-bit atomic
+//                        maximum.
+//   stream_finish_kernel one CTA per row: certify the draw and write the outputs.
+// The persistent kernels bulk-copy the chunk of the item after next into the shared-memory buffer their last
+// item has released, so copies stream while they compute. No CTA waits for another inside a kernel.
 // ------------------------------------------------------------------------------------------------
+struct StreamHeader {       // the first 256 bytes of the workspace (reserved, left zero)
+  uint32_t reserved[64];
+};
+static_assert(sizeof(StreamHeader) == 256, "StreamHeader layout");
+
+struct StreamShared {
+  SplitShared sp;
+  unsigned long long bar[2];      // chunk buffers: the bulk copy of each use has landed
+  uint4 plan[2][8];               // draw kernel: the plan of each buffer's row (copied with the chunk)
+  uint4 dplan[8];                 // draw kernel: the plan read directly (after a copy timed out)
+  uint4 fplan[8];                 // the plan of a row being finished
+  int32_t issued[2];              // a copy into the buffer was started for its item
+  int32_t dead;                   // a copy timed out: no more copies start; items read global memory
+  int32_t flag;
+  int64_t frow;
+  float bs[8];                    // per-warp partials
+  int32_t bi[8];
+  float wm[8];
+  uint32_t wbad[8];
+  unsigned long long ws[8];
+  uint32_t wc[8];
+  uint32_t wt[8][kStreamVec];     // per-warp totals of a chunk scan
+  int32_t found;
+};
+
+// Item cursor of the static schedule: chunk `chunk` of row `row`; advance() steps by the grid size.
+struct ItemCursor {
+  int64_t row;
+  int chunk;
+  int64_t gq;   // grid size / nc
+  int gr;       // grid size % nc
+  int nc;
+  __device__ __forceinline__ ItemCursor(int64_t first, int64_t grid, int nchunks) {
+    nc = nchunks;
+    row = first / nc;
+    chunk = (int)(first % nc);
+    gq = grid / nc;
+    gr = (int)(grid % nc);
+  }
+  __device__ __forceinline__ void advance() {
+    row += gq;
+    chunk += gr;
+    if (chunk >= nc) { chunk -= nc; ++row; }
+  }
+};
+
+// A chunk of a row as one thread sees it: vector j of thread t is vector j * 256 + t of the chunk (element
+// e_begin + (j * 256 + t) * VE of the row). Vectors inside the bulk-copied part come from shared memory,
+// others (unaligned rows, the last partial vector of a row) from global memory.
 template <typename T>
-__global__ void __launch_bounds__(kSplitThreads) split_stats_kernel(const Params p, RowPlan* plans,
-                                                                    ChunkStat* stats, int nchunks) {
+struct ChunkView {
+  using Tr = Traits<T>;
+  static constexpr int VE = Tr::VE;
+  const unsigned char* xr;   // the row in global memory
+  int64_t V;                 // row length
+  int32_t tma;               // the row is 16-byte aligned
+  uint32_t sbuf;             // the chunk in shared memory (shared-window address)
+  int64_t e_begin;
+  int32_t smem_vecs;         // leading vectors of the chunk held in shared memory
+  __device__ __forceinline__ int get(int j, uint4& v) const {
+    const int vi = j * kSplitThreads + (int)threadIdx.x;
+    if (vi < smem_vecs) {
+      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                   : "r"(sbuf + (uint32_t)vi * 16u));
+      return VE;
+    }
+    // outside the copied part: 16-byte or element loads, fewer than VE past the row end
+    const int64_t e = e_begin + (int64_t)vi * VE;
+    const int64_t left = V - e;
+    const int cnt = left <= 0 ? 0 : (left >= VE ? VE : (int)left);
+    if (cnt == VE && tma) {
+      v = *reinterpret_cast<const uint4*>(xr + e * Tr::ESIZE);
+    } else {
+      uint32_t w[4] = {0u, 0u, 0u, 0u};
+      for (int i = 0; i < cnt; ++i) {
+        if (Tr::ESIZE == 4) w[i] = reinterpret_cast<const uint32_t*>(xr)[e + i];
+        else w[i >> 1] |= (uint32_t)reinterpret_cast<const uint16_t*>(xr)[e + i] << (16 * (i & 1));
+      }
+      v = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    return cnt;
+  }
+};
+
+// Bytes of a chunk the bulk copy brings into shared memory (a multiple of 16; the rest is read directly).
+template <typename T>
+__device__ __forceinline__ uint32_t chunk_copy_bytes(const Params& p, int c) {
+  const int64_t K = split_chunk_elems(Traits<T>::ESIZE);
+  const int64_t e_begin = (int64_t)c * K;
+  const int64_t n = p.V - e_begin < K ? p.V - e_begin : K;
+  return p.tma ? (uint32_t)((n * Traits<T>::ESIZE) & ~(int64_t)15) : 0u;
+}
+
+// S item: the chunk's statistics.
+template <typename T>
+__device__ __forceinline__ void stream_stats(const Params& p, ChunkStat* stats, int nc, int64_t row, int c, const uint4* sbuf, int32_t smem_vecs, StreamShared& ss) {
   using Tr = Traits<T>;
   constexpr int VE = Tr::VE;
-  __shared__ SplitShared sh;
-  const int64_t row = p.row0 + blockIdx.y;
-  const int64_t c = blockIdx.x;
-  const int t = threadIdx.x;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const float temp0 = p.temperature ? p.temperature[row] : 1.f;
   const float Teff = temp0 > 0.f ? temp0 : 1.f;   // greedy rows use T = 1 for their statistics
   const float c1 = kLog2e * (1.f / Teff);
-  const unsigned char* xr = p.x + (int64_t)row * p.ld * Tr::ESIZE;
   const int64_t K = split_chunk_elems(Tr::ESIZE);
+  const ChunkView<T> cv{p.x + (int64_t)row * p.ld * Tr::ESIZE, p.V, p.tma, smem_addr(sbuf), (int64_t)c * K, smem_vecs};
 
-  // ---- one pass: running maximum m_t, binary32 mass relative to it, its count, non-finite check.
-  // Vectors are loaded four at a time, the next four while the current ones are reduced. ----
-  float m_t = -INFINITY, s_t = 0.f, nf = 0.f;
-  uint32_t cnt_t = 0;
-  const float2 cc = make_float2(c1, c1);
-  auto vec = [&](const uint4& v, int cnt) {
-    float x[VE];
-    Tr::values(v, x);
-    float vm = -INFINITY;
-    if (cnt == VE) {
+  // ---- maximum and non-finite check ----
+  float mt = -INFINITY, nf = 0.f;
+  {
+    if constexpr (VE == 8) {
+      const __nv_bfloat162 zero2 = __float2bfloat162_rn(0.f);
+      __nv_bfloat162 ma = __float2bfloat162_rn(-INFINITY), mb = ma, na = zero2, nb = zero2;
+#pragma unroll 4
+      for (int j = 0; j < kStreamVec; ++j) {
+        uint4 v;
+        const int cnt = cv.get(j, v);
+        if (cnt == VE) {
+          ma = __hmax2(ma, __hmax2(Tr::pair(v.x), Tr::pair(v.y)));
+          mb = __hmax2(mb, __hmax2(Tr::pair(v.z), Tr::pair(v.w)));
+          na = __hfma2(Tr::pair(v.x), zero2, __hfma2(Tr::pair(v.y), zero2, na));
+          nb = __hfma2(Tr::pair(v.z), zero2, __hfma2(Tr::pair(v.w), zero2, nb));
+        } else if (cnt > 0) {
+          float x[VE];
+          Tr::values(v, x);
 #pragma unroll
-      for (int i = 0; i < VE; ++i) { vm = fmaxf(vm, x[i]); nf = fmaf(x[i], 0.f, nf); }
-    } else {
-#pragma unroll
-      for (int i = 0; i < VE; ++i)
-        if (i < cnt) { vm = fmaxf(vm, x[i]); nf = fmaf(x[i], 0.f, nf); }
-    }
-    if (vm > m_t) {
-      s_t = m_t == -INFINITY ? 0.f : s_t * ex2_approx((m_t - vm) * c1);
-      cnt_t = 0;
-      m_t = vm;
-    }
-    float w[VE];
-    if (cnt == VE) {
-      const float2 mM = make_float2(-m_t, -m_t);
-#pragma unroll
-      for (int h = 0; h < VE / 2; ++h) {
-        const float2 a = __fmul2_rn(__fadd2_rn(make_float2(x[2 * h], x[2 * h + 1]), mM), cc);
-        w[2 * h] = ex2_approx(a.x);
-        w[2 * h + 1] = ex2_approx(a.y);
+          for (int i = 0; i < VE; ++i)
+            if (i < cnt) { mt = fmaxf(mt, x[i]); nf = fmaf(x[i], 0.f, nf); }
+        }
       }
-#pragma unroll
-      for (int i = 0; i < VE; ++i) cnt_t += x[i] == m_t ? 1u : 0u;
+      ma = __hmax2(ma, mb);
+      na = __hadd2(na, nb);
+      mt = fmaxf(mt, fmaxf(__low2float(ma), __high2float(ma)));
+      if (__low2float(na) != 0.f || __high2float(na) != 0.f) nf = 1.f;
     } else {
+      float mb = -INFINITY, nb = 0.f;
+#pragma unroll 4
+      for (int j = 0; j < kStreamVec; ++j) {
+        uint4 v;
+        const int cnt = cv.get(j, v);
+        float x[VE];
+        Tr::values(v, x);
+        if (cnt == VE) {
+          mt = fmaxf(mt, fmaxf(x[0], x[1]));
+          mb = fmaxf(mb, fmaxf(x[2], x[3]));
+          nf = fmaf(x[0], 0.f, fmaf(x[1], 0.f, nf));
+          nb = fmaf(x[2], 0.f, fmaf(x[3], 0.f, nb));
+        } else {
 #pragma unroll
-      for (int i = 0; i < VE; ++i) {
-        const bool ok = i < cnt;
-        const float d = x[i] - m_t;
-        w[i] = ok ? ex2_approx(d * c1) : 0.f;
-        cnt_t += (ok && d == 0.f) ? 1u : 0u;
+          for (int i = 0; i < VE; ++i)
+            if (i < cnt) { mt = fmaxf(mt, x[i]); nf = fmaf(x[i], 0.f, nf); }
+        }
+      }
+      mt = fmaxf(mt, mb);
+      nf += nb;
+    }
+  }
+  {
+    const float wmx = warp_max_f(mt);
+    const uint32_t wb = __any_sync(kFullMask, nf != 0.f) ? 1u : 0u;
+    if (lane == 0) { ss.wm[warp] = wmx; ss.wbad[warp] = wb; }
+  }
+  __syncthreads();
+  float mc = ss.wm[0];
+  uint32_t bad = ss.wbad[0];
+#pragma unroll
+  for (int w = 1; w < kSplitThreads / 32; ++w) { mc = fmaxf(mc, ss.wm[w]); bad |= ss.wbad[w]; }
+
+  // ---- mass relative to the chunk maximum (2^-40 fixed point per vector) and the count of maxima ----
+  unsigned long long s = 0ull;
+  uint32_t cm = 0u;
+  if (!bad) {
+    const float2 mM = make_float2(-mc, -mc), cc = make_float2(c1, c1);
+    uint32_t cm2 = 0u;
+#pragma unroll 2
+    for (int j = 0; j < kStreamVec; ++j) {
+      uint4 v;
+      const int cnt = cv.get(j, v);
+      float x[VE];
+      Tr::values(v, x);
+      if (cnt == VE) {
+        float2 w2[VE / 2];
+#pragma unroll
+        for (int h = 0; h < VE / 2; ++h) {
+          const float2 e = __fmul2_rn(__fadd2_rn(make_float2(x[2 * h], x[2 * h + 1]), mM), cc);
+          w2[h] = make_float2(ex2_approx(e.x), ex2_approx(e.y));
+        }
+        float2 a;
+        if constexpr (VE == 8) a = __fadd2_rn(__fadd2_rn(w2[0], w2[2]), __fadd2_rn(w2[1], w2[3]));
+        else a = __fadd2_rn(w2[0], w2[1]);
+        s += mass_fx(a.x + a.y);
+        if constexpr (VE == 8) {
+          const __nv_bfloat162 M2 = __float2bfloat162_rn(mc);   // a bf16 value: exact
+          cm2 += __heq2_mask(Tr::pair(v.x), M2) & 0x00010001u;
+          cm2 += __heq2_mask(Tr::pair(v.y), M2) & 0x00010001u;
+          cm2 += __heq2_mask(Tr::pair(v.z), M2) & 0x00010001u;
+          cm2 += __heq2_mask(Tr::pair(v.w), M2) & 0x00010001u;
+        } else {
+#pragma unroll
+          for (int i = 0; i < VE; ++i) cm += x[i] == mc ? 1u : 0u;
+        }
+      } else if (cnt > 0) {
+        float w[VE];
+#pragma unroll
+        for (int i = 0; i < VE; ++i) {
+          const bool ok = i < cnt;
+          const float d = x[i] - mc;
+          w[i] = ok ? ex2_approx(d * c1) : 0.f;
+          cm += (ok && d == 0.f) ? 1u : 0u;
+        }
+#pragma unroll
+        for (int h = VE / 2; h >= 1; h >>= 1)
+#pragma unroll
+          for (int i = 0; i < h; ++i) w[i] += w[i + h];
+        s += mass_fx(w[0]);
       }
     }
-#pragma unroll
-    for (int h = VE / 2; h >= 1; h >>= 1)
-#pragma unroll
-      for (int i = 0; i < h; ++i) w[i] += w[i + h];
-    s_t += w[0];
-  };
-  constexpr int kBatch = 4;
-  const int64_t base = c * K + (int64_t)t * VE;
-  uint4 cur[kBatch], nxt[kBatch];
-  int ccnt[kBatch], ncnt[kBatch];
-#pragma unroll
-  for (int i = 0; i < kBatch; ++i) ccnt[i] = load_vec<T, false>(p, xr, base + (int64_t)i * kSplitThreads * VE, cur[i]);
-#pragma unroll 1
-  for (int j0 = 0; j0 < kSplitVec; j0 += kBatch) {
-    if (j0 + kBatch < kSplitVec) {
-#pragma unroll
-      for (int i = 0; i < kBatch; ++i)
-        ncnt[i] = load_vec<T, false>(p, xr, base + (int64_t)(j0 + kBatch + i) * kSplitThreads * VE, nxt[i]);
-    }
-#pragma unroll
-    for (int i = 0; i < kBatch; ++i)
-      if (ccnt[i]) vec(cur[i], ccnt[i]);
-#pragma unroll
-    for (int i = 0; i < kBatch; ++i) { cur[i] = nxt[i]; ccnt[i] = ncnt[i]; }
+    cm += (cm2 & 0xFFFFu) + (cm2 >> 16);
   }
-  const uint32_t bad = __syncthreads_or(nf != 0.f ? 1 : 0);
-  const float mc = block_max_f(m_t, sh);
-  // the threads' masses rescaled to the chunk maximum, in 2^-40 fixed point (binary64 for the product)
-  unsigned long long s = 0;
-  uint32_t cm = 0;
-  if (m_t == mc) {
-    s = __double2ull_rn((double)s_t * 1099511627776.0);
-    cm = cnt_t;
-  } else if (m_t != -INFINITY) {
-    s = __double2ull_rn((double)s_t * (double)ex2_approx((m_t - mc) * c1) * 1099511627776.0);
-  }
-  s = block_sum_u64(s, sh);
-  cm = block_sum_u32(cm, sh);
+  s = warp_sum_u64(s);
+  cm = warp_sum_u32(cm);
+  if (lane == 0) { ss.ws[warp] = s; ss.wc[warp] = cm; }
+  __syncthreads();
   if (t == 0) {
     ChunkStat cs;
     cs.m = bad ? __int_as_float(0x7FC00000) : mc;
-    cs.cnt = cm;
-    cs.s = s;
-    stats[row * nchunks + c] = cs;
-    __threadfence();
-    sh.ticket = atomicAdd(&plans[row].done1, 1u);
+    cs.cnt = 0u;
+    cs.s = 0ull;
+#pragma unroll
+    for (int w = 0; w < kSplitThreads / 32; ++w) { cs.s += ss.ws[w]; cs.cnt += ss.wc[w]; }
+    stats[row * nc + c] = cs;
   }
-  __syncthreads();
-  if (sh.ticket != (uint32_t)(nchunks - 1)) return;
-  __threadfence();
-  plan_row<T>(p, plans, stats, stats, nchunks, row, temp0, Teff, c1, sh);
 }
 
-// ------------------------------------------------------------------------------------------------
-// Kernel 2: the draw. Every chunk's best candidate meets the row's in a 64-bit atomic maximum; the last
-// chunk certifies it and writes the outputs.
-// ------------------------------------------------------------------------------------------------
+// The index of the need-th element (1-based, index order) equal to xv in a chunk; kNoIndex if there are
+// fewer. Element order inside the chunk is (vector j, thread t, lane i): one scan per j over the threads.
 template <typename T>
-__global__ void __launch_bounds__(kSplitThreads) split_draw_kernel(const Params p, RowPlan* plans, int nchunks) {
+__device__ __noinline__ int32_t chunk_nth_equal(const ChunkView<T>& cv, float xv, uint32_t need, StreamShared& ss) {
   using Tr = Traits<T>;
   constexpr int VE = Tr::VE;
-  constexpr int kWarps = kSplitThreads / 32;
-  __shared__ uint4 splan[8];
-  const int64_t row = p.row0 + blockIdx.y;
-  const int t = threadIdx.x, lane = t & 31;
-  RowPlan* gpl = plans + row;
-  if (t < 8) splan[t] = reinterpret_cast<const uint4*>(gpl)[t];
-  __syncthreads();
-  const RowPlan& pl = *reinterpret_cast<const RowPlan*>(splan);
-  if (pl.status != VSAMP_OK || !pl.draw) return;
-  const float M = pl.M, xP = pl.xP;
-  const int32_t It = pl.It;
-  const uint32_t bk = pl.bk, rid = pl.rid, st_lo = pl.st_lo, st_hi = pl.st_hi;
-  const bool all_cand = pl.all_cand != 0;
-  const PhiloxKey key{pl.k0, pl.k1};
-
-  // indices fit 32 bits (V < 2^31, checked on the host)
-  const unsigned char* xr = p.x + (int64_t)row * p.ld * Tr::ESIZE;
-  const int32_t n = (int32_t)p.V;
-  const int32_t K = (int32_t)split_chunk_elems(Tr::ESIZE);
-  const int32_t cbeg = (int32_t)blockIdx.x * K;
-  const int32_t ebase = cbeg + t * VE;              // the thread's vector j starts at ebase + j * kStep
-  constexpr int32_t kStep = kSplitThreads * VE;
-  // kept: x > xP, or x == xP and index <= It; the groups of four tokens of a vector holding a kept token
-  auto kept_groups = [&](const uint4& v, int32_t e0, int cnt) -> uint32_t {
-    if (cnt == VE && e0 + VE - 1 <= It && Tr::all_ge(v, xP)) return (1u << (VE / 4)) - 1u;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  uint32_t cnt[kStreamVec], inc[kStreamVec];
+#pragma unroll
+  for (int j = 0; j < kStreamVec; ++j) {
+    uint4 v;
+    const int n = cv.get(j, v);
     float x[VE];
     Tr::values(v, x);
-    uint32_t gm = 0u;
+    uint32_t c = 0;
 #pragma unroll
-    for (int i = 0; i < VE; ++i)
-      if (i < cnt && (x[i] > xP || (x[i] == xP && e0 + i <= It))) gm |= 1u << (i >> 2);
-    return gm;
-  };
-  const PhiloxRoundKeys rk(key);
-  auto min_word = [&](int32_t e0, uint32_t gmask) -> uint32_t {
-    uint32_t bmin = 0xFFFFFFFFu;
-    const uint32_t g0 = (uint32_t)e0 >> 2;
+    for (int i = 0; i < VE; ++i) c += (i < n && x[i] == xv) ? 1u : 0u;
+    cnt[j] = c;
+    inc[j] = c;
 #pragma unroll
-    for (int g = 0; g < VE / 4; ++g) {
-      if (!((gmask >> g) & 1u)) continue;
-      const uint4 w4 = philox4x32_10_rk(make_uint4(g0 + (uint32_t)g, rid, st_lo, st_hi), rk);
-      bmin = min(bmin, min(min(w4.x, w4.y), min(w4.z, w4.w)));
-    }
-    return bmin;
-  };
-
-  // ---- one Philox word per kept token; a vector is flagged when a kept token's word is below bk ----
-  uint32_t flagged = 0;
-  if (!all_cand && cbeg + K <= n && p.tma) {
-    // a whole aligned chunk: 16-byte loads, four vectors in flight ahead of the ones being drawn
-    const uint4* src = reinterpret_cast<const uint4*>(xr) + (ebase / VE);
-    constexpr int kBatch = 4;
-    uint4 cur[kBatch], nxt[kBatch];
-#pragma unroll
-    for (int i = 0; i < kBatch; ++i) cur[i] = __ldcs(src + i * kSplitThreads);
-#pragma unroll 1
-    for (int j0 = 0; j0 < kSplitVec; j0 += kBatch) {
-      if (j0 + kBatch < kSplitVec) {
-#pragma unroll
-        for (int i = 0; i < kBatch; ++i) nxt[i] = __ldcs(src + (j0 + kBatch + i) * kSplitThreads);
-      }
-      // every vector of the batch lies at or before the cut's last index: only the values decide
-      const bool below = ebase + (j0 + kBatch - 1) * kStep + VE - 1 <= It;
-#pragma unroll 1
-      for (int i = 0; i < kBatch; ++i) {
-        const int32_t e0 = ebase + (j0 + i) * kStep;
-        const uint32_t gm = (below && Tr::all_ge(cur[i], xP)) ? (1u << (VE / 4)) - 1u : kept_groups(cur[i], e0, VE);
-        if (gm && min_word(e0, gm) < bk) flagged |= 1u << (j0 + i);
-      }
-#pragma unroll
-      for (int i = 0; i < kBatch; ++i) cur[i] = nxt[i];
-    }
-  } else {
-    for (int j = 0; j < kSplitVec; ++j) {
-      const int32_t e0 = ebase + j * kStep;
-      uint4 v;
-      const int cnt = load_vec<T, true>(p, xr, e0, v);
-      if (cnt == 0) break;
-      const uint32_t gm = kept_groups(v, e0, cnt);
-      if (!gm) continue;
-      if (all_cand || min_word(e0, gm) < bk) flagged |= 1u << j;
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFullMask, inc[j], o);
+      if (lane >= o) inc[j] += y;
     }
   }
-  // ---- the flagged vectors' kept tokens: exact perturbed scores ----
+  if (lane == 31) {
+#pragma unroll
+    for (int j = 0; j < kStreamVec; ++j) ss.wt[warp][j] = inc[j];
+  }
+  if (t == 0) ss.found = kNoIndex;
+  __syncthreads();
+  uint32_t base = 0;
+#pragma unroll
+  for (int j = 0; j < kStreamVec; ++j) {
+    uint32_t before = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < kSplitThreads / 32; ++w) {
+      const uint32_t y = ss.wt[w][j];
+      if (w < warp) before += y;
+      tot += y;
+    }
+    const uint32_t excl = base + before + inc[j] - cnt[j];
+    if (cnt[j] && excl < need && need <= excl + cnt[j]) {
+      uint4 v;
+      const int n = cv.get(j, v);
+      float x[VE];
+      Tr::values(v, x);
+      uint32_t seen = excl;
+      const int64_t e0 = cv.e_begin + (int64_t)(j * kSplitThreads + t) * VE;
+#pragma unroll
+      for (int i = 0; i < VE; ++i)
+        if (i < n && x[i] == xv && ++seen == need) ss.found = (int32_t)(e0 + i);
+    }
+    base += tot;
+  }
+  __syncthreads();
+  return ss.found;
+}
+
+// Exact perturbed scores of one vector's kept tokens that pass the prune bound (every kept token when the
+// plan makes all of them candidates); the running arg-max is updated in place.
+template <typename T>
+__device__ __noinline__ void draw_exact(uint4 v, int cnt, int64_t e0, const RowPlan* plp, int32_t It, float& bscore,
+                                        int32_t& bidx) {
+  using Tr = Traits<T>;
+  constexpr int VE = Tr::VE;
+  const RowPlan& pl = *plp;
+  const bool all_cand = pl.all_cand != 0;
+  const PhiloxKey key{pl.k0, pl.k1};
+  float x[VE];
+  Tr::values(v, x);
+  uint32_t b[VE];
+#pragma unroll
+  for (int g = 0; g < VE / 4; ++g) {
+    const uint4 w4 = philox4x32_10(make_uint4((uint32_t)(e0 >> 2) + (uint32_t)g, pl.rid, pl.st_lo, pl.st_hi), key);
+    b[4 * g + 0] = w4.x; b[4 * g + 1] = w4.y; b[4 * g + 2] = w4.z; b[4 * g + 3] = w4.w;
+  }
+#pragma unroll
+  for (int i = 0; i < VE; ++i) {
+    if (!(i < cnt && (x[i] > pl.xP || (x[i] == pl.xP && e0 + i <= (int64_t)It)))) continue;
+    if (!all_cand && b[i] >= pl.bk) continue;
+    const float d = x[i] - pl.M;
+    const float sv = d * pl.invT;
+    if (!all_cand) {
+      const float w = ex2_approx(d * pl.c1);
+      const float u = fmaf((float)b[i], kTwoM32, kTwoM33);
+      if (!(u < w * pl.kappa * 1.00001f)) continue;
+    }
+    const float score = gumbel_score(sv, b[i]);
+    const int32_t idx = (int32_t)(e0 + i);
+    if (argmax_better(score, idx, bscore, bidx)) { bscore = score; bidx = idx; }
+  }
+}
+
+// D item: the draw over one chunk of a row, with the row's plan in shared memory.
+template <typename T>
+__device__ __forceinline__ void stream_draw(const Params& p, RowPlan* plans, int nc, int64_t row, int c,
+                                             const uint4* sbuf, int32_t smem_vecs, const RowPlan& pl,
+                                             StreamShared& ss) {
+  using Tr = Traits<T>;
+  constexpr int VE = Tr::VE;
+  constexpr int G = VE / 4;                 // groups of four tokens (one Philox counter) per vector
+  constexpr int NG = kStreamVec * G;        // groups per thread
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  RowPlan* gpl = plans + row;
   float bscore = -INFINITY;
   int32_t bidx = 0x7FFFFFFF;
-  if (flagged) {
-    const float invT = pl.invT, c1 = pl.c1, kappa = pl.kappa;
+  if (pl.status == VSAMP_OK && pl.draw) {
+    const float xP = pl.xP;
+    const int64_t K = split_chunk_elems(Tr::ESIZE);
+    const ChunkView<T> cv{p.x + (int64_t)row * p.ld * Tr::ESIZE, p.V, p.tma, smem_addr(sbuf), (int64_t)c * K, smem_vecs};
+    const int64_t e_begin = cv.e_begin;
+    // the cut's last kept index: inside the maximum's tie group it lies in chunk cb, found here
+    int32_t It = pl.It;
+    if (It == kDeferIndex) It = c < pl.cb ? kAllIndex : (c > pl.cb ? kNoIndex : chunk_nth_equal<T>(cv, xP, pl.cneed, ss));
+    const uint32_t bk = pl.bk;
+    const bool all_cand = pl.all_cand != 0;
+    if (pl.one) {
+      // one token is kept: the chunk holding it publishes it (score +inf), the others have nothing to do
+      if (c == pl.cb && It >= 0) { bscore = INFINITY; bidx = It; }
+    } else {
+    uint32_t gmask = 0u;   // kept groups: bit j * G + g
+#pragma unroll
+    for (int j = 0; j < kStreamVec; ++j) {
+      uint4 v;
+      const int cnt = cv.get(j, v);
+      const int32_t e0 = (int32_t)(e_begin + (int64_t)(j * kSplitThreads + t) * VE);
+      if (cnt == VE && e0 + VE - 1 <= It && Tr::all_ge(v, xP)) {
+        gmask |= ((1u << G) - 1u) << (j * G);
+      } else if (cnt > 0) {
+        float x[VE];
+        Tr::values(v, x);
+#pragma unroll
+        for (int i = 0; i < VE; ++i)
+          if (i < cnt && (x[i] > xP || (x[i] == xP && e0 + i <= It))) gmask |= 1u << (j * G + (i >> 2));
+      }
+    }
+    // ---- one Philox word per kept token: the smallest word of each vector's kept groups ----
+    uint32_t flagged = 0u;
+    if (all_cand) {
+#pragma unroll
+      for (int j = 0; j < kStreamVec; ++j)
+        if ((gmask >> (j * G)) & ((1u << G) - 1u)) flagged |= 1u << j;
+    } else if (gmask) {
+      const PhiloxRow ph(PhiloxKey{pl.k0, pl.k1}, pl.rid, pl.st_lo, pl.st_hi);
+      // counter word of group gi = j * G + g: (first element of vector j) / 4 + g
+      const uint32_t cb0 = (uint32_t)((e_begin + (int64_t)t * VE) >> 2);
+      auto ctr = [&](int gi) -> uint32_t { return cb0 + (uint32_t)((gi / G) * kSplitThreads * G + gi % G); };
+      uint32_t wmin = 0xFFFFFFFFu;
+      uint32_t vmin[kStreamVec];
+#pragma unroll
+      for (int j = 0; j < kStreamVec; ++j) vmin[j] = 0xFFFFFFFFu;
+      if (gmask == (uint32_t)((1ull << NG) - 1ull)) {
+        // every token of the thread's vectors is kept: straight-line, four counters at a time
+#pragma unroll
+        for (int g0 = 0; g0 < NG; g0 += 4) {
+          const uint4 a = ph(ctr(g0)), b = ph(ctr(g0 + 1)), cq = ph(ctr(g0 + 2)), d = ph(ctr(g0 + 3));
+          const uint32_t m[4] = {min4_u32(a), min4_u32(b), min4_u32(cq), min4_u32(d)};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) vmin[(g0 + k) / G] = min(vmin[(g0 + k) / G], m[k]);
+        }
+      } else {
+#pragma unroll 1
+        for (int gi = 0; gi < NG; ++gi)
+          if (((gmask >> gi) & 1u) && min4_u32(ph(ctr(gi))) < bk) flagged |= 1u << (gi / G);
+      }
+#pragma unroll
+      for (int j = 0; j < kStreamVec; ++j) wmin = min(wmin, vmin[j]);
+      if (wmin < bk) {
+#pragma unroll
+        for (int j = 0; j < kStreamVec; ++j)
+          if (vmin[j] < bk) flagged |= 1u << j;
+      }
+    }
+    // ---- flagged vectors: exact perturbed scores of the kept tokens that pass the bound ----
     while (flagged) {
       const int j = __ffs(flagged) - 1;
       flagged &= flagged - 1u;
-      const int32_t e0 = ebase + j * kStep;
       uint4 v;
-      const int cnt = load_vec<T, false>(p, xr, e0, v);
-      float x[VE];
-      Tr::values(v, x);
-      uint32_t b[VE];
-      const uint32_t g0 = (uint32_t)e0 >> 2;
-#pragma unroll
-      for (int g = 0; g < VE / 4; ++g) {
-        const uint4 w4 = philox4x32_10(make_uint4(g0 + (uint32_t)g, rid, st_lo, st_hi), key);
-        b[4 * g + 0] = w4.x; b[4 * g + 1] = w4.y; b[4 * g + 2] = w4.z; b[4 * g + 3] = w4.w;
-      }
-#pragma unroll
-      for (int i = 0; i < VE; ++i) {
-        if (!(i < cnt && (x[i] > xP || (x[i] == xP && e0 + i <= It)))) continue;
-        if (!all_cand && b[i] >= bk) continue;
-        const float d = x[i] - M;
-        const float sv = d * invT;
-        if (!all_cand) {
-          const float w = ex2_approx(d * c1);
-          const float u = fmaf((float)b[i], kTwoM32, kTwoM33);
-          if (!(u < w * kappa * 1.00001f)) continue;
-        }
-        const float score = gumbel_score(sv, b[i]);
-        const int32_t idx = e0 + i;
-        if (argmax_better(score, idx, bscore, bidx)) { bscore = score; bidx = idx; }
-      }
+      const int cnt = cv.get(j, v);
+      draw_exact<T>(v, cnt, e_begin + (int64_t)(j * kSplitThreads + t) * VE, &pl, It, bscore, bidx);
+    }
     }
   }
-  // ---- each warp's best -> the row's 64-bit maximum; the last warp of the row finishes it ----
+  // ---- the CTA's best -> the row's 64-bit maximum ----
   const ArgMax a = warp_argmax(ArgMax{bscore, bidx, 0.f});
-  uint32_t ticket = 0u;
-  if (lane == 0) {
-    if (a.idx != 0x7FFFFFFF) {
-      const unsigned long long k = ((unsigned long long)score_key(a.score) << 32) | (0xFFFFFFFFu - (uint32_t)a.idx);
+  if (lane == 0) { ss.bs[warp] = a.score; ss.bi[warp] = a.idx; }
+  __syncthreads();
+  if (t == 0) {
+    ArgMax b{ss.bs[0], ss.bi[0], 0.f};
+    for (int w = 1; w < kSplitThreads / 32; ++w)
+      if (argmax_better(ss.bs[w], ss.bi[w], b.score, b.idx)) b = ArgMax{ss.bs[w], ss.bi[w], 0.f};
+    if (b.idx != 0x7FFFFFFF) {
+      const unsigned long long k = ((unsigned long long)score_key(b.score) << 32) | (0xFFFFFFFFu - (uint32_t)b.idx);
       atomicMax(&gpl->best, k);
     }
-    __threadfence();
-    ticket = atomicAdd(&gpl->done2, 1u);
   }
-  ticket = __shfl_sync(kFullMask, ticket, 0);
-  if (ticket != (uint32_t)(nchunks * kWarps - 1)) return;
-  __threadfence();
-  // ---- the last warp: certify, write the outputs, reset the row's draw state ----
-  unsigned long long best = 0ull;
-  if (lane == 0) best = atomicAdd(&gpl->best, 0ull);
-  best = __shfl_sync(kFullMask, best, 0);
-  const float gscore = best ? score_of_key((uint32_t)(best >> 32)) : -INFINITY;
-  const int32_t gidx = best ? (int32_t)(0xFFFFFFFFu - (uint32_t)best) : -1;
-  const float B0 = pl.B0;
-  int32_t tok = gidx;
-  int path = pl.path;
-  if (!(all_cand || (best && gscore > B0 + 1e-4f * fmaxf(1.f, fabsf(B0))))) {
-    // the prune bound did not certify the draw (probability ~1e-9): every kept token of the row, exactly
-    path |= PATH_FALLBACK;
-    const float invT = pl.invT;
-    float fs = -INFINITY;
-    int32_t fi = 0x7FFFFFFF;
-    for (int32_t e = lane; e < n; e += 32) {
-      const float xv = Tr::load_global(p.x, (int64_t)row * p.ld + e);
-      if (!(xv > xP || (xv == xP && e <= It))) continue;
-      const uint4 w4 = philox4x32_10(make_uint4((uint32_t)e >> 2, rid, st_lo, st_hi), key);
-      const float score = gumbel_score((xv - M) * invT, philox_word(w4, (int)(e & 3)));
-      if (argmax_better(score, e, fs, fi)) { fs = score; fi = e; }
+}
+
+// stream_finish_kernel: one CTA per row certifies the draw, writes the outputs and resets the row's draw
+// slot. Rows whose plan does not draw were finished by the planner.
+template <typename T>
+__global__ void __launch_bounds__(kSplitThreads) stream_finish_kernel(const Params p, RowPlan* plans) {
+  using Tr = Traits<T>;
+  __shared__ uint4 fplan[8];
+  __shared__ float bs[8];
+  __shared__ int32_t bi[8];
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int64_t row = blockIdx.x;
+  RowPlan* gpl = plans + row;
+  if (t < 8) fplan[t] = reinterpret_cast<const uint4*>(gpl)[t];
+  __syncthreads();
+  const RowPlan& pl = *reinterpret_cast<const RowPlan*>(fplan);
+  if (pl.status == VSAMP_OK && pl.draw) {
+    const unsigned long long best = pl.best;
+    const float gscore = best ? score_of_key((uint32_t)(best >> 32)) : -INFINITY;
+    int32_t tok = best ? (int32_t)(0xFFFFFFFFu - (uint32_t)best) : -1;
+    int path = pl.path;
+    const bool all_cand = pl.all_cand != 0;
+    const float B0 = pl.B0;
+    if (!pl.one && !(all_cand || (best && gscore > B0 + 1e-4f * fmaxf(1.f, fabsf(B0))))) {
+      // the prune bound did not certify the draw (probability ~1e-9): every kept token of the row, exactly
+      path |= PATH_FALLBACK;
+      const PhiloxKey key{pl.k0, pl.k1};
+      const float xP = pl.xP, M = pl.M, invT = pl.invT;
+      const int32_t It = pl.It;
+      float fs = -INFINITY;
+      int32_t fi = 0x7FFFFFFF;
+      for (int64_t e = t; e < p.V; e += kSplitThreads) {
+        const float xv = Tr::load_global(p.x, row * p.ld + e);
+        if (!(xv > xP || (xv == xP && e <= (int64_t)It))) continue;
+        const uint4 w4 = philox4x32_10(make_uint4((uint32_t)(e >> 2), pl.rid, pl.st_lo, pl.st_hi), key);
+        const float score = gumbel_score((xv - M) * invT, philox_word(w4, (int)(e & 3)));
+        if (argmax_better(score, (int32_t)e, fs, fi)) { fs = score; fi = (int32_t)e; }
+      }
+      const ArgMax a = warp_argmax(ArgMax{fs, fi, 0.f});
+      if (lane == 0) { bs[warp] = a.score; bi[warp] = a.idx; }
+      __syncthreads();
+      ArgMax b{bs[0], bi[0], 0.f};
+      for (int w = 1; w < kSplitThreads / 32; ++w)
+        if (argmax_better(bs[w], bi[w], b.score, b.idx)) b = ArgMax{bs[w], bi[w], 0.f};
+      tok = b.idx;
     }
-    tok = warp_argmax(ArgMax{fs, fi, 0.f}).idx;
+    if (t == 0) {
+      int st = VSAMP_OK;
+      if (tok >= 0 && (int64_t)tok < p.V) {
+        const float xt = Tr::load_global(p.x, row * p.ld + tok);
+        p.token[row] = tok;
+        if (p.logprob) p.logprob[row] = pl.one ? fminf(-pl.logS, 0.f) : fminf((xt - pl.M) * pl.invT - pl.logS, 0.f);
+      } else {
+        st = VSAMP_ERR_INVALID_ARG;
+        p.token[row] = -1;
+        if (p.logprob) p.logprob[row] = __int_as_float(0x7FC00000);
+      }
+      if (p.row_status) p.row_status[row] = st;
+      if (p.stats) {
+        p.stats[row * 4 + 0] = pl.passes;
+        p.stats[row * 4 + 1] = pl.rounds;
+        p.stats[row * 4 + 2] = (int32_t)pl.kept;
+        p.stats[row * 4 + 3] = path;
+      }
+    }
   }
-  if (lane == 0) {
-    int st = VSAMP_OK;
-    if (tok >= 0 && tok < n) {
-      const float xt = Tr::load_global(p.x, (int64_t)row * p.ld + tok);
-      p.token[row] = tok;
-      if (p.logprob) p.logprob[row] = fminf((xt - M) * pl.invT - pl.logS, 0.f);
-    } else {
-      st = VSAMP_ERR_INVALID_ARG;
-      p.token[row] = -1;
-      if (p.logprob) p.logprob[row] = __int_as_float(0x7FC00000);
-    }
-    if (p.row_status) p.row_status[row] = st;
-    if (p.stats) {
-      p.stats[row * 4 + 0] = pl.passes;
-      p.stats[row * 4 + 1] = pl.rounds;
-      p.stats[row * 4 + 2] = (int32_t)pl.kept;
-      p.stats[row * 4 + 3] = path;
-    }
-    gpl->best = 0ull;   // the workspace is left as it was found
-    gpl->done2 = 0u;
+  if (t == 0) gpl->best = 0ull;   // the draw slot is left zero
+}
+
+// Start the bulk copy of item `it`'s chunk (and, for the draw kernel, its row's plan) into buffer `slot`.
+template <typename T, bool PLAN>
+__device__ __forceinline__ void stream_issue(const Params& p, const RowPlan* plans, const ItemCursor& it, int slot,
+                                             uint4* buf, StreamShared& ss) {
+  using Tr = Traits<T>;
+  if (it.row >= p.B || ss.dead) {
+    ss.issued[slot] = 0;
+    return;
   }
+  const uint32_t bytes = chunk_copy_bytes<T>(p, it.chunk);
+  mbar_arrive_expect_tx(&ss.bar[slot], bytes + (PLAN ? (uint32_t)sizeof(RowPlan) : 0u));
+  if (bytes) {
+    const int64_t e_begin = (int64_t)it.chunk * split_chunk_elems(Tr::ESIZE);
+    bulk_copy_g2s(buf, p.x + (it.row * p.ld + e_begin) * Tr::ESIZE, bytes, &ss.bar[slot]);
+  }
+  if (PLAN) bulk_copy_g2s(ss.plan[slot], plans + it.row, (uint32_t)sizeof(RowPlan), &ss.bar[slot]);
+  ss.issued[slot] = 1;
+}
+
+// Bounded wait for buffer `slot`'s copy (every thread); a timeout marks the CTA dead. Returns the number of
+// 16-byte vectors of the item's chunk available in shared memory.
+template <typename T>
+__device__ __forceinline__ int32_t stream_wait(const Params& p, const ItemCursor& it, int slot, uint32_t (&uses)[2],
+                                               bool (&pend)[2], StreamShared& ss) {
+  const bool issued = ss.issued[slot] != 0;
+  if (issued) {
+    // thread 0 waits (the others are parked at the barrier, issuing nothing); the barrier then passes the
+    // landed bytes on to every thread
+    const bool ok = threadIdx.x != 0 || mbar_wait_bounded(&ss.bar[slot], uses[slot] & 1u, p.wait_cycles);
+    if (!__syncthreads_or(!ok)) {
+      ++uses[slot];
+      pend[slot] = false;
+    } else if (threadIdx.x == 0) {
+      ss.dead = 1;
+    }
+  }
+  __syncthreads();
+  return (issued && !ss.dead) ? (int32_t)(chunk_copy_bytes<T>(p, it.chunk) / 16) : 0;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kSplitThreads, 3) stream_stats_kernel(const Params p, ChunkStat* stats, int nc) {
+  extern __shared__ __align__(128) unsigned char dyn[];
+  __shared__ StreamShared ss;
+  const int t = threadIdx.x;
+  uint4* buf[2] = {reinterpret_cast<uint4*>(dyn), reinterpret_cast<uint4*>(dyn + kChunkBytes)};
+  ItemCursor cur(blockIdx.x, gridDim.x, nc);
+  uint32_t uses[2] = {0u, 0u};
+  bool pend[2] = {false, false};   // a copy was started and not yet seen to land
+  if (t == 0) {
+    mbar_init(&ss.bar[0], 1);
+    mbar_init(&ss.bar[1], 1);
+    ss.dead = 0;
+    fence_mbar_init();
+    ItemCursor nx = cur;
+    stream_issue<T, false>(p, nullptr, nx, 0, buf[0], ss);
+    nx.advance();
+    stream_issue<T, false>(p, nullptr, nx, 1, buf[1], ss);
+  }
+  __syncthreads();
+  pend[0] = ss.issued[0] != 0;
+  pend[1] = ss.issued[1] != 0;
+  for (int k = 0; cur.row < p.B; ++k) {
+    const int slot = k & 1;
+    const int32_t svecs = stream_wait<T>(p, cur, slot, uses, pend, ss);
+    stream_stats<T>(p, stats, nc, cur.row, cur.chunk, buf[slot], svecs, ss);
+    __syncthreads();
+    // every thread is done with the buffer: the item after next may overwrite it
+    if (t == 0) {
+      fence_proxy_async_shared();
+      ItemCursor nx = cur;
+      nx.advance();
+      nx.advance();
+      stream_issue<T, false>(p, nullptr, nx, slot, buf[slot], ss);
+    }
+    __syncthreads();
+    if (ss.issued[slot]) pend[slot] = true;
+    cur.advance();
+  }
+  if (t == 0)   // copies still landing after a timed-out wait: wait for them, again bounded
+    for (int b = 0; b < 2; ++b)
+      if (pend[b]) (void)mbar_wait_bounded(&ss.bar[b], uses[b] & 1u, p.wait_cycles);
+}
+
+// One CTA per row: the row's plan from its chunk statistics.
+template <typename T>
+__global__ void __launch_bounds__(kSplitThreads) stream_plan_kernel(const Params p, RowPlan* plans, ChunkStat* stats,
+                                                                   int nc) {
+  __shared__ SplitShared sh;
+  const int64_t r = blockIdx.x;
+  const float temp0 = p.temperature ? p.temperature[r] : 1.f;
+  const float Teff = temp0 > 0.f ? temp0 : 1.f;
+  plan_row<T>(p, plans, stats, stats, nc, r, temp0, Teff, kLog2e * (1.f / Teff), sh);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kSplitThreads, 3) stream_draw_kernel(const Params p, RowPlan* plans, int nc) {
+  extern __shared__ __align__(128) unsigned char dyn[];
+  __shared__ StreamShared ss;
+  const int t = threadIdx.x;
+  uint4* buf[2] = {reinterpret_cast<uint4*>(dyn), reinterpret_cast<uint4*>(dyn + kChunkBytes)};
+  ItemCursor cur(blockIdx.x, gridDim.x, nc);
+  uint32_t uses[2] = {0u, 0u};
+  bool pend[2] = {false, false};
+  if (t == 0) {
+    mbar_init(&ss.bar[0], 1);
+    mbar_init(&ss.bar[1], 1);
+    ss.dead = 0;
+    fence_mbar_init();
+    ItemCursor nx = cur;
+    stream_issue<T, true>(p, plans, nx, 0, buf[0], ss);
+    nx.advance();
+    stream_issue<T, true>(p, plans, nx, 1, buf[1], ss);
+  }
+  __syncthreads();
+  pend[0] = ss.issued[0] != 0;
+  pend[1] = ss.issued[1] != 0;
+  for (int k = 0; cur.row < p.B; ++k) {
+    const int slot = k & 1;
+    const int32_t svecs = stream_wait<T>(p, cur, slot, uses, pend, ss);
+    const RowPlan* pl = reinterpret_cast<const RowPlan*>(ss.plan[slot]);
+    if (!(ss.issued[slot] && !ss.dead)) {   // the plan did not come with a copy: read it directly
+      if (t < 8) ss.dplan[t] = reinterpret_cast<const uint4*>(plans + cur.row)[t];
+      __syncthreads();
+      pl = reinterpret_cast<const RowPlan*>(ss.dplan);
+    }
+    stream_draw<T>(p, plans, nc, cur.row, cur.chunk, buf[slot], svecs, *pl, ss);
+    __syncthreads();
+    if (t == 0) {
+      fence_proxy_async_shared();
+      ItemCursor nx = cur;
+      nx.advance();
+      nx.advance();
+      stream_issue<T, true>(p, plans, nx, slot, buf[slot], ss);
+    }
+    __syncthreads();
+    if (ss.issued[slot]) pend[slot] = true;
+    cur.advance();
+  }
+  if (t == 0)
+    for (int b = 0; b < 2; ++b)
+      if (pend[b]) (void)mbar_wait_bounded(&ss.bar[b], uses[b] & 1u, p.wait_cycles);
 }
 
 }  // namespace vsamp

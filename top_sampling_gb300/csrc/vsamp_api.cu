@@ -27,6 +27,54 @@ long long env_ll(const char* name, long long dflt) {
   return std::strtoll(v, nullptr, 10);
 }
 
+int cached_max_clusters(const void* kern, int threads, int smem, int C) {
+  struct Entry {
+    int dev;
+    const void* kern;
+    int threads, smem, C, n;
+  };
+  static Entry cache[256];
+  static int used = 0;
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  // the kernel's shared-memory limit only ever grows, so every launch seen so far stays valid
+  int limit = 0;
+  for (int i = 0; i < used; ++i)
+    if (cache[i].dev == dev && cache[i].kern == kern && cache[i].smem > limit) limit = cache[i].smem;
+  for (int i = 0; i < used; ++i) {
+    const Entry& e = cache[i];
+    if (e.dev == dev && e.kern == kern && e.threads == threads && e.smem == smem && e.C == C) return e.n;
+  }
+  if ((smem > limit && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) ||
+      (C > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3((unsigned)threads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.gridDim = dim3((unsigned)C, 1, 1);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  if (used < 256) cache[used++] = Entry{dev, kern, threads, smem, C, n};
+  return n;
+}
+
 vsamp_status device_info(int dev, DeviceInfo& out) {
   if (dev < 0 || dev >= kMaxDevices) return VSAMP_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lk(g_mu);

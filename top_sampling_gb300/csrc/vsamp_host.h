@@ -29,6 +29,11 @@ struct Geometry {
   int smem = 0;    // dynamic shared memory bytes
 };
 
+// Clusters of `kern` resident at once for a launch of cluster size C with `smem` bytes of dynamic shared
+// memory on the current device; the kernel's shared-memory and cluster attributes are set on the first query
+// of each (device, kernel, smem, C) and the answer is cached. 0 when the device cannot run the launch.
+int cached_max_clusters(const void* kern, int threads, int smem, int C);
+
 int env_int(const char* name, int dflt);
 long long env_ll(const char* name, long long dflt);
 vsamp_status device_info(int dev, DeviceInfo& out);

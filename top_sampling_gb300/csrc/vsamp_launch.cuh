@@ -8,14 +8,6 @@ namespace vsamp {
 template <typename T, int NT, int MODE>
 static vsamp_status launch_nt(Params p, int64_t B, const Geometry& g, cudaStream_t stream) {
   auto kern = row_kernel<T, NT, MODE>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem) != cudaSuccess) {
-    cudaGetLastError();
-    return VSAMP_ERR_UNSUPPORTED;
-  }
-  if (g.C > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
-    cudaGetLastError();
-    return VSAMP_ERR_UNSUPPORTED;
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(NT, 1, 1);
   cfg.dynamicSmemBytes = (size_t)g.smem;
@@ -30,11 +22,8 @@ static vsamp_status launch_nt(Params p, int64_t B, const Geometry& g, cudaStream
   // persistent clusters: as many as fit at once, then evened out so every cluster has the same number
   // of rows (+-1)
   cfg.gridDim = dim3((unsigned)g.C, 1, 1);
-  int nclusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&nclusters, kern, &cfg) != cudaSuccess || nclusters < 1) {
-    cudaGetLastError();
-    return VSAMP_ERR_UNSUPPORTED;
-  }
+  const int nclusters = cached_max_clusters(reinterpret_cast<const void*>(kern), NT, g.smem, g.C);
+  if (nclusters < 1) return VSAMP_ERR_UNSUPPORTED;
   const int fit = env_int("VSAMP_GRID_CLUSTERS", 0) > 0 ? env_int("VSAMP_GRID_CLUSTERS", 0) : nclusters;
   int64_t G = B < fit ? B : fit;
   const int64_t rounds = (B + G - 1) / G;

@@ -21,14 +21,6 @@ static vsamp_status launch_sample_cfg(Params p, int64_t B, int esize, const Devi
   p.wait_cycles = wc > 0 ? wc : 4000000000LL;   // ~2 s at the maximum SM clock
   p.drop_loads = env_int("VSAMP_TEST_DROP_LOADS", 0) != 0 ? 1 : 0;
   auto kern = sample_kernel<T, NDW, PER_SM>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem) != cudaSuccess) {
-    cudaGetLastError();
-    return VSAMP_ERR_UNSUPPORTED;
-  }
-  if (g.C > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
-    cudaGetLastError();
-    return VSAMP_ERR_UNSUPPORTED;
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kSampleThreads, 1, 1);
   cfg.dynamicSmemBytes = (size_t)g.smem;
@@ -41,11 +33,8 @@ static vsamp_status launch_sample_cfg(Params p, int64_t B, int esize, const Devi
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cfg.gridDim = dim3((unsigned)g.C, 1, 1);
-  int nclusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&nclusters, kern, &cfg) != cudaSuccess || nclusters < 1) {
-    cudaGetLastError();
-    return VSAMP_ERR_UNSUPPORTED;
-  }
+  const int nclusters = cached_max_clusters(reinterpret_cast<const void*>(kern), kSampleThreads, g.smem, g.C);
+  if (nclusters < 1) return VSAMP_ERR_UNSUPPORTED;
   const int fit = env_int("VSAMP_GRID_CLUSTERS", 0) > 0 ? env_int("VSAMP_GRID_CLUSTERS", 0) : nclusters;
   int64_t G = B < fit ? B : fit;
   const int64_t rounds = (B + G - 1) / G;   // every cluster gets the same number of rows (+-1)

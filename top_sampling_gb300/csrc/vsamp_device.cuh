@@ -249,6 +249,57 @@ struct PhiloxRow {
 
 __device__ __forceinline__ uint32_t min4_u32(uint4 w) { return min(__vimin3_u32(w.x, w.y, w.z), w.w); }
 
+// PhiloxRow with few live registers: the round keys from the third round on are formed as the rounds run
+// (one add per key word and round, shared by the counters drawn together), and only the smallest of each
+// counter's four output words is returned. Same words as philox4x32_10.
+struct PhiloxRowMin {
+  uint32_t k0_2, k1_2;       // round keys of the third round
+  uint32_t y1, z1k, x2k, hi2, w2;
+  __device__ __forceinline__ PhiloxRowMin(PhiloxKey key, uint32_t c1, uint32_t c2, uint32_t c3) {
+    constexpr uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u, W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+    const unsigned long long p1 = (unsigned long long)M1 * c2;
+    const uint32_t x1 = (uint32_t)(p1 >> 32) ^ c1 ^ key.k0;
+    y1 = (uint32_t)p1;
+    z1k = c3 ^ key.k1;
+    const unsigned long long p2 = (unsigned long long)M0 * x1;
+    x2k = y1 ^ (key.k0 + W0);
+    hi2 = (uint32_t)(p2 >> 32) ^ (key.k1 + W1);
+    w2 = (uint32_t)p2;
+    k0_2 = key.k0 + 2u * W0;
+    k1_2 = key.k1 + 2u * W1;
+  }
+  // the smallest output word of each of N counters
+  template <int N>
+  __device__ __forceinline__ void min_words(const uint32_t (&c0)[N], uint32_t (&m)[N]) const {
+    constexpr uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u, W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+    uint4 c[N];
+#pragma unroll
+    for (int n = 0; n < N; ++n) {
+      unsigned long long p0, p1;
+      asm("mul.wide.u32 %0, %1, %2;" : "=l"(p0) : "r"(c0[n]), "r"(M0));
+      const uint32_t z1 = (uint32_t)(p0 >> 32) ^ z1k, w1 = (uint32_t)p0;
+      asm("mul.wide.u32 %0, %1, %2;" : "=l"(p1) : "r"(z1), "r"(M1));
+      c[n] = make_uint4((uint32_t)(p1 >> 32) ^ x2k, (uint32_t)p1, hi2 ^ w1, w2);
+    }
+    uint32_t k0 = k0_2, k1 = k1_2;
+#pragma unroll
+    for (int r = 2; r < 10; ++r) {
+#pragma unroll
+      for (int n = 0; n < N; ++n) {
+        unsigned long long p0, p1;
+        asm("mul.wide.u32 %0, %1, %2;" : "=l"(p0) : "r"(c[n].x), "r"(M0));
+        asm("mul.wide.u32 %0, %1, %2;" : "=l"(p1) : "r"(c[n].z), "r"(M1));
+        c[n] = make_uint4((uint32_t)(p1 >> 32) ^ c[n].y ^ k0, (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c[n].w ^ k1,
+                          (uint32_t)p0);
+      }
+      k0 += W0;
+      k1 += W1;
+    }
+#pragma unroll
+    for (int n = 0; n < N; ++n) m[n] = min4_u32(c[n]);
+  }
+};
+
 __device__ __forceinline__ uint32_t philox_word(uint4 w, int lane) {
   return lane == 0 ? w.x : lane == 1 ? w.y : lane == 2 ? w.z : w.w;
 }

@@ -1400,11 +1400,28 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
 
   // ---------------- mask ----------------
   if (MODE & MODE_MASK) {
+    // one VE-byte store per vector (8 bytes for bf16, 4 for fp32) where the mask row allows it
     uint8_t* mrow = p.mask + (int64_t)row * p.V;
-    E.for_each([&](int64_t e, float x) {
-      const bool k = fin_valid && (x > xP || (x == xP && e <= (int64_t)It));
-      mrow[e] = k ? 1 : 0;
-    });
+    const bool vec_ok = ((reinterpret_cast<uintptr_t>(mrow) + (uintptr_t)E.thr_e0) & (uintptr_t)(VE - 1)) == 0;
+    const int nvec = (E.thr_n + VE - 1) / VE;
+    for (int j = 0; j < nvec; ++j) {
+      float x[VE];
+      Tr::values(E.mine[j], x);
+      const int64_t e0 = E.thr_e0 + (int64_t)j * VE;
+      const int cnt = E.thr_n - j * VE < VE ? E.thr_n - j * VE : VE;
+      uint32_t b[2] = {0u, 0u};
+#pragma unroll
+      for (int i = 0; i < VE; ++i) {
+        const bool k = fin_valid && i < cnt && (x[i] > xP || (x[i] == xP && e0 + i <= (int64_t)It));
+        b[i >> 2] |= (k ? 1u : 0u) << (8 * (i & 3));
+      }
+      if (vec_ok && cnt == VE) {
+        if (VE == 8) *reinterpret_cast<uint2*>(mrow + e0) = make_uint2(b[0], b[1]);
+        else *reinterpret_cast<uint32_t*>(mrow + e0) = b[0];
+      } else {
+        for (int i = 0; i < cnt; ++i) mrow[e0 + i] = (uint8_t)((b[i >> 2] >> (8 * (i & 3))) & 1u);
+      }
+    }
   }
 
   // ---------------- finalisation ----------------

@@ -1,6 +1,6 @@
-// The split-vocabulary sampling path (vsamp_sample_ws): every row is cut into fixed 32 KB chunks and two
-// persistent streaming kernels sweep all (row, chunk) pairs of the batch (see the section "The streaming
-// sampler" below). Chunking depends only on V, so results are deterministic and do not depend on the batch.
+// The split-vocabulary sampling path (vsamp_sample_ws): every row is cut into fixed pieces of 1024 logits and
+// streaming kernels sweep all (row, piece) pairs of the batch (see the section "The streaming sampler" below).
+// The cut into pieces depends only on V, so results are deterministic and do not depend on the batch.
 #pragma once
 
 #include "vsamp_row.cuh"
@@ -8,8 +8,13 @@
 namespace vsamp {
 
 constexpr int kSplitThreads = 256;
-constexpr int kStreamVec = 8;        // 16-byte vectors per thread per chunk
-constexpr int kChunkBytes = kSplitThreads * kStreamVec * 16;   // 32 KB
+constexpr int kStreamThreads = 256;  // threads per CTA of the streaming kernels (independent warps)
+constexpr int kPieceBytes = 4096;    // bytes of logits per piece (the unit of a warp's work and of the row statistics)
+template <typename T>
+constexpr int kPieceElems = kPieceBytes / Traits<T>::ESIZE;     // 2048 bf16 or 1024 fp32 logits
+template <typename T>
+constexpr int kPieceVecs = kPieceBytes / 32 / 16;               // 16-byte vectors per lane per piece: 8
+constexpr int kDrawRun = 4;          // pieces of one row per draw item
 
 struct ChunkStat {                   // 16 bytes per (row, chunk)
   float m;                           // chunk maximum (NaN flags a non-finite value)
@@ -39,7 +44,7 @@ struct RowPlan {                     // 128 bytes per row
 static_assert(sizeof(RowPlan) == 128, "RowPlan layout");
 static_assert(sizeof(ChunkStat) == 16, "ChunkStat layout");
 
-__host__ __device__ inline int64_t split_chunk_elems(int esize) { return kChunkBytes / esize; }
+__host__ __device__ inline int64_t split_chunk_elems(int esize) { return kPieceBytes / esize; }
 __host__ __device__ inline int64_t split_nchunks(int64_t V, int esize) {
   const int64_t k = split_chunk_elems(esize);
   return (V + k - 1) / k;
@@ -673,93 +678,54 @@ static __device__ __noinline__ void plan_row(const Params p, RowPlan* plans, con
 
 // ------------------------------------------------------------------------------------------------
 // The streaming sampler: four kernels, ordered by the stream.
-//   stream_stats_kernel  persistent, over (row, chunk) items in a static schedule (CTA b takes items b, b + G,
-//                        b + 2G, ...; item i is chunk i mod nc of row i / nc): each chunk read once from HBM,
-//                        its maximum m_c, count of maxima and mass relative to m_c in 2^-40 fixed point summed
-//                        per 16-byte vector.
-//   stream_plan_kernel   one CTA per row: the row's plan from its chunk statistics (radix rounds over the row
+//   warp_stats_kernel    every warp independently takes 4 KB pieces of consecutive logits (grid-stride
+//                        over (row, piece) items; lane l holds vectors u * 32 + l of the piece): the piece's
+//                        maximum m_p, count of maxima and mass relative to m_p in 2^-40 fixed point summed per
+//                        16-byte vector, read once from HBM.
+//   stream_plan_kernel   one CTA per row: the row's plan from its piece statistics (radix rounds over the row
 //                        only when the cut leaves the maximum's tie group).
-//   stream_draw_kernel   persistent, the same schedule: each chunk read again (mostly from L2) with the row's
-//                        128-byte plan copied beside it; one Philox4x32-10 word per kept token, the prune bound,
-//                        exact scores of the few candidates; each CTA's best meets the row's in a 64-bit atomic
-//                        maximum.
+//   warp_draw_kernel     the same items, each piece read again (mostly from L2): one Philox4x32-10 word per
+//                        kept token, the prune bound, exact scores of the few candidates; a warp with a
+//                        candidate meets the row's best in a 64-bit atomic maximum.
 //   stream_finish_kernel one CTA per row: certify the draw and write the outputs.
-// The persistent kernels bulk-copy the chunk of the item after next into the shared-memory buffer their last
-// item has released, so copies stream while they compute. No CTA waits for another inside a kernel.
+// No warp waits for another inside a kernel, and the streaming kernels use no shared memory or CTA barriers.
 // ------------------------------------------------------------------------------------------------
 struct StreamHeader {       // the first 256 bytes of the workspace (reserved, left zero)
   uint32_t reserved[64];
 };
 static_assert(sizeof(StreamHeader) == 256, "StreamHeader layout");
 
-struct StreamShared {
-  SplitShared sp;
-  unsigned long long bar[2];      // chunk buffers: the bulk copy of each use has landed
-  uint4 plan[2][8];               // draw kernel: the plan of each buffer's row (copied with the chunk)
-  uint4 dplan[8];                 // draw kernel: the plan read directly (after a copy timed out)
-  uint4 fplan[8];                 // the plan of a row being finished
-  int32_t issued[2];              // a copy into the buffer was started for its item
-  int32_t dead;                   // a copy timed out: no more copies start; items read global memory
-  int32_t flag;
-  int64_t frow;
-  float bs[8];                    // per-warp partials
-  int32_t bi[8];
-  float wm[8];
-  uint32_t wbad[8];
-  unsigned long long ws[8];
-  uint32_t wc[8];
-  uint32_t wt[8][kStreamVec];     // per-warp totals of a chunk scan
-  int32_t found;
-};
-
-// Item cursor of the static schedule: chunk `chunk` of row `row`; advance() steps by the grid size.
-struct ItemCursor {
-  int64_t row;
-  int chunk;
-  int64_t gq;   // grid size / nc
-  int gr;       // grid size % nc
-  int nc;
-  __device__ __forceinline__ ItemCursor(int64_t first, int64_t grid, int nchunks) {
-    nc = nchunks;
-    row = first / nc;
-    chunk = (int)(first % nc);
-    gq = grid / nc;
-    gr = (int)(grid % nc);
-  }
-  __device__ __forceinline__ void advance() {
-    row += gq;
-    chunk += gr;
-    if (chunk >= nc) { chunk -= nc; ++row; }
-  }
-};
-
-// A chunk of a row as one thread sees it: vector j of thread t is vector j * 256 + t of the chunk (element
-// e_begin + (j * 256 + t) * VE of the row). Vectors inside the bulk-copied part come from shared memory,
-// others (unaligned rows, the last partial vector of a row) from global memory.
+// A piece of a row as one lane sees it: vector u of lane l is vector u * 32 + l of the piece. Aligned rows
+// take 16-byte loads; the last, partial vector of a row and unaligned rows are read element by element.
 template <typename T>
-struct ChunkView {
+struct PieceView {
   using Tr = Traits<T>;
   static constexpr int VE = Tr::VE;
-  const unsigned char* xr;   // the row in global memory
+  const unsigned char* xr;   // the row
   int64_t V;                 // row length
   int32_t tma;               // the row is 16-byte aligned
-  uint32_t sbuf;             // the chunk in shared memory (shared-window address)
-  int64_t e_begin;
-  int32_t smem_vecs;         // leading vectors of the chunk held in shared memory
-  __device__ __forceinline__ int get(int j, uint4& v) const {
-    const int vi = j * kSplitThreads + (int)threadIdx.x;
-    if (vi < smem_vecs) {
-      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                   : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                   : "r"(sbuf + (uint32_t)vi * 16u));
-      return VE;
-    }
-    // outside the copied part: 16-byte or element loads, fewer than VE past the row end
-    const int64_t e = e_begin + (int64_t)vi * VE;
+  int64_t e_begin;           // first element of the piece
+  __device__ __forceinline__ int64_t elem(int u) const {
+    return e_begin + (int64_t)(u * 32 + (int)(threadIdx.x & 31)) * VE;
+  }
+  // the whole piece lies in an aligned row: plain 16-byte loads without bounds
+  __device__ __forceinline__ bool full() const { return tma && e_begin + kPieceElems<T> <= V; }
+  // start moving the lane's vectors of a full piece towards L1 (the warp's next item, while this one computes)
+  __device__ __forceinline__ void prefetch() const {
+    if (!full()) return;
+    const uint4* b = reinterpret_cast<const uint4*>(xr + e_begin * Tr::ESIZE) + (int)(threadIdx.x & 31);
+#pragma unroll
+    for (int u = 0; u < kPieceVecs<T>; ++u) asm volatile("prefetch.global.L1 [%0];" ::"l"(b + u * 32));
+  }
+  __device__ __forceinline__ void get_full(int u, uint4& v) const {
+    v = __ldg(reinterpret_cast<const uint4*>(xr + e_begin * Tr::ESIZE) + u * 32 + (int)(threadIdx.x & 31));
+  }
+  __device__ __forceinline__ int get(int u, uint4& v) const {
+    const int64_t e = elem(u);
     const int64_t left = V - e;
     const int cnt = left <= 0 ? 0 : (left >= VE ? VE : (int)left);
     if (cnt == VE && tma) {
-      v = *reinterpret_cast<const uint4*>(xr + e * Tr::ESIZE);
+      v = __ldg(reinterpret_cast<const uint4*>(xr + e * Tr::ESIZE));
     } else {
       uint32_t w[4] = {0u, 0u, 0u, 0u};
       for (int i = 0; i < cnt; ++i) {
@@ -772,211 +738,139 @@ struct ChunkView {
   }
 };
 
-// Bytes of a chunk the bulk copy brings into shared memory (a multiple of 16; the rest is read directly).
+// Statistics of every piece: one warp per item, grid-stride.
 template <typename T>
-__device__ __forceinline__ uint32_t chunk_copy_bytes(const Params& p, int c) {
-  const int64_t K = split_chunk_elems(Traits<T>::ESIZE);
-  const int64_t e_begin = (int64_t)c * K;
-  const int64_t n = p.V - e_begin < K ? p.V - e_begin : K;
-  return p.tma ? (uint32_t)((n * Traits<T>::ESIZE) & ~(int64_t)15) : 0u;
-}
-
-// S item: the chunk's statistics.
-template <typename T>
-__device__ __forceinline__ void stream_stats(const Params& p, ChunkStat* stats, int nc, int64_t row, int c, const uint4* sbuf, int32_t smem_vecs, StreamShared& ss) {
+__global__ void __launch_bounds__(kStreamThreads) warp_stats_kernel(const Params p, ChunkStat* stats, int np) {
   using Tr = Traits<T>;
   constexpr int VE = Tr::VE;
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const float temp0 = p.temperature ? p.temperature[row] : 1.f;
-  const float Teff = temp0 > 0.f ? temp0 : 1.f;   // greedy rows use T = 1 for their statistics
-  const float c1 = kLog2e * (1.f / Teff);
-  const int64_t K = split_chunk_elems(Tr::ESIZE);
-  const ChunkView<T> cv{p.x + (int64_t)row * p.ld * Tr::ESIZE, p.V, p.tma, smem_addr(sbuf), (int64_t)c * K, smem_vecs};
-
-  // ---- maximum and non-finite check ----
-  float mt = -INFINITY, nf = 0.f;
-  {
-    if constexpr (VE == 8) {
-      const __nv_bfloat162 zero2 = __float2bfloat162_rn(0.f);
-      __nv_bfloat162 ma = __float2bfloat162_rn(-INFINITY), mb = ma, na = zero2, nb = zero2;
-#pragma unroll 4
-      for (int j = 0; j < kStreamVec; ++j) {
-        uint4 v;
-        const int cnt = cv.get(j, v);
-        if (cnt == VE) {
-          ma = __hmax2(ma, __hmax2(Tr::pair(v.x), Tr::pair(v.y)));
-          mb = __hmax2(mb, __hmax2(Tr::pair(v.z), Tr::pair(v.w)));
-          na = __hfma2(Tr::pair(v.x), zero2, __hfma2(Tr::pair(v.y), zero2, na));
-          nb = __hfma2(Tr::pair(v.z), zero2, __hfma2(Tr::pair(v.w), zero2, nb));
-        } else if (cnt > 0) {
-          float x[VE];
-          Tr::values(v, x);
-#pragma unroll
-          for (int i = 0; i < VE; ++i)
-            if (i < cnt) { mt = fmaxf(mt, x[i]); nf = fmaf(x[i], 0.f, nf); }
-        }
-      }
-      ma = __hmax2(ma, mb);
-      na = __hadd2(na, nb);
-      mt = fmaxf(mt, fmaxf(__low2float(ma), __high2float(ma)));
-      if (__low2float(na) != 0.f || __high2float(na) != 0.f) nf = 1.f;
-    } else {
-      float mb = -INFINITY, nb = 0.f;
-#pragma unroll 4
-      for (int j = 0; j < kStreamVec; ++j) {
-        uint4 v;
-        const int cnt = cv.get(j, v);
-        float x[VE];
-        Tr::values(v, x);
-        if (cnt == VE) {
-          mt = fmaxf(mt, fmaxf(x[0], x[1]));
-          mb = fmaxf(mb, fmaxf(x[2], x[3]));
-          nf = fmaf(x[0], 0.f, fmaf(x[1], 0.f, nf));
-          nb = fmaf(x[2], 0.f, fmaf(x[3], 0.f, nb));
-        } else {
-#pragma unroll
-          for (int i = 0; i < VE; ++i)
-            if (i < cnt) { mt = fmaxf(mt, x[i]); nf = fmaf(x[i], 0.f, nf); }
-        }
-      }
-      mt = fmaxf(mt, mb);
-      nf += nb;
+  constexpr int U = kPieceVecs<T>;
+  const int lane = threadIdx.x & 31;
+  const long long total = (long long)p.B * np;
+  const long long nw = (long long)gridDim.x * (kStreamThreads / 32);
+  for (long long it = (long long)blockIdx.x * (kStreamThreads / 32) + (threadIdx.x >> 5); it < total; it += nw) {
+    const int64_t row = it / np;
+    const int pc = (int)(it - row * np);
+    const float temp0 = p.temperature ? p.temperature[row] : 1.f;
+    const float Teff = temp0 > 0.f ? temp0 : 1.f;   // greedy rows use T = 1 for their statistics
+    const float c1 = kLog2e * (1.f / Teff);
+    const PieceView<T> pv{p.x + row * p.ld * Tr::ESIZE, p.V, p.tma, (int64_t)pc * kPieceElems<T>};
+    if (it + nw < total) {
+      const int64_t r2 = (it + nw) / np;
+      const int pc2 = (int)(it + nw - r2 * np);
+      PieceView<T>{p.x + r2 * p.ld * Tr::ESIZE, p.V, p.tma, (int64_t)pc2 * kPieceElems<T>}.prefetch();
     }
-  }
-  {
-    const float wmx = warp_max_f(mt);
-    const uint32_t wb = __any_sync(kFullMask, nf != 0.f) ? 1u : 0u;
-    if (lane == 0) { ss.wm[warp] = wmx; ss.wbad[warp] = wb; }
-  }
-  __syncthreads();
-  float mc = ss.wm[0];
-  uint32_t bad = ss.wbad[0];
+    uint4 v[U];
+    int cnt[U];
+    if (pv.full()) {
 #pragma unroll
-  for (int w = 1; w < kSplitThreads / 32; ++w) { mc = fmaxf(mc, ss.wm[w]); bad |= ss.wbad[w]; }
-
-  // ---- mass relative to the chunk maximum (2^-40 fixed point per vector) and the count of maxima ----
-  unsigned long long s = 0ull;
-  uint32_t cm = 0u;
-  if (!bad) {
-    const float2 mM = make_float2(-mc, -mc), cc = make_float2(c1, c1);
-    uint32_t cm2 = 0u;
-#pragma unroll 2
-    for (int j = 0; j < kStreamVec; ++j) {
-      uint4 v;
-      const int cnt = cv.get(j, v);
+      for (int u = 0; u < U; ++u) { pv.get_full(u, v[u]); cnt[u] = VE; }
+    } else {
+#pragma unroll
+      for (int u = 0; u < U; ++u) cnt[u] = pv.get(u, v[u]);
+    }
+    // ---- maximum and non-finite check ----
+    float mt = -INFINITY, nf = 0.f;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
       float x[VE];
-      Tr::values(v, x);
-      if (cnt == VE) {
-        float2 w2[VE / 2];
+      Tr::values(v[u], x);
 #pragma unroll
-        for (int h = 0; h < VE / 2; ++h) {
-          const float2 e = __fmul2_rn(__fadd2_rn(make_float2(x[2 * h], x[2 * h + 1]), mM), cc);
-          w2[h] = make_float2(ex2_approx(e.x), ex2_approx(e.y));
-        }
-        float2 a;
-        if constexpr (VE == 8) a = __fadd2_rn(__fadd2_rn(w2[0], w2[2]), __fadd2_rn(w2[1], w2[3]));
-        else a = __fadd2_rn(w2[0], w2[1]);
-        s += mass_fx(a.x + a.y);
-        if constexpr (VE == 8) {
-          const __nv_bfloat162 M2 = __float2bfloat162_rn(mc);   // a bf16 value: exact
-          cm2 += __heq2_mask(Tr::pair(v.x), M2) & 0x00010001u;
-          cm2 += __heq2_mask(Tr::pair(v.y), M2) & 0x00010001u;
-          cm2 += __heq2_mask(Tr::pair(v.z), M2) & 0x00010001u;
-          cm2 += __heq2_mask(Tr::pair(v.w), M2) & 0x00010001u;
-        } else {
+      for (int i = 0; i < VE; ++i)
+        if (i < cnt[u]) { mt = fmaxf(mt, x[i]); nf = fmaf(x[i], 0.f, nf); }
+    }
+    const float mc = warp_max_f(mt);
+    const bool bad = __any_sync(kFullMask, nf != 0.f);
+    // ---- mass relative to the piece maximum (2^-40 fixed point per vector) and the count of maxima ----
+    unsigned long long s = 0ull;
+    uint32_t cm = 0u;
+    if (!bad) {
+      const float2 mM = make_float2(-mc, -mc), cc = make_float2(c1, c1);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        float x[VE];
+        Tr::values(v[u], x);
+        if (cnt[u] == VE) {
+          float2 w2[VE / 2];
+#pragma unroll
+          for (int h = 0; h < VE / 2; ++h) {
+            const float2 e = __fmul2_rn(__fadd2_rn(make_float2(x[2 * h], x[2 * h + 1]), mM), cc);
+            w2[h] = make_float2(ex2_approx(e.x), ex2_approx(e.y));
+          }
+          float2 a;
+          if constexpr (VE == 8) a = __fadd2_rn(__fadd2_rn(w2[0], w2[2]), __fadd2_rn(w2[1], w2[3]));
+          else a = __fadd2_rn(w2[0], w2[1]);
+          s += mass_fx(a.x + a.y);
 #pragma unroll
           for (int i = 0; i < VE; ++i) cm += x[i] == mc ? 1u : 0u;
+        } else if (cnt[u] > 0) {
+          float w[VE];
+#pragma unroll
+          for (int i = 0; i < VE; ++i) {
+            const bool ok = i < cnt[u];
+            const float d = x[i] - mc;
+            w[i] = ok ? ex2_approx(d * c1) : 0.f;
+            cm += (ok && d == 0.f) ? 1u : 0u;
+          }
+#pragma unroll
+          for (int h = VE / 2; h >= 1; h >>= 1)
+#pragma unroll
+            for (int i = 0; i < h; ++i) w[i] += w[i + h];
+          s += mass_fx(w[0]);
         }
-      } else if (cnt > 0) {
-        float w[VE];
-#pragma unroll
-        for (int i = 0; i < VE; ++i) {
-          const bool ok = i < cnt;
-          const float d = x[i] - mc;
-          w[i] = ok ? ex2_approx(d * c1) : 0.f;
-          cm += (ok && d == 0.f) ? 1u : 0u;
-        }
-#pragma unroll
-        for (int h = VE / 2; h >= 1; h >>= 1)
-#pragma unroll
-          for (int i = 0; i < h; ++i) w[i] += w[i + h];
-        s += mass_fx(w[0]);
       }
     }
-    cm += (cm2 & 0xFFFFu) + (cm2 >> 16);
-  }
-  s = warp_sum_u64(s);
-  cm = warp_sum_u32(cm);
-  if (lane == 0) { ss.ws[warp] = s; ss.wc[warp] = cm; }
-  __syncthreads();
-  if (t == 0) {
-    ChunkStat cs;
-    cs.m = bad ? __int_as_float(0x7FC00000) : mc;
-    cs.cnt = 0u;
-    cs.s = 0ull;
-#pragma unroll
-    for (int w = 0; w < kSplitThreads / 32; ++w) { cs.s += ss.ws[w]; cs.cnt += ss.wc[w]; }
-    stats[row * nc + c] = cs;
+    s = warp_sum_u64(s);
+    cm = warp_sum_u32(cm);
+    if (lane == 0) {
+      ChunkStat cs;
+      cs.m = bad ? __int_as_float(0x7FC00000) : mc;
+      cs.cnt = cm;
+      cs.s = s;
+      stats[it] = cs;
+    }
   }
 }
 
-// The index of the need-th element (1-based, index order) equal to xv in a chunk; kNoIndex if there are
-// fewer. Element order inside the chunk is (vector j, thread t, lane i): one scan per j over the threads.
+// The index of the need-th element (1-based, index order) equal to xv in a piece; kNoIndex if there are fewer.
+// Element order in the piece is (vector u, lane, element i): one warp scan per u. Warp-collective.
 template <typename T>
-__device__ __noinline__ int32_t chunk_nth_equal(const ChunkView<T>& cv, float xv, uint32_t need, StreamShared& ss) {
+__device__ __noinline__ int32_t piece_nth_equal(const PieceView<T>& pv, float xv, uint32_t need) {
   using Tr = Traits<T>;
   constexpr int VE = Tr::VE;
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  uint32_t cnt[kStreamVec], inc[kStreamVec];
-#pragma unroll
-  for (int j = 0; j < kStreamVec; ++j) {
+  constexpr int U = kPieceVecs<T>;
+  const int lane = threadIdx.x & 31;
+  uint32_t base = 0;
+  int32_t found = kNoIndex;
+  for (int u = 0; u < U; ++u) {
     uint4 v;
-    const int n = cv.get(j, v);
+    const int n = pv.get(u, v);
     float x[VE];
     Tr::values(v, x);
     uint32_t c = 0;
 #pragma unroll
     for (int i = 0; i < VE; ++i) c += (i < n && x[i] == xv) ? 1u : 0u;
-    cnt[j] = c;
-    inc[j] = c;
+    uint32_t inc = c;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(kFullMask, inc[j], o);
-      if (lane >= o) inc[j] += y;
+      const uint32_t y = __shfl_up_sync(kFullMask, inc, o);
+      if (lane >= o) inc += y;
     }
-  }
-  if (lane == 31) {
-#pragma unroll
-    for (int j = 0; j < kStreamVec; ++j) ss.wt[warp][j] = inc[j];
-  }
-  if (t == 0) ss.found = kNoIndex;
-  __syncthreads();
-  uint32_t base = 0;
-#pragma unroll
-  for (int j = 0; j < kStreamVec; ++j) {
-    uint32_t before = 0, tot = 0;
-#pragma unroll
-    for (int w = 0; w < kSplitThreads / 32; ++w) {
-      const uint32_t y = ss.wt[w][j];
-      if (w < warp) before += y;
-      tot += y;
-    }
-    const uint32_t excl = base + before + inc[j] - cnt[j];
-    if (cnt[j] && excl < need && need <= excl + cnt[j]) {
-      uint4 v;
-      const int n = cv.get(j, v);
-      float x[VE];
-      Tr::values(v, x);
+    const uint32_t excl = base + inc - c;
+    int32_t idx = kNoIndex;
+    if (c && excl < need && need <= excl + c) {
       uint32_t seen = excl;
-      const int64_t e0 = cv.e_begin + (int64_t)(j * kSplitThreads + t) * VE;
 #pragma unroll
       for (int i = 0; i < VE; ++i)
-        if (i < n && x[i] == xv && ++seen == need) ss.found = (int32_t)(e0 + i);
+        if (idx < 0 && i < n && x[i] == xv && ++seen == need) idx = (int32_t)(pv.elem(u) + i);
     }
-    base += tot;
+    const uint32_t hit = __ballot_sync(kFullMask, idx >= 0);
+    if (hit) {
+      found = __shfl_sync(kFullMask, idx, __ffs(hit) - 1);
+      break;
+    }
+    base += __shfl_sync(kFullMask, inc, 31);
   }
-  __syncthreads();
-  return ss.found;
+  return found;
 }
 
 // Exact perturbed scores of one vector's kept tokens that pass the prune bound (every kept token when the
@@ -1011,111 +905,6 @@ __device__ __noinline__ void draw_exact(uint4 v, int cnt, int64_t e0, const RowP
     const float score = gumbel_score(sv, b[i]);
     const int32_t idx = (int32_t)(e0 + i);
     if (argmax_better(score, idx, bscore, bidx)) { bscore = score; bidx = idx; }
-  }
-}
-
-// D item: the draw over one chunk of a row, with the row's plan in shared memory.
-template <typename T>
-__device__ __forceinline__ void stream_draw(const Params& p, RowPlan* plans, int nc, int64_t row, int c,
-                                             const uint4* sbuf, int32_t smem_vecs, const RowPlan& pl,
-                                             StreamShared& ss) {
-  using Tr = Traits<T>;
-  constexpr int VE = Tr::VE;
-  constexpr int G = VE / 4;                 // groups of four tokens (one Philox counter) per vector
-  constexpr int NG = kStreamVec * G;        // groups per thread
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  RowPlan* gpl = plans + row;
-  float bscore = -INFINITY;
-  int32_t bidx = 0x7FFFFFFF;
-  if (pl.status == VSAMP_OK && pl.draw) {
-    const float xP = pl.xP;
-    const int64_t K = split_chunk_elems(Tr::ESIZE);
-    const ChunkView<T> cv{p.x + (int64_t)row * p.ld * Tr::ESIZE, p.V, p.tma, smem_addr(sbuf), (int64_t)c * K, smem_vecs};
-    const int64_t e_begin = cv.e_begin;
-    // the cut's last kept index: inside the maximum's tie group it lies in chunk cb, found here
-    int32_t It = pl.It;
-    if (It == kDeferIndex) It = c < pl.cb ? kAllIndex : (c > pl.cb ? kNoIndex : chunk_nth_equal<T>(cv, xP, pl.cneed, ss));
-    const uint32_t bk = pl.bk;
-    const bool all_cand = pl.all_cand != 0;
-    if (pl.one) {
-      // one token is kept: the chunk holding it publishes it (score +inf), the others have nothing to do
-      if (c == pl.cb && It >= 0) { bscore = INFINITY; bidx = It; }
-    } else {
-    uint32_t gmask = 0u;   // kept groups: bit j * G + g
-#pragma unroll
-    for (int j = 0; j < kStreamVec; ++j) {
-      uint4 v;
-      const int cnt = cv.get(j, v);
-      const int32_t e0 = (int32_t)(e_begin + (int64_t)(j * kSplitThreads + t) * VE);
-      if (cnt == VE && e0 + VE - 1 <= It && Tr::all_ge(v, xP)) {
-        gmask |= ((1u << G) - 1u) << (j * G);
-      } else if (cnt > 0) {
-        float x[VE];
-        Tr::values(v, x);
-#pragma unroll
-        for (int i = 0; i < VE; ++i)
-          if (i < cnt && (x[i] > xP || (x[i] == xP && e0 + i <= It))) gmask |= 1u << (j * G + (i >> 2));
-      }
-    }
-    // ---- one Philox word per kept token: the smallest word of each vector's kept groups ----
-    uint32_t flagged = 0u;
-    if (all_cand) {
-#pragma unroll
-      for (int j = 0; j < kStreamVec; ++j)
-        if ((gmask >> (j * G)) & ((1u << G) - 1u)) flagged |= 1u << j;
-    } else if (gmask) {
-      const PhiloxRow ph(PhiloxKey{pl.k0, pl.k1}, pl.rid, pl.st_lo, pl.st_hi);
-      // counter word of group gi = j * G + g: (first element of vector j) / 4 + g
-      const uint32_t cb0 = (uint32_t)((e_begin + (int64_t)t * VE) >> 2);
-      auto ctr = [&](int gi) -> uint32_t { return cb0 + (uint32_t)((gi / G) * kSplitThreads * G + gi % G); };
-      uint32_t wmin = 0xFFFFFFFFu;
-      uint32_t vmin[kStreamVec];
-#pragma unroll
-      for (int j = 0; j < kStreamVec; ++j) vmin[j] = 0xFFFFFFFFu;
-      if (gmask == (uint32_t)((1ull << NG) - 1ull)) {
-        // every token of the thread's vectors is kept: straight-line, four counters at a time
-#pragma unroll
-        for (int g0 = 0; g0 < NG; g0 += 4) {
-          const uint4 a = ph(ctr(g0)), b = ph(ctr(g0 + 1)), cq = ph(ctr(g0 + 2)), d = ph(ctr(g0 + 3));
-          const uint32_t m[4] = {min4_u32(a), min4_u32(b), min4_u32(cq), min4_u32(d)};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) vmin[(g0 + k) / G] = min(vmin[(g0 + k) / G], m[k]);
-        }
-      } else {
-#pragma unroll 1
-        for (int gi = 0; gi < NG; ++gi)
-          if (((gmask >> gi) & 1u) && min4_u32(ph(ctr(gi))) < bk) flagged |= 1u << (gi / G);
-      }
-#pragma unroll
-      for (int j = 0; j < kStreamVec; ++j) wmin = min(wmin, vmin[j]);
-      if (wmin < bk) {
-#pragma unroll
-        for (int j = 0; j < kStreamVec; ++j)
-          if (vmin[j] < bk) flagged |= 1u << j;
-      }
-    }
-    // ---- flagged vectors: exact perturbed scores of the kept tokens that pass the bound ----
-    while (flagged) {
-      const int j = __ffs(flagged) - 1;
-      flagged &= flagged - 1u;
-      uint4 v;
-      const int cnt = cv.get(j, v);
-      draw_exact<T>(v, cnt, e_begin + (int64_t)(j * kSplitThreads + t) * VE, &pl, It, bscore, bidx);
-    }
-    }
-  }
-  // ---- the CTA's best -> the row's 64-bit maximum ----
-  const ArgMax a = warp_argmax(ArgMax{bscore, bidx, 0.f});
-  if (lane == 0) { ss.bs[warp] = a.score; ss.bi[warp] = a.idx; }
-  __syncthreads();
-  if (t == 0) {
-    ArgMax b{ss.bs[0], ss.bi[0], 0.f};
-    for (int w = 1; w < kSplitThreads / 32; ++w)
-      if (argmax_better(ss.bs[w], ss.bi[w], b.score, b.idx)) b = ArgMax{ss.bs[w], ss.bi[w], 0.f};
-    if (b.idx != 0x7FFFFFFF) {
-      const unsigned long long k = ((unsigned long long)score_key(b.score) << 32) | (0xFFFFFFFFu - (uint32_t)b.idx);
-      atomicMax(&gpl->best, k);
-    }
   }
 }
 
@@ -1186,90 +975,6 @@ __global__ void __launch_bounds__(kSplitThreads) stream_finish_kernel(const Para
   if (t == 0) gpl->best = 0ull;   // the draw slot is left zero
 }
 
-// Start the bulk copy of item `it`'s chunk (and, for the draw kernel, its row's plan) into buffer `slot`.
-template <typename T, bool PLAN>
-__device__ __forceinline__ void stream_issue(const Params& p, const RowPlan* plans, const ItemCursor& it, int slot,
-                                             uint4* buf, StreamShared& ss) {
-  using Tr = Traits<T>;
-  if (it.row >= p.B || ss.dead) {
-    ss.issued[slot] = 0;
-    return;
-  }
-  const uint32_t bytes = chunk_copy_bytes<T>(p, it.chunk);
-  mbar_arrive_expect_tx(&ss.bar[slot], bytes + (PLAN ? (uint32_t)sizeof(RowPlan) : 0u));
-  if (bytes) {
-    const int64_t e_begin = (int64_t)it.chunk * split_chunk_elems(Tr::ESIZE);
-    bulk_copy_g2s(buf, p.x + (it.row * p.ld + e_begin) * Tr::ESIZE, bytes, &ss.bar[slot]);
-  }
-  if (PLAN) bulk_copy_g2s(ss.plan[slot], plans + it.row, (uint32_t)sizeof(RowPlan), &ss.bar[slot]);
-  ss.issued[slot] = 1;
-}
-
-// Bounded wait for buffer `slot`'s copy (every thread); a timeout marks the CTA dead. Returns the number of
-// 16-byte vectors of the item's chunk available in shared memory.
-template <typename T>
-__device__ __forceinline__ int32_t stream_wait(const Params& p, const ItemCursor& it, int slot, uint32_t (&uses)[2],
-                                               bool (&pend)[2], StreamShared& ss) {
-  const bool issued = ss.issued[slot] != 0;
-  if (issued) {
-    // thread 0 waits (the others are parked at the barrier, issuing nothing); the barrier then passes the
-    // landed bytes on to every thread
-    const bool ok = threadIdx.x != 0 || mbar_wait_bounded(&ss.bar[slot], uses[slot] & 1u, p.wait_cycles);
-    if (!__syncthreads_or(!ok)) {
-      ++uses[slot];
-      pend[slot] = false;
-    } else if (threadIdx.x == 0) {
-      ss.dead = 1;
-    }
-  }
-  __syncthreads();
-  return (issued && !ss.dead) ? (int32_t)(chunk_copy_bytes<T>(p, it.chunk) / 16) : 0;
-}
-
-template <typename T>
-__global__ void __launch_bounds__(kSplitThreads, 3) stream_stats_kernel(const Params p, ChunkStat* stats, int nc) {
-  extern __shared__ __align__(128) unsigned char dyn[];
-  __shared__ StreamShared ss;
-  const int t = threadIdx.x;
-  uint4* buf[2] = {reinterpret_cast<uint4*>(dyn), reinterpret_cast<uint4*>(dyn + kChunkBytes)};
-  ItemCursor cur(blockIdx.x, gridDim.x, nc);
-  uint32_t uses[2] = {0u, 0u};
-  bool pend[2] = {false, false};   // a copy was started and not yet seen to land
-  if (t == 0) {
-    mbar_init(&ss.bar[0], 1);
-    mbar_init(&ss.bar[1], 1);
-    ss.dead = 0;
-    fence_mbar_init();
-    ItemCursor nx = cur;
-    stream_issue<T, false>(p, nullptr, nx, 0, buf[0], ss);
-    nx.advance();
-    stream_issue<T, false>(p, nullptr, nx, 1, buf[1], ss);
-  }
-  __syncthreads();
-  pend[0] = ss.issued[0] != 0;
-  pend[1] = ss.issued[1] != 0;
-  for (int k = 0; cur.row < p.B; ++k) {
-    const int slot = k & 1;
-    const int32_t svecs = stream_wait<T>(p, cur, slot, uses, pend, ss);
-    stream_stats<T>(p, stats, nc, cur.row, cur.chunk, buf[slot], svecs, ss);
-    __syncthreads();
-    // every thread is done with the buffer: the item after next may overwrite it
-    if (t == 0) {
-      fence_proxy_async_shared();
-      ItemCursor nx = cur;
-      nx.advance();
-      nx.advance();
-      stream_issue<T, false>(p, nullptr, nx, slot, buf[slot], ss);
-    }
-    __syncthreads();
-    if (ss.issued[slot]) pend[slot] = true;
-    cur.advance();
-  }
-  if (t == 0)   // copies still landing after a timed-out wait: wait for them, again bounded
-    for (int b = 0; b < 2; ++b)
-      if (pend[b]) (void)mbar_wait_bounded(&ss.bar[b], uses[b] & 1u, p.wait_cycles);
-}
-
 // One CTA per row: the row's plan from its chunk statistics.
 template <typename T>
 __global__ void __launch_bounds__(kSplitThreads) stream_plan_kernel(const Params p, RowPlan* plans, ChunkStat* stats,
@@ -1281,53 +986,133 @@ __global__ void __launch_bounds__(kSplitThreads) stream_plan_kernel(const Params
   plan_row<T>(p, plans, stats, stats, nc, r, temp0, Teff, kLog2e * (1.f / Teff), sh);
 }
 
+
+// The draw over every piece of the rows whose plan draws: one warp per item of kDrawRun consecutive pieces of
+// a row, grid-stride.
 template <typename T>
-__global__ void __launch_bounds__(kSplitThreads, 3) stream_draw_kernel(const Params p, RowPlan* plans, int nc) {
-  extern __shared__ __align__(128) unsigned char dyn[];
-  __shared__ StreamShared ss;
-  const int t = threadIdx.x;
-  uint4* buf[2] = {reinterpret_cast<uint4*>(dyn), reinterpret_cast<uint4*>(dyn + kChunkBytes)};
-  ItemCursor cur(blockIdx.x, gridDim.x, nc);
-  uint32_t uses[2] = {0u, 0u};
-  bool pend[2] = {false, false};
-  if (t == 0) {
-    mbar_init(&ss.bar[0], 1);
-    mbar_init(&ss.bar[1], 1);
-    ss.dead = 0;
-    fence_mbar_init();
-    ItemCursor nx = cur;
-    stream_issue<T, true>(p, plans, nx, 0, buf[0], ss);
-    nx.advance();
-    stream_issue<T, true>(p, plans, nx, 1, buf[1], ss);
-  }
-  __syncthreads();
-  pend[0] = ss.issued[0] != 0;
-  pend[1] = ss.issued[1] != 0;
-  for (int k = 0; cur.row < p.B; ++k) {
-    const int slot = k & 1;
-    const int32_t svecs = stream_wait<T>(p, cur, slot, uses, pend, ss);
-    const RowPlan* pl = reinterpret_cast<const RowPlan*>(ss.plan[slot]);
-    if (!(ss.issued[slot] && !ss.dead)) {   // the plan did not come with a copy: read it directly
-      if (t < 8) ss.dplan[t] = reinterpret_cast<const uint4*>(plans + cur.row)[t];
-      __syncthreads();
-      pl = reinterpret_cast<const RowPlan*>(ss.dplan);
+__global__ void __launch_bounds__(kStreamThreads, 2) warp_draw_kernel(const Params p, RowPlan* plans, int np) {
+  using Tr = Traits<T>;
+  constexpr int VE = Tr::VE;
+  constexpr int U = kPieceVecs<T>;
+  constexpr int G = VE / 4;          // groups of four tokens (one Philox counter) per vector
+  constexpr int NG = U * G;          // groups per lane and piece
+  const int lane = threadIdx.x & 31;
+  const int nruns = (np + kDrawRun - 1) / kDrawRun;
+  const long long total = (long long)p.B * nruns;
+  const long long nw = (long long)gridDim.x * (kStreamThreads / 32);
+  for (long long it = (long long)blockIdx.x * (kStreamThreads / 32) + (threadIdx.x >> 5); it < total; it += nw) {
+    const int64_t row = it / nruns;
+    const int run = (int)(it - row * nruns);
+    RowPlan* gp = plans + row;
+    if (!(__ldg(&gp->status) == VSAMP_OK && __ldg(&gp->draw))) continue;
+    const float xP = __ldg(&gp->xP);
+    const int32_t It0 = __ldg(&gp->It);
+    const int32_t cbp = __ldg(&gp->cb);
+    const bool one = __ldg(&gp->one) != 0;
+    const uint32_t bk = __ldg(&gp->bk);
+    const bool all_cand = __ldg(&gp->all_cand) != 0;
+    const PhiloxRowMin ph(PhiloxKey{__ldg(&gp->k0), __ldg(&gp->k1)}, __ldg(&gp->rid), __ldg(&gp->st_lo),
+                          __ldg(&gp->st_hi));
+    if (it + nw < total) {
+      const int64_t r2 = (it + nw) / nruns;
+      const int run2 = (int)(it + nw - r2 * nruns);
+      for (int k = 0; k < kDrawRun && run2 * kDrawRun + k < np; ++k)
+        PieceView<T>{p.x + r2 * p.ld * Tr::ESIZE, p.V, p.tma, (int64_t)(run2 * kDrawRun + k) * kPieceElems<T>}.prefetch();
     }
-    stream_draw<T>(p, plans, nc, cur.row, cur.chunk, buf[slot], svecs, *pl, ss);
-    __syncthreads();
-    if (t == 0) {
-      fence_proxy_async_shared();
-      ItemCursor nx = cur;
-      nx.advance();
-      nx.advance();
-      stream_issue<T, true>(p, plans, nx, slot, buf[slot], ss);
+    float bscore = -INFINITY;
+    int32_t bidx = 0x7FFFFFFF;
+    bool cand = false;   // warp-uniform: some lane evaluated a candidate
+#pragma unroll 1
+    for (int k = 0; k < kDrawRun; ++k) {
+      const int pc = run * kDrawRun + k;
+      if (pc >= np) break;
+      const PieceView<T> pv{p.x + row * p.ld * Tr::ESIZE, p.V, p.tma, (int64_t)pc * kPieceElems<T>};
+      // the cut's last kept index: inside the maximum's tie group it lies in piece cb, found here
+      int32_t It = It0;
+      if (It == kDeferIndex)
+        It = pc < cbp ? kAllIndex : (pc > cbp ? kNoIndex : piece_nth_equal<T>(pv, xP, __ldg(&gp->cneed)));
+      if (one) {
+        // one token is kept: the piece holding it publishes it (score +inf)
+        if (pc == cbp && lane == 0 && It >= 0)
+          atomicMax(&gp->best, ((unsigned long long)score_key(INFINITY) << 32) | (0xFFFFFFFFu - (uint32_t)It));
+        continue;
+      }
+      uint32_t gmask = 0u;   // kept groups: bit u * G + g
+      {
+        uint4 v[U];
+        int cnt[U];
+        if (pv.full()) {
+#pragma unroll
+          for (int u = 0; u < U; ++u) { pv.get_full(u, v[u]); cnt[u] = VE; }
+        } else {
+#pragma unroll
+          for (int u = 0; u < U; ++u) cnt[u] = pv.get(u, v[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int64_t e0 = pv.elem(u);
+          if (cnt[u] == VE && e0 + VE - 1 <= (int64_t)It && Tr::all_ge(v[u], xP)) {
+            gmask |= ((1u << G) - 1u) << (u * G);
+          } else if (cnt[u] > 0) {
+            float x[VE];
+            Tr::values(v[u], x);
+#pragma unroll
+            for (int i = 0; i < VE; ++i)
+              if (i < cnt[u] && (x[i] > xP || (x[i] == xP && e0 + i <= (int64_t)It))) gmask |= 1u << (u * G + (i >> 2));
+          }
+        }
+      }
+      // ---- one Philox word per kept token; a vector is flagged when a kept token's word is below bk ----
+      uint32_t flagged = 0u;
+      if (all_cand) {
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if ((gmask >> (u * G)) & ((1u << G) - 1u)) flagged |= 1u << u;
+      } else if (gmask) {
+        // counter word of group gi = u * G + g: (first element of vector u) / 4 + g
+        const uint32_t cb0 = (uint32_t)(pv.elem(0) >> 2);
+        auto ctr = [&](int gi) -> uint32_t { return cb0 + (uint32_t)((gi / G) * 32 * G + gi % G); };
+        if (gmask == (uint32_t)((1ull << NG) - 1ull)) {
+          // every token of the lane's vectors is kept: four counters at a time
+#pragma unroll 1
+          for (int g0 = 0; g0 < NG; g0 += 4) {
+            const uint32_t c4[4] = {ctr(g0), ctr(g0 + 1), ctr(g0 + 2), ctr(g0 + 3)};
+            uint32_t m[4];
+            ph.min_words<4>(c4, m);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              if (m[q] < bk) flagged |= 1u << ((g0 + q) / G);
+          }
+        } else {
+#pragma unroll 1
+          for (int gi = 0; gi < NG; ++gi) {
+            if (!((gmask >> gi) & 1u)) continue;
+            const uint32_t c1[1] = {ctr(gi)};
+            uint32_t m[1];
+            ph.min_words<1>(c1, m);
+            if (m[0] < bk) flagged |= 1u << (gi / G);
+          }
+        }
+      }
+      // ---- flagged vectors (rare): exact perturbed scores ----
+      if (__any_sync(kFullMask, flagged != 0u)) {
+        cand = true;
+        while (flagged) {
+          const int u = __ffs(flagged) - 1;
+          flagged &= flagged - 1u;
+          uint4 v;
+          const int cnt = pv.get(u, v);
+          draw_exact<T>(v, cnt, pv.elem(u), gp, It, bscore, bidx);
+        }
+      }
     }
-    __syncthreads();
-    if (ss.issued[slot]) pend[slot] = true;
-    cur.advance();
+    // ---- the warp's best meets the row's ----
+    if (cand) {
+      const ArgMax a = warp_argmax(ArgMax{bscore, bidx, 0.f});
+      if (lane == 0 && a.idx != 0x7FFFFFFF)
+        atomicMax(&gp->best, ((unsigned long long)score_key(a.score) << 32) | (0xFFFFFFFFu - (uint32_t)a.idx));
+    }
   }
-  if (t == 0)
-    for (int b = 0; b < 2; ++b)
-      if (pend[b]) (void)mbar_wait_bounded(&ss.bar[b], uses[b] & 1u, p.wait_cycles);
 }
 
 }  // namespace vsamp

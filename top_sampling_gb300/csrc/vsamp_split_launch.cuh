@@ -13,16 +13,14 @@ inline size_t split_workspace_bytes(int64_t B, int64_t V, int esize) {
          (size_t)B * (size_t)split_nchunks(V, esize) * sizeof(ChunkStat);
 }
 
-// CTAs of `kern` resident per SM on `dev` with two chunk buffers of dynamic shared memory (queried once per
-// device and kernel; the shared-memory attribute is set at the same time)
+// CTAs of `kern` resident per SM on `dev` (queried once per device and kernel)
 template <typename K>
 static int stream_blocks_per_sm(K kern, int dev, int (&cache)[64], std::mutex& mu) {
   if (dev < 0 || dev >= 64) return 0;
   std::lock_guard<std::mutex> lk(mu);
   if (!cache[dev]) {
     int n = 0;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * kChunkBytes) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kSplitThreads, 2 * kChunkBytes) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kStreamThreads, 0) != cudaSuccess) {
       cudaGetLastError();
       return 0;
     }
@@ -35,35 +33,32 @@ template <typename T>
 vsamp_status launch_sample_split(Params p, int64_t B, int esize, void* workspace, cudaStream_t stream) {
   static int occ_stats[64] = {0}, occ_draw[64] = {0};
   static std::mutex mu;
-  const int64_t nch = split_nchunks(p.V, esize);
-  if (nch > 0x7FFFFFFF) return VSAMP_ERR_UNSUPPORTED;
+  const int64_t np = split_nchunks(p.V, esize);
+  if (np > 0x7FFFFFFF) return VSAMP_ERR_UNSUPPORTED;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return VSAMP_ERR_CUDA; }
   DeviceInfo d;
   vsamp_status st = device_info(dev, d);
   if (st != VSAMP_OK) return st;
-  const int ps = stream_blocks_per_sm(stream_stats_kernel<T>, dev, occ_stats, mu);
-  const int pd = stream_blocks_per_sm(stream_draw_kernel<T>, dev, occ_draw, mu);
+  const int ps = stream_blocks_per_sm(warp_stats_kernel<T>, dev, occ_stats, mu);
+  const int pd = stream_blocks_per_sm(warp_draw_kernel<T>, dev, occ_draw, mu);
   if (ps < 1 || pd < 1) return VSAMP_ERR_UNSUPPORTED;
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   RowPlan* plans = reinterpret_cast<RowPlan*>(ws + sizeof(StreamHeader));
   ChunkStat* stats = reinterpret_cast<ChunkStat*>(ws + sizeof(StreamHeader) + (size_t)B * sizeof(RowPlan));
-  const long long total = (long long)B * nch;
-  const int cap = env_int("VSAMP_STREAM_CTAS", 0);
+  const long long warps = (long long)B * np;   // one warp per item at most
   auto grid_of = [&](int per_sm) {
     long long g = (long long)per_sm * d.sm_count;
-    if (cap > 0 && cap < g) g = cap;
-    return g > total ? total : g;
+    const long long need = (warps + kStreamThreads / 32 - 1) / (kStreamThreads / 32);
+    return g > need ? need : g;
   };
   p.row0 = 0;
-  const long long wc = env_ll("VSAMP_WAIT_CYCLES", 0);
-  p.wait_cycles = wc > 0 ? wc : 4000000000LL;   // ~2 s at the maximum SM clock
   const unsigned rows = (unsigned)B;
-  stream_stats_kernel<T><<<(unsigned)grid_of(ps), kSplitThreads, 2 * kChunkBytes, stream>>>(p, stats, (int)nch);
+  warp_stats_kernel<T><<<(unsigned)grid_of(ps), kStreamThreads, 0, stream>>>(p, stats, (int)np);
   if (cudaGetLastError() != cudaSuccess) return VSAMP_ERR_CUDA;
-  stream_plan_kernel<T><<<rows, kSplitThreads, 0, stream>>>(p, plans, stats, (int)nch);
+  stream_plan_kernel<T><<<rows, kSplitThreads, 0, stream>>>(p, plans, stats, (int)np);
   if (cudaGetLastError() != cudaSuccess) return VSAMP_ERR_CUDA;
-  stream_draw_kernel<T><<<(unsigned)grid_of(pd), kSplitThreads, 2 * kChunkBytes, stream>>>(p, plans, (int)nch);
+  warp_draw_kernel<T><<<(unsigned)grid_of(pd), kStreamThreads, 0, stream>>>(p, plans, (int)np);
   if (cudaGetLastError() != cudaSuccess) return VSAMP_ERR_CUDA;
   stream_finish_kernel<T><<<rows, kSplitThreads, 0, stream>>>(p, plans);
   if (cudaGetLastError() != cudaSuccess) return VSAMP_ERR_CUDA;

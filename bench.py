@@ -43,7 +43,7 @@ WORKLOAD = ("c4: B=256 x V=151936 bf16 logits N(0,2.5^2)+1e4 (seed 3), top_p=0.9
 # algorithmic work per step
 BYTES_PER_STEP = B_ROWS * V_COLS * 2                      # one read of every logit
 KEPT_PER_ROW = 144340                                      # ceil(0.95f * 151936): every token ties
-PHILOX_MULS_PER_TOKEN = 10                                 # 10 rounds x 2 products x (lo, hi) / 4 tokens
+WIDE_MULS_PER_COUNTER = 18                                 # 10 rounds x 2 products, 2 formed once per row
 
 
 def _peaks():
@@ -55,7 +55,7 @@ def _peaks():
         return 6800.0, "fallback", 2070.0
 
 
-PROFILE = os.path.join(ROOT, "profiles", "row_kernel_c4_sample.md")
+PROFILE = os.path.join(ROOT, "profiles", "sample_kernel_c4.md")
 
 
 def _csrc_digest() -> str:
@@ -320,10 +320,12 @@ def run_gpu(args):
     hbm_peak, peak_kind, sm_max_mhz = _peaks()
     gbs = BYTES_PER_STEP / (launch_us * 1e-6) / 1e9
     traffic = _traffic()
-    # integer-multiply roofline of the Philox draws: 64 lanes/clk/SM of 32-bit multiplies at the max clock
+    # integer-multiply roofline of the Philox draws: one Philox4x32-10 counter per four kept tokens costs 18 wide
+    # 32x32->64 multiplies; the FMA-heavy pipe retires 32 of them per clock per SM
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    imul_peak = sms * 64 * sm_max_mhz * 1e6 / 1e12                     # T ops/s
-    imul_ach = B_ROWS * KEPT_PER_ROW * PHILOX_MULS_PER_TOKEN / (launch_us * 1e-6) / 1e12
+    counters = B_ROWS * KEPT_PER_ROW / 4
+    alu_peak = sms * 32 * sm_max_mhz * 1e6 / WIDE_MULS_PER_COUNTER / 1e9          # G counters/s
+    alu_ach = counters / (launch_us * 1e-6) / 1e9
     out = {
         "metric": METRIC,
         "value": rows_s,
@@ -343,10 +345,11 @@ def run_gpu(args):
         "logits_read_gbs": gbs * world,
         "hbm_frac": gbs / hbm_peak,
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
-                     "traffic": traffic, "peak_kind": peak_kind, "kernel": "row_kernel<bf16,256,SAMPLE>",
+                     "traffic": traffic, "peak_kind": peak_kind, "kernel": "sample_kernel<bf16,8,3>",
                      "launch_us": launch_us},
-        "roofline_alu": {"bound": "alu", "achieved": imul_ach, "peak": imul_peak, "unit": "Tops/s (32-bit imul)",
-                         "frac": imul_ach / imul_peak},
+        "roofline_alu": {"bound": "alu", "achieved": alu_ach, "peak": alu_peak,
+                         "unit": "G Philox4x32-10 counters/s (18 wide multiplies each, 32 per clock per SM)",
+                         "frac": alu_ach / alu_peak},
         "e2e": {"value": e2e_rows_s, "unit": "rows/s", "h2d_bytes_per_step": BYTES_PER_STEP,
                 "d2h_bytes_per_step": B_ROWS * 8, "steps": e2e_steps},
         "gpu_launches": args.steps,
@@ -408,6 +411,54 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+def run_call(spec: str, repeat: int):
+    """Call one entry point `repeat` times on one workload (`c4:sample`, `c3:topk_select`, ...), untimed: the
+    command the committed ncu summaries capture."""
+    import torch
+
+    import top_sampling_gb300 as ts
+    import workloads
+    from top_sampling_gb300 import build as tb
+
+    tb.build()
+    ts.load()
+    name, fn = spec.split(":")
+    dev = torch.device("cuda:0")
+    b = getattr(workloads, name)()
+
+    def T(a):
+        a = np.asarray(a)
+        return torch.from_numpy(np.ascontiguousarray(a.view(np.int64) if a.dtype == np.uint64 else a)).to(dev)
+
+    if name == "c3":
+        x = torch.from_numpy(np.ascontiguousarray(b.scores)).to(dev)
+        k, lengths = T(b.k), T(b.lengths)
+        for _ in range(repeat):
+            ts.vsamp_topk_select(x, k, k_max=b.k_max, lengths=lengths)
+    else:
+        if b.dtype == "bf16":
+            x = torch.from_numpy(np.ascontiguousarray(b.logits).view(np.int16)).to(dev).view(torch.bfloat16)
+        else:
+            x = torch.from_numpy(np.ascontiguousarray(b.logits)).to(dev)
+        kw = dict(temperature=T(b.temperature), top_k=T(b.top_k), top_p=T(b.top_p), min_p=T(b.min_p), V=b.V)
+        seed, step, token = T(b.seed), T(b.step), torch.zeros(b.B, dtype=torch.int32, device=dev)
+        for _ in range(repeat):
+            if fn in ("sample", "sample_ws"):
+                getattr(ts, "vsamp_" + fn)(x, seed=seed, step=step, **kw)
+            elif fn == "cut":
+                ts.vsamp_topp_minp_mask(x, want_mask=False, **kw)
+            elif fn == "mask":
+                ts.vsamp_topp_minp_mask(x, want_mask=True, **kw)
+            elif fn == "softmax_lse":
+                ts.vsamp_softmax_lse(x, temperature=kw["temperature"], V=b.V)
+            elif fn == "logprob":
+                ts.vsamp_logprob(x, token, temperature=kw["temperature"], V=b.V)
+            else:
+                raise ValueError(f"unknown entry point {fn}")
+    torch.cuda.synchronize()
+    print("ok", spec)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -415,7 +466,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="vsamp", choices=["vsamp", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
+    ap.add_argument("--call", default=None, help="WORKLOAD:ENTRY (e.g. c4:sample): call it --repeat times, untimed")
+    ap.add_argument("--repeat", type=int, default=3)
     args = ap.parse_args()
+    if args.call:
+        run_call(args.call, args.repeat)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -258,9 +258,9 @@ _WORKSPACES = {}
 
 
 def sample_workspace(device, nbytes: int, stream=None) -> torch.Tensor:
-    """A zero-filled workspace of at least nbytes for vsamp_sample_ws, cached per (device, stream).
+    """A workspace of at least nbytes for vsamp_sample_ws, cached per (device, stream).
 
-    The library leaves a workspace zero-filled after every completed call, so it is reused as is; calls
+    A call writes everything it reads in the workspace, so it is reused as is; calls
     on one stream never overlap, so a workspace per stream is enough."""
     dev = torch.device(device)
     key = (dev.index if dev.index is not None else torch.cuda.current_device(), _stream(stream))

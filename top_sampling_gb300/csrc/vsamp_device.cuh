@@ -140,6 +140,11 @@ __device__ __forceinline__ uint4 dsmem_load_v4(uint32_t addr) {
                : "memory");
   return v;
 }
+__device__ __forceinline__ uint32_t dsmem_load_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
 __device__ __forceinline__ void dsmem_store_u32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }

@@ -460,15 +460,26 @@ struct RowEngine {
       ++rounds;
       exchange();
       // cluster-sum the histograms
+      // four peers' values of a bin are loaded before any is added (one round trip per four ranks)
       for (int b = t; b < 256; b += NT) {
         uint32_t cs = 0;
         unsigned long long ms = 0;
-        for (int r = 0; r < C; ++r) {
-          cs += cluster.map_shared_rank(&sh.hcnt[par][b], r)[0];
-          if (hist_mass) {
-            const unsigned long long lo = cluster.map_shared_rank(&sh.hlo[par][b], r)[0];
-            const unsigned long long hi = cluster.map_shared_rank(&sh.hhi[par][b], r)[0];
-            ms += lo + (hi << 32);
+        for (int r0 = 0; r0 < C; r0 += 4) {
+          uint32_t cv[4] = {0u, 0u, 0u, 0u}, lv[4] = {0u, 0u, 0u, 0u}, hv[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            if (r0 + k < C) {
+              cv[k] = dsmem_load_u32(dsmem_map(&sh.hcnt[par][b], (uint32_t)(r0 + k)));
+              if (hist_mass) {
+                lv[k] = dsmem_load_u32(dsmem_map(&sh.hlo[par][b], (uint32_t)(r0 + k)));
+                hv[k] = dsmem_load_u32(dsmem_map(&sh.hhi[par][b], (uint32_t)(r0 + k)));
+              }
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            cs += cv[k];
+            ms += (unsigned long long)lv[k] + ((unsigned long long)hv[k] << 32);
           }
         }
         sh.gcnt[b] = cs;

@@ -19,6 +19,8 @@
 // counters and prune bound.
 #pragma once
 
+#include <cstddef>
+
 #include "vsamp_row.cuh"
 
 namespace vsamp {
@@ -43,11 +45,6 @@ __device__ __forceinline__ void nb_sync(int id, int nthreads) {
 }
 __device__ __forceinline__ void nb_arrive(int id, int nthreads) {
   asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-__device__ __forceinline__ uint32_t dsmem_load_u32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
 }
 
 // Control -> data message (written by the control warp before it arrives on SB_CTL).
@@ -79,10 +76,14 @@ struct SampleSmem {
   uint4 aslot[2][16];                    // CTA 0's copy: each CTA's P4 partial, per row parity
   uint32_t acnt[2];                      // CTA 0's copy: CTAs that have published, per row parity
   SampleCtl ctl;
-  uint32_t hcnt[2][256];                 // radix histograms (count, mass low / high words), per round parity
-  uint32_t hlo[2][256];
-  uint32_t hhi[2][256];
+  __align__(16) uint32_t hcnt[2][256];   // radix histograms (count, mass low / high words), per round parity;
+  __align__(16) uint32_t hlo[2][256];    // 16-byte aligned: the cluster sum reads them as 16-byte vectors
+  __align__(16) uint32_t hhi[2][256];
 };
+
+static_assert(offsetof(SampleSmem, hcnt) % 16 == 0 && offsetof(SampleSmem, hlo) % 16 == 0 &&
+                  offsetof(SampleSmem, hhi) % 16 == 0,
+              "the histograms are read as 16-byte vectors");
 
 __host__ __device__ constexpr int sample_slice_offset() {
   return (int)((sizeof(SampleSmem) + 127) / 128 * 128);
@@ -866,19 +867,38 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
           unsigned long long bm[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) { bc[i] = 0u; bm[i] = 0ull; }
+          // bins 248 - 8l .. 255 - 8l are 32-byte aligned: two 16-byte loads per array and rank, all of a rank's
+          // loads issued before any is used, so a rank costs one round trip
+          const int b0 = 248 - 8 * lane;
           for (int r = 0; r < C; ++r) {
+            uint4 c0, c1, l0 = make_uint4(0u, 0u, 0u, 0u), l1 = l0, h0 = l0, h1 = l0;
+            if (C == 1) {
+              c0 = *reinterpret_cast<const uint4*>(&sh.hcnt[hp][b0]);
+              c1 = *reinterpret_cast<const uint4*>(&sh.hcnt[hp][b0 + 4]);
+              if (hist_mass) {
+                l0 = *reinterpret_cast<const uint4*>(&sh.hlo[hp][b0]);
+                l1 = *reinterpret_cast<const uint4*>(&sh.hlo[hp][b0 + 4]);
+                h0 = *reinterpret_cast<const uint4*>(&sh.hhi[hp][b0]);
+                h1 = *reinterpret_cast<const uint4*>(&sh.hhi[hp][b0 + 4]);
+              }
+            } else {
+              c0 = dsmem_load_v4(dsmem_map(&sh.hcnt[hp][b0], (uint32_t)r));
+              c1 = dsmem_load_v4(dsmem_map(&sh.hcnt[hp][b0 + 4], (uint32_t)r));
+              if (hist_mass) {
+                l0 = dsmem_load_v4(dsmem_map(&sh.hlo[hp][b0], (uint32_t)r));
+                l1 = dsmem_load_v4(dsmem_map(&sh.hlo[hp][b0 + 4], (uint32_t)r));
+                h0 = dsmem_load_v4(dsmem_map(&sh.hhi[hp][b0], (uint32_t)r));
+                h1 = dsmem_load_v4(dsmem_map(&sh.hhi[hp][b0 + 4], (uint32_t)r));
+              }
+            }
+            // bc[i] / bm[i] hold bin 255 - 8l - i = b0 + 7 - i
+            const uint32_t cc[8] = {c1.w, c1.z, c1.y, c1.x, c0.w, c0.z, c0.y, c0.x};
+            const uint32_t ll[8] = {l1.w, l1.z, l1.y, l1.x, l0.w, l0.z, l0.y, l0.x};
+            const uint32_t hh[8] = {h1.w, h1.z, h1.y, h1.x, h0.w, h0.z, h0.y, h0.x};
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              const int b = 255 - 8 * lane - i;
-              if (C == 1) {
-                bc[i] += sh.hcnt[hp][b];
-                if (hist_mass) bm[i] += u64_of(sh.hlo[hp][b], sh.hhi[hp][b]);
-              } else {
-                bc[i] += dsmem_load_u32(dsmem_map(&sh.hcnt[hp][b], (uint32_t)r));
-                if (hist_mass)
-                  bm[i] += u64_of(dsmem_load_u32(dsmem_map(&sh.hlo[hp][b], (uint32_t)r)),
-                                  dsmem_load_u32(dsmem_map(&sh.hhi[hp][b], (uint32_t)r)));
-              }
+              bc[i] += cc[i];
+              if (hist_mass) bm[i] += u64_of(ll[i], hh[i]);
             }
           }
           if (mass_mode && gp >= 0.f && shift == Tr::KB - 8) {

@@ -317,3 +317,33 @@ def topk_select_row(scores, length: int, k: int, k_max: int):
     sel = np.sort(canonical_order(x)[:min(k, n)])
     out[:sel.size] = sel
     return STATUS_OK, out
+
+
+def topn_logprobs_row(row, dtype: str, temperature, n_top: int):
+    """The n_top most probable tokens of a row and their log-probabilities (a top-N logprob list).
+
+    [LOGP] "Design: the numeric contract" gives the per-token log-probability min(z_t - lse, 0) with the
+    temperature applied to the statistics; the list holds the first n_top tokens of the order (logit
+    descending, token id ascending; [TOPP] step 2, [TOPK] Changes for ties), i.e. the most probable first.
+    Returns (status, m, log S, idx[n_top], lp[n_top]); slots past the row length are -1 / NaN, and a row
+    with a non-finite logit or temperature returns the error with every slot -1 / NaN.
+    """
+    x = widen(row, dtype)
+    T = as_f32(temperature)
+    idx = np.full(int(n_top), -1, dtype=np.int64)
+    lp = np.full(int(n_top), np.nan, dtype=np.float64)
+    if not np.all(np.isfinite(x)):
+        return STATUS_NONFINITE, math.nan, math.nan, idx, lp
+    if math.isnan(T) or math.isinf(T):
+        return STATUS_INVALID_ARG, math.nan, math.nan, idx, lp
+    t_eff = T if T > 0 else 1.0
+    m = float(x.max())
+    s = (x - m) / t_eff
+    log_s = math.log(math.fsum(np.exp(s).tolist()))
+    order = canonical_order(x)
+    take = min(int(n_top), x.size)
+    for j in range(take):
+        v = int(order[j])
+        idx[j] = v
+        lp[j] = min(float(s[v]) - log_s, 0.0)
+    return STATUS_OK, m, log_s, idx, lp

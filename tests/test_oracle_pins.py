@@ -475,3 +475,57 @@ def test_argmax_ties_go_to_the_lowest_index():
     assert sm.argmax_lowest(np.array([2.0, 5.0, 5.0, 1.0]), cand)[0] == 3
     assert sm.argmax_lowest(np.array([5.0, 5.0, 5.0, 5.0]), cand)[0] == 1
     assert list(sm.argmax_lowest(np.array([[1.0, 0.0, 1.0, 0.0], [0.0, 2.0, 0.0, 2.0]]), cand)) == [7, 1]
+
+
+# ----------------------------------------------------------------------------------------------
+# Top-N log-probability lists
+# ----------------------------------------------------------------------------------------------
+def test_topn_list_dominates_everything_after_it_on_tiny_rows():
+    """The defining property, checked pairwise (no sorting): every listed token precedes every later one and
+    every unlisted one in the order (logit descending, index ascending)."""
+    rng = np.random.default_rng(11)
+    for trial in range(300):
+        n = int(rng.integers(1, 9))
+        x = (rng.integers(-3, 4, size=n) / 2.0).astype(np.float32)   # many ties
+        N = int(rng.integers(1, 10))
+        st, m, ls, idx, lp = sm.topn_logprobs_row(x, "f32", 1.0, N)
+        assert st == 0
+        listed = [int(v) for v in idx if v >= 0]
+        assert len(listed) == min(N, n)
+        assert all(v == -1 for v in idx[len(listed):]) and all(math.isnan(v) for v in lp[len(listed):])
+
+        def before(a, b):
+            return x[a] > x[b] or (x[a] == x[b] and a < b)
+
+        for i, a in enumerate(listed):
+            for b in listed[i + 1:]:
+                assert before(a, b), (trial, x, listed)
+            for b in set(range(n)) - set(listed):
+                assert before(a, b), (trial, x, listed)
+
+
+def test_topn_logprobs_closed_forms():
+    # uniform row: the first N indices, each with log-probability -log V
+    V = 1000
+    st, m, ls, idx, lp = sm.topn_logprobs_row(np.zeros(V, np.float32), "f32", 1.0, 20)
+    assert st == 0 and list(idx) == list(range(20))
+    assert np.allclose(lp, -math.log(V), atol=1e-12, rtol=0)
+    # two levels: n_a tokens at a, n_b at b; log p(a-token) = -log(n_a + n_b e^{(b - a)/T}) in closed form
+    a, b, n_a, n_b, T = 1.5, -0.25, 3, 17, 0.75
+    x = np.full(n_a + n_b, b, np.float32)
+    pos = [4, 9, 13]
+    x[pos] = a
+    st, m, ls, idx, lp = sm.topn_logprobs_row(x, "f32", T, 5)
+    assert list(idx[:3]) == pos and list(idx[3:]) == [0, 1]
+    want_a = -math.log(n_a + n_b * math.exp((float(np.float32(b)) - float(np.float32(a))) / float(np.float32(T))))
+    want_b = want_a + (float(np.float32(b)) - float(np.float32(a))) / float(np.float32(T))
+    assert abs(lp[0] - want_a) < 1e-12 and abs(lp[4] - want_b) < 1e-12
+    # the whole row listed: probabilities sum to one and the list is non-increasing
+    x = np.random.default_rng(5).normal(0, 2, 257).astype(np.float32)
+    st, m, ls, idx, lp = sm.topn_logprobs_row(x, "f32", 1.3, 257)
+    assert abs(math.fsum(np.exp(lp).tolist()) - 1.0) < 1e-12
+    assert np.all(np.diff(lp) <= 0)
+    # greedy temperature reads as T = 1; a non-finite logit is a row error
+    assert sm.topn_logprobs_row(x, "f32", 0.0, 3)[4][0] == sm.topn_logprobs_row(x, "f32", 1.0, 3)[4][0]
+    x[7] = np.inf
+    assert sm.topn_logprobs_row(x, "f32", 1.0, 3)[0] == sm.STATUS_NONFINITE

@@ -453,6 +453,8 @@ def run_call(spec: str, repeat: int):
                 ts.vsamp_softmax_lse(x, temperature=kw["temperature"], V=b.V)
             elif fn == "logprob":
                 ts.vsamp_logprob(x, token, temperature=kw["temperature"], V=b.V)
+            elif fn == "topn_logprobs":
+                ts.vsamp_topn_logprobs(x, 20, temperature=kw["temperature"], V=b.V)
             else:
                 raise ValueError(f"unknown entry point {fn}")
     torch.cuda.synchronize()

@@ -190,6 +190,25 @@ vsamp_status vsamp_logprob(const void* logits, vsamp_dtype dt, int64_t B, int64_
                            const float* temperature, const int32_t* token, const float* row_max,
                            const float* row_logsum, float* out, int32_t* row_status, void* stream);
 
+/* Top-N log-probability lists ("[Kernel] Make persistent_topk deterministic", details of the probe: per
+ * generated token the list of the 20 most probable (token, logprob) pairs, hashed to compare runs; the
+ * log-probabilities follow "[WS2][Logprob] ...", Design: logp = min(z_v - lse, 0)).
+ *   N            list length, 1 <= N <= VSAMP_TOPN_MAX (else VSAMP_ERR_INVALID_ARG, nothing enqueued).
+ *   row_max, row_logsum  [B] fp32, required: written as by vsamp_softmax_lse at the row's temperature.
+ *   out_idx      [B, N] int32: slot j holds the (j+1)-th token of the row in the order (logit descending,
+ *                index ascending); equal logits keep ascending index order, -0 equals +0.
+ *   out_lp       [B, N] fp32: min((x[r, v] - row_max[r]) / T_r - row_logsum[r], 0) for the token in slot j,
+ *                T_r <= 0 read as 1.
+ *   Slots past min(N, V), and every slot of an error row (a non-finite logit, a NaN or infinite
+ *   temperature; row_status as vsamp_softmax_lse reports it), hold -1 and NaN.
+ * Three launches on `stream`: a top-N select, the row statistics, and one CTA per row that orders the N
+ * tokens (O(N^2 / 256) comparisons per thread) and writes their log-probabilities. The list is a function
+ * of the row alone: it does not depend on B, the launch geometry or neighbouring rows. */
+#define VSAMP_TOPN_MAX 4096
+vsamp_status vsamp_topn_logprobs(const void* logits, vsamp_dtype dt, int64_t B, int64_t V, int64_t ld,
+                                 const float* temperature, int32_t N, float* row_max, float* row_logsum,
+                                 int32_t* out_idx, float* out_lp, int32_t* row_status, void* stream);
+
 /* Static description of a status code. */
 const char* vsamp_status_string(vsamp_status s);
 

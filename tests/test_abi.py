@@ -101,3 +101,25 @@ def test_workspace_size_and_host_checks_of_the_workspace_entry_point(lib):
     assert l2.vsamp_sample_ws(*args, None, 4096, None) == ts.VSAMP_ERR_INVALID_ARG          # no workspace
     assert l2.vsamp_sample_ws(*args, ctypes.c_void_p(4096 + 8), 4096, None) == ts.VSAMP_ERR_INVALID_ARG   # unaligned
     assert l2.vsamp_sample_ws(*args, ctypes.c_void_p(4096), 16, None) == ts.VSAMP_ERR_INVALID_ARG  # too small
+
+
+def test_host_checks_of_the_topn_entry_point(lib):
+    # list length and the required outputs are checked on the host, before any CUDA call
+    import top_sampling_gb300 as ts
+    l2 = ts.load()
+    hdr = open(os.path.join(ROOT, "include", "vsamp.h")).read()
+    assert "#define VSAMP_TOPN_MAX 4096" in hdr
+    d = ctypes.c_void_p(4096)
+    good = dict(rm=d, rl=d, oi=d, ol=d)
+
+    def call(N, rm, rl, oi, ol):
+        return l2.vsamp_topn_logprobs(d, ts.VSAMP_F32, 4, 100, 100, None, N, rm, rl, oi, ol, None, None)
+
+    assert call(0, **good) == ts.VSAMP_ERR_INVALID_ARG
+    assert call(4097, **good) == ts.VSAMP_ERR_INVALID_ARG
+    assert call(20, **{**good, "rm": None}) == ts.VSAMP_ERR_INVALID_ARG
+    assert call(20, **{**good, "rl": None}) == ts.VSAMP_ERR_INVALID_ARG
+    assert call(20, **{**good, "oi": None}) == ts.VSAMP_ERR_INVALID_ARG
+    assert call(20, **{**good, "ol": None}) == ts.VSAMP_ERR_INVALID_ARG
+    assert l2.vsamp_topn_logprobs(None, ts.VSAMP_F32, 4, 100, 100, None, 20, d, d, d, d, None, None) == \
+        ts.VSAMP_ERR_INVALID_ARG

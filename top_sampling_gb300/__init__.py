@@ -29,7 +29,8 @@ VSAMP_F32 = 0
 VSAMP_BF16 = 1
 
 EXPORTED = ("vsamp_softmax_lse", "vsamp_topk_select", "vsamp_topp_minp_mask", "vsamp_sample",
-            "vsamp_sample_ws", "vsamp_sample_workspace_size", "vsamp_sample_static", "vsamp_logprob", "vsamp_status_string",
+            "vsamp_sample_ws", "vsamp_sample_workspace_size", "vsamp_sample_static", "vsamp_logprob", "vsamp_topn_logprobs",
+            "vsamp_status_string",
             "vsamp_device_info", "vsamp_version")
 
 
@@ -71,10 +72,11 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.vsamp_sample_ws.argtypes = [vp, st, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                     ctypes.c_size_t, vp]
     lib.vsamp_sample_static.argtypes = [vp, st, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.vsamp_topn_logprobs.argtypes = [vp, st, i64, i64, i64, vp, i32, vp, vp, vp, vp, vp, vp]
     lib.vsamp_sample_workspace_size.argtypes = [st, i64, i64]
     lib.vsamp_sample_workspace_size.restype = ctypes.c_size_t
     for f in ("vsamp_softmax_lse", "vsamp_topk_select", "vsamp_topp_minp_mask", "vsamp_sample", "vsamp_logprob",
-              "vsamp_sample_ws", "vsamp_sample_static"):
+              "vsamp_sample_ws", "vsamp_sample_static", "vsamp_topn_logprobs"):
         getattr(lib, f).restype = st
     lib.vsamp_status_string.argtypes = [st]
     lib.vsamp_status_string.restype = ctypes.c_char_p
@@ -355,3 +357,26 @@ def vsamp_logprob(logits, token, temperature=None, row_max=None, row_logsum=None
         _ptr(row_status, torch.int32, dev, B, "row_status"), _stream(stream))
     _check(st, "vsamp_logprob")
     return out, row_status
+
+
+def vsamp_topn_logprobs(logits, n, temperature=None, V=None, row_max=None, row_logsum=None, out_idx=None,
+                        out_lp=None, row_status=None, stream=None):
+    """The n most probable tokens per row by (logit desc, index asc) with their log-probabilities.
+    Returns (out_idx [B, n] int32, out_lp [B, n] fp32, row_max, row_logsum, row_status)."""
+    B, V, ld = _rows(logits, V)
+    dev = logits.device
+    n = int(n)
+    temperature = _param(temperature, B, torch.float32, dev, "temperature")
+    row_max = torch.empty(B, dtype=torch.float32, device=dev) if row_max is None else row_max
+    row_logsum = torch.empty(B, dtype=torch.float32, device=dev) if row_logsum is None else row_logsum
+    out_idx = torch.empty((B, max(n, 1)), dtype=torch.int32, device=dev) if out_idx is None else out_idx
+    out_lp = torch.empty((B, max(n, 1)), dtype=torch.float32, device=dev) if out_lp is None else out_lp
+    row_status = torch.empty(B, dtype=torch.int32, device=dev) if row_status is None else row_status
+    st = load().vsamp_topn_logprobs(
+        logits.data_ptr(), _dtype_code(logits), B, V, ld, _ptr(temperature, torch.float32, dev, B, "temperature"),
+        n, _ptr(row_max, torch.float32, dev, B, "row_max"), _ptr(row_logsum, torch.float32, dev, B, "row_logsum"),
+        _ptr(out_idx, torch.int32, dev, B * max(n, 1), "out_idx"),
+        _ptr(out_lp, torch.float32, dev, B * max(n, 1), "out_lp"),
+        _ptr(row_status, torch.int32, dev, B, "row_status"), _stream(stream))
+    _check(st, "vsamp_topn_logprobs")
+    return out_idx, out_lp, row_max, row_logsum, row_status

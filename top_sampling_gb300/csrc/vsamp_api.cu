@@ -219,6 +219,58 @@ __global__ void logprob_from_stats_kernel(const unsigned char* x, int64_t B, int
   if (row_status) row_status[r] = st;
 }
 
+// Top-N log-probability lists from a top-N select (indices in ascending order) and the row statistics: one
+// CTA per row, grid-stride over rows. A token's place in the list is the number of listed tokens before it
+// in the order (logit descending, index ascending); equal logits keep their ascending index order.
+constexpr int kTopnThreads = 256;
+
+template <typename T>
+__global__ void __launch_bounds__(kTopnThreads) topn_rank_kernel(const unsigned char* x, int64_t B, int64_t V,
+                                                                 int64_t ld, const float* temperature, int32_t N,
+                                                                 const float* row_max, const float* row_logsum,
+                                                                 int32_t* out_idx, float* out_lp) {
+  extern __shared__ float topn_smem[];
+  float* sv = topn_smem;                                        // [N] logits of the listed tokens
+  int32_t* si = reinterpret_cast<int32_t*>(topn_smem + N);      // [N] their indices
+  const int n = (int)(V < (int64_t)N ? V : (int64_t)N);
+  const float qnan = __int_as_float(0x7FC00000);
+  for (int64_t r = blockIdx.x; r < B; r += gridDim.x) {
+    int32_t* oi = out_idx + r * N;
+    float* ol = out_lp + r * N;
+    const float m = row_max[r], ls = row_logsum[r];
+    if (!(isfinite(m) && isfinite(ls))) {   // the statistics of an error row are NaN: an empty list
+      for (int j = threadIdx.x; j < N; j += blockDim.x) {
+        oi[j] = -1;
+        ol[j] = qnan;
+      }
+      continue;
+    }
+    const float temp = temperature ? temperature[r] : 1.f;
+    const float invT = 1.f / (temp > 0.f ? temp : 1.f);
+    for (int j = threadIdx.x; j < n; j += blockDim.x) {
+      const int32_t v = oi[j];
+      si[j] = v;
+      sv[j] = (v >= 0 && (int64_t)v < V) ? Traits<T>::load_global(x, r * ld + v) : -INFINITY;
+    }
+    __syncthreads();
+    for (int j = threadIdx.x; j < n; j += blockDim.x) {
+      const float xj = sv[j];
+      int rank = 0;
+      for (int i = 0; i < n; ++i) {
+        const float xi = sv[i];
+        rank += (xi > xj || (xi == xj && i < j)) ? 1 : 0;
+      }
+      oi[rank] = si[j];
+      ol[rank] = (float)fmin((double)((xj - m) * invT) - (double)ls, 0.0);
+    }
+    for (int j = n + threadIdx.x; j < N; j += blockDim.x) {
+      oi[j] = -1;
+      ol[j] = qnan;
+    }
+    __syncthreads();   // the next row reuses the shared arrays
+  }
+}
+
 }  // namespace vsamp
 
 namespace vsamp {
@@ -404,6 +456,51 @@ vsamp_status vsamp_logprob(const void* logits, vsamp_dtype dt, int64_t B, int64_
   p.logprob = out;
   p.row_status = row_status;
   return dispatch<MODE_LOGPROB>(p, dt, B, s);
+}
+
+vsamp_status vsamp_topn_logprobs(const void* logits, vsamp_dtype dt, int64_t B, int64_t V, int64_t ld,
+                                 const float* temperature, int32_t N, float* row_max, float* row_logsum,
+                                 int32_t* out_idx, float* out_lp, int32_t* row_status, void* stream) {
+  vsamp_status st = check_common(logits, dt, B, V, ld);
+  if (st != VSAMP_OK) return st;
+  if (N <= 0 || N > VSAMP_TOPN_MAX || !row_max || !row_logsum || !out_idx || !out_lp) return VSAMP_ERR_INVALID_ARG;
+  if (V > 0x7FFFFFFFLL) return VSAMP_ERR_UNSUPPORTED;   // 32-bit token indices
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // 1. the N best indices in ascending index order
+  Params p = base_params(logits, dt, B, V, ld);
+  p.k_max = N;
+  p.out_idx = out_idx;
+  st = dispatch<MODE_SELECT>(p, dt, B, s);
+  if (st != VSAMP_OK) return st;
+  // 2. the row statistics at the row's temperature (and the row status)
+  p = base_params(logits, dt, B, V, ld);
+  p.temperature = temperature;
+  p.row_max = row_max;
+  p.row_logsum = row_logsum;
+  p.row_status = row_status;
+  st = dispatch<MODE_LSE>(p, dt, B, s);
+  if (st != VSAMP_OK) return st;
+  // 3. order the list and attach the log-probabilities
+  DeviceInfo d;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return VSAMP_ERR_CUDA;
+  }
+  st = device_info(dev, d);
+  if (st != VSAMP_OK) return st;
+  const int64_t cap = (int64_t)d.sm_count * 8;
+  const unsigned blocks = (unsigned)(B < cap ? B : cap);
+  const size_t smem = (size_t)N * (sizeof(float) + sizeof(int32_t));
+  const unsigned char* x = static_cast<const unsigned char*>(logits);
+  if (dt == VSAMP_F32)
+    topn_rank_kernel<float><<<blocks, kTopnThreads, smem, s>>>(x, B, V, ld, temperature, N, row_max, row_logsum,
+                                                               out_idx, out_lp);
+  else
+    topn_rank_kernel<__nv_bfloat16><<<blocks, kTopnThreads, smem, s>>>(x, B, V, ld, temperature, N, row_max,
+                                                                       row_logsum, out_idx, out_lp);
+  if (cudaGetLastError() != cudaSuccess) return VSAMP_ERR_CUDA;
+  return VSAMP_OK;
 }
 
 const char* vsamp_status_string(vsamp_status s) {

@@ -201,7 +201,8 @@ vsamp_status vsamp_logprob(const void* logits, vsamp_dtype dt, int64_t B, int64_
  *                T_r <= 0 read as 1.
  *   Slots past min(N, V), and every slot of an error row (a non-finite logit, a NaN or infinite
  *   temperature; row_status as vsamp_softmax_lse reports it), hold -1 and NaN.
- * Three launches on `stream`: a top-N select, the row statistics, and one CTA per row that orders the N
+ * Two launches on `stream`: one pass over each row (row statistics and the top-k cut with k = N, the N
+ * indices emitted in ascending order), then one CTA per row that orders the N
  * tokens (O(N^2 / 256) comparisons per thread) and writes their log-probabilities. The list is a function
  * of the row alone: it does not depend on B, the launch geometry or neighbouring rows. */
 #define VSAMP_TOPN_MAX 4096

@@ -466,21 +466,18 @@ vsamp_status vsamp_topn_logprobs(const void* logits, vsamp_dtype dt, int64_t B, 
   if (N <= 0 || N > VSAMP_TOPN_MAX || !row_max || !row_logsum || !out_idx || !out_lp) return VSAMP_ERR_INVALID_ARG;
   if (V > 0x7FFFFFFFLL) return VSAMP_ERR_UNSUPPORTED;   // 32-bit token indices
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // 1. the N best indices in ascending index order
+  // 1. one pass over each row: the row statistics at the row's temperature, the row status, and the N best
+  //    indices (the top-k cut with k = N) in ascending index order
   Params p = base_params(logits, dt, B, V, ld);
-  p.k_max = N;
-  p.out_idx = out_idx;
-  st = dispatch<MODE_SELECT>(p, dt, B, s);
-  if (st != VSAMP_OK) return st;
-  // 2. the row statistics at the row's temperature (and the row status)
-  p = base_params(logits, dt, B, V, ld);
   p.temperature = temperature;
   p.row_max = row_max;
   p.row_logsum = row_logsum;
   p.row_status = row_status;
-  st = dispatch<MODE_LSE>(p, dt, B, s);
+  p.k_max = N;
+  p.out_idx = out_idx;
+  st = dispatch<MODE_LSE | MODE_TOPN>(p, dt, B, s);
   if (st != VSAMP_OK) return st;
-  // 3. order the list and attach the log-probabilities
+  // 2. order the list and attach the log-probabilities
   DeviceInfo d;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {

@@ -34,6 +34,7 @@ enum Mode : int {
   MODE_MASK = 8,      // uint8 mask of the cut
   MODE_SAMPLE = 16,   // Gumbel-max draw + log-probability
   MODE_LOGPROB = 32,  // log-probability of given tokens (statistics recomputed)
+  MODE_TOPN = 64,     // the k_max best tokens (out_idx, ascending index order): the top-k cut, any temperature
 };
 
 // Path flags reported in stats[r][3].
@@ -750,7 +751,8 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
   constexpr int VE = Tr::VE;
   constexpr int ES = Tr::ESIZE;
   constexpr bool kSel = (MODE & MODE_SELECT) != 0;
-  constexpr bool kCutLike = (MODE & (MODE_CUT | MODE_SAMPLE)) != 0;
+  constexpr bool kTopn = (MODE & MODE_TOPN) != 0;
+  constexpr bool kCutLike = (MODE & (MODE_CUT | MODE_SAMPLE | MODE_TOPN)) != 0;
   extern __shared__ __align__(128) unsigned char dyn[];
   Smem<NT>& sh = *reinterpret_cast<Smem<NT>*>(dyn);
   unsigned char* slice = dyn + slice_offset<NT>();
@@ -834,6 +836,7 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
   if (p.min_p) minp = p.min_p[row];
   int32_t ksel = p.k_max;
   if (kSel && p.k_sel) ksel = p.k_sel[row];
+  if (kTopn) topk = p.k_max;
   uint64_t sd = 0ull, st = 0ull;
   uint32_t rid = (uint32_t)row;
   if (MODE & MODE_SAMPLE) {
@@ -937,6 +940,7 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
       }
     }
   }
+  const float thr_mx = mx;   // this thread's maximum, before the reductions
   E.passes = 1;
   float M, Mmin;
   uint32_t gflags;
@@ -978,8 +982,9 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
     tok_in = p.token_in[row];
     if (tok_in < 0 || (int64_t)tok_in >= n) status = VSAMP_ERR_INVALID_ARG;
   }
-  const bool greedy = !(temp > 0.f);
-  const float Teff = greedy ? 1.f : temp;
+  // T <= 0 means greedy sampling; a top-N list is the same at every temperature (T <= 0 read as 1)
+  const bool greedy = !kTopn && !(temp > 0.f);
+  const float Teff = temp > 0.f ? temp : 1.f;
   const float invT = 1.f / Teff;
   const float c1 = kLog2e * invT;
   const bool minp_on = kCutLike && !greedy && minp > 0.f;
@@ -1385,24 +1390,28 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
     }
   }
 
-  // ---------------- top-k select emission (ascending index order) ----------------
-  if (kSel) {
+  // ---------------- top-k select / top-N emission (ascending index order) ----------------
+  if (kSel || kTopn) {
     int32_t* orow = p.out_idx + (int64_t)row * p.k_max;
     uint32_t total = 0;
     if (fin_valid && !select_none) {
+      // a thread whose maximum is below the cut, or equal to it with the boundary before its chunk, keeps nothing
+      const bool none_here = !(thr_mx > xP || (thr_mx == xP && (int64_t)It >= E.thr_e0));
       uint32_t c = 0;
-      E.for_each([&](int64_t e, float x) { c += (x > xP || (x == xP && e <= (int64_t)It)) ? 1u : 0u; });
+      if (!none_here)
+        E.for_each([&](int64_t e, float x) { c += (x > xP || (x == xP && e <= (int64_t)It)) ? 1u : 0u; });
       sh.tcount[t] = c;
       const uint32_t ctot = E.block_scan_tcount();
       uint32_t cpre;
       E.cluster_prefix_u32(ctot, 1, cpre, total);
       uint32_t pos = cpre + sh.tpre[t];
-      E.for_each([&](int64_t e, float x) {
-        if (x > xP || (x == xP && e <= (int64_t)It)) {
-          if (pos < (uint32_t)p.k_max) orow[pos] = (int32_t)e;
-          ++pos;
-        }
-      });
+      if (c)
+        E.for_each([&](int64_t e, float x) {
+          if (x > xP || (x == xP && e <= (int64_t)It)) {
+            if (pos < (uint32_t)p.k_max) orow[pos] = (int32_t)e;
+            ++pos;
+          }
+        });
       E.passes += 2;
     }
     if (crank == 0)

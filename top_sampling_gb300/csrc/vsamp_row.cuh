@@ -322,6 +322,31 @@ struct RowEngine {
     }
   }
 
+  // Calls f(global index, value) -> bool for every valid element of the vectors of this thread's chunk whose
+  // bit is set in cand (bit b of word w: vector 32 w + b), in index order; out gets the bits of the vectors
+  // where f returned true for some element.
+  template <class F>
+  __device__ __forceinline__ void for_each_cand(const uint32_t (&cand)[2], uint32_t (&out)[2], F&& f) {
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+      uint32_t bits = cand[w], hit = 0u;
+      while (bits) {
+        const int b = __ffs(bits) - 1;
+        bits &= bits - 1u;
+        const int j = w * 32 + b;
+        const int cnt = thr_n - j * VE < VE ? thr_n - j * VE : VE;
+        float x[VE];
+        Tr::values(mine[j], x);
+        bool any = false;
+#pragma unroll
+        for (int i = 0; i < VE; ++i)
+          if (i < cnt && f(thr_e0 + (int64_t)j * VE + i, x[i])) any = true;
+        if (any) hit |= 1u << b;
+      }
+      out[w] = hit;
+    }
+  }
+
   // Cluster exclusive prefix of a per-CTA value: returns (sum over lower ranks, total) to every thread.
   __device__ void cluster_prefix_u32(uint32_t mine_val, int slot, uint32_t& pre, uint32_t& total) {
     if (t == 0) my_mail().u[slot] = mine_val;
@@ -413,13 +438,22 @@ struct RowEngine {
   // MASS: the group where the cumulative mass (from the largest key down) first reaches the goal;
   //       if goal_p >= 0 the goal is ceil(goal_p * total mass of the row) taken in the first round.
   // want_mass: also histogram masses (mass_above / mass_eq are valid).
+  // floor_rk: keys below it are left out of the histograms. The caller passes a floor only when the goal is
+  //   reached within the keys at or above it, so the group found and its counts do not change.
+  // Each round visits only the vectors of the thread's chunk that held an element matching the previous
+  // round's prefix (chunks of at most 64 vectors; longer chunks visit every vector).
   __device__ RadixOut radix_search(bool mass_mode, unsigned long long goal, float goal_p, bool want_mass, float M,
-                                   float c1) {
+                                   float c1, uint32_t floor_rk = 0u) {
     RadixOut out{};
     out.ok = 1;
     uint32_t prefix = 0;
     unsigned long long cnt_above = 0, mass_above = 0;
     const bool hist_mass = want_mass || mass_mode;
+    const int nvec = (thr_n + VE - 1) / VE;
+    const bool masked = nvec <= 64;
+    uint32_t cand[2];
+    cand[0] = nvec >= 32 ? 0xFFFFFFFFu : ((1u << nvec) - 1u);
+    cand[1] = nvec >= 64 ? 0xFFFFFFFFu : (nvec > 32 ? ((1u << (nvec - 32)) - 1u) : 0u);
     for (int shift = Tr::KB - 8; shift >= 0; shift -= 8) {
       const int par = xc & 1;
       uint32_t* hc = sh.hcnt[par];
@@ -442,9 +476,10 @@ struct RowEngine {
           }
         }
       };
-      for_each([&](int64_t, float x) {
+      auto visit = [&](int64_t, float x) -> bool {
         const uint32_t rk = Tr::rkey_of_value(x);
-        if ((rk & hmask) == (prefix & hmask)) {
+        const bool match = (rk & hmask) == (prefix & hmask) && rk >= floor_rk;
+        if (match) {
           const uint32_t bin = (rk >> shift) & 255u;
           if (bin != run_bin) {
             flush();
@@ -455,7 +490,16 @@ struct RowEngine {
           ++run_cnt;
           if (hist_mass) run_mass += mass_fx(ex2_approx((x - M) * c1));
         }
-      });
+        return match;
+      };
+      if (masked) {
+        uint32_t next[2];
+        for_each_cand(cand, next, visit);
+        cand[0] = next[0];
+        cand[1] = next[1];
+      } else {
+        for_each([&](int64_t e, float x) { (void)visit(e, x); });
+      }
       flush();
       ++passes;
       ++rounds;
@@ -1150,7 +1194,9 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
           }
         }
         if (plan.cp_mode == 2 && plan.status == VSAMP_OK) {
-          const RadixOut r = E.radix_search(true, plan.cp_goal, plan.goal_p, true, M, c1);
+          // after a top-k cut the goal lies within the keys at or above its pivot
+          const uint32_t floor_rk = plan.ck_mode == 2 ? plan.ck.rk : 0u;
+          const RadixOut r = E.radix_search(true, plan.cp_goal, plan.goal_p, true, M, c1, floor_rk);
           {
             if (!r.ok) plan.status = VSAMP_ERR_INVALID_ARG;
             const unsigned long long wP = mass_fx(ex2_approx((Tr::value_of_rkey(r.rk) - M) * c1));

@@ -59,6 +59,7 @@ struct SampleCtl {
   int32_t hpar;             // REQ_HIST: histogram buffer
   int32_t shift;            // REQ_HIST: bin = (key >> shift) & 255 for keys matching prefix above shift + 8
   uint32_t prefix;
+  uint32_t floor_rk;        // REQ_HIST: keys below it are left out
   uint32_t kmin32;          // min-p threshold (fp32 key space)
   uint32_t bk;              // prune bound on the Philox word
   uint32_t rid, st_lo, st_hi, k0, k1;
@@ -430,6 +431,11 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
 
       // ---- requests of the control warp: radix histograms, tie counts ----
       uint32_t eq_thr = 0u, eq_pre = 0u;
+      // vectors of this thread's chunk that held an element matching the previous round's prefix (bit j:
+      // vector j; chunks of at most 64 vectors, longer ones visit every vector)
+      const int nvec_thr = (thr_n + VE - 1) / VE;
+      const bool masked = nvec_thr <= 64;
+      uint32_t cand0 = 0u, cand1 = 0u;
       int req;
       for (;;) {
         nb_sync(SB_CTL, kSampleThreads);
@@ -439,6 +445,7 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
           const int shift = sh.ctl.shift, hp = sh.ctl.hpar;
           const bool hist_mass = sh.ctl.hist_mass != 0;
           const uint32_t prefix = sh.ctl.prefix;
+          const uint32_t floor_rk = sh.ctl.floor_rk;
           const float c1 = sh.ctl.c1;
           const int hi_shift = shift + 8;
           const uint32_t hmask = hi_shift >= 32 ? 0u : (0xFFFFFFFFu << hi_shift);
@@ -458,14 +465,17 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
               }
             }
           };
-          for (int j = 0; j * VE < thr_n; ++j) {
+          // the vector's elements into the running bin; true if one matched
+          auto visit = [&](int j) -> bool {
             float x[VE];
             Tr::values(mine[j], x);
+            bool any = false;
 #pragma unroll
             for (int i = 0; i < VE; ++i) {
               if (j * VE + i >= thr_n) break;
               const uint32_t rk = Tr::rkey_of_value(x[i]);
-              if ((rk & hmask) == (prefix & hmask)) {
+              if ((rk & hmask) == (prefix & hmask) && rk >= floor_rk) {
+                any = true;
                 const uint32_t bin = (rk >> shift) & 255u;
                 if (bin != run_bin) {
                   flush();
@@ -477,6 +487,26 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
                 if (hist_mass) run_mass += mass_fx(ex2_approx((x[i] - M) * c1));
               }
             }
+            return any;
+          };
+          if (masked) {
+            if (shift == Tr::KB - 8) {   // the first round of a search visits every vector
+              cand0 = nvec_thr >= 32 ? 0xFFFFFFFFu : ((1u << nvec_thr) - 1u);
+              cand1 = nvec_thr >= 64 ? 0xFFFFFFFFu : (nvec_thr > 32 ? ((1u << (nvec_thr - 32)) - 1u) : 0u);
+            }
+            uint32_t next0 = 0u, next1 = 0u;
+            for (uint32_t bits = cand0; bits; bits &= bits - 1u) {
+              const int b = __ffs(bits) - 1;
+              if (visit(b)) next0 |= 1u << b;
+            }
+            for (uint32_t bits = cand1; bits; bits &= bits - 1u) {
+              const int b = __ffs(bits) - 1;
+              if (visit(32 + b)) next1 |= 1u << b;
+            }
+            cand0 = next0;
+            cand1 = next1;
+          } else {
+            for (int j = 0; j * VE < thr_n; ++j) (void)visit(j);
           }
           flush();
         } else {   // REQ_COUNT: elements equal to xP, prefixed inside the warp
@@ -834,7 +864,10 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
       unsigned long long cp_goal = 0ull;
       Cut ck{}, cp{}, fin{};
       // one radix search, driven through the data warps; false on an exchange timeout
-      auto radix = [&](bool mass_mode, unsigned long long goal, float gp, bool want_mass, RadixOut& out) -> bool {
+      // floor_rk: keys below it are left out of the histograms (only where the goal is reached within the keys
+      // at or above it, so the group found and its counts do not change)
+      auto radix = [&](bool mass_mode, unsigned long long goal, float gp, bool want_mass, uint32_t floor_rk,
+                       RadixOut& out) -> bool {
         out = RadixOut{};
         out.ok = 1;
         uint32_t prefix = 0;
@@ -854,6 +887,7 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
             sh.ctl.hpar = hp;
             sh.ctl.hist_mass = hist_mass ? 1 : 0;
             sh.ctl.prefix = prefix;
+            sh.ctl.floor_rk = floor_rk;
           }
           __syncwarp();
           nb_arrive(SB_CTL, kSampleThreads);
@@ -1007,7 +1041,7 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
         bool rok = true;
         if (ck_mode == 2) {
           RadixOut r;
-          rok = radix(false, ck.need, -1.f, cp_mode == 2, r);
+          rok = radix(false, ck.need, -1.f, cp_mode == 2, 0u, r);
           if (rok) {
             if (!r.ok) plan_status = VSAMP_ERR_INVALID_ARG;
             const unsigned long long need = ck.need - r.cnt_above;
@@ -1019,7 +1053,8 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
         }
         if (rok && cp_mode == 2 && plan_status == VSAMP_OK) {
           RadixOut r;
-          rok = radix(true, cp_goal, goal_p, true, r);
+          // after a top-k cut the goal lies within the keys at or above its pivot
+          rok = radix(true, cp_goal, goal_p, true, ck_mode == 2 ? ck.rk : 0u, r);
           if (rok) {
             if (!r.ok) plan_status = VSAMP_ERR_INVALID_ARG;
             const unsigned long long wP = mass_fx(ex2_approx((Tr::value_of_rkey(r.rk) - M) * c1));

@@ -364,6 +364,27 @@ struct RowEngine {
     exchange_done();
   }
 
+  // Fixed-point mass (as the radix histograms sum it) of the row's keys above rk0, summed over the cluster.
+  // Collective over the cluster; one exchange.
+  __device__ unsigned long long mass_above_key(uint32_t rk0, float M, float c1) {
+    unsigned long long s = 0ull;
+    for_each([&](int64_t, float x) {
+      if (Tr::rkey_of_value(x) > rk0) s += mass_fx(ex2_approx((x - M) * c1));
+    });
+    ++passes;
+    s = warp_sum_u64(s);
+    if (lane == 0) sh.ws[xc & 1][warp][0] = make_uint4((uint32_t)s, (uint32_t)(s >> 32), 0u, 0u);
+    exchange();
+    unsigned long long a = 0ull;
+    for (int i = lane; i < C * NW; i += 32) {
+      const uint4 v = wslot(i / NW, i % NW, 0);
+      a += ((unsigned long long)v.y << 32) | v.x;
+    }
+    a = warp_sum_u64(a);
+    exchange_done();
+    return a;
+  }
+
   // Per-thread count of elements equal to xv, into tcount[].
   __device__ void count_equal_pass(float xv) {
     uint32_t c = 0;
@@ -1183,12 +1204,14 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
       if (kCutLike && !greedy) {
         // ---------------- radix rounds where the cut leaves the maximum's group ----------------
         if (plan.ck_mode == 2) {
-          const RadixOut r = E.radix_search(false, plan.ck.need, -1.f, plan.cp_mode == 2, M, c1);
+          // a count search; the kept mass, where the top-p goal needs it, in one pass after it
+          const RadixOut r = E.radix_search(false, plan.ck.need, -1.f, false, M, c1);
           {
             if (!r.ok) plan.status = VSAMP_ERR_INVALID_ARG;
             const unsigned long long need = plan.ck.need - r.cnt_above;
             const unsigned long long wP = mass_fx(ex2_approx((Tr::value_of_rkey(r.rk) - M) * c1));
-            plan.ck = Cut{r.rk, r.cnt_above, need, r.cnt_eq, r.mass_above + need * wP, 0};
+            const unsigned long long above = plan.cp_mode == 2 ? E.mass_above_key(r.rk, M, c1) : 0ull;
+            plan.ck = Cut{r.rk, r.cnt_above, need, r.cnt_eq, above + need * wP, 0};
             plan.path |= PATH_RADIX_K;
             if (plan.cp_mode == 2) plan.cp_goal = ceil_mul_frac(topp, plan.ck.mass);
           }

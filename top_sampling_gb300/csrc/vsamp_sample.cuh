@@ -30,7 +30,7 @@ constexpr int kMaxDataWarps = 8;
 // named barriers (0 is __syncthreads)
 enum SampleBarrier : int { SB_P1 = 1, SB_CTL = 2, SB_P2 = 3, SB_HIST = 4, SB_P4 = 5 };
 // control -> data requests after P2
-enum SampleRequest : int { REQ_DONE = 0, REQ_HIST = 1, REQ_COUNT = 2, REQ_ABORT = 3 };
+enum SampleRequest : int { REQ_DONE = 0, REQ_HIST = 1, REQ_COUNT = 2, REQ_ABORT = 3, REQ_MASS = 4 };
 // how the data warps find the cut's last kept element
 enum CutGroup : int {
   GROUP_MAX = 0,     // inside the maxima: counts and prefixes from P2
@@ -58,7 +58,7 @@ struct SampleCtl {
   int32_t hist_mass;        // REQ_HIST: also histogram masses
   int32_t hpar;             // REQ_HIST: histogram buffer
   int32_t shift;            // REQ_HIST: bin = (key >> shift) & 255 for keys matching prefix above shift + 8
-  uint32_t prefix;
+  uint32_t prefix;           // REQ_HIST: the prefix; REQ_MASS: keys above it are summed
   uint32_t floor_rk;        // REQ_HIST: keys below it are left out
   uint32_t kmin32;          // min-p threshold (fp32 key space)
   uint32_t bk;              // prune bound on the Philox word
@@ -509,6 +509,19 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
             for (int j = 0; j * VE < thr_n; ++j) (void)visit(j);
           }
           flush();
+        } else if (req == REQ_MASS) {   // fixed-point mass of the keys above a pivot, per warp
+          const uint32_t rk0 = sh.ctl.prefix;
+          const float c1 = sh.ctl.c1;
+          unsigned long long sm = 0ull;
+          for (int j = 0; j * VE < thr_n; ++j) {
+            float x[VE];
+            Tr::values(mine[j], x);
+#pragma unroll
+            for (int i = 0; i < VE; ++i)
+              if (j * VE + i < thr_n && Tr::rkey_of_value(x[i]) > rk0) sm += mass_fx(ex2_approx((x[i] - M) * c1));
+          }
+          sm = warp_sum_u64(sm);
+          if (lane == 0) sh.dp[warp][0] = make_uint4((uint32_t)sm, (uint32_t)(sm >> 32), 0u, 0u);
         } else {   // REQ_COUNT: elements equal to xP, prefixed inside the warp
           const float xv = sh.ctl.xP;
           uint32_t c = 0;
@@ -1040,13 +1053,39 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
         }
         bool rok = true;
         if (ck_mode == 2) {
+          // a count search, then the kept mass (the top-p goal and the prune bound of the draw use it) in one
+          // pass over the keys above the pivot
           RadixOut r;
-          rok = radix(false, ck.need, -1.f, cp_mode == 2, 0u, r);
+          rok = radix(false, ck.need, -1.f, false, 0u, r);
+          unsigned long long above = 0ull;
+          if (rok && r.ok) {
+            if (lane == 0) {
+              sh.ctl.req = REQ_MASS;
+              sh.ctl.prefix = r.rk;
+            }
+            __syncwarp();
+            nb_arrive(SB_CTL, kSampleThreads);
+            nb_sync(SB_HIST, kSampleThreads);
+            ++passes;
+            unsigned long long w = 0ull;
+            if (lane < kDataWarps) w = ((unsigned long long)sh.dp[lane][0].y << 32) | sh.dp[lane][0].x;
+            w = warp_sum_u64(w);
+            rok = X.run(sh, C, crank, make_uint4((uint32_t)w, (uint32_t)(w >> 32), 0u, 0u),
+                        make_uint4(0u, 0u, 0u, 0u), p.wait_cycles);
+            if (rok) {
+              unsigned long long a = 0ull;
+              if (lane < C) {
+                const uint4 m = sh.xm[X.par() ^ 1][lane][0];
+                a = ((unsigned long long)m.y << 32) | m.x;
+              }
+              above = warp_sum_u64(a);
+            }
+          }
           if (rok) {
             if (!r.ok) plan_status = VSAMP_ERR_INVALID_ARG;
             const unsigned long long need = ck.need - r.cnt_above;
             const unsigned long long wP = mass_fx(ex2_approx((Tr::value_of_rkey(r.rk) - M) * c1));
-            ck = Cut{r.rk, r.cnt_above, need, r.cnt_eq, r.mass_above + need * wP, 0};
+            ck = Cut{r.rk, r.cnt_above, need, r.cnt_eq, above + need * wP, 0};
             path |= PATH_RADIX_K;
             if (cp_mode == 2) cp_goal = ceil_mul_frac(topp, ck.mass);
           }

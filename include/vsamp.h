@@ -139,12 +139,12 @@ vsamp_status vsamp_sample(const void* logits, vsamp_dtype dt, int64_t B, int64_t
                           const uint32_t* row_id, int32_t* token, float* logprob,
                           int32_t* row_status, int32_t* stats, void* stream);
 
-/* vsamp_sample with a workspace. The same draw, computed by streaming kernels over fixed 32 KB chunks of
- * every row instead of one thread-block cluster per row: chunk statistics (one HBM read), a plan per row, the
- * draw over the chunks (read again, mostly from L2) and the outputs, in four launches on `stream`. Results are
- * deterministic and do not depend on the batch; they agree with vsamp_sample except for the last bits of the
- * row mass (chunk masses are rescaled to the row maximum in binary64), which moves a top-p cut only inside
- * the 1e-6 tolerance band.
+/* vsamp_sample with a workspace. The same draw, computed by streaming kernels over fixed 4 KB pieces of
+ * every row (one warp per piece) instead of one thread-block cluster per row: piece statistics (one HBM read),
+ * a plan per row, the draw over the pieces (read again, mostly from L2) and the outputs, in four launches on
+ * `stream`. Results are deterministic and do not depend on the batch; they agree with vsamp_sample except for
+ * the last bits of the row mass (piece masses are rescaled to the row maximum in binary64), which moves a
+ * top-p cut only inside the 1e-6 tolerance band.
  *   workspace        device buffer of at least vsamp_sample_workspace_size(dt, B, V) bytes, 16-byte aligned.
  *                    It needs no initialisation: every call writes what it reads. Calls sharing a workspace
  *                    must not run at the same time (use one workspace per stream).

@@ -347,3 +347,28 @@ def topn_logprobs_row(row, dtype: str, temperature, n_top: int):
         idx[j] = v
         lp[j] = min(float(s[v]) - log_s, 0.0)
     return STATUS_OK, m, log_s, idx, lp
+
+
+def kept_logprob_row(row, dtype: str, temperature, top_k, top_p, min_p, token: int,
+                     kept: Optional[int] = None):
+    """Log-probability of ``token`` under the processed distribution: the softmax renormalised over the
+    kept prefix of pi (temperature, then top-k, top-p, min-p, as in sample_row), -inf for a token outside
+    it -- "[WS2][Logprob] ..." (Background: processed_logprobs derived from the rollout's logits, after
+    the sampling transforms) with the clamp of [LOGP]: min(s_t - log sum_{kept} exp(s_v), 0).
+
+    ``kept`` evaluates it for another kept prefix length (a parity test passes the CUDA path's count when
+    that count lies in the 1e-6 band [kept_lo, kept_hi]). Greedy rows keep the first maximum alone.
+    Returns (status, lp, kept_lo, kept_hi, rank of the token in pi).
+    """
+    res = sample_row(row, dtype, temperature, top_k, top_p, min_p, keep_order=True)
+    if res.status != STATUS_OK:
+        return res.status, math.nan, 0, 0, -1
+    t = int(token)
+    if not 0 <= t < res.n:
+        return STATUS_INVALID_ARG, math.nan, 0, 0, -1
+    c = res.kept if kept is None else int(kept)
+    rank = int(np.flatnonzero(res.order == t)[0])
+    if rank >= c:
+        return STATUS_OK, -math.inf, res.kept_lo, res.kept_hi, rank
+    log_sk = math.log(math.fsum(np.exp(res.s[res.order[:c]]).tolist()))
+    return STATUS_OK, min(float(res.s[t]) - log_sk, 0.0), res.kept_lo, res.kept_hi, rank

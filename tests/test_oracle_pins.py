@@ -529,3 +529,61 @@ def test_topn_logprobs_closed_forms():
     assert sm.topn_logprobs_row(x, "f32", 0.0, 3)[4][0] == sm.topn_logprobs_row(x, "f32", 1.0, 3)[4][0]
     x[7] = np.inf
     assert sm.topn_logprobs_row(x, "f32", 1.0, 3)[0] == sm.STATUS_NONFINITE
+
+
+# ----------------------------------------------------------------------------------------------
+# Processed (kept-set renormalised) log-probabilities
+# ----------------------------------------------------------------------------------------------
+def test_kept_logprobs_against_exact_rational_kept_sets():
+    """On tiny rows the kept set comes from exact rational prefix sums; the processed probabilities of
+    the kept tokens are their weights over the kept weights' sum, every other token has probability 0."""
+    rng = np.random.default_rng(31)
+    checked = 0
+    for trial in range(200):
+        n = int(rng.integers(1, 10))
+        x = (rng.standard_normal(n) * 2).astype(np.float32)
+        T = float(np.float32(rng.choice([0.5, 1.0, 1.7])))
+        k = int(rng.integers(0, n + 2))
+        p = float(np.float32(rng.choice([1.0, rng.uniform(0.05, 1.0)])))
+        mp = float(np.float32(rng.choice([0.0, rng.uniform(0.0, 0.5)])))
+        want = _exact_kept(x.astype(np.float64), T, k, p, mp)
+        if want is None:
+            continue
+        order = _brute_order(list(x.astype(np.float64)))
+        keep = set(order[:want])
+        xs = x.astype(np.float64)
+        z = sum(math.exp((xs[v] - xs.max()) / T) for v in keep)
+        for t in range(n):
+            st, lp, lo, hi, rank = sm.kept_logprob_row(x, "f32", T, k, p, mp, t)
+            assert st == 0
+            if t in keep:
+                assert abs(math.exp(lp) - math.exp((xs[t] - xs.max()) / T) / z) < 1e-12, (x, t)
+            else:
+                assert lp == -math.inf
+        checked += 1
+    assert checked > 150
+
+
+def test_kept_logprob_closed_forms():
+    # uniform row, top-p p: ceil(p V) tokens kept, each at -log(ceil(p V)); the rest at -inf
+    V, p = 1000, 0.3
+    kept = math.ceil(Fraction(float(np.float32(p))) * V)
+    x = np.zeros(V, np.float32)
+    assert sm.kept_logprob_row(x, "f32", 1.0, 0, p, 0.0, kept - 1)[1] == pytest.approx(-math.log(kept), abs=1e-12)
+    assert sm.kept_logprob_row(x, "f32", 1.0, 0, p, 0.0, kept)[1] == -math.inf
+    # top-k alone on distinct logits: s_t - log sum over the k largest
+    x = np.array([0.5, 3.0, -1.0, 2.0, 1.0], np.float32)
+    want = 2.0 - math.log(math.exp(3.0) + math.exp(2.0) + math.exp(1.0))
+    assert sm.kept_logprob_row(x, "f32", 1.0, 3, 1.0, 0.0, 3)[1] == pytest.approx(want, abs=1e-12)
+    assert sm.kept_logprob_row(x, "f32", 1.0, 3, 1.0, 0.0, 0)[1] == -math.inf
+    # greedy: the first maximum alone, probability one
+    y = np.array([1.0, 4.0, 4.0, 2.0], np.float32)
+    assert sm.kept_logprob_row(y, "f32", 0.0, 0, 0.9, 0.0, 1)[1] == 0.0
+    assert sm.kept_logprob_row(y, "f32", 0.0, 0, 0.9, 0.0, 2)[1] == -math.inf
+    # nothing filtered: the processed log-probability is the full-row one
+    assert sm.kept_logprob_row(x, "f32", 0.8, 0, 1.0, 0.0, 4)[1] == pytest.approx(
+        sm.logprob_row(x, "f32", 0.8, 4), abs=1e-12)
+    # error rows and tokens outside the row
+    assert sm.kept_logprob_row(y, "f32", 1.0, 0, 1.0, 0.0, 4)[0] == sm.STATUS_INVALID_ARG
+    y[2] = np.nan
+    assert sm.kept_logprob_row(y, "f32", 1.0, 0, 1.0, 0.0, 1)[0] == sm.STATUS_NONFINITE

@@ -455,6 +455,8 @@ def run_call(spec: str, repeat: int):
                 ts.vsamp_logprob(x, token, temperature=kw["temperature"], V=b.V)
             elif fn == "topn_logprobs":
                 ts.vsamp_topn_logprobs(x, 20, temperature=kw["temperature"], V=b.V)
+            elif fn == "kept_logprob":
+                ts.vsamp_kept_logprob(x, token, **kw)
             else:
                 raise ValueError(f"unknown entry point {fn}")
     torch.cuda.synchronize()

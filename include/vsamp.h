@@ -190,6 +190,19 @@ vsamp_status vsamp_logprob(const void* logits, vsamp_dtype dt, int64_t B, int64_
                            const float* temperature, const int32_t* token, const float* row_max,
                            const float* row_logsum, float* out, int32_t* row_status, void* stream);
 
+/* Processed log-probability of given tokens: the softmax renormalised over the kept set of the cut that
+ * vsamp_topp_minp_mask computes (temperature, then top-k, top-p, min-p; greedy rows keep the first maximum)
+ * ("[WS2][Logprob] ...", Background: the rollout's processed_logprobs, derived from its logits after the
+ * sampling transforms; the clamp of the Design's logp = min(z_t - lse, 0)):
+ *   out[r] = min((x[r, t] - m) / T_r - log S_kept, 0) if token t = token[r] is kept, -inf if it is not;
+ *   m = row maximum, S_kept = sum over the kept tokens of exp((x - m) / T_r) (T_r <= 0 read as 1).
+ * Parameters and errors as for vsamp_topp_minp_mask; token[r] outside [0, V) is a row error; error rows
+ * give NaN. One launch on `stream`, one read of each row. */
+vsamp_status vsamp_kept_logprob(const void* logits, vsamp_dtype dt, int64_t B, int64_t V, int64_t ld,
+                                const float* temperature, const int32_t* top_k, const float* top_p,
+                                const float* min_p, const int32_t* token, float* out, int32_t* row_status,
+                                void* stream);
+
 /* Top-N log-probability lists ("[Kernel] Make persistent_topk deterministic", details of the probe: per
  * generated token the list of the 20 most probable (token, logprob) pairs, hashed to compare runs; the
  * log-probabilities follow "[WS2][Logprob] ...", Design: logp = min(z_v - lse, 0)).

@@ -123,3 +123,14 @@ def test_host_checks_of_the_topn_entry_point(lib):
     assert call(20, **{**good, "ol": None}) == ts.VSAMP_ERR_INVALID_ARG
     assert l2.vsamp_topn_logprobs(None, ts.VSAMP_F32, 4, 100, 100, None, 20, d, d, d, d, None, None) == \
         ts.VSAMP_ERR_INVALID_ARG
+
+
+def test_host_checks_of_the_kept_logprob_entry_point(lib):
+    import top_sampling_gb300 as ts
+    l2 = ts.load()
+    d = ctypes.c_void_p(4096)
+    args = (d, ts.VSAMP_F32, 4, 100, 100, None, None, None, None)
+    assert l2.vsamp_kept_logprob(*args, None, d, None, None) == ts.VSAMP_ERR_INVALID_ARG   # no tokens
+    assert l2.vsamp_kept_logprob(*args, d, None, None, None) == ts.VSAMP_ERR_INVALID_ARG   # no output
+    assert l2.vsamp_kept_logprob(None, ts.VSAMP_F32, 4, 100, 100, None, None, None, None, d, d, None, None) == \
+        ts.VSAMP_ERR_INVALID_ARG

@@ -29,7 +29,7 @@ VSAMP_F32 = 0
 VSAMP_BF16 = 1
 
 EXPORTED = ("vsamp_softmax_lse", "vsamp_topk_select", "vsamp_topp_minp_mask", "vsamp_sample",
-            "vsamp_sample_ws", "vsamp_sample_workspace_size", "vsamp_sample_static", "vsamp_logprob", "vsamp_topn_logprobs",
+            "vsamp_sample_ws", "vsamp_sample_workspace_size", "vsamp_sample_static", "vsamp_logprob", "vsamp_topn_logprobs", "vsamp_kept_logprob",
             "vsamp_status_string",
             "vsamp_device_info", "vsamp_version")
 
@@ -73,10 +73,11 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                                     ctypes.c_size_t, vp]
     lib.vsamp_sample_static.argtypes = [vp, st, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.vsamp_topn_logprobs.argtypes = [vp, st, i64, i64, i64, vp, i32, vp, vp, vp, vp, vp, vp]
+    lib.vsamp_kept_logprob.argtypes = [vp, st, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.vsamp_sample_workspace_size.argtypes = [st, i64, i64]
     lib.vsamp_sample_workspace_size.restype = ctypes.c_size_t
     for f in ("vsamp_softmax_lse", "vsamp_topk_select", "vsamp_topp_minp_mask", "vsamp_sample", "vsamp_logprob",
-              "vsamp_sample_ws", "vsamp_sample_static", "vsamp_topn_logprobs"):
+              "vsamp_sample_ws", "vsamp_sample_static", "vsamp_topn_logprobs", "vsamp_kept_logprob"):
         getattr(lib, f).restype = st
     lib.vsamp_status_string.argtypes = [st]
     lib.vsamp_status_string.restype = ctypes.c_char_p
@@ -380,3 +381,26 @@ def vsamp_topn_logprobs(logits, n, temperature=None, V=None, row_max=None, row_l
         _ptr(row_status, torch.int32, dev, B, "row_status"), _stream(stream))
     _check(st, "vsamp_topn_logprobs")
     return out_idx, out_lp, row_max, row_logsum, row_status
+
+
+def vsamp_kept_logprob(logits, token, temperature=None, top_k=None, top_p=None, min_p=None, V=None, out=None,
+                       row_status=None, stream=None):
+    """Log-probability of token[r] renormalised over the kept set of the row's cut (-inf outside it).
+    Returns (out [B] fp32, row_status)."""
+    B, V, ld = _rows(logits, V)
+    dev = logits.device
+    temperature = _param(temperature, B, torch.float32, dev, "temperature")
+    top_k = _param(top_k, B, torch.int32, dev, "top_k")
+    top_p = _param(top_p, B, torch.float32, dev, "top_p")
+    min_p = _param(min_p, B, torch.float32, dev, "min_p")
+    token = _param(token, B, torch.int32, dev, "token")
+    out = torch.empty(B, dtype=torch.float32, device=dev) if out is None else out
+    row_status = torch.empty(B, dtype=torch.int32, device=dev) if row_status is None else row_status
+    st = load().vsamp_kept_logprob(
+        logits.data_ptr(), _dtype_code(logits), B, V, ld, _ptr(temperature, torch.float32, dev, B, "temperature"),
+        _ptr(top_k, torch.int32, dev, B, "top_k"), _ptr(top_p, torch.float32, dev, B, "top_p"),
+        _ptr(min_p, torch.float32, dev, B, "min_p"), _ptr(token, torch.int32, dev, B, "token"),
+        _ptr(out, torch.float32, dev, B, "out"), _ptr(row_status, torch.int32, dev, B, "row_status"),
+        _stream(stream))
+    _check(st, "vsamp_kept_logprob")
+    return out, row_status

@@ -500,6 +500,24 @@ vsamp_status vsamp_topn_logprobs(const void* logits, vsamp_dtype dt, int64_t B, 
   return VSAMP_OK;
 }
 
+vsamp_status vsamp_kept_logprob(const void* logits, vsamp_dtype dt, int64_t B, int64_t V, int64_t ld,
+                                const float* temperature, const int32_t* top_k, const float* top_p,
+                                const float* min_p, const int32_t* token, float* out, int32_t* row_status,
+                                void* stream) {
+  vsamp_status st = check_common(logits, dt, B, V, ld);
+  if (st != VSAMP_OK) return st;
+  if (!token || !out) return VSAMP_ERR_INVALID_ARG;
+  Params p = base_params(logits, dt, B, V, ld);
+  p.temperature = temperature;
+  p.top_k = top_k;
+  p.top_p = top_p;
+  p.min_p = min_p;
+  p.token_in = token;
+  p.logprob = out;
+  p.row_status = row_status;
+  return dispatch<MODE_KEPT>(p, dt, B, static_cast<cudaStream_t>(stream));
+}
+
 const char* vsamp_status_string(vsamp_status s) {
   switch (s) {
     case VSAMP_OK: return "ok";

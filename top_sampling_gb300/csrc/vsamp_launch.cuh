@@ -66,4 +66,5 @@ vsamp_status launch(Params p, int64_t B, int esize, cudaStream_t stream) {
   template vsamp_status launch<T, MODE_CUT | MODE_MASK>(Params, int64_t, int, cudaStream_t); \
   template vsamp_status launch<T, MODE_SAMPLE>(Params, int64_t, int, cudaStream_t);       \
   template vsamp_status launch<T, MODE_LOGPROB>(Params, int64_t, int, cudaStream_t);       \
-  template vsamp_status launch<T, MODE_LSE | MODE_TOPN>(Params, int64_t, int, cudaStream_t);
+  template vsamp_status launch<T, MODE_LSE | MODE_TOPN>(Params, int64_t, int, cudaStream_t);       \
+  template vsamp_status launch<T, MODE_KEPT>(Params, int64_t, int, cudaStream_t);

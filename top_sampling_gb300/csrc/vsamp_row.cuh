@@ -35,6 +35,7 @@ enum Mode : int {
   MODE_SAMPLE = 16,   // Gumbel-max draw + log-probability
   MODE_LOGPROB = 32,  // log-probability of given tokens (statistics recomputed)
   MODE_TOPN = 64,     // the k_max best tokens (out_idx, ascending index order): the top-k cut, any temperature
+  MODE_KEPT = 128,    // log-probability of given tokens renormalised over the cut's kept set (-inf outside it)
 };
 
 // Path flags reported in stats[r][3].
@@ -817,7 +818,7 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
   constexpr int ES = Tr::ESIZE;
   constexpr bool kSel = (MODE & MODE_SELECT) != 0;
   constexpr bool kTopn = (MODE & MODE_TOPN) != 0;
-  constexpr bool kCutLike = (MODE & (MODE_CUT | MODE_SAMPLE | MODE_TOPN)) != 0;
+  constexpr bool kCutLike = (MODE & (MODE_CUT | MODE_SAMPLE | MODE_TOPN | MODE_KEPT)) != 0;
   extern __shared__ __align__(128) unsigned char dyn[];
   Smem<NT>& sh = *reinterpret_cast<Smem<NT>*>(dyn);
   unsigned char* slice = dyn + slice_offset<NT>();
@@ -1043,7 +1044,7 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
   else if ((MODE & (MODE_LSE | MODE_LOGPROB)) && (isnan(temp) || isinf(temp)))
     status = VSAMP_ERR_INVALID_ARG;
   int32_t tok_in = 0;
-  if ((MODE & MODE_LOGPROB) && status == VSAMP_OK) {
+  if ((MODE & (MODE_LOGPROB | MODE_KEPT)) && status == VSAMP_OK) {
     tok_in = p.token_in[row];
     if (tok_in < 0 || (int64_t)tok_in >= n) status = VSAMP_ERR_INVALID_ARG;
   }
@@ -1210,7 +1211,8 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
             if (!r.ok) plan.status = VSAMP_ERR_INVALID_ARG;
             const unsigned long long need = plan.ck.need - r.cnt_above;
             const unsigned long long wP = mass_fx(ex2_approx((Tr::value_of_rkey(r.rk) - M) * c1));
-            const unsigned long long above = plan.cp_mode == 2 ? E.mass_above_key(r.rk, M, c1) : 0ull;
+            const bool want_mass = plan.cp_mode == 2 || (MODE & MODE_KEPT) != 0;
+            const unsigned long long above = want_mass ? E.mass_above_key(r.rk, M, c1) : 0ull;
             plan.ck = Cut{r.rk, r.cnt_above, need, r.cnt_eq, above + need * wP, 0};
             plan.path |= PATH_RADIX_K;
             if (plan.cp_mode == 2) plan.cp_goal = ceil_mul_frac(topp, plan.ck.mass);
@@ -1515,6 +1517,14 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
 
   // ---------------- finalisation ----------------
   if ((MODE & MODE_CUT) && fin_valid && boundary >= 0) p.cut[row].idx_cut = boundary;
+  // the kept-set log-probability: written by the thread whose chunk holds the token (its cut index It
+  // decides whether the token is kept)
+  if ((MODE & MODE_KEPT) && fin_valid && (int64_t)tok_in >= E.thr_e0 && (int64_t)tok_in < E.thr_e0 + E.thr_n) {
+    const float xt = Tr::load_global(p.x, (int64_t)row * p.ld + tok_in);
+    const bool kept = xt > xP || (xt == xP && tok_in <= It);
+    const float log_sk = logf(u64_to_float(fin.mass) * 9.094947017729282379e-13f);   // 2^-40
+    p.logprob[row] = kept ? fminf((xt - M) * invT - log_sk, 0.f) : -INFINITY;
+  }
   // the row's outputs come from thread 0, except a Gumbel draw's, which come from lane 0 of the warp
   // that reduced it
   const bool p4_path = (MODE & MODE_SAMPLE) && fin_valid && !(greedy || fin.kept() == 1);
@@ -1524,6 +1534,7 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
       if (p.row_max) p.row_max[row] = status == VSAMP_OK ? M : __int_as_float(0x7FC00000);
       if (p.row_logsum) p.row_logsum[row] = status == VSAMP_OK ? (float)plan.logS : __int_as_float(0x7FC00000);
     }
+    if ((MODE & MODE_KEPT) && !fin_valid) p.logprob[row] = __int_as_float(0x7FC00000);
     if (MODE & MODE_LOGPROB) {
       float lp = __int_as_float(0x7FC00000);
       if (status == VSAMP_OK) {

@@ -111,7 +111,7 @@ vsamp_status choose_geometry(int64_t V, int esize, int64_t B, const DeviceInfo& 
 }
 
 vsamp_status choose_geometry_for(int64_t V, int esize, int64_t B, const DeviceInfo& d, int NT, int head, int per_sm,
-                                 Geometry& g, int max_nbuf) {
+                                 Geometry& g, int max_nbuf, int max_spread) {
   const int64_t VE = 16 / esize;
   const int64_t nvec = (V + VE - 1) / VE;
   const int smem_sm = d.smem_per_sm > 0 ? d.smem_per_sm : d.optin;
@@ -144,7 +144,9 @@ vsamp_status choose_geometry_for(int64_t V, int esize, int64_t B, const DeviceIn
         for (int c = cmin + 1; c <= cmin + 3 && c <= d.max_cluster; ++c)
           if ((int64_t)c * q_for(c) < best) { best = (int64_t)c * q_for(c); C = c; }
         // small batches: more CTAs per row while slices stay >= 8 KB
-        while (C < d.max_cluster && B * C < 2LL * d.sm_count && (int64_t)NT * q_for(C + 1) * 16 >= 8192) ++C;
+        while (C < d.max_cluster && C < max_spread && B * C < 2LL * d.sm_count &&
+               (int64_t)NT * q_for(C + 1) * 16 >= 8192)
+          ++C;
       }
     }
     if (!C) continue;

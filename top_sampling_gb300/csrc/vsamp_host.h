@@ -38,9 +38,10 @@ int env_int(const char* name, int dflt);
 long long env_ll(const char* name, long long dflt);
 vsamp_status device_info(int dev, DeviceInfo& out);
 vsamp_status choose_geometry(int64_t V, int esize, int64_t B, const DeviceInfo& d, Geometry& g);
-// NT data threads per CTA, head bytes of shared memory before the slice, per_sm CTAs resident per SM
+// NT data threads per CTA, head bytes of shared memory before the slice, per_sm CTAs resident per SM; small
+// batches spread a row over more CTAs, up to max_spread per cluster
 vsamp_status choose_geometry_for(int64_t V, int esize, int64_t B, const DeviceInfo& d, int NT, int head, int per_sm,
-                                 Geometry& g, int max_nbuf = 1);
+                                 Geometry& g, int max_nbuf = 1, int max_spread = 16);
 
 // vsamp_sample's kernel (specialised warps), in its own translation units
 template <typename T>

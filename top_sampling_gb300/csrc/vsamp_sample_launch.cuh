@@ -12,8 +12,11 @@ static vsamp_status launch_sample_cfg(Params p, int64_t B, int esize, const Devi
   constexpr int kDataThreads = NDW * 32;
   constexpr int kSampleThreads = kDataThreads + 32;
   Geometry g;
+  // small batches: at most 6 CTAs per row. Every radix round and plan of the sampling kernel is a cluster
+  // exchange through the control warps, whose cost grows with the cluster (B = 4 x V = 32,000 fp32: 106 us at
+  // 16 CTAs per row, 55 us at 4-6, 68 us at 2).
   vsamp_status st = choose_geometry_for(p.V, esize, B, d, kDataThreads, sample_slice_offset(), PER_SM, g,
-                                        env_int("VSAMP_NBUF", 1) == 2 ? 2 : 1);
+                                        env_int("VSAMP_NBUF", 1) == 2 ? 2 : 1, 6);
   if (st != VSAMP_OK) return st;
   p.q = g.q;
   p.nbuf = g.nbuf;

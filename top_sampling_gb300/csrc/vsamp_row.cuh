@@ -1188,6 +1188,8 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
                 plan.cp_mode = 2;   // goal from the top-k mass, after the top-k rounds
               }
             }
+            // top-p keeping the first maximum alone is the shortest cut: no radix search for top-k
+            if (plan.cp_mode == 1 && plan.cp.kept() == 1 && plan.ck_mode == 2) plan.ck_mode = 0;
             if (plan.ck_mode == 1 || plan.cp_mode == 1) plan.path |= PATH_MAXGROUP;
             if (minp_on) {
               // min-p keeps the whole group of the smallest key at or above its threshold

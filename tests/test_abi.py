@@ -134,3 +134,19 @@ def test_host_checks_of_the_kept_logprob_entry_point(lib):
     assert l2.vsamp_kept_logprob(*args, d, None, None, None) == ts.VSAMP_ERR_INVALID_ARG   # no output
     assert l2.vsamp_kept_logprob(None, ts.VSAMP_F32, 4, 100, 100, None, None, None, None, d, d, None, None) == \
         ts.VSAMP_ERR_INVALID_ARG
+
+
+def test_binding_rejects_host_tensors_and_bad_dtypes():
+    # argument marshalling refuses what the library cannot take, before any call into it
+    torch = pytest.importorskip("torch")
+    import top_sampling_gb300 as ts
+    x = torch.zeros(2, 8)
+    for fn in (ts.vsamp_sample, ts.vsamp_softmax_lse, ts.vsamp_topp_minp_mask):
+        with pytest.raises(ValueError):
+            fn(x)
+    with pytest.raises(ValueError):
+        ts.vsamp_topn_logprobs(x, 4)
+    with pytest.raises(ValueError):
+        ts.vsamp_kept_logprob(x, torch.zeros(2, dtype=torch.int32))
+    with pytest.raises(TypeError):
+        ts._dtype_code(torch.zeros(2, 8, dtype=torch.float16))

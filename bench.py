@@ -216,6 +216,34 @@ def cpu_baseline(n_rows: int = B_ROWS, step: int = 0):
 # ------------------------------------------------------------------------------------------------
 # GPU arm
 # ------------------------------------------------------------------------------------------------
+def c5_passes(ts, dev) -> dict:
+    """Passes over each row's on-chip slice and radix rounds per row of one `vsamp_sample` call on the
+    near-uniform B = 512 x V = 262,144 fp32 workload (top-k 4096, top-p 0.99, min-p 0.01), outside the timed
+    region. Never raises: an error is reported in the returned object."""
+    try:
+        import torch
+
+        import workloads
+
+        b = workloads.c5()
+        x = torch.from_numpy(np.ascontiguousarray(b.logits)).to(dev)
+        T = lambda a: torch.from_numpy(np.ascontiguousarray(a.view(np.int64) if a.dtype == np.uint64 else a)).to(dev)
+        _, _, st, stats = ts.vsamp_sample(x, temperature=T(b.temperature), top_k=T(b.top_k), top_p=T(b.top_p),
+                                          min_p=T(b.min_p), seed=T(b.seed), step=T(b.step), V=b.V,
+                                          want_logprob=False, want_stats=True)
+        torch.cuda.synchronize()
+        s = stats.cpu().numpy()
+        bad = int(st.ne(0).sum())
+        del x
+        torch.cuda.empty_cache()
+        summ = lambda v: {"min": int(v.min()), "median": float(np.median(v)), "max": int(v.max())}
+        return {"workload": "c5: B=512 x V=262144 fp32 N(0,1e-4^2) (seed 4), top_k=4096, top_p=0.99, min_p=0.01",
+                "passes_per_row": summ(s[:, 0]), "radix_rounds_per_row": summ(s[:, 1]),
+                "kept_per_row": summ(s[:, 2]), "hbm_reads_per_row": 1, "bad_rows": bad}
+    except Exception as e:  # the benchmark line must not depend on this record
+        return {"error": f"{type(e).__name__}: {e}"[:200]}
+
+
 def run_gpu(args):
     import torch
 
@@ -357,6 +385,8 @@ def run_gpu(args):
     }
     if cpu is not None:
         out["cpu_baseline"] = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    if world == 1 and not args.no_cpu:
+        out["c5_pivot_search"] = c5_passes(ts, dev)
     if dist:
         dist.destroy_process_group()
     if rank == 0:

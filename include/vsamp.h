@@ -170,7 +170,10 @@ size_t vsamp_sample_workspace_size(vsamp_dtype dt, int64_t B, int64_t V);
  *   Size limit: vsamp_sample_workspace_size(dt, B, V) must not exceed VSAMP_STATIC_SCRATCH_BYTES, else
  *     the call returns VSAMP_ERR_SCRATCH_LIMIT and enqueues nothing.
  *   Set-up: the first call on each device (with that device current) looks up the array's address once.
- *   Zeroing: every call first enqueues a clear, on `stream`, of the bytes it uses, then the kernels.
+ *   Contents: the array keeps what the last call left in it. Nothing needs clearing first: as for
+ *     vsamp_sample_ws, the kernels write every value they read, so each call enqueues only the kernels.
+ *   Largest batch (from vsamp_sample_workspace_size): V = 151,936: 417 rows fp32, 789 rows bf16;
+ *     V = 262,144: 248 rows fp32, 481 rows bf16.
  *   Races: one array per device is shared by every caller of this function, so calls whose kernels
  *     overlap on one device (from two streams or two host threads) race on it and give wrong results;
  *     serialise them, or use vsamp_sample_ws with a workspace per stream.

@@ -297,17 +297,18 @@ def logprob_row(row, dtype: str, temperature, token: int) -> float:
     return min(float(s[int(token)]) - lse, 0.0)
 
 
-def topk_select_row(scores, length: int, k: int, k_max: int):
+def topk_select_row(scores, length: int, k: int, k_max: int, dtype: str = "f32"):
     """[TOPK]: the k largest of scores[:length] by (value desc, index asc), in ascending index order.
 
     Returns (status, out[k_max]) with unused slots -1. NaN in the valid prefix is an error; +-inf are
-    ordinary keys. k <= 0 selects nothing; k > k_max is an argument error.
+    ordinary keys. k <= 0 selects nothing; k > k_max is an argument error. ``dtype`` "bf16" reads the
+    scores as bfloat16 bit patterns, widened exactly ([TOPP] step 1), so equal bf16 values tie.
     """
     out = np.full(int(k_max), -1, dtype=np.int32)
     n = int(length)
     if n <= 0 or n > len(scores):
         return STATUS_INVALID_ARG, out
-    x = widen(np.asarray(scores)[:n], "f32")
+    x = widen(np.asarray(scores)[:n], dtype)
     if np.any(np.isnan(x)):                       # data errors are reported before parameter errors
         return STATUS_NONFINITE, out
     if k > k_max:

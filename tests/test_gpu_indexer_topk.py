@@ -5,6 +5,7 @@ binary64 oracle bit for bit, and repeated calls must be identical."""
 import numpy as np
 import pytest
 
+import workloads
 from oracle import sampler as osm
 
 torch = pytest.importorskip("torch")
@@ -42,9 +43,14 @@ def _keys(rng, kind, n):
     raise ValueError(kind)
 
 
-def _run_and_check(ts, dev, x, lengths, k, repeats=2):
+def _run_and_check(ts, dev, x, lengths, k, repeats=2, dtype="f32"):
+    """fp32 keys x, selected as fp32 or as their bfloat16 roundings (dtype "bf16")."""
     B, ld = x.shape
-    xd = torch.from_numpy(x).to(dev)
+    if dtype == "bf16":
+        x = workloads.f32_to_bf16_bits(x)
+        xd = torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
+    else:
+        xd = torch.from_numpy(x).to(dev)
     outs = []
     for _ in range(repeats):
         idx, st = ts.vsamp_topk_select(xd, k, k_max=k, lengths=t(lengths, dev), max_len=ld)
@@ -54,7 +60,7 @@ def _run_and_check(ts, dev, x, lengths, k, repeats=2):
         assert np.array_equal(idx, outs[0][0]) and np.array_equal(st, outs[0][1])
     idx, st = outs[0]
     for r in range(B):
-        s_o, want = osm.topk_select_row(x[r], int(lengths[r]), k, k)
+        s_o, want = osm.topk_select_row(x[r], int(lengths[r]), k, k, dtype=dtype)
         assert st[r] == s_o, f"row {r}"
         assert np.array_equal(idx[r], want), f"row {r} (length {lengths[r]}, k {k})"
 
@@ -68,16 +74,17 @@ def test_short_rows_are_padded(ts, dev, k):
     _run_and_check(ts, dev, x, lengths, k)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("rows", [1, 8, 64])
 @pytest.mark.parametrize("k", [512, 2048])
 @pytest.mark.parametrize("kind", ["random", "ties"])
-def test_indexer_lengths(ts, dev, rows, k, kind):
-    """Rows {1, 8, 64} x lengths {1k, 4k, 8k, 20k, 40k} x k {512, 2048} x {random, tie-heavy}."""
+def test_indexer_lengths(ts, dev, rows, k, kind, dtype):
+    """Rows {1, 8, 64} x lengths {1k, 4k, 8k, 20k, 40k} x k {512, 2048} x {random, tie-heavy}, fp32 and bf16."""
     rng = np.random.default_rng(rows * 7 + k)
     lens = np.array([1024, 4096, 8192, 20480, 40960], dtype=np.int32)
     lengths = lens[np.arange(rows) % lens.size]
     x = np.stack([_keys(rng, kind, 40960) for _ in range(rows)])
-    _run_and_check(ts, dev, x, lengths, k)
+    _run_and_check(ts, dev, x, lengths, k, dtype=dtype)
 
 
 @pytest.mark.parametrize("kind", ["equal", "narrow"])
@@ -93,8 +100,9 @@ def test_all_equal_and_narrow_range(ts, dev, kind):
         assert np.array_equal(idx[0], np.arange(2048))
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("ties", [2047, 4096, 16385])
-def test_pivot_tie_populations(ts, dev, ties):
+def test_pivot_tie_populations(ts, dev, ties, dtype):
     """k - 1 keys above one level that is shared by `ties` keys: the lowest-index one of them is taken."""
     rng = np.random.default_rng(ties)
     n, k = 40960, 2048
@@ -102,13 +110,17 @@ def test_pivot_tie_populations(ts, dev, ties):
     pos = rng.permutation(n)
     x[pos[:k - 1]] = rng.uniform(1.0, 2.0, k - 1).astype(np.float32)
     x[pos[k - 1:k - 1 + ties]] = 0.5
-    _run_and_check(ts, dev, x[None, :].copy(), np.array([n], np.int32), k)
+    if dtype == "bf16":   # keep the populations exact after rounding: above 1.0, at 0.5, below -1.0
+        x[pos[:k - 1]] = 1.5
+        x[pos[k - 1 + ties:]] = -1.5
+    _run_and_check(ts, dev, x[None, :].copy(), np.array([n], np.int32), k, dtype=dtype)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("width", [355588, 400000, 474112])
 @pytest.mark.parametrize("k", [512, 2048])
-def test_wide_rows(ts, dev, width, k):
+def test_wide_rows(ts, dev, width, k, dtype):
     """Contiguous rows (stride = length) of 355,588 to 474,112 keys: random, tie-heavy, all-equal."""
     rng = np.random.default_rng(width + k)
     x = np.stack([_keys(rng, kind, width) for kind in ("random", "ties", "equal", "random")])
-    _run_and_check(ts, dev, x, np.full(4, width, np.int32), k)
+    _run_and_check(ts, dev, x, np.full(4, width, np.int32), k, dtype=dtype)

@@ -61,6 +61,9 @@ def _check(ts, dev, b, rows, seed=0):
               min_p=t(b.min_p, dev), V=b.V)
     cut, _, _ = ts.vsamp_topp_minp_mask(x, want_mask=False, **kw)
     cut = cut.cpu().numpy()
+    for r in rows:   # an ambiguous oracle boundary stops the comparison ([TOPP] step 6)
+        assert not osm.sample_row(b.logits[r, :b.V], b.dtype, b.temperature[r], b.top_k[r], b.top_p[r],
+                                  b.min_p[r]).ambiguous, f"row {r}: oracle_boundary_ambiguous"
     for tokens in _tokens(b, rows, np.random.default_rng(seed)):
         out, st = ts.vsamp_kept_logprob(x, t(tokens, dev), **kw)
         torch.cuda.synchronize()

@@ -77,18 +77,62 @@ def test_c2_dominant_token_rows(ts, dev):
     ties = TieCounter()
     tok, lp, st, stats = run_sample(ts, b, dev)
     check_sample(b, range(b.B), tok, lp, st, stats, ties)
-    cut, mask, cstats = run_cut(ts, b, dev, want_mask=False)
-    check_cut(b, range(0, b.B, 4), cut, None, cstats)
+    cut, mask, cstats = run_cut(ts, b, dev, want_mask=True)
+    check_cut(b, range(0, b.B, 2), cut, mask, cstats)
     ties.check()
 
 
-def test_c3_topk_select_ties(ts, dev):
+def test_c2_one_million_draws_z_test(ts, dev):
+    """C2's own distribution test: 15,625 steps x 64 rows = 1e6 draws under the workload's per-row mix of
+    temperature, top-k, top-p and min-p. The oracle gives each row's kept set and renormalised law; the hits
+    of the dominant tokens and the draws outside them are compared with their expectations (|Z| < 10, the
+    Gumbel precision page's bound; where the law leaves no variance the count must be exact)."""
+    b = workloads.c2()
+    B, steps = b.B, 15625
+    p_dom = np.zeros(B)
+    for r in range(B):
+        ref = oracle_row(b, r)
+        assert ref.status == 0 and not ref.ambiguous
+        kept = ref.order[:ref.kept]
+        w = np.exp(ref.s[kept] - ref.s[kept].max())
+        p_dom[r] = float(w[kept == int(b.meta["dominant"][r])].sum() / w.sum())
+    x = to_device(b.logits, b.dtype, dev)
+    dom = t(b.meta["dominant"].astype(np.int32), dev)
+    kw = dict(temperature=t(b.temperature, dev), top_k=t(b.top_k, dev), top_p=t(b.top_p, dev),
+              min_p=t(b.min_p, dev), seed=t(b.seed, dev), want_logprob=False)
+    hits = torch.zeros(B, dtype=torch.int64, device=dev)
+    bad = torch.zeros(B, dtype=torch.int64, device=dev)
+    for s in range(steps):
+        tok, _, st, _ = parity_util.sample_fn(ts)(x, step=torch.full((B,), s, dtype=torch.int64, device=dev), **kw)
+        hits += (tok == dom)
+        bad += (st != 0) | (tok < 0)
+    torch.cuda.synchronize()
+    hits, bad = hits.cpu().numpy(), bad.cpu().numpy()
+    assert not bad.any()
+    N = B * steps
+    e_hit = float((steps * p_dom).sum())
+    var = float((steps * p_dom * (1.0 - p_dom)).sum())
+    tail = N - int(hits.sum())
+    for r in np.flatnonzero(p_dom == 1.0):          # a one-token law: every draw is the dominant token
+        assert hits[r] == steps, f"row {r}: {hits[r]} of {steps}"
+    if var > 0:
+        z_hit = (hits.sum() - e_hit) / math.sqrt(var)
+        z_tail = (tail - (N - e_hit)) / math.sqrt(var)
+        assert abs(z_hit) < 10 and abs(z_tail) < 10, (z_hit, z_tail)
+    else:
+        assert tail == 0
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_c3_topk_select_ties(ts, dev, dtype):
+    """All 128 rows bit-exact; the 256 score levels (q - 128) / 16 are exact in bf16 too."""
     b = workloads.c3()
-    x = torch.from_numpy(b.scores).to(dev)
+    scores = b.scores if dtype == "f32" else workloads.f32_to_bf16_bits(b.scores)
+    x = to_device(scores, dtype, dev)
     idx, st = ts.vsamp_topk_select(x, t(b.k, dev), k_max=b.k_max, lengths=t(b.lengths, dev))
     idx, st = idx.cpu().numpy(), st.cpu().numpy()
     for r in range(b.B):
-        s_o, want = osm.topk_select_row(b.scores[r], int(b.lengths[r]), int(b.k[r]), b.k_max)
+        s_o, want = osm.topk_select_row(scores[r], int(b.lengths[r]), int(b.k[r]), b.k_max, dtype=dtype)
         assert st[r] == s_o
         assert np.array_equal(idx[r], want), f"row {r} (len {b.lengths[r]})"
     # repeated calls are bit-identical
@@ -111,15 +155,47 @@ def test_c4_full_size_bf16(ts, dev):
     ties.check()
 
 
+def test_c4_full_size_cut_mask_and_statistics(ts, dev):
+    """The C4 cut with its 38.9 MB mask, and the row statistics, at full size: every row keeps the 144,340
+    lowest indices (uniform rows), element by element; sampled rows against the oracle's kept prefix; the
+    maximum 9984.0 and log S = log 151,936 on every row."""
+    b = workloads.c4()
+    cut, mask, cstats = run_cut(ts, b, dev, want_mask=True)
+    assert np.all(cut[:, 3] == 0) and np.all(cut[:, 2] == 144340) and np.all(cut[:, 1] == 144339)
+    assert mask[:, :144340].all() and not mask[:, 144340:].any()
+    check_cut(b, range(0, b.B, 32), cut, mask, cstats)
+    x = to_device(b.logits, b.dtype, dev)
+    m, ls, st = ts.vsamp_softmax_lse(x, temperature=t(b.temperature, dev))
+    m, ls, st = m.cpu().numpy(), ls.cpu().numpy(), st.cpu().numpy()
+    assert np.all(st == 0) and np.all(m == np.float32(9984.0))
+    assert np.all(np.abs(ls - math.log(151936)) <= LOGP_TOL)
+    for r in range(0, b.B, 64):
+        st_o, m_o, ls_o = osm.softmax_lse_row(b.logits[r], b.dtype, b.temperature[r])
+        assert m[r] == np.float32(m_o) and abs(ls[r] - ls_o) <= LOGP_TOL
+
+
 def test_c5_near_uniform_rows(ts, dev):
     b = workloads.c5(B=64)
     ties = TieCounter()
     tok, lp, st, stats = run_sample(ts, b, dev)
     rows = sorted(set(range(0, 64, 4)) | set(int(r) for r in b.meta["dup_rows"]))
     check_sample(b, rows, tok, lp, st, stats, ties)
-    cut, mask, cstats = run_cut(ts, b, dev, want_mask=False)
-    check_cut(b, rows[:6], cut, None, cstats)
+    cut, mask, cstats = run_cut(ts, b, dev, want_mask=True)
+    check_cut(b, rows[:8], cut, mask, cstats)
     ties.check()
+
+
+def test_c5_full_size_statistics(ts, dev):
+    """Row maxima and log-sum-exp at the full C5 size (512 x 262,144 fp32) against the oracle on sampled rows,
+    including the rows with a duplicated maximum."""
+    b = workloads.c5()
+    x = to_device(b.logits, b.dtype, dev)
+    m, ls, st = ts.vsamp_softmax_lse(x, temperature=t(b.temperature, dev))
+    m, ls, st = m.cpu().numpy(), ls.cpu().numpy(), st.cpu().numpy()
+    assert np.all(st == 0)
+    for r in sorted(set(range(0, 512, 37)) | set(int(v) for v in b.meta["dup_rows"])):
+        st_o, m_o, ls_o = osm.softmax_lse_row(b.logits[r], b.dtype, b.temperature[r])
+        assert m[r] == np.float32(m_o) and abs(ls[r] - ls_o) <= LOGP_TOL, r
 
 
 def test_c5_full_batch_properties(ts, dev):

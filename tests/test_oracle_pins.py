@@ -13,6 +13,7 @@
 import itertools
 import math
 import os
+import struct
 import subprocess
 import sys
 from fractions import Fraction
@@ -178,6 +179,32 @@ def test_canonical_order_and_topk_brute_force():
             assert st == 0
             want = sorted(_brute_topk_set(list(x64), min(k, n))) if k > 0 else []
             assert list(out[:len(want)]) == want and all(v == -1 for v in out[len(want):])
+
+
+def _bf16_value(bits):
+    """A bfloat16 bit pattern as a Python float: the high half of an IEEE single."""
+    return struct.unpack("<f", struct.pack("<I", (int(bits) & 0xFFFF) << 16))[0]
+
+
+def test_topk_select_bf16_brute_force_with_ties():
+    """bf16 scores: values equal as bf16 tie even where their fp32 sources differed; -0 ties +0; the k-set is
+    the unique dominating subset and comes out in ascending index order."""
+    rng = np.random.default_rng(17)
+    src = np.array([1.0, 1.001, 0.999, -0.0, 0.0, 2.5, 2.5078125, -1.25, np.inf, -np.inf], np.float32)
+    for trial in range(60):
+        n = int(rng.integers(1, 9))
+        bits = workloads.f32_to_bf16_bits(src[rng.integers(0, len(src), n)])
+        vals = [_bf16_value(b) for b in bits]
+        for k in range(0, n + 2):
+            st, out = sm.topk_select_row(bits, n, k, n + 2, dtype="bf16")
+            assert st == 0
+            want = sorted(_brute_topk_set(vals, min(k, n))) if k > 0 else []
+            assert list(out[:len(want)]) == want and all(v == -1 for v in out[len(want):]), (trial, vals, k)
+    # 1.0 and 1.001 are one bf16 value: the lowest indices win the tie
+    bits = workloads.f32_to_bf16_bits(np.array([0.5, 1.001, 1.0, 1.0, 0.25], np.float32))
+    assert list(sm.topk_select_row(bits, 5, 2, 2, dtype="bf16")[1]) == [1, 2]
+    nan = workloads.f32_to_bf16_bits(np.array([1.0, np.nan], np.float32))
+    assert sm.topk_select_row(nan, 2, 1, 1, dtype="bf16")[0] == sm.STATUS_NONFINITE
 
 
 def test_topk_select_contract():
@@ -587,3 +614,116 @@ def test_kept_logprob_closed_forms():
     assert sm.kept_logprob_row(y, "f32", 1.0, 0, 1.0, 0.0, 4)[0] == sm.STATUS_INVALID_ARG
     y[2] = np.nan
     assert sm.kept_logprob_row(y, "f32", 1.0, 0, 1.0, 0.0, 1)[0] == sm.STATUS_NONFINITE
+
+
+# ----------------------------------------------------------------------------------------------
+# The parity tolerances the oracle reports: the 1e-6 band of top-p / min-p and near-tie draws
+# ----------------------------------------------------------------------------------------------
+BAND = Fraction(1, 10**6)
+
+
+def _band_counts_exact(w_sorted, nk, target):
+    """(kept_lo, kept, kept_hi) of a top-p cut by exact rational prefixes: rank j is kept iff the mass
+    before it is below the target; ranks whose prefix lies within 1e-6 * S_k of the target may go either
+    way (the tolerance of the stage's contract, read in probability units)."""
+    Sk = sum(w_sorted[:nk])
+    pref, lo, mid, hi = Fraction(0), 0, 0, 0
+    for j in range(nk):
+        lo += pref < target - BAND * Sk
+        mid += pref < target
+        hi += pref <= target + BAND * Sk
+        pref += w_sorted[j]
+    return max(1, lo), max(1, mid), max(1, hi)
+
+
+@pytest.mark.parametrize("n,k,T", [(1000, 0, 1.0), (12, 0, 1.0), (12, 9, 0.7), (40, 25, 1.3)])
+def test_topp_band_bounds_at_half_and_twice_the_tolerance(n, k, T):
+    """The target p * S_k is placed 0.5e-6 * S_k and 2e-6 * S_k on either side of a prefix mass (p rounded to
+    fp32, the exact offset recomputed in rationals): inside the band the boundary token may go either way
+    (kept_lo < kept_hi), outside it the three counts agree. A band of the wrong width, or a sign slip in
+    either bound, moves one of the eight cases."""
+    rng = np.random.default_rng(n * 100 + k)
+    if n == 1000:
+        x = np.zeros(n, dtype=np.float32)                       # uniform: prefixes are the integers
+    else:
+        x = (rng.uniform(-2.0, 0.0, n)).astype(np.float32)     # every weight >= e^-2/T of the max
+    x64 = [float(v) for v in x]
+    order = sorted(range(n), key=lambda v: (-x64[v], v))
+    m = x64[order[0]]
+    Tf = float(np.float32(T))
+    w = [Fraction(math.exp((x64[v] - m) / Tf)) for v in order]
+    nk = k if 0 < k < n else n
+    Sk = sum(w[:nk])
+    checked = 0
+    for j in (1, nk // 2, nk - 2):
+        Pj = sum(w[:j])                                         # mass before rank j
+        for delta, pattern in ((Fraction(1, 2 * 10**6), (j, j + 1, j + 1)), (Fraction(-1, 2 * 10**6), (j, j, j + 1)),
+                               (Fraction(2, 10**6), (j + 1, j + 1, j + 1)), (Fraction(-2, 10**6), (j, j, j))):
+            p = float(np.float32(float((Pj + delta * Sk) / Sk)))
+            off = (Fraction(p) * Sk - Pj) / Sk                   # realised offset, exact
+            assert abs(off - delta) < Fraction(1, 10**7)
+            want = _band_counts_exact(w, nk, Fraction(p) * Sk)
+            assert want == pattern                              # the construction lands where intended
+            r = sm.sample_row(x, "f32", T, k, p, 0.0)
+            assert (r.kept_lo, r.kept, r.kept_hi) == want, (j, float(delta), (r.kept_lo, r.kept, r.kept_hi), want)
+            assert not r.ambiguous
+            checked += 1
+    assert checked == 12
+
+
+@pytest.mark.parametrize("T", [1.0, 0.6])
+def test_minp_band_bounds_at_half_and_twice_the_tolerance(T):
+    """min_p placed at w_j (1 -+ 0.5e-6) and w_j (1 -+ 2e-6) for the weight w_j of rank j: a weight within
+    1e-6 * min_p of min_p may go either way, one further out may not."""
+    n = 16
+    x = np.linspace(-3.0, 0.0, n).astype(np.float32)[::-1].copy()  # distinct, decreasing: rank j = index j
+    Tf = float(np.float32(T))
+    w = [math.exp((float(v) - float(x[0])) / Tf) for v in x]
+    for j in (1, 7, 14):
+        for rel, pattern in ((0.5e-6, (j, j, j + 1)), (-0.5e-6, (j, j + 1, j + 1)),
+                             (2e-6, (j, j, j)), (-2e-6, (j + 1, j + 1, j + 1))):
+            mp = float(np.float32(w[j] * (1.0 + rel)))
+            r = sm.sample_row(x, "f32", T, 0, 1.0, mp)
+            assert (r.kept_lo, r.kept, r.kept_hi) == pattern, (j, rel, (r.kept_lo, r.kept, r.kept_hi))
+
+
+def _two_token_row(g_a, g_b, gap):
+    """fp32 logits (0, x_b) whose perturbed scores (x - max) + g differ by about ``gap`` in favour of token 0;
+    returns the row and the realised scores, computed exactly from the rounded x_b."""
+    xb = np.float32(g_a - g_b - gap)
+    x = np.array([0.0, xb], dtype=np.float32)
+    m = max(0.0, float(xb))
+    sa, sb = (0.0 - m) + g_a, (float(xb) - m) + g_b
+    return x, sa, sb
+
+
+def test_near_tie_flag_is_one_part_in_a_million_of_the_best_score():
+    """Two-token rows built from the pinned Philox words and Gumbel map, with the runner-up 0.5e-6 or 2e-6
+    (relative to max(1, |best|)) below the winner: only the first is a near tie. Draws with |best| well above
+    1 separate the relative reading from an absolute 1e-6."""
+    seed, rid = 77, 5
+    steps = np.arange(4000, dtype=np.uint64)
+    g = sm.gumbel_from_uniform(sm.uniform_from_word(ph.token_words(np.array([0, 1]), seed, rid, steps)))
+    found = {"small": 0, "large": 0}
+    for st in range(len(steps)):
+        g_a, g_b = float(g[st, 0]), float(g[st, 1])
+        if not (0.05 < g_a - g_b < 0.9):                       # x_b in (0, 1): fp32 spacing below 6e-8
+            continue
+        # the winner's score is g_b + gap (token 1 holds the maximum logit)
+        kind = "large" if g_b > 3.0 else ("small" if abs(g_b) < 0.9 else None)
+        if kind is None or found[kind] >= 3:
+            continue
+        scale = max(1.0, abs(g_b))
+        for rel, want in ((0.5e-6, True), (2e-6, False)):
+            x, sa, sb = _two_token_row(g_a, g_b, rel * scale)
+            realised = (sa - sb) / max(1.0, abs(sa))
+            assert 0.8 * rel < realised < 1.2 * rel             # the fp32 logit kept the intended gap
+            r = sm.sample_row(x, "f32", 1.0, 0, 1.0, 0.0, seed=seed, row_id=rid, step=st)
+            assert r.token == 0 and abs(r.best - sa) < 1e-12 and abs(r.second - sb) < 1e-12
+            assert r.near_tie is want, (st, g_b, rel, realised)
+            if kind == "large" and want:
+                assert sa - sb > 1e-6                           # an absolute 1e-6 band would miss it
+        found[kind] += 1
+        if found["small"] >= 3 and found["large"] >= 3:
+            break
+    assert found == {"small": 3, "large": 3}

@@ -70,6 +70,30 @@ def test_static_scratch_matches_the_workspace_entry_point_on_two_calls_in_a_row(
 
 
 @pytest.mark.gpu
+def test_static_scratch_calls_leave_free_device_memory_unchanged(ts, dev):
+    """The property the entry point exists for: after a first call (which looks up the array's address),
+    further calls with caller-owned outputs change no device allocation."""
+    b = workloads.c2(B=16)
+    x = parity_util.to_device(b.logits, b.dtype, dev)
+    t = parity_util.t
+    args = dict(temperature=t(b.temperature, dev), top_k=t(b.top_k, dev), top_p=t(b.top_p, dev),
+                min_p=t(b.min_p, dev), seed=t(b.seed, dev), step=t(b.step, dev), V=b.V,
+                token=torch.empty(b.B, dtype=torch.int32, device=dev),
+                logprob=torch.empty(b.B, dtype=torch.float32, device=dev),
+                row_status=torch.empty(b.B, dtype=torch.int32, device=dev),
+                stats=torch.empty((b.B, 4), dtype=torch.int32, device=dev), want_stats=True)
+    ts.vsamp_sample_static(x, **args)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info(dev)
+    for _ in range(5):
+        ts.vsamp_sample_static(x, **args)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info(dev)
+    assert free1 == free0, (free0, free1)
+    assert int(args["row_status"].ne(0).sum()) == 0
+
+
+@pytest.mark.gpu
 def test_static_scratch_refuses_a_batch_beyond_its_size(ts, dev):
     lib = ts.load()
     V = 151936

@@ -425,8 +425,8 @@ vsamp_status vsamp_sample_static(const void* logits, vsamp_dtype dt, int64_t B, 
   void* scratch = nullptr;
   st = static_scratch(&scratch);
   if (st != VSAMP_OK) return st;
-  // the row counters and chunk statistics the kernels accumulate into start at zero
-  if (cudaMemsetAsync(scratch, 0, need, static_cast<cudaStream_t>(stream)) != cudaSuccess) return VSAMP_ERR_CUDA;
+  // no clear: the streaming kernels write every plan and piece statistic before reading it, and reset the
+  // draw slot themselves, so the previous call's contents are never read
   return vsamp_sample_ws(logits, dt, B, V, ld, temperature, top_k, top_p, min_p, seed, step, row_id, token,
                          logprob, row_status, stats, scratch, (size_t)VSAMP_STATIC_SCRATCH_BYTES, stream);
 }

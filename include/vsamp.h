@@ -139,17 +139,22 @@ vsamp_status vsamp_sample(const void* logits, vsamp_dtype dt, int64_t B, int64_t
                           const uint32_t* row_id, int32_t* token, float* logprob,
                           int32_t* row_status, int32_t* stats, void* stream);
 
-/* vsamp_sample with a workspace. The same draw, computed by streaming kernels over fixed 4 KB pieces of
- * every row (one warp per piece) instead of one thread-block cluster per row: piece statistics (one HBM read),
- * a plan per row, the draw over the pieces (read again, mostly from L2) and the outputs, in four launches on
- * `stream`. Results are deterministic and do not depend on the batch; they agree with vsamp_sample except for
- * the last bits of the row mass (piece masses are rescaled to the row maximum in binary64), which moves a
- * top-p cut only inside the 1e-6 tolerance band.
+/* vsamp_sample with a workspace: the same draw by two streaming launches over fixed 4 KB pieces of every row
+ * (2048 bf16 or 1024 fp32 logits) instead of one thread-block cluster per row. In the first, each warp reads
+ * pieces from HBM once and writes their statistics (maximum, count of maxima, mass relative to the maximum)
+ * and, for rows without top-k and with T > 0, a 4-bit code per 16-byte vector from the smallest Philox word of
+ * its tokens (the words do not depend on the logits). In the second, one CTA per row combines the row's pieces
+ * in a fixed order, plans the cut (radix rounds re-read the row, mostly from L2, only when the cut leaves the
+ * maximum's tie group) and draws: only vectors whose code passes the prune bound are scored again.
+ * Results are deterministic and do not depend on the batch; they agree with vsamp_sample except for the last
+ * bits of the row mass (piece masses are rescaled to the row maximum in binary64), which moves a top-p cut
+ * only inside the 1e-6 tolerance band. Rows with top-k are drawn by scanning their kept tokens instead; for
+ * rows whose kept set is small relative to V, vsamp_sample is usually faster.
  *   workspace        device buffer of at least vsamp_sample_workspace_size(dt, B, V) bytes, 16-byte aligned.
  *                    It needs no initialisation: every call writes what it reads. Calls sharing a workspace
  *                    must not run at the same time (use one workspace per stream).
  *   workspace_bytes  its size in bytes; too small, unaligned or NULL is VSAMP_ERR_INVALID_ARG.
- * Every other argument is as for vsamp_sample. */
+ * Every other argument is as for vsamp_sample. Two launches on `stream`. */
 vsamp_status vsamp_sample_ws(const void* logits, vsamp_dtype dt, int64_t B, int64_t V, int64_t ld,
                              const float* temperature, const int32_t* top_k, const float* top_p,
                              const float* min_p, const uint64_t* seed, const uint64_t* step,
@@ -157,11 +162,12 @@ vsamp_status vsamp_sample_ws(const void* logits, vsamp_dtype dt, int64_t B, int6
                              int32_t* row_status, int32_t* stats, void* workspace, size_t workspace_bytes,
                              void* stream);
 
-/* Workspace bytes vsamp_sample_ws needs for B rows of V logits of type dt (0 for invalid arguments). */
+/* Workspace bytes vsamp_sample_ws needs for B rows of V logits of type dt (0 for invalid arguments):
+ * 256 + 160 B * ceil(V / piece) with pieces of 2048 bf16 or 1024 fp32 logits. */
 size_t vsamp_sample_workspace_size(vsamp_dtype dt, int64_t B, int64_t V);
 
 /* Bytes of the fixed device array that vsamp_sample_static uses as its workspace. */
-#define VSAMP_STATIC_SCRATCH_BYTES 1048576
+#define VSAMP_STATIC_SCRATCH_BYTES 4194304
 
 /* vsamp_sample_ws on a fixed scratch array of VSAMP_STATIC_SCRATCH_BYTES bytes that the library holds in
  * device memory (a file-scope __device__ array of its module), so the call allocates nothing: no device
@@ -170,10 +176,10 @@ size_t vsamp_sample_workspace_size(vsamp_dtype dt, int64_t B, int64_t V);
  *   Size limit: vsamp_sample_workspace_size(dt, B, V) must not exceed VSAMP_STATIC_SCRATCH_BYTES, else
  *     the call returns VSAMP_ERR_SCRATCH_LIMIT and enqueues nothing.
  *   Set-up: the first call on each device (with that device current) looks up the array's address once.
- *   Contents: the array keeps what the last call left in it. Nothing needs clearing first: as for
- *     vsamp_sample_ws, the kernels write every value they read, so each call enqueues only the kernels.
- *   Largest batch (from vsamp_sample_workspace_size): V = 151,936: 417 rows fp32, 789 rows bf16;
- *     V = 262,144: 248 rows fp32, 481 rows bf16.
+ *   Contents: the array keeps what the last call left in it. As for vsamp_sample_ws nothing needs clearing
+ *     (every call writes what it reads), so each call enqueues only the two kernels.
+ *   Largest batch (from vsamp_sample_workspace_size): V = 151,936: 175 rows fp32, 349 rows bf16;
+ *     V = 262,144: 102 rows fp32, 204 rows bf16.
  *   Races: one array per device is shared by every caller of this function, so calls whose kernels
  *     overlap on one device (from two streams or two host threads) race on it and give wrong results;
  *     serialise them, or use vsamp_sample_ws with a workspace per stream.

@@ -91,9 +91,9 @@ def test_workspace_size_and_host_checks_of_the_workspace_entry_point(lib):
     import top_sampling_gb300 as ts
 
     l2 = ts.load()
-    # a 256-byte reserved header, 128 bytes per row and 16 per 4 KB piece of the row
-    assert l2.vsamp_sample_workspace_size(ts.VSAMP_BF16, 256, 151936) == 256 + 256 * 128 + 256 * 75 * 16
-    assert l2.vsamp_sample_workspace_size(ts.VSAMP_F32, 4, 32000) == 256 + 4 * 128 + 4 * 32 * 16
+    # a 256-byte reserved header and 32 + 128 bytes per 4 KB piece of a row (piece record, draw codes)
+    assert l2.vsamp_sample_workspace_size(ts.VSAMP_BF16, 256, 151936) == 256 + 256 * 75 * 160
+    assert l2.vsamp_sample_workspace_size(ts.VSAMP_F32, 4, 32000) == 256 + 4 * 32 * 160
     assert l2.vsamp_sample_workspace_size(7, 4, 100) == 0
     assert l2.vsamp_sample_workspace_size(ts.VSAMP_F32, 0, 100) == 0
     dummy = ctypes.c_void_p(16)

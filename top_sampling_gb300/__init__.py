@@ -24,7 +24,7 @@ VSAMP_ERR_CUDA = 3
 VSAMP_ERR_NONFINITE = 4
 VSAMP_ERR_TIMEOUT = 5
 VSAMP_ERR_SCRATCH_LIMIT = 6
-VSAMP_STATIC_SCRATCH_BYTES = 1 << 20   # the fixed scratch array of vsamp_sample_static
+VSAMP_STATIC_SCRATCH_BYTES = 1 << 22   # the fixed scratch array of vsamp_sample_static
 VSAMP_F32 = 0
 VSAMP_BF16 = 1
 

@@ -381,7 +381,7 @@ vsamp_status vsamp_sample(const void* logits, vsamp_dtype dt, int64_t B, int64_t
 size_t vsamp_sample_workspace_size(vsamp_dtype dt, int64_t B, int64_t V) {
   if ((dt != VSAMP_F32 && dt != VSAMP_BF16) || B <= 0 || V <= 0) return 0;
   const int es = dt == VSAMP_F32 ? 4 : 2;
-  return sizeof(StreamHeader) + (size_t)B * sizeof(RowPlan) + (size_t)B * (size_t)split_nchunks(V, es) * sizeof(ChunkStat);
+  return split_workspace_bytes(B, V, es);
 }
 
 vsamp_status vsamp_sample_ws(const void* logits, vsamp_dtype dt, int64_t B, int64_t V, int64_t ld,

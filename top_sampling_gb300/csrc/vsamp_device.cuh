@@ -305,6 +305,34 @@ struct PhiloxRowMin {
   }
 };
 
+// PhiloxRowMin's rounds returning all four output words of each of N counters (same words as philox4x32_10).
+template <int N>
+__device__ __forceinline__ void philox_row_words(const PhiloxRowMin& ph, const uint32_t (&c0)[N], uint4 (&out)[N]) {
+  constexpr uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u, W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+#pragma unroll
+  for (int n = 0; n < N; ++n) {
+    unsigned long long p0, p1;
+    asm("mul.wide.u32 %0, %1, %2;" : "=l"(p0) : "r"(c0[n]), "r"(M0));
+    const uint32_t z1 = (uint32_t)(p0 >> 32) ^ ph.z1k, w1 = (uint32_t)p0;
+    asm("mul.wide.u32 %0, %1, %2;" : "=l"(p1) : "r"(z1), "r"(M1));
+    out[n] = make_uint4((uint32_t)(p1 >> 32) ^ ph.x2k, (uint32_t)p1, ph.hi2 ^ w1, ph.w2);
+  }
+  uint32_t k0 = ph.k0_2, k1 = ph.k1_2;
+#pragma unroll
+  for (int r = 2; r < 10; ++r) {
+#pragma unroll
+    for (int n = 0; n < N; ++n) {
+      unsigned long long p0, p1;
+      asm("mul.wide.u32 %0, %1, %2;" : "=l"(p0) : "r"(out[n].x), "r"(M0));
+      asm("mul.wide.u32 %0, %1, %2;" : "=l"(p1) : "r"(out[n].z), "r"(M1));
+      out[n] = make_uint4((uint32_t)(p1 >> 32) ^ out[n].y ^ k0, (uint32_t)p1, (uint32_t)(p0 >> 32) ^ out[n].w ^ k1,
+                          (uint32_t)p0);
+    }
+    k0 += W0;
+    k1 += W1;
+  }
+}
+
 __device__ __forceinline__ uint32_t philox_word(uint4 w, int lane) {
   return lane == 0 ? w.x : lane == 1 ? w.y : lane == 2 ? w.z : w.w;
 }

@@ -1,6 +1,7 @@
-// The split-vocabulary sampling path (vsamp_sample_ws): every row is cut into fixed pieces of 1024 logits and
-// streaming kernels sweep all (row, piece) pairs of the batch (see the section "The streaming sampler" below).
-// The cut into pieces depends only on V, so results are deterministic and do not depend on the batch.
+// The split-vocabulary sampling path (vsamp_sample_ws, vsamp_sample_static): every row is cut into fixed pieces of
+// 4 KB (2048 bf16 or 1024 fp32 logits) and one fused streaming kernel sweeps all (row, piece) pairs of the batch
+// (see "The fused streaming sampler" below). The cut into pieces depends only on V, so results are deterministic
+// and do not depend on the batch.
 #pragma once
 
 #include "vsamp_row.cuh"
@@ -22,26 +23,6 @@ struct ChunkStat {                   // 16 bytes per (row, chunk)
   unsigned long long s;              // sum of 2^((x - m) * c1), 2^-40 fixed point
 };
 
-constexpr int32_t kDeferIndex = -2;   // RowPlan::It: the draw kernel finds the cut's last kept index
-
-struct RowPlan {                     // 128 bytes per row
-  uint32_t done1, done2;             // reserved (zero)
-  unsigned long long best;           // draw: (orderable score << 32) | (0xFFFFFFFF - index); 0 = none
-  int32_t status;                    // the row's status; the draw kernel skips rows that are not VSAMP_OK
-  int32_t draw;                      // 1: the draw kernel draws the token; 0: the outputs are written
-  float M, invT, c1, xP, logS, B0, kappa;
-  int32_t It;                        // kept: x > xP, or x == xP and index <= It
-  uint32_t bk;
-  int32_t all_cand;
-  uint32_t rid, st_lo, st_hi, k0, k1;
-  int32_t passes, rounds, path;
-  uint32_t kept;
-  int32_t cb;                        // It == kDeferIndex: the chunk holding the cut's last kept maximum,
-  uint32_t cneed;                    //   which is the cneed-th maximum of that chunk (the draw finds it)
-  int32_t one;                       // the cut keeps one token (the first maximum): no draw
-  uint32_t pad[4];
-};
-static_assert(sizeof(RowPlan) == 128, "RowPlan layout");
 static_assert(sizeof(ChunkStat) == 16, "ChunkStat layout");
 
 __host__ __device__ inline int64_t split_chunk_elems(int esize) { return kPieceBytes / esize; }
@@ -229,7 +210,7 @@ struct RowPlanner {
   }
 
   // radix search over the whole row (as the row engine's, with the row read from L2 by this CTA)
-  __device__ RadixOut radix(bool mass_mode, unsigned long long goal, float goal_p, bool want_mass) {
+  __device__ __noinline__ RadixOut radix(bool mass_mode, unsigned long long goal, float goal_p, bool want_mass) {
     RadixOut out{};
     out.ok = 1;
     uint32_t prefix = 0;
@@ -341,7 +322,7 @@ struct RowPlanner {
 
   // min-p statistics: elements with key >= kmin32 (fp32 key space), their mass, the smallest such key and
   // its count
-  __device__ void minp_stats(uint32_t kmin32, uint32_t& cnt_ge, unsigned long long& mass_ge, uint32_t& minkey,
+  __device__ __noinline__ void minp_stats(uint32_t kmin32, uint32_t& cnt_ge, unsigned long long& mass_ge, uint32_t& minkey,
                              uint32_t& cnt_minkey) {
     uint32_t c = 0, mk = 0xFFFFFFFFu, cmk = 0;
     unsigned long long m = 0;
@@ -367,7 +348,7 @@ struct RowPlanner {
 
   // the index of the need-th element (1-based, index order) equal to xv, visiting vectors from begin_vec;
   // -1 if there are fewer. Tiles of 256 threads x 4 consecutive vectors, one block scan per tile.
-  __device__ int32_t nth_equal(float xv, unsigned long long need, int64_t begin_vec) {
+  __device__ __noinline__ int32_t nth_equal(float xv, unsigned long long need, int64_t begin_vec) {
     constexpr int PV = 4;
     const unsigned char* xr = p.x + (int64_t)row * p.ld * Tr::ESIZE;
     const int64_t nvec = (n + VE - 1) / VE;
@@ -414,58 +395,390 @@ struct RowPlanner {
   }
 };
 
-// ------------------------------------------------------------------------------------------------
-// The row's plan, by the CTA of its last chunk (out of line: the chunk pass keeps its registers).
-// ------------------------------------------------------------------------------------------------
+// A piece of a row as one lane sees it: vector u of lane l is vector u * 32 + l of the piece. Aligned rows
+// take 16-byte loads; the last, partial vector of a row and unaligned rows are read element by element.
 template <typename T>
-static __device__ __noinline__ void plan_row(const Params p, RowPlan* plans, const ChunkStat* stats_c,
-                                            ChunkStat* stats, int nchunks, int64_t row, float temp0, float Teff,
-                                            float c1, SplitShared& sh) {
+struct PieceView {
+  using Tr = Traits<T>;
+  static constexpr int VE = Tr::VE;
+  const unsigned char* xr;   // the row
+  int64_t V;                 // row length
+  int32_t tma;               // the row is 16-byte aligned
+  int64_t e_begin;           // first element of the piece
+  __device__ __forceinline__ int64_t elem(int u) const {
+    return e_begin + (int64_t)(u * 32 + (int)(threadIdx.x & 31)) * VE;
+  }
+  // the whole piece lies in an aligned row: plain 16-byte loads without bounds
+  __device__ __forceinline__ bool full() const { return tma && e_begin + kPieceElems<T> <= V; }
+  // start moving the lane's vectors of a full piece towards L1 (the warp's next item, while this one computes)
+  __device__ __forceinline__ void prefetch() const {
+    if (!full()) return;
+    const uint4* b = reinterpret_cast<const uint4*>(xr + e_begin * Tr::ESIZE) + (int)(threadIdx.x & 31);
+#pragma unroll
+    for (int u = 0; u < kPieceVecs<T>; ++u) asm volatile("prefetch.global.L1 [%0];" ::"l"(b + u * 32));
+  }
+  __device__ __forceinline__ void get_full(int u, uint4& v) const {
+    v = __ldg(reinterpret_cast<const uint4*>(xr + e_begin * Tr::ESIZE) + u * 32 + (int)(threadIdx.x & 31));
+  }
+  __device__ __forceinline__ int get(int u, uint4& v) const {
+    const int64_t e = elem(u);
+    const int64_t left = V - e;
+    const int cnt = left <= 0 ? 0 : (left >= VE ? VE : (int)left);
+    if (cnt == VE && tma) {
+      v = __ldg(reinterpret_cast<const uint4*>(xr + e * Tr::ESIZE));
+    } else {
+      uint32_t w[4] = {0u, 0u, 0u, 0u};
+      for (int i = 0; i < cnt; ++i) {
+        if (Tr::ESIZE == 4) w[i] = reinterpret_cast<const uint32_t*>(xr)[e + i];
+        else w[i >> 1] |= (uint32_t)reinterpret_cast<const uint16_t*>(xr)[e + i] << (16 * (i & 1));
+      }
+      v = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    return cnt;
+  }
+};
+
+// The index of the need-th element (1-based, index order) equal to xv in a piece; kNoIndex if there are fewer.
+// Element order in the piece is (vector u, lane, element i): one warp scan per u. Warp-collective.
+template <typename T>
+__device__ __noinline__ int32_t piece_nth_equal(const PieceView<T>& pv, float xv, uint32_t need) {
   using Tr = Traits<T>;
   constexpr int VE = Tr::VE;
-  const int t = threadIdx.x;
-  (void)stats_c;
-  RowPlan& pl = plans[row];
-  const int64_t n = p.V;
-  // ---- combine the chunks: M, non-finite flag, S rescaled to M, count of maxima ----
-  float m = -INFINITY;
-  uint32_t nonfin = 0;
-  for (int k = t; k < nchunks; k += kSplitThreads) {
-    const float mk = load_stat(stats + row * nchunks + k).m;
-    if (mk != mk) nonfin = 1;
-    else m = fmaxf(m, mk);
+  constexpr int U = kPieceVecs<T>;
+  const int lane = threadIdx.x & 31;
+  uint32_t base = 0;
+  int32_t found = kNoIndex;
+  for (int u = 0; u < U; ++u) {
+    uint4 v;
+    const int n = pv.get(u, v);
+    float x[VE];
+    Tr::values(v, x);
+    uint32_t c = 0;
+#pragma unroll
+    for (int i = 0; i < VE; ++i) c += (i < n && x[i] == xv) ? 1u : 0u;
+    uint32_t inc = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFullMask, inc, o);
+      if (lane >= o) inc += y;
+    }
+    const uint32_t excl = base + inc - c;
+    int32_t idx = kNoIndex;
+    if (c && excl < need && need <= excl + c) {
+      uint32_t seen = excl;
+#pragma unroll
+      for (int i = 0; i < VE; ++i)
+        if (idx < 0 && i < n && x[i] == xv && ++seen == need) idx = (int32_t)(pv.elem(u) + i);
+    }
+    const uint32_t hit = __ballot_sync(kFullMask, idx >= 0);
+    if (hit) {
+      found = __shfl_sync(kFullMask, idx, __ffs(hit) - 1);
+      break;
+    }
+    base += __shfl_sync(kFullMask, inc, 31);
   }
-  nonfin = __syncthreads_or(nonfin);
-  const float M = block_max_f(m, sh);
+  return found;
+}
+
+// ------------------------------------------------------------------------------------------------
+// The streaming sampler (vsamp_sample_ws, vsamp_sample_static): two launches, no waiting inside either.
+//   piece_kernel   every warp takes 4 KB pieces of the batch, grid-stride, each arriving in shared memory by a
+//                  bulk copy issued one piece ahead (plain loads for a partial piece or an unaligned row). It
+//                  writes the piece's record: maximum, minimum, count of maxima and mass relative to its maximum
+//                  (2^-40 fixed point per 16-byte vector). For a row that draws over a possibly large kept set
+//                  (no top-k, T > 0) it also forms every token's Philox word (the words depend only on (seed,
+//                  row_id, step), not on the logits) and writes a 4-bit draw code per vector.
+//   row_kernel     one CTA per row combines the row's piece records in a fixed order, plans the cut (radix rounds
+//                  re-read the row from L2 only when the cut leaves the maximum's tie group), and draws: in every
+//                  piece that holds a kept token, the vectors whose code passes the row's prune bound are read
+//                  again and scored exactly; rows without codes scan their kept tokens. It writes the outputs.
+// Per row the result is a function of the row alone (pieces are fixed by V, combined in a fixed order). Every
+// call writes the workspace before reading it, so the workspace needs no initialisation.
+// ------------------------------------------------------------------------------------------------
+struct StreamHeader {                // the first 256 bytes of the workspace (reserved)
+  uint32_t reserved[64];
+};
+static_assert(sizeof(StreamHeader) == 256, "StreamHeader layout");
+
+struct PieceRec {                    // 32 bytes per (row, piece)
+  float m;                           // piece maximum (NaN: a non-finite value, or the load timed out)
+  uint32_t cnt;                      // elements equal to m (kTimeoutCnt when the load timed out)
+  unsigned long long s;              // sum of 2^((x - m) * c1), 2^-40 fixed point
+  float mn;                          // piece minimum
+  uint32_t reserved[3];
+};
+static_assert(sizeof(PieceRec) == 32, "PieceRec layout");
+
+constexpr int kItemPieces = kStreamThreads / 32;   // warps per CTA
+constexpr uint32_t kTimeoutCnt = 0xFFFFFFFFu;
+constexpr int kFlagMax = 1024;                     // flagged vectors a row finish collects before it scans instead
+
+struct StreamWs {
+  PieceRec* recs;                    // [B, np]
+  uint32_t* codes;                   // [B, np, 32]: lane l's word holds the codes of vectors u * 32 + l
+};
+
+// Workspace bytes: header | PieceRec[B, np] | codes[B, np, 32].
+inline size_t split_workspace_bytes(int64_t B, int64_t V, int esize) {
+  const size_t np = (size_t)split_nchunks(V, esize);
+  return sizeof(StreamHeader) + (size_t)B * np * sizeof(PieceRec) + (size_t)B * np * 32u * sizeof(uint32_t);
+}
+
+// A piece record written by the other launch: read through L2.
+__device__ __forceinline__ PieceRec load_rec(const PieceRec* a) {
+  const uint4 v0 = __ldcg(reinterpret_cast<const uint4*>(a));
+  const uint4 v1 = __ldcg(reinterpret_cast<const uint4*>(a) + 1);
+  PieceRec r;
+  r.m = __uint_as_float(v0.x);
+  r.cnt = v0.y;
+  r.s = ((unsigned long long)v0.w << 32) | v0.z;
+  r.mn = __uint_as_float(v1.x);
+  return r;
+}
+
+// 4-bit draw code of a 16-byte vector from the smallest Philox word w of its tokens: min(clz(w), 15).
+// w < bk implies code(w) >= code(bk), so testing codes flags a superset of the vectors the prune bound keeps.
+__device__ __forceinline__ uint32_t draw_code(uint32_t w) { return min((uint32_t)__clz(w), 15u); }
+
+// Shared memory of a piece_kernel CTA: per warp, two 4 KB piece buffers and their mbarriers.
+struct PieceSmem {
+  unsigned long long bar[kItemPieces][2];
+  __align__(128) uint4 buf[kItemPieces][2][kPieceBytes / 16];
+};
+
+constexpr int kCodeSmem = 4800;   // code words a row finish stages in shared memory: rows of up to 150 pieces
+
+// Shared memory of a row_kernel CTA.
+struct FinishSmem {
+  SplitShared sh;
+  int32_t it;                                          // the cut's last kept index
+  uint32_t nflag;                                      // flagged vectors
+  float bs[kItemPieces], bsv[kItemPieces];             // per-warp best score, its scaled logit
+  int32_t bi[kItemPieces];                             //   and index
+  uint32_t flist[kFlagMax];                            // flagged vector indices
+  uint32_t codes[kCodeSmem];                           // the row's draw codes
+  __align__(16) uint4 piece[kPieceBytes / 16];         // the boundary piece
+};
+
+// The parameters of one row's draw.
+struct DrawRow {
+  float M, invT, c1, xP, kappa;
+  int32_t It;
+  uint32_t bk, rid, st_lo, st_hi;
+  PhiloxKey key;
+  bool all_cand;
+};
+
+// Exact perturbed scores of one vector's kept tokens that pass the prune bound (every kept token when all
+// kept tokens are candidates); the running arg-max (score, index, scaled logit) is updated in place.
+template <typename T>
+__device__ __noinline__ void score_vector(uint4 v, int cnt, int64_t e0, const DrawRow& d, float& bscore, int32_t& bidx,
+                                          float& bs) {
+  using Tr = Traits<T>;
+  constexpr int VE = Tr::VE;
+  float x[VE];
+  Tr::values(v, x);
+  uint32_t kmask = 0u;
+#pragma unroll
+  for (int i = 0; i < VE; ++i)
+    if (i < cnt && (x[i] > d.xP || (x[i] == d.xP && e0 + i <= (int64_t)d.It))) kmask |= 1u << i;
+  if (!kmask) return;
+  uint32_t b[VE];
+#pragma unroll
+  for (int g = 0; g < VE / 4; ++g) {
+    const uint4 w4 = philox4x32_10(make_uint4((uint32_t)(e0 >> 2) + (uint32_t)g, d.rid, d.st_lo, d.st_hi), d.key);
+    b[4 * g + 0] = w4.x; b[4 * g + 1] = w4.y; b[4 * g + 2] = w4.z; b[4 * g + 3] = w4.w;
+  }
+#pragma unroll
+  for (int i = 0; i < VE; ++i) {
+    if (!((kmask >> i) & 1u)) continue;
+    if (!d.all_cand && b[i] >= d.bk) continue;
+    const float dx = x[i] - d.M;
+    const float sv = dx * d.invT;
+    if (!d.all_cand) {
+      const float w = ex2_approx(dx * d.c1);
+      const float u = fmaf((float)b[i], kTwoM32, kTwoM33);
+      if (!(u < w * d.kappa * 1.00001f)) continue;
+    }
+    const float score = gumbel_score(sv, b[i]);
+    const int32_t idx = (int32_t)(e0 + i);
+    if (argmax_better(score, idx, bscore, bidx)) { bscore = score; bidx = idx; bs = sv; }
+  }
+}
+
+// Every kept token of a row scored (pruned unless all are candidates), the row read from L2: each thread takes
+// vectors t, t + 256, ... (rows drawn without codes, and the certification fallback).
+template <typename T>
+__device__ __noinline__ void score_row(const Params& p, int64_t row, const DrawRow& d, float& bscore, int32_t& bidx,
+                                       float& bs) {
+  using Tr = Traits<T>;
+  constexpr int VE = Tr::VE;
+  const unsigned char* xr = p.x + row * p.ld * Tr::ESIZE;
+  const int64_t nvec = (p.V + VE - 1) / VE;
+  for (int64_t vi = threadIdx.x; vi < nvec; vi += kStreamThreads) {
+    uint4 v;
+    const int cnt = load_vec<T, false>(p, xr, vi * VE, v);
+    score_vector<T>(v, cnt, vi * VE, d, bscore, bidx, bs);
+  }
+}
+
+// The CTA's arg-max of (score, index), ties to the lower index; every thread gets it.
+__device__ __forceinline__ ArgMax block_argmax(ArgMax a, FinishSmem& S) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  a = warp_argmax(a);
+  __syncthreads();
+  if (lane == 0) { S.bs[warp] = a.score; S.bi[warp] = a.idx; S.bsv[warp] = a.s; }
+  __syncthreads();
+  ArgMax b{S.bs[0], S.bi[0], S.bsv[0]};
+#pragma unroll
+  for (int w = 1; w < kItemPieces; ++w)
+    if (argmax_better(S.bs[w], S.bi[w], b.score, b.idx)) b = ArgMax{S.bs[w], S.bi[w], S.bsv[w]};
+  return b;
+}
+
+// A row draws with codes when its parameters allow a large kept set: sampled (T > 0) and no top-k.
+__device__ __forceinline__ bool row_coded(const Params& p, int64_t row) {
+  const float temp0 = p.temperature ? p.temperature[row] : 1.f;
+  const int32_t topk = p.top_k ? p.top_k[row] : 0;
+  return temp0 > 0.f && !(topk > 0 && (int64_t)topk < p.V);
+}
+
+// The index of the need-th element (1-based, index order) equal to xv in a piece, kNoIndex if there are fewer.
+// One warp: the piece is staged in shared memory (all of the lane's loads issued at once), then scanned in the
+// piece's order (vector u, lane, element) with compact loops.
+template <typename T>
+__device__ __noinline__ int32_t piece_nth_equal_staged(const PieceView<T>& pv, float xv, uint32_t need, uint4* stage) {
+  using Tr = Traits<T>;
+  constexpr int VE = Tr::VE;
+  constexpr int U = kPieceVecs<T>;
+  const int lane = threadIdx.x & 31;
+  int n[U];
+  {
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) n[u] = pv.get(u, v[u]);
+#pragma unroll
+    for (int u = 0; u < U; ++u) stage[u * 32 + lane] = v[u];
+  }
+  const int64_t left = pv.V - pv.e_begin;   // valid elements of the piece (its vectors past them count nothing)
+  __syncwarp();
+  uint32_t base = 0;
+#pragma unroll 1
+  for (int u = 0; u < U; ++u) {
+    float x[VE];
+    Tr::values(stage[u * 32 + lane], x);
+    const int64_t e_in = (int64_t)(u * 32 + lane) * VE;
+    const int cnt = left - e_in >= VE ? VE : (left - e_in > 0 ? (int)(left - e_in) : 0);
+    uint32_t c = 0;
+#pragma unroll 1
+    for (int i = 0; i < cnt; ++i) c += x[i] == xv ? 1u : 0u;
+    uint32_t inc = c;
+#pragma unroll 1
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFullMask, inc, o);
+      if (lane >= o) inc += y;
+    }
+    const uint32_t excl = base + inc - c;
+    int32_t idx = kNoIndex;
+    if (c && excl < need && need <= excl + c) {
+      uint32_t seen = excl;
+#pragma unroll 1
+      for (int i = 0; i < cnt; ++i)
+        if (x[i] == xv && ++seen == need) { idx = (int32_t)(pv.e_begin + e_in + i); break; }
+    }
+    const uint32_t hit = __ballot_sync(kFullMask, idx >= 0);
+    if (hit) return __shfl_sync(kFullMask, idx, __ffs(hit) - 1);
+    base += __shfl_sync(kFullMask, inc, 31);
+  }
+  (void)n;
+  return kNoIndex;
+}
+
+// ------------------------------------------------------------------------------------------------
+// Row finish: one CTA (all 256 threads) per row. The row's dependent memory accesses are batched: the piece
+// records and the draw codes come in one round of loads, and after the plan the boundary piece and the flagged
+// vectors in another.
+// ------------------------------------------------------------------------------------------------
+template <typename T>
+static __device__ __forceinline__ void finish_row(const Params& p, const StreamWs& ws, int64_t row, int nchunks,
+                                                  FinishSmem& S) {
+  using Tr = Traits<T>;
+  constexpr int VE = Tr::VE;
+  SplitShared& sh = S.sh;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int64_t n = p.V;
+  const PieceRec* recs = ws.recs + row * nchunks;
+  const float temp0 = p.temperature ? p.temperature[row] : 1.f;
+  const float Teff = temp0 > 0.f ? temp0 : 1.f;   // greedy rows use T = 1 for their statistics
+  const float invT = 1.f / Teff;
+  const float c1 = kLog2e * invT;
+  const bool coded = row_coded(p, row);
+  const int64_t nwords = (int64_t)nchunks * 32;
+  const bool codes_staged = coded && nwords <= (int64_t)kCodeSmem;
+  // ---- one round of loads: the thread's first two piece records and the row's codes into shared memory ----
+  PieceRec r0{}, r1{};
+  if (t < nchunks) r0 = load_rec(recs + t);
+  if (t + kStreamThreads < nchunks) r1 = load_rec(recs + t + kStreamThreads);
+  if (codes_staged) {
+    const uint32_t* src = ws.codes + row * nwords;
+#pragma unroll 4
+    for (int w = t; w < (int)nwords; w += kStreamThreads) S.codes[w] = __ldcg(src + w);
+  }
+  auto rec_at = [&](int k) -> PieceRec {
+    return k == t ? r0 : (k == t + kStreamThreads ? r1 : load_rec(recs + k));
+  };
+  // ---- combine the pieces: M and the flags, then S rescaled to M and the count of maxima ----
+  float m = -INFINITY;
+  uint32_t flags = 0;   // 1: a non-finite value, 2: a load timed out
+  for (int k = t; k < nchunks; k += kStreamThreads) {
+    const PieceRec r = rec_at(k);
+    if (r.m != r.m) flags |= r.cnt == kTimeoutCnt ? 3u : 1u;
+    else m = fmaxf(m, r.m);
+  }
+  m = warp_max_f(m);
+  flags = __reduce_or_sync(kFullMask, flags);
+  if (lane == 0) { sh.f[warp] = m; sh.u[warp][0] = flags; }
+  __syncthreads();
+  float M = sh.f[0];
+  flags = sh.u[0][0];
+#pragma unroll
+  for (int w = 1; w < kItemPieces; ++w) { M = fmaxf(M, sh.f[w]); flags |= sh.u[w][0]; }
+  const bool nonfin = flags != 0u;
   unsigned long long Sp = 0;
   uint32_t cMp = 0;
-  for (int k = t; k < nchunks; k += kSplitThreads) {
-    const ChunkStat cs = load_stat(stats + row * nchunks + k);
-    if (cs.m == M) {
-      Sp += cs.s;
-      cMp += cs.cnt;
+  for (int k = t; k < nchunks; k += kStreamThreads) {
+    const PieceRec r = rec_at(k);
+    if (r.m == M) {
+      Sp += r.s;
+      cMp += r.cnt;
     } else if (!nonfin) {
-      // 2^((m_c - M) * c1) is below 1: the chunk's fixed-point mass rescaled in binary64
-      const double f = exp2((double)((cs.m - M) * c1));
-      Sp += (unsigned long long)__double2ull_rn((double)cs.s * f);
+      // 2^((m_p - M) * c1) is below 1: the piece's fixed-point mass rescaled in binary64
+      const double f = exp2((double)((r.m - M) * c1));
+      Sp += (unsigned long long)__double2ull_rn((double)r.s * f);
     }
   }
-  const unsigned long long Sfx = block_sum_u64(Sp, sh);
-  const uint32_t cM = block_sum_u32(cMp, sh);
+  Sp = warp_sum_u64(Sp);
+  cMp = warp_sum_u32(cMp);
+  if (lane == 0) { sh.q[warp][0] = Sp; sh.u[warp][1] = cMp; }
+  __syncthreads();
+  unsigned long long Sfx = 0;
+  uint32_t cM = 0;
+#pragma unroll
+  for (int w = 0; w < kItemPieces; ++w) { Sfx += sh.q[w][0]; cM += sh.u[w][1]; }
 
   // ---- status ----
-  float topp = p.top_p ? p.top_p[row] : 1.f;
-  float minp = p.min_p ? p.min_p[row] : 0.f;
+  const float topp = p.top_p ? p.top_p[row] : 1.f;
+  const float minp = p.min_p ? p.min_p[row] : 0.f;
   const int32_t topk = p.top_k ? p.top_k[row] : 0;
   int status = VSAMP_OK;
-  if (nonfin) status = VSAMP_ERR_NONFINITE;
+  if (flags & 2u) status = VSAMP_ERR_TIMEOUT;
+  else if (flags) status = VSAMP_ERR_NONFINITE;
   else if (isnan(temp0) || isinf(temp0) || isnan(topp) || !(topp > 0.f) || isnan(minp) || minp > 1.f)
     status = VSAMP_ERR_INVALID_ARG;
   const bool greedy = !(temp0 > 0.f);
-  const float invT = 1.f / Teff;
   int path = p.tma ? 0 : PATH_NOTMA;
   RowPlanner<T> P{p, sh, row, n, M, c1};
-  P.passes = 2;
+  P.passes = 1;
   auto write_outputs = [&](int32_t tok, float lp, int st, uint32_t kept) {
     if (t == 0) {
       p.token[row] = tok;
@@ -479,20 +792,8 @@ static __device__ __noinline__ void plan_row(const Params p, RowPlan* plans, con
       }
     }
   };
-  // the row's status, whether the draw kernel draws it, and its draw slot (the atomic maximum) cleared
-  auto finish = [&](int st, int draw) {
-    __syncthreads();
-    if (t == 0) {
-      pl.status = st;
-      pl.draw = draw;
-      pl.done1 = 0u;
-      pl.done2 = 0u;
-      pl.best = 0ull;
-    }
-  };
   if (status != VSAMP_OK) {
     write_outputs(-1, __int_as_float(0x7FC00000), status, 0u);
-    finish(status, 0);
     return;
   }
   const float logS = logf(u64_to_float(Sfx) * 9.094947017729282379e-13f);   // 2^-40
@@ -587,30 +888,73 @@ static __device__ __noinline__ void plan_row(const Params p, RowPlan* plans, con
   }
   if (plan_status != VSAMP_OK) {
     write_outputs(-1, __int_as_float(0x7FC00000), plan_status, 0u);
-    finish(plan_status, 0);
     return;
   }
 
-  // ---- the cut's last kept index ----
+  // ---- the cut, the prune bound, and the flagged vectors ----
   const unsigned long long kept = fin.kept();
   const bool one_token = greedy || kept == 1;
   float xP = Tr::value_of_rkey(fin.rk);
+  const float skept = fmaxf(u64_to_float(fin.mass) * 9.094947017729282379e-13f, 1.f);
+  DrawRow d;
+  d.M = M;
+  d.invT = invT;
+  d.c1 = c1;
+  d.kappa = 20.085536923187668f / skept;
+  d.all_cand = d.kappa >= 0.99f;
+  d.bk = d.all_cand ? 0xFFFFFFFFu : __float2uint_ru(d.kappa * 1.00001f * 4294967296.0f);
+  // the flagged vectors of a coded row, from the staged codes (their loads do not need the cut's index)
+  const bool from_codes = !one_token && codes_staged && !d.all_cand;
+  uint32_t nflag = 0;
+  if (from_codes) {
+    if (t == 0) S.nflag = 0u;
+    __syncthreads();   // also: the staged codes are visible
+    const uint32_t cbk = draw_code(d.bk);
+    const int64_t nvec = (n + VE - 1) / VE;
+    // nibbles >= cbk, eight at a time: even and odd nibbles in separate bytes, so adding 16 - cbk carries into
+    // bit 4 of a byte exactly when its nibble is >= cbk
+    const uint32_t addk = (16u - cbk) * 0x01010101u;
+#pragma unroll 1
+    for (int w = t; w < (int)nwords; w += kStreamThreads) {
+      const uint32_t word = S.codes[w];
+      const uint32_t ge = (((word & 0x0F0F0F0Fu) + addk) & 0x10101010u) | ((((word >> 4) & 0x0F0F0F0Fu) + addk) & 0x10101010u);
+      if (!ge && cbk) continue;
+#pragma unroll 1
+      for (int u = 0; u < kPieceVecs<T>; ++u) {
+        if (((word >> (4 * u)) & 15u) < cbk) continue;
+        const int64_t vi = (int64_t)(w >> 5) * (kPieceElems<T> / VE) + u * 32 + (w & 31);
+        if (vi >= nvec) continue;
+        const uint32_t slot = atomicAdd(&S.nflag, 1u);
+        if (slot < (uint32_t)kFlagMax) S.flist[slot] = (uint32_t)vi;
+      }
+    }
+    __syncthreads();
+    nflag = S.nflag;
+  }
+  // this thread's first flagged vector, loaded now (the boundary search below runs meanwhile)
+  const unsigned char* xr = p.x + row * p.ld * Tr::ESIZE;
+  uint4 fv = make_uint4(0u, 0u, 0u, 0u);
+  int fcnt = 0;
+  int64_t fe0 = 0;
+  const bool have_f = from_codes && nflag <= (uint32_t)kFlagMax && (uint32_t)t < nflag;
+  if (have_f) {
+    fe0 = (int64_t)S.flist[t] * VE;
+    fcnt = load_vec<T, false>(p, xr, fe0, fv);
+  }
   int32_t It = kAllIndex;
-  int32_t cb_def = -1;
-  uint32_t cneed_def = 0u;
   if (fin.whole && !one_token) {
     if (fin.above == 0 && fin.cnt_eq == 0) xP = -INFINITY;   // every element
   } else if (fin.rk == rkM) {
-    // the need-th maximum: find its chunk from the chunk counts, then scan that chunk
+    // the need-th maximum: its piece from the piece counts, then one warp scans that piece
     const unsigned long long need = fin.whole ? cM : fin.need;
     unsigned long long before = 0;
     int64_t cb = -1;
-    for (int64_t k0 = 0; k0 < nchunks && cb < 0; k0 += kSplitThreads) {
+    for (int64_t k0 = 0; k0 < nchunks && cb < 0; k0 += kStreamThreads) {
       const int64_t k = k0 + t;
       uint32_t ck = 0;
       if (k < nchunks) {
-        const ChunkStat cs = load_stat(stats + row * nchunks + k);
-        ck = cs.m == M ? cs.cnt : 0u;
+        const PieceRec r = rec_at((int)k);
+        ck = r.m == M ? r.cnt : 0u;
       }
       uint32_t tot;
       const uint32_t pre = block_scan_u32(ck, tot, sh);
@@ -624,494 +968,364 @@ static __device__ __noinline__ void plan_row(const Params p, RowPlan* plans, con
       if (done) cb = (int64_t)sh.bq[2];
       __syncthreads();
     }
-    // the draw kernel finds it in chunk cb, which it holds in shared memory anyway
-    cb_def = (int32_t)cb;
-    cneed_def = (uint32_t)(need - sh.bq[3]);
-    It = kDeferIndex;
+    if (warp == 0) {
+      int32_t found = kNoIndex;
+      if (cb >= 0) {
+        const PieceView<T> pv{xr, n, p.tma, cb * kPieceElems<T>};
+        found = piece_nth_equal_staged<T>(pv, M, (uint32_t)(need - sh.bq[3]), S.piece);
+      }
+      if (lane == 0) S.it = found;
+    }
+    __syncthreads();
+    It = S.it;
+    ++P.passes;
   } else {
     const unsigned long long need = fin.whole ? fin.cnt_eq : fin.need;
     It = P.nth_equal(xP, need, 0);
   }
-  if (It < 0 && It != kDeferIndex) {   // cannot happen with consistent counts; reported as an error
+  if (It < 0) {   // cannot happen with consistent counts; reported as an error
     write_outputs(-1, __int_as_float(0x7FC00000), VSAMP_ERR_INVALID_ARG, 0u);
-    finish(VSAMP_ERR_INVALID_ARG, 0);
     return;
   }
-  if (one_token && It != kDeferIndex) {
+  if (one_token) {
     // the first maximum; (x - M) / T = 0
     write_outputs(It, fminf(-logS, 0.f), VSAMP_OK, (uint32_t)kept);
-    finish(VSAMP_OK, 0);
     return;
   }
-  // ---- the draw's prune bound: a token can beat B0 = ln(S_kept) - 3 only if u < w * kappa ----
-  const float skept = fmaxf(u64_to_float(fin.mass) * 9.094947017729282379e-13f, 1.f);
-  const float kappa = 20.085536923187668f / skept;
-  const bool all_cand = kappa >= 0.99f;
-  if (t == 0) {
-    const uint64_t sd = p.seed ? p.seed[row] : 0ull;
-    const uint64_t st = p.step ? p.step[row] : 0ull;
-    pl.M = M;
-    pl.invT = invT;
-    pl.c1 = c1;
-    pl.xP = xP;
-    pl.It = It;
-    pl.logS = logS;
-    pl.kappa = kappa;
-    pl.all_cand = all_cand ? 1 : 0;
-    pl.bk = all_cand ? 0xFFFFFFFFu : __float2uint_ru(kappa * 1.00001f * 4294967296.0f);
-    pl.B0 = -logf(kappa);
-    pl.rid = p.row_id ? p.row_id[row] : (uint32_t)row;
-    pl.st_lo = (uint32_t)st;
-    pl.st_hi = (uint32_t)(st >> 32);
-    pl.k0 = (uint32_t)sd;
-    pl.k1 = (uint32_t)(sd >> 32);
-    pl.passes = P.passes + 1;
-    pl.rounds = P.rounds;
-    pl.path = path;
-    pl.kept = (uint32_t)kept;
-    pl.cb = cb_def;
-    pl.cneed = cneed_def;
-    pl.one = one_token ? 1 : 0;
+
+  // ---- the draw: a token can beat B0 = ln(S_kept) - 3 only if u < w * kappa ----
+  d.xP = xP;
+  d.It = It;
+  const uint64_t sd = p.seed ? p.seed[row] : 0ull;
+  const uint64_t stp = p.step ? p.step[row] : 0ull;
+  d.rid = p.row_id ? p.row_id[row] : (uint32_t)row;
+  d.st_lo = (uint32_t)stp;
+  d.st_hi = (uint32_t)(stp >> 32);
+  d.key = PhiloxKey{(uint32_t)sd, (uint32_t)(sd >> 32)};
+  const float B0 = -logf(d.kappa);
+  float bscore = -INFINITY, bs = 0.f;
+  int32_t bidx = 0x7FFFFFFF;
+  if (from_codes && nflag <= (uint32_t)kFlagMax) {
+    if (have_f) score_vector<T>(fv, fcnt, fe0, d, bscore, bidx, bs);
+    for (uint32_t i = t + kStreamThreads; i < nflag; i += kStreamThreads) {
+      const int64_t e0 = (int64_t)S.flist[i] * VE;
+      uint4 v;
+      const int cnt = load_vec<T, false>(p, xr, e0, v);
+      score_vector<T>(v, cnt, e0, d, bscore, bidx, bs);
+    }
+  } else {
+    score_row<T>(p, row, d, bscore, bidx, bs);
   }
-  finish(VSAMP_OK, 1);
+  ++P.passes;
+  ArgMax g = block_argmax(ArgMax{bscore, bidx, bs}, S);
+  if (!(d.all_cand || (g.idx != 0x7FFFFFFF && g.score > B0 + 1e-4f * fmaxf(1.f, fabsf(B0))))) {
+    // the prune bound did not certify the draw (probability ~1e-9): every kept token of the row, exactly
+    path |= PATH_FALLBACK;
+    DrawRow all = d;
+    all.all_cand = true;
+    bscore = -INFINITY;
+    bs = 0.f;
+    bidx = 0x7FFFFFFF;
+    score_row<T>(p, row, all, bscore, bidx, bs);
+    g = block_argmax(ArgMax{bscore, bidx, bs}, S);
+  }
+  if (g.idx >= 0 && (int64_t)g.idx < n) write_outputs(g.idx, fminf(g.s - logS, 0.f), VSAMP_OK, (uint32_t)kept);
+  else write_outputs(-1, __int_as_float(0x7FC00000), VSAMP_ERR_INVALID_ARG, 0u);
 }
 
 // ------------------------------------------------------------------------------------------------
-// The streaming sampler: four kernels, ordered by the stream.
-//   warp_stats_kernel    every warp independently takes 4 KB pieces of consecutive logits (grid-stride
-//                        over (row, piece) items; lane l holds vectors u * 32 + l of the piece): the piece's
-//                        maximum m_p, count of maxima and mass relative to m_p in 2^-40 fixed point summed per
-//                        16-byte vector, read once from HBM.
-//   stream_plan_kernel   one CTA per row: the row's plan from its piece statistics (radix rounds over the row
-//                        only when the cut leaves the maximum's tie group).
-//   warp_draw_kernel     the same items, each piece read again (mostly from L2): one Philox4x32-10 word per
-//                        kept token, the prune bound, exact scores of the few candidates; a warp with a
-//                        candidate meets the row's best in a 64-bit atomic maximum.
-//   stream_finish_kernel one CTA per row: certify the draw and write the outputs.
-// No warp waits for another inside a kernel, and the streaming kernels use no shared memory or CTA barriers.
+// Draw codes of one piece: the smallest Philox word of each of the lane's vectors, four counters at a time. The
+// words do not depend on the logits; vectors past the row's end get codes too (their tokens are never kept).
 // ------------------------------------------------------------------------------------------------
-struct StreamHeader {       // the first 256 bytes of the workspace (reserved, left zero)
-  uint32_t reserved[64];
-};
-static_assert(sizeof(StreamHeader) == 256, "StreamHeader layout");
-
-// A piece of a row as one lane sees it: vector u of lane l is vector u * 32 + l of the piece. Aligned rows
-// take 16-byte loads; the last, partial vector of a row and unaligned rows are read element by element.
 template <typename T>
-struct PieceView {
-  using Tr = Traits<T>;
-  static constexpr int VE = Tr::VE;
-  const unsigned char* xr;   // the row
-  int64_t V;                 // row length
-  int32_t tma;               // the row is 16-byte aligned
-  int64_t e_begin;           // first element of the piece
-  __device__ __forceinline__ int64_t elem(int u) const {
-    return e_begin + (int64_t)(u * 32 + (int)(threadIdx.x & 31)) * VE;
-  }
-  // the whole piece lies in an aligned row: plain 16-byte loads without bounds
-  __device__ __forceinline__ bool full() const { return tma && e_begin + kPieceElems<T> <= V; }
-  // start moving the lane's vectors of a full piece towards L1 (the warp's next item, while this one computes)
-  __device__ __forceinline__ void prefetch() const {
-    if (!full()) return;
-    const uint4* b = reinterpret_cast<const uint4*>(xr + e_begin * Tr::ESIZE) + (int)(threadIdx.x & 31);
+static __device__ __forceinline__ void piece_codes(int64_t e_begin, uint32_t k0, uint32_t k1, uint32_t rid,
+                                                   uint32_t st_lo, uint32_t st_hi, uint32_t* code_out) {
+  constexpr int VE = Traits<T>::VE;
+  constexpr int U = kPieceVecs<T>;
+  constexpr int G = VE / 4;            // Philox counters per vector
+  const int lane = threadIdx.x & 31;
+  const PhiloxRowMin ph(PhiloxKey{k0, k1}, rid, st_lo, st_hi);
+  // counter of group g of vector u: (first element of the piece) / 4 + (u * 32 + lane) * G + g
+  const uint32_t cb0 = (uint32_t)(e_begin >> 2) + (uint32_t)(lane * G);
+  uint32_t word = 0u;
+#pragma unroll 1
+  for (int u0 = 0; u0 < U; u0 += 4 / G) {
+    uint32_t c[4], mw[4];
 #pragma unroll
-    for (int u = 0; u < kPieceVecs<T>; ++u) asm volatile("prefetch.global.L1 [%0];" ::"l"(b + u * 32));
-  }
-  __device__ __forceinline__ void get_full(int u, uint4& v) const {
-    v = __ldg(reinterpret_cast<const uint4*>(xr + e_begin * Tr::ESIZE) + u * 32 + (int)(threadIdx.x & 31));
-  }
-  __device__ __forceinline__ int get(int u, uint4& v) const {
-    const int64_t e = elem(u);
-    const int64_t left = V - e;
-    const int cnt = left <= 0 ? 0 : (left >= VE ? VE : (int)left);
-    if (cnt == VE && tma) {
-      v = __ldg(reinterpret_cast<const uint4*>(xr + e * Tr::ESIZE));
-    } else {
-      uint32_t w[4] = {0u, 0u, 0u, 0u};
-      for (int i = 0; i < cnt; ++i) {
-        if (Tr::ESIZE == 4) w[i] = reinterpret_cast<const uint32_t*>(xr)[e + i];
-        else w[i >> 1] |= (uint32_t)reinterpret_cast<const uint16_t*>(xr)[e + i] << (16 * (i & 1));
-      }
-      v = make_uint4(w[0], w[1], w[2], w[3]);
+    for (int i = 0; i < 4; ++i) c[i] = cb0 + (uint32_t)((u0 + i / G) * 32 * G + i % G);
+    ph.min_words<4>(c, mw);
+#pragma unroll
+    for (int q = 0; q < 4 / G; ++q) {
+      uint32_t mu = mw[q * G];
+#pragma unroll
+      for (int g = 1; g < G; ++g) mu = min(mu, mw[q * G + g]);
+      word |= draw_code(mu) << (4 * (u0 + q));
     }
-    return cnt;
   }
-};
+  code_out[lane] = word;
+}
 
-// Statistics of every piece: one warp per item, grid-stride.
+// ------------------------------------------------------------------------------------------------
+// Statistics of a partial piece, or of a piece of an unaligned row: the lanes' vectors from global memory, with
+// element counts per vector (out of line: the full-piece path keeps its registers). No winner, no codes.
+// ------------------------------------------------------------------------------------------------
 template <typename T>
-__global__ void __launch_bounds__(kStreamThreads) warp_stats_kernel(const Params p, ChunkStat* stats, int np) {
+static __device__ __noinline__ void piece_stats_partial(const unsigned char* xr, int64_t V, int32_t tma,
+                                                        int64_t e_begin, float c1, bool timeout, PieceRec* rec_out) {
   using Tr = Traits<T>;
   constexpr int VE = Tr::VE;
   constexpr int U = kPieceVecs<T>;
   const int lane = threadIdx.x & 31;
-  const long long total = (long long)p.B * np;
-  const long long nw = (long long)gridDim.x * (kStreamThreads / 32);
-  for (long long it = (long long)blockIdx.x * (kStreamThreads / 32) + (threadIdx.x >> 5); it < total; it += nw) {
-    const int64_t row = it / np;
-    const int pc = (int)(it - row * np);
-    const float temp0 = p.temperature ? p.temperature[row] : 1.f;
-    const float Teff = temp0 > 0.f ? temp0 : 1.f;   // greedy rows use T = 1 for their statistics
-    const float c1 = kLog2e * (1.f / Teff);
-    const PieceView<T> pv{p.x + row * p.ld * Tr::ESIZE, p.V, p.tma, (int64_t)pc * kPieceElems<T>};
-    if (it + nw < total) {
-      const int64_t r2 = (it + nw) / np;
-      const int pc2 = (int)(it + nw - r2 * np);
-      PieceView<T>{p.x + r2 * p.ld * Tr::ESIZE, p.V, p.tma, (int64_t)pc2 * kPieceElems<T>}.prefetch();
-    }
-    uint4 v[U];
-    int cnt[U];
-    if (pv.full()) {
+  uint4 v[U];
+  int cnt[U];
+  const PieceView<T> pv{xr, V, tma, e_begin};
 #pragma unroll
-      for (int u = 0; u < U; ++u) { pv.get_full(u, v[u]); cnt[u] = VE; }
-    } else {
+  for (int u = 0; u < U; ++u) cnt[u] = pv.get(u, v[u]);
+  float mt = -INFINITY, mn = INFINITY, nf = 0.f;
 #pragma unroll
-      for (int u = 0; u < U; ++u) cnt[u] = pv.get(u, v[u]);
+  for (int u = 0; u < U; ++u) {
+    float x[VE];
+    Tr::values(v[u], x);
+#pragma unroll
+    for (int i = 0; i < VE; ++i)
+      if (i < cnt[u]) { mt = fmaxf(mt, x[i]); mn = fminf(mn, x[i]); nf = fmaf(x[i], 0.f, nf); }
+  }
+  const float mc = warp_max_f(mt);
+  mn = -warp_max_f(-mn);
+  const bool bad = timeout || __any_sync(kFullMask, nf != 0.f);
+  unsigned long long s = 0ull;
+  uint32_t cm = 0u;
+  if (!bad) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (cnt[u] <= 0) continue;
+      float x[VE], w[VE];
+      Tr::values(v[u], x);
+      if (cnt[u] == VE) {
+        // the same order of additions as a full vector
+        const float2 mM = make_float2(-mc, -mc), cc = make_float2(c1, c1);
+        float2 w2[VE / 2];
+#pragma unroll
+        for (int h = 0; h < VE / 2; ++h) {
+          const float2 e = __fmul2_rn(__fadd2_rn(make_float2(x[2 * h], x[2 * h + 1]), mM), cc);
+          w2[h] = make_float2(ex2_approx(e.x), ex2_approx(e.y));
+        }
+        float2 a;
+        if constexpr (VE == 8) a = __fadd2_rn(__fadd2_rn(w2[0], w2[2]), __fadd2_rn(w2[1], w2[3]));
+        else a = __fadd2_rn(w2[0], w2[1]);
+        s += mass_fx_split(a.x + a.y);
+#pragma unroll
+        for (int i = 0; i < VE; ++i) cm += x[i] == mc ? 1u : 0u;
+      } else {
+#pragma unroll
+        for (int i = 0; i < VE; ++i) {
+          const bool ok = i < cnt[u];
+          const float d = x[i] - mc;
+          w[i] = ok ? ex2_approx(d * c1) : 0.f;
+          cm += (ok && d == 0.f) ? 1u : 0u;
+        }
+#pragma unroll
+        for (int h = VE / 2; h >= 1; h >>= 1)
+#pragma unroll
+          for (int i = 0; i < h; ++i) w[i] += w[i + h];
+        s += mass_fx_split(w[0]);
+      }
     }
-    // ---- maximum and non-finite check ----
-    float mt = -INFINITY, nf = 0.f;
+  }
+  s = warp_sum_u64(s);
+  cm = warp_sum_u32(cm);
+  if (lane == 0) {
+    uint4* o = reinterpret_cast<uint4*>(rec_out);
+    o[0] = make_uint4(bad ? 0x7FC00000u : __float_as_uint(mc), timeout ? kTimeoutCnt : cm, (uint32_t)s, (uint32_t)(s >> 32));
+    o[1] = make_uint4(__float_as_uint(mn), 0u, 0u, 0u);
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// Piece pass of one warp over a full piece in shared memory: the record, and for a coded row the draw codes.
+// ------------------------------------------------------------------------------------------------
+template <typename T>
+static __device__ __forceinline__ void piece_pass_full(const uint4* sbuf, int64_t e_begin, float c1,
+                                                       bool timeout, bool coded, uint32_t k0, uint32_t k1,
+                                                       uint32_t rid, uint32_t st_lo, uint32_t st_hi,
+                                                       PieceRec* rec_out, uint32_t* code_out) {
+  using Tr = Traits<T>;
+  constexpr int VE = Tr::VE;
+  constexpr int U = kPieceVecs<T>;     // vectors per lane and piece: 8
+  constexpr int G = VE / 4;            // Philox counters per vector
+  const int lane = threadIdx.x & 31;
+  // ---- maximum, minimum, non-finite check ----
+  float mt, mn, nf;
+  if constexpr (VE == 8) {
+    const __nv_bfloat162 zero2 = __float2bfloat162_rn(0.f);
+    __nv_bfloat162 mx2 = __float2bfloat162_rn(-INFINITY), mn2 = __float2bfloat162_rn(INFINITY), nf2 = zero2;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint4 v = sbuf[u * 32 + lane];
+      const __nv_bfloat162 a = Tr::pair(v.x), b = Tr::pair(v.y), c = Tr::pair(v.z), d = Tr::pair(v.w);
+      mx2 = __hmax2(mx2, __hmax2(__hmax2(a, b), __hmax2(c, d)));
+      mn2 = __hmin2(mn2, __hmin2(__hmin2(a, b), __hmin2(c, d)));
+      nf2 = __hfma2(a, zero2, __hfma2(b, zero2, __hfma2(c, zero2, __hfma2(d, zero2, nf2))));
+    }
+    mt = fmaxf(__low2float(mx2), __high2float(mx2));
+    mn = fminf(__low2float(mn2), __high2float(mn2));
+    nf = (__low2float(nf2) != 0.f || __high2float(nf2) != 0.f) ? 1.f : 0.f;
+  } else {
+    mt = -INFINITY;
+    mn = INFINITY;
+    nf = 0.f;
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       float x[VE];
-      Tr::values(v[u], x);
-#pragma unroll
-      for (int i = 0; i < VE; ++i)
-        if (i < cnt[u]) { mt = fmaxf(mt, x[i]); nf = fmaf(x[i], 0.f, nf); }
+      Tr::values(sbuf[u * 32 + lane], x);
+      mt = fmaxf(mt, fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])));
+      mn = fminf(mn, fminf(fminf(x[0], x[1]), fminf(x[2], x[3])));
+      nf = fmaf(x[0], 0.f, fmaf(x[1], 0.f, fmaf(x[2], 0.f, fmaf(x[3], 0.f, nf))));
     }
-    const float mc = warp_max_f(mt);
-    const bool bad = __any_sync(kFullMask, nf != 0.f);
-    // ---- mass relative to the piece maximum (2^-40 fixed point per vector) and the count of maxima ----
-    unsigned long long s = 0ull;
-    uint32_t cm = 0u;
-    if (!bad) {
-      const float2 mM = make_float2(-mc, -mc), cc = make_float2(c1, c1);
+  }
+  const float mc = warp_max_f(mt);
+  mn = -warp_max_f(-mn);
+  const bool bad = timeout || __any_sync(kFullMask, nf != 0.f);
+  // ---- mass relative to the piece maximum (2^-40 fixed point per vector) and the count of maxima ----
+  unsigned long long s = 0ull;
+  uint32_t cm = 0u;
+  if (!bad) {
+    const float2 mM = make_float2(-mc, -mc), cc = make_float2(c1, c1);
+    uint32_t cm2 = 0u;
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        float x[VE];
-        Tr::values(v[u], x);
-        if (cnt[u] == VE) {
-          float2 w2[VE / 2];
+    for (int u = 0; u < U; ++u) {
+      const uint4 v = sbuf[u * 32 + lane];
+      float x[VE];
+      Tr::values(v, x);
+      float2 w2[VE / 2];
 #pragma unroll
-          for (int h = 0; h < VE / 2; ++h) {
-            const float2 e = __fmul2_rn(__fadd2_rn(make_float2(x[2 * h], x[2 * h + 1]), mM), cc);
-            w2[h] = make_float2(ex2_approx(e.x), ex2_approx(e.y));
-          }
-          float2 a;
-          if constexpr (VE == 8) a = __fadd2_rn(__fadd2_rn(w2[0], w2[2]), __fadd2_rn(w2[1], w2[3]));
-          else a = __fadd2_rn(w2[0], w2[1]);
-          s += mass_fx(a.x + a.y);
-#pragma unroll
-          for (int i = 0; i < VE; ++i) cm += x[i] == mc ? 1u : 0u;
-        } else if (cnt[u] > 0) {
-          float w[VE];
-#pragma unroll
-          for (int i = 0; i < VE; ++i) {
-            const bool ok = i < cnt[u];
-            const float d = x[i] - mc;
-            w[i] = ok ? ex2_approx(d * c1) : 0.f;
-            cm += (ok && d == 0.f) ? 1u : 0u;
-          }
-#pragma unroll
-          for (int h = VE / 2; h >= 1; h >>= 1)
-#pragma unroll
-            for (int i = 0; i < h; ++i) w[i] += w[i + h];
-          s += mass_fx(w[0]);
-        }
+      for (int h = 0; h < VE / 2; ++h) {
+        const float2 e = __fmul2_rn(__fadd2_rn(make_float2(x[2 * h], x[2 * h + 1]), mM), cc);
+        w2[h] = make_float2(ex2_approx(e.x), ex2_approx(e.y));
       }
-    }
-    s = warp_sum_u64(s);
-    cm = warp_sum_u32(cm);
-    if (lane == 0) {
-      ChunkStat cs;
-      cs.m = bad ? __int_as_float(0x7FC00000) : mc;
-      cs.cnt = cm;
-      cs.s = s;
-      stats[it] = cs;
-    }
-  }
-}
-
-// The index of the need-th element (1-based, index order) equal to xv in a piece; kNoIndex if there are fewer.
-// Element order in the piece is (vector u, lane, element i): one warp scan per u. Warp-collective.
-template <typename T>
-__device__ __noinline__ int32_t piece_nth_equal(const PieceView<T>& pv, float xv, uint32_t need) {
-  using Tr = Traits<T>;
-  constexpr int VE = Tr::VE;
-  constexpr int U = kPieceVecs<T>;
-  const int lane = threadIdx.x & 31;
-  uint32_t base = 0;
-  int32_t found = kNoIndex;
-  for (int u = 0; u < U; ++u) {
-    uint4 v;
-    const int n = pv.get(u, v);
-    float x[VE];
-    Tr::values(v, x);
-    uint32_t c = 0;
-#pragma unroll
-    for (int i = 0; i < VE; ++i) c += (i < n && x[i] == xv) ? 1u : 0u;
-    uint32_t inc = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(kFullMask, inc, o);
-      if (lane >= o) inc += y;
-    }
-    const uint32_t excl = base + inc - c;
-    int32_t idx = kNoIndex;
-    if (c && excl < need && need <= excl + c) {
-      uint32_t seen = excl;
-#pragma unroll
-      for (int i = 0; i < VE; ++i)
-        if (idx < 0 && i < n && x[i] == xv && ++seen == need) idx = (int32_t)(pv.elem(u) + i);
-    }
-    const uint32_t hit = __ballot_sync(kFullMask, idx >= 0);
-    if (hit) {
-      found = __shfl_sync(kFullMask, idx, __ffs(hit) - 1);
-      break;
-    }
-    base += __shfl_sync(kFullMask, inc, 31);
-  }
-  return found;
-}
-
-// Exact perturbed scores of one vector's kept tokens that pass the prune bound (every kept token when the
-// plan makes all of them candidates); the running arg-max is updated in place.
-template <typename T>
-__device__ __noinline__ void draw_exact(uint4 v, int cnt, int64_t e0, const RowPlan* plp, int32_t It, float& bscore,
-                                        int32_t& bidx) {
-  using Tr = Traits<T>;
-  constexpr int VE = Tr::VE;
-  const RowPlan& pl = *plp;
-  const bool all_cand = pl.all_cand != 0;
-  const PhiloxKey key{pl.k0, pl.k1};
-  float x[VE];
-  Tr::values(v, x);
-  uint32_t b[VE];
-#pragma unroll
-  for (int g = 0; g < VE / 4; ++g) {
-    const uint4 w4 = philox4x32_10(make_uint4((uint32_t)(e0 >> 2) + (uint32_t)g, pl.rid, pl.st_lo, pl.st_hi), key);
-    b[4 * g + 0] = w4.x; b[4 * g + 1] = w4.y; b[4 * g + 2] = w4.z; b[4 * g + 3] = w4.w;
-  }
-#pragma unroll
-  for (int i = 0; i < VE; ++i) {
-    if (!(i < cnt && (x[i] > pl.xP || (x[i] == pl.xP && e0 + i <= (int64_t)It)))) continue;
-    if (!all_cand && b[i] >= pl.bk) continue;
-    const float d = x[i] - pl.M;
-    const float sv = d * pl.invT;
-    if (!all_cand) {
-      const float w = ex2_approx(d * pl.c1);
-      const float u = fmaf((float)b[i], kTwoM32, kTwoM33);
-      if (!(u < w * pl.kappa * 1.00001f)) continue;
-    }
-    const float score = gumbel_score(sv, b[i]);
-    const int32_t idx = (int32_t)(e0 + i);
-    if (argmax_better(score, idx, bscore, bidx)) { bscore = score; bidx = idx; }
-  }
-}
-
-// stream_finish_kernel: one CTA per row certifies the draw, writes the outputs and resets the row's draw
-// slot. Rows whose plan does not draw were finished by the planner.
-template <typename T>
-__global__ void __launch_bounds__(kSplitThreads) stream_finish_kernel(const Params p, RowPlan* plans) {
-  using Tr = Traits<T>;
-  __shared__ uint4 fplan[8];
-  __shared__ float bs[8];
-  __shared__ int32_t bi[8];
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const int64_t row = blockIdx.x;
-  RowPlan* gpl = plans + row;
-  if (t < 8) fplan[t] = reinterpret_cast<const uint4*>(gpl)[t];
-  __syncthreads();
-  const RowPlan& pl = *reinterpret_cast<const RowPlan*>(fplan);
-  if (pl.status == VSAMP_OK && pl.draw) {
-    const unsigned long long best = pl.best;
-    const float gscore = best ? score_of_key((uint32_t)(best >> 32)) : -INFINITY;
-    int32_t tok = best ? (int32_t)(0xFFFFFFFFu - (uint32_t)best) : -1;
-    int path = pl.path;
-    const bool all_cand = pl.all_cand != 0;
-    const float B0 = pl.B0;
-    if (!pl.one && !(all_cand || (best && gscore > B0 + 1e-4f * fmaxf(1.f, fabsf(B0))))) {
-      // the prune bound did not certify the draw (probability ~1e-9): every kept token of the row, exactly
-      path |= PATH_FALLBACK;
-      const PhiloxKey key{pl.k0, pl.k1};
-      const float xP = pl.xP, M = pl.M, invT = pl.invT;
-      const int32_t It = pl.It;
-      float fs = -INFINITY;
-      int32_t fi = 0x7FFFFFFF;
-      for (int64_t e = t; e < p.V; e += kSplitThreads) {
-        const float xv = Tr::load_global(p.x, row * p.ld + e);
-        if (!(xv > xP || (xv == xP && e <= (int64_t)It))) continue;
-        const uint4 w4 = philox4x32_10(make_uint4((uint32_t)(e >> 2), pl.rid, pl.st_lo, pl.st_hi), key);
-        const float score = gumbel_score((xv - M) * invT, philox_word(w4, (int)(e & 3)));
-        if (argmax_better(score, (int32_t)e, fs, fi)) { fs = score; fi = (int32_t)e; }
-      }
-      const ArgMax a = warp_argmax(ArgMax{fs, fi, 0.f});
-      if (lane == 0) { bs[warp] = a.score; bi[warp] = a.idx; }
-      __syncthreads();
-      ArgMax b{bs[0], bi[0], 0.f};
-      for (int w = 1; w < kSplitThreads / 32; ++w)
-        if (argmax_better(bs[w], bi[w], b.score, b.idx)) b = ArgMax{bs[w], bi[w], 0.f};
-      tok = b.idx;
-    }
-    if (t == 0) {
-      int st = VSAMP_OK;
-      if (tok >= 0 && (int64_t)tok < p.V) {
-        const float xt = Tr::load_global(p.x, row * p.ld + tok);
-        p.token[row] = tok;
-        if (p.logprob) p.logprob[row] = pl.one ? fminf(-pl.logS, 0.f) : fminf((xt - pl.M) * pl.invT - pl.logS, 0.f);
+      float2 a;
+      if constexpr (VE == 8) a = __fadd2_rn(__fadd2_rn(w2[0], w2[2]), __fadd2_rn(w2[1], w2[3]));
+      else a = __fadd2_rn(w2[0], w2[1]);
+      s += mass_fx_split(a.x + a.y);
+      if constexpr (VE == 8) {
+        const __nv_bfloat162 M2 = __float2bfloat162_rn(mc);   // a bf16 value: exact
+        cm2 += __heq2_mask(Tr::pair(v.x), M2) & 0x00010001u;
+        cm2 += __heq2_mask(Tr::pair(v.y), M2) & 0x00010001u;
+        cm2 += __heq2_mask(Tr::pair(v.z), M2) & 0x00010001u;
+        cm2 += __heq2_mask(Tr::pair(v.w), M2) & 0x00010001u;
       } else {
-        st = VSAMP_ERR_INVALID_ARG;
-        p.token[row] = -1;
-        if (p.logprob) p.logprob[row] = __int_as_float(0x7FC00000);
+#pragma unroll
+        for (int i = 0; i < VE; ++i) cm += x[i] == mc ? 1u : 0u;
       }
-      if (p.row_status) p.row_status[row] = st;
-      if (p.stats) {
-        p.stats[row * 4 + 0] = pl.passes;
-        p.stats[row * 4 + 1] = pl.rounds;
-        p.stats[row * 4 + 2] = (int32_t)pl.kept;
-        p.stats[row * 4 + 3] = path;
+    }
+    cm += (cm2 & 0xFFFFu) + (cm2 >> 16);
+  }
+  s = warp_sum_u64(s);
+  cm = warp_sum_u32(cm);
+  if (coded && !bad) piece_codes<T>(e_begin, k0, k1, rid, st_lo, st_hi, code_out);
+  if (lane == 0) {
+    uint4* o = reinterpret_cast<uint4*>(rec_out);
+    o[0] = make_uint4(bad ? 0x7FC00000u : __float_as_uint(mc), timeout ? kTimeoutCnt : cm, (uint32_t)s, (uint32_t)(s >> 32));
+    o[1] = make_uint4(__float_as_uint(mn), 0u, 0u, 0u);
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// The two kernels.
+// ------------------------------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(kStreamThreads, 3) piece_kernel(const Params p, const StreamWs ws, int np) {
+  using Tr = Traits<T>;
+  extern __shared__ __align__(128) unsigned char dyn[];
+  PieceSmem& S = *reinterpret_cast<PieceSmem*>(dyn);
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const long long total = (long long)p.B * np;
+  const long long nw = (long long)gridDim.x * kItemPieces;
+  const long long first = (long long)blockIdx.x * kItemPieces + warp;
+  if (t < 2 * kItemPieces) mbar_init(&S.bar[t >> 1][t & 1], 1);
+  fence_mbar_init();
+  __syncthreads();   // the only CTA barrier: the mbarriers are initialised
+
+  auto full_piece = [&](int pc) -> bool { return p.tma && (int64_t)(pc + 1) * kPieceElems<T> <= p.V; };
+  int uses[2] = {0, 0};
+  bool armed[2] = {false, false}, inflight[2] = {false, false};
+  bool dead = false;   // a load wait ran out: no more bulk copies from this warp
+  // the bulk copy of piece `it` (a full piece of an aligned row) into this warp's buffer b
+  auto issue = [&](long long it, int b) {
+    if (dead || it >= total) return;
+    const int64_t row = it / np;
+    const int pc = (int)(it - row * np);
+    if (!full_piece(pc)) return;
+    if (lane == 0) {
+      fence_proxy_async_shared();
+      mbar_arrive_expect_tx(&S.bar[warp][b], (uint32_t)kPieceBytes);
+      if (!p.drop_loads)
+        bulk_copy_g2s(&S.buf[warp][b][0], p.x + (row * p.ld + (int64_t)pc * kPieceElems<T>) * Tr::ESIZE,
+                      (uint32_t)kPieceBytes, &S.bar[warp][b]);
+    }
+    armed[b] = true;
+    inflight[b] = !p.drop_loads;
+  };
+
+  issue(first, 0);
+  int k = 0;
+  for (long long it = first; it < total; it += nw, ++k) {
+    const int b = k & 1;
+    __syncwarp();      // every lane has finished reading buffer b ^ 1 (the previous piece)
+    issue(it + nw, b ^ 1);
+    const int64_t row = it / np;
+    const int pc = (int)(it - row * np);
+    bool timeout = false;
+    const uint4* sbuf = nullptr;
+    if (armed[b]) {
+      armed[b] = false;
+      if (mbar_wait_bounded(&S.bar[warp][b], (uint32_t)(uses[b] & 1), p.wait_cycles)) {
+        ++uses[b];
+        inflight[b] = false;
+        sbuf = &S.buf[warp][b][0];
+      } else {
+        timeout = true;
+        dead = true;
       }
+    }
+    timeout = __any_sync(kFullMask, timeout);
+    const float temp0 = p.temperature ? p.temperature[row] : 1.f;
+    const float Teff = temp0 > 0.f ? temp0 : 1.f;
+    const float invT = 1.f / Teff;
+    const float c1 = kLog2e * invT;
+    PieceRec* rec = ws.recs + row * np + pc;
+    const bool coded = row_coded(p, row);
+    uint32_t k0 = 0u, k1 = 0u, rid = (uint32_t)row, st_lo = 0u, st_hi = 0u;
+    if (coded) {
+      const uint64_t sd = p.seed ? p.seed[row] : 0ull;
+      const uint64_t stp = p.step ? p.step[row] : 0ull;
+      k0 = (uint32_t)sd;
+      k1 = (uint32_t)(sd >> 32);
+      st_lo = (uint32_t)stp;
+      st_hi = (uint32_t)(stp >> 32);
+      if (p.row_id) rid = p.row_id[row];
+    }
+    if (sbuf) {
+      piece_pass_full<T>(sbuf, (int64_t)pc * kPieceElems<T>, c1, timeout, coded, k0, k1, rid, st_lo, st_hi, rec,
+                         ws.codes + (row * np + pc) * 32);
+    } else {
+      piece_stats_partial<T>(p.x + row * p.ld * Tr::ESIZE, p.V, p.tma, (int64_t)pc * kPieceElems<T>, c1, timeout, rec);
+      if (coded && !timeout) piece_codes<T>((int64_t)pc * kPieceElems<T>, k0, k1, rid, st_lo, st_hi,
+                                            ws.codes + (row * np + pc) * 32);
     }
   }
-  if (t == 0) gpl->best = 0ull;   // the draw slot is left zero
+  // a bulk copy of this warp that may still be landing (after a timed-out wait)
+  for (int b2 = 0; b2 < 2; ++b2)
+    if (inflight[b2]) (void)mbar_wait_bounded(&S.bar[warp][b2], (uint32_t)(uses[b2] & 1), 4000000000LL);
 }
 
-// One CTA per row: the row's plan from its chunk statistics.
+// One CTA per row (rows blockIdx.x, blockIdx.x + gridDim.x, ...).
 template <typename T>
-__global__ void __launch_bounds__(kSplitThreads) stream_plan_kernel(const Params p, RowPlan* plans, ChunkStat* stats,
-                                                                   int nc) {
-  __shared__ SplitShared sh;
-  const int64_t r = blockIdx.x;
-  const float temp0 = p.temperature ? p.temperature[r] : 1.f;
-  const float Teff = temp0 > 0.f ? temp0 : 1.f;
-  plan_row<T>(p, plans, stats, stats, nc, r, temp0, Teff, kLog2e * (1.f / Teff), sh);
-}
-
-
-// The draw over every piece of the rows whose plan draws: one warp per item of kDrawRun consecutive pieces of
-// a row, grid-stride.
-template <typename T>
-__global__ void __launch_bounds__(kStreamThreads, 2) warp_draw_kernel(const Params p, RowPlan* plans, int np) {
-  using Tr = Traits<T>;
-  constexpr int VE = Tr::VE;
-  constexpr int U = kPieceVecs<T>;
-  constexpr int G = VE / 4;          // groups of four tokens (one Philox counter) per vector
-  constexpr int NG = U * G;          // groups per lane and piece
-  const int lane = threadIdx.x & 31;
-  const int nruns = (np + kDrawRun - 1) / kDrawRun;
-  const long long total = (long long)p.B * nruns;
-  const long long nw = (long long)gridDim.x * (kStreamThreads / 32);
-  for (long long it = (long long)blockIdx.x * (kStreamThreads / 32) + (threadIdx.x >> 5); it < total; it += nw) {
-    const int64_t row = it / nruns;
-    const int run = (int)(it - row * nruns);
-    RowPlan* gp = plans + row;
-    if (!(__ldg(&gp->status) == VSAMP_OK && __ldg(&gp->draw))) continue;
-    const float xP = __ldg(&gp->xP);
-    const int32_t It0 = __ldg(&gp->It);
-    const int32_t cbp = __ldg(&gp->cb);
-    const bool one = __ldg(&gp->one) != 0;
-    const uint32_t bk = __ldg(&gp->bk);
-    const bool all_cand = __ldg(&gp->all_cand) != 0;
-    const PhiloxRowMin ph(PhiloxKey{__ldg(&gp->k0), __ldg(&gp->k1)}, __ldg(&gp->rid), __ldg(&gp->st_lo),
-                          __ldg(&gp->st_hi));
-    if (it + nw < total) {
-      const int64_t r2 = (it + nw) / nruns;
-      const int run2 = (int)(it + nw - r2 * nruns);
-      for (int k = 0; k < kDrawRun && run2 * kDrawRun + k < np; ++k)
-        PieceView<T>{p.x + r2 * p.ld * Tr::ESIZE, p.V, p.tma, (int64_t)(run2 * kDrawRun + k) * kPieceElems<T>}.prefetch();
-    }
-    float bscore = -INFINITY;
-    int32_t bidx = 0x7FFFFFFF;
-    bool cand = false;   // warp-uniform: some lane evaluated a candidate
-#pragma unroll 1
-    for (int k = 0; k < kDrawRun; ++k) {
-      const int pc = run * kDrawRun + k;
-      if (pc >= np) break;
-      const PieceView<T> pv{p.x + row * p.ld * Tr::ESIZE, p.V, p.tma, (int64_t)pc * kPieceElems<T>};
-      // the cut's last kept index: inside the maximum's tie group it lies in piece cb, found here
-      int32_t It = It0;
-      if (It == kDeferIndex)
-        It = pc < cbp ? kAllIndex : (pc > cbp ? kNoIndex : piece_nth_equal<T>(pv, xP, __ldg(&gp->cneed)));
-      if (one) {
-        // one token is kept: the piece holding it publishes it (score +inf)
-        if (pc == cbp && lane == 0 && It >= 0)
-          atomicMax(&gp->best, ((unsigned long long)score_key(INFINITY) << 32) | (0xFFFFFFFFu - (uint32_t)It));
-        continue;
-      }
-      uint32_t gmask = 0u;   // kept groups: bit u * G + g
-      {
-        uint4 v[U];
-        int cnt[U];
-        if (pv.full()) {
-#pragma unroll
-          for (int u = 0; u < U; ++u) { pv.get_full(u, v[u]); cnt[u] = VE; }
-        } else {
-#pragma unroll
-          for (int u = 0; u < U; ++u) cnt[u] = pv.get(u, v[u]);
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int64_t e0 = pv.elem(u);
-          if (cnt[u] == VE && e0 + VE - 1 <= (int64_t)It && Tr::all_ge(v[u], xP)) {
-            gmask |= ((1u << G) - 1u) << (u * G);
-          } else if (cnt[u] > 0) {
-            float x[VE];
-            Tr::values(v[u], x);
-#pragma unroll
-            for (int i = 0; i < VE; ++i)
-              if (i < cnt[u] && (x[i] > xP || (x[i] == xP && e0 + i <= (int64_t)It))) gmask |= 1u << (u * G + (i >> 2));
-          }
-        }
-      }
-      // ---- one Philox word per kept token; a vector is flagged when a kept token's word is below bk ----
-      uint32_t flagged = 0u;
-      if (all_cand) {
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-          if ((gmask >> (u * G)) & ((1u << G) - 1u)) flagged |= 1u << u;
-      } else if (gmask) {
-        // counter word of group gi = u * G + g: (first element of vector u) / 4 + g
-        const uint32_t cb0 = (uint32_t)(pv.elem(0) >> 2);
-        auto ctr = [&](int gi) -> uint32_t { return cb0 + (uint32_t)((gi / G) * 32 * G + gi % G); };
-        if (gmask == (uint32_t)((1ull << NG) - 1ull)) {
-          // every token of the lane's vectors is kept: four counters at a time
-#pragma unroll 1
-          for (int g0 = 0; g0 < NG; g0 += 4) {
-            const uint32_t c4[4] = {ctr(g0), ctr(g0 + 1), ctr(g0 + 2), ctr(g0 + 3)};
-            uint32_t m[4];
-            ph.min_words<4>(c4, m);
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              if (m[q] < bk) flagged |= 1u << ((g0 + q) / G);
-          }
-        } else {
-#pragma unroll 1
-          for (int gi = 0; gi < NG; ++gi) {
-            if (!((gmask >> gi) & 1u)) continue;
-            const uint32_t c1[1] = {ctr(gi)};
-            uint32_t m[1];
-            ph.min_words<1>(c1, m);
-            if (m[0] < bk) flagged |= 1u << (gi / G);
-          }
-        }
-      }
-      // ---- flagged vectors (rare): exact perturbed scores ----
-      if (__any_sync(kFullMask, flagged != 0u)) {
-        cand = true;
-        while (flagged) {
-          const int u = __ffs(flagged) - 1;
-          flagged &= flagged - 1u;
-          uint4 v;
-          const int cnt = pv.get(u, v);
-          draw_exact<T>(v, cnt, pv.elem(u), gp, It, bscore, bidx);
-        }
-      }
-    }
-    // ---- the warp's best meets the row's ----
-    if (cand) {
-      const ArgMax a = warp_argmax(ArgMax{bscore, bidx, 0.f});
-      if (lane == 0 && a.idx != 0x7FFFFFFF)
-        atomicMax(&gp->best, ((unsigned long long)score_key(a.score) << 32) | (0xFFFFFFFFu - (uint32_t)a.idx));
-    }
+__global__ void __launch_bounds__(kStreamThreads) row_finish_kernel(const Params p, const StreamWs ws, int np) {
+  __shared__ FinishSmem S;
+  for (int64_t row = blockIdx.x; row < p.B; row += gridDim.x) {
+    finish_row<T>(p, ws, row, np, S);
+    __syncthreads();
   }
 }
 

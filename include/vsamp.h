@@ -232,6 +232,81 @@ vsamp_status vsamp_topn_logprobs(const void* logits, vsamp_dtype dt, int64_t B, 
                                  const float* temperature, int32_t N, float* row_max, float* row_logsum,
                                  int32_t* out_idx, float* out_lp, int32_t* row_status, void* stream);
 
+/* ---------------------------------------------------------------------------------------------------
+ * Vocabulary-sharded sampling ("[WS2][Logprob] Deterministic SM90 linear_logp ...", Tensor parallelism:
+ * rank order + owned merge: each rank computes rank-local tile summaries over its vocabulary shard, the
+ * partials are exchanged without reduction in transit (an all-gather) and placed in rank order, and one
+ * fixed merge owned by the library folds them).
+ *
+ * A row's vocabulary [0, V) is split over R shards in rank order; shard r holds the logits [v0_r, v0_r + V_r)
+ * of every row. Protocol:
+ *   1. every shard calls vsamp_shard_partial on its logits: it writes NP piece records per row (the tile
+ *      summaries: one per 4 KB piece of the shard) and one winner record per row;
+ *   2. the records of all shards are gathered in rank order into recs [R, B, NP] and wins [R, B] (for
+ *      example with an all-gather; on one device the shards simply write their slices of these arrays);
+ *   3. vsamp_shard_merge folds them: the row maximum, log S (piece masses rescaled to the maximum and summed
+ *      as integers), the drawn token and its log-probability, and the log-probability of a target token
+ *      taken from the one shard that owns it.
+ * The draw is a Philox4x32-10 Gumbel-max over the full temperature-scaled distribution (no top-k, top-p or
+ * min-p: those cuts depend on the whole row). Max and arg-max decompose over shards, so the token equals the
+ * unsharded vsamp_sample / vsamp_sample_ws token with top_k, top_p and min_p off. When every shard boundary
+ * v0_r is a multiple of the piece length (2048 bf16 or 1024 fp32 logits), the records are exactly those of an
+ * unsharded row, and every output is bit-identical to vsamp_sample_ws for any R; otherwise the fold differs
+ * only in the last bits of S.
+ * --------------------------------------------------------------------------------------------------- */
+typedef struct vsamp_piece_rec {   /* 32 bytes: a piece's summary */
+  float m;                         /* maximum (NaN: a non-finite value in the piece) */
+  uint32_t cnt;                    /* elements equal to m */
+  uint64_t s;                      /* sum of exp((x - m) / T) over the piece, 2^-40 fixed point */
+  float mn;                        /* minimum */
+  uint32_t reserved[3];
+} vsamp_piece_rec;
+
+typedef struct vsamp_shard_win {   /* 16 bytes: a shard's winner for one row */
+  int32_t idx;                     /* global index of the shard's Gumbel-max winner (-1 on a row error) */
+  float x;                         /* its logit */
+  float xt;                        /* the target token's logit when this shard owns it */
+  int32_t flags;                   /* bit 0: owns the target; bits 8..15: the shard's row status */
+} vsamp_shard_win;
+
+/* Piece records per row that a shard of V_shard logits of type dt writes (ceil(V_shard / piece)); the NP of
+ * vsamp_shard_partial / vsamp_shard_merge is the largest of these over the shards (0 for invalid arguments). */
+int64_t vsamp_shard_pieces(vsamp_dtype dt, int64_t V_shard);
+
+/* Workspace bytes of vsamp_shard_partial for B rows of a shard of V_shard logits (0 for invalid arguments). */
+size_t vsamp_shard_workspace_size(vsamp_dtype dt, int64_t B, int64_t V_shard);
+
+/* Rank-local summaries of one vocabulary shard.
+ *   logits     [B, ld] the shard's logits; element j of row r is the logit of token v0 + j.
+ *   v0         the shard's first token (a multiple of 8 for bf16, 4 for fp32, so that the Philox groups of four
+ *              tokens start inside the shard).
+ *   NP         record slots per row in recs (>= vsamp_shard_pieces(dt, V_shard)); slots past the shard's pieces
+ *              get empty records (maximum -inf, no mass).
+ *   temperature, seed, step, row_id: as for vsamp_sample (the same arrays on every shard).
+ *   target     [B] global token ids whose log-probability the merge reports, or NULL.
+ *   recs       [B, NP] vsamp_piece_rec (device): this shard's slice of the gathered records.
+ *   win        [B] vsamp_shard_win (device).
+ *   workspace  device buffer of vsamp_shard_workspace_size bytes, 16-byte aligned (no initialisation needed).
+ * Two launches on `stream`. */
+vsamp_status vsamp_shard_partial(const void* logits, vsamp_dtype dt, int64_t B, int64_t V_shard, int64_t ld,
+                                 int64_t v0, int64_t NP, const float* temperature, const uint64_t* seed,
+                                 const uint64_t* step, const uint32_t* row_id, const int32_t* target,
+                                 vsamp_piece_rec* recs, vsamp_shard_win* win, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
+/* The owned merge of R shards' records, rank order: recs [R, B, NP], wins [R, B] (device).
+ *   V          the full vocabulary size.
+ *   outputs    [B] each, any may be NULL: row_max (fp32), row_logsum = log S at temperature T (T <= 0 read
+ *              as 1), token (-1 on error), logprob = min((x_t - max) / T - log S, 0) of the drawn token,
+ *              target_logprob of the target given to vsamp_shard_partial, row_status.
+ *   Row errors: a non-finite logit or a NaN / infinite temperature; a requested target that no shard owns.
+ * One launch on `stream`; it reads only the records, never the logits. */
+vsamp_status vsamp_shard_merge(const vsamp_piece_rec* recs, const vsamp_shard_win* wins, int32_t R, int64_t B,
+                               int64_t NP, int64_t V, const float* temperature, const uint64_t* seed,
+                               const uint64_t* step, const uint32_t* row_id, float* row_max, float* row_logsum,
+                               int32_t* token, float* logprob, float* target_logprob, int32_t* row_status,
+                               void* stream);
+
 /* Static description of a status code. */
 const char* vsamp_status_string(vsamp_status s);
 

@@ -30,6 +30,7 @@ VSAMP_BF16 = 1
 
 EXPORTED = ("vsamp_softmax_lse", "vsamp_topk_select", "vsamp_topp_minp_mask", "vsamp_sample",
             "vsamp_sample_ws", "vsamp_sample_workspace_size", "vsamp_sample_static", "vsamp_logprob", "vsamp_topn_logprobs", "vsamp_kept_logprob",
+            "vsamp_shard_pieces", "vsamp_shard_workspace_size", "vsamp_shard_partial", "vsamp_shard_merge",
             "vsamp_status_string",
             "vsamp_device_info", "vsamp_version")
 
@@ -73,6 +74,15 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                                     ctypes.c_size_t, vp]
     lib.vsamp_sample_static.argtypes = [vp, st, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.vsamp_topn_logprobs.argtypes = [vp, st, i64, i64, i64, vp, i32, vp, vp, vp, vp, vp, vp]
+    lib.vsamp_shard_pieces.argtypes = [st, i64]
+    lib.vsamp_shard_pieces.restype = i64
+    lib.vsamp_shard_workspace_size.argtypes = [st, i64, i64]
+    lib.vsamp_shard_workspace_size.restype = ctypes.c_size_t
+    lib.vsamp_shard_partial.argtypes = [vp, st, i64, i64, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp,
+                                        ctypes.c_size_t, vp]
+    lib.vsamp_shard_merge.argtypes = [vp, vp, i32, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.vsamp_shard_partial.restype = st
+    lib.vsamp_shard_merge.restype = st
     lib.vsamp_kept_logprob.argtypes = [vp, st, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.vsamp_sample_workspace_size.argtypes = [st, i64, i64]
     lib.vsamp_sample_workspace_size.restype = ctypes.c_size_t
@@ -404,3 +414,122 @@ def vsamp_kept_logprob(logits, token, temperature=None, top_k=None, top_p=None, 
         _stream(stream))
     _check(st, "vsamp_kept_logprob")
     return out, row_status
+
+
+# ------------------------------------------------------------------------------------------------
+# vocabulary-sharded sampling: rank-local summaries, rank-ordered exchange, the owned merge
+# ------------------------------------------------------------------------------------------------
+PIECE_REC_BYTES = 32
+SHARD_WIN_BYTES = 16
+
+
+def shard_bounds(V: int, R: int, dtype=torch.bfloat16, align_to_pieces: bool = True):
+    """Split [0, V) into R contiguous shards in rank order: [(v0, V_r)]. With align_to_pieces every boundary is a
+    multiple of the 4 KB piece (2048 bf16 or 1024 fp32 logits), which makes the merged outputs bit-identical to the
+    unsharded streaming sampler; otherwise boundaries are multiples of the 16-byte vector (8 bf16 or 4 fp32)."""
+    if R <= 0 or V <= 0:
+        raise ValueError("V and R must be positive")
+    unit = (2048 if dtype == torch.bfloat16 else 1024) if align_to_pieces else (8 if dtype == torch.bfloat16 else 4)
+    units = -(-V // unit)
+    out, start = [], 0
+    for r in range(R):
+        end = min(V, (units * (r + 1) // R) * unit)
+        out.append((start, max(0, end - start)))
+        start = end
+    if any(n <= 0 for _, n in out):
+        raise ValueError(f"V = {V} is too short for {R} shards of whole {unit}-logit units")
+    return out
+
+
+def shard_record_slots(bounds, dtype=torch.bfloat16) -> int:
+    """NP: the record slots per row every shard writes (the most pieces of any shard)."""
+    dt = VSAMP_F32 if dtype == torch.float32 else VSAMP_BF16
+    return max(int(load().vsamp_shard_pieces(dt, n)) for _, n in bounds)
+
+
+def vsamp_shard_partial(logits_shard, v0: int, NP: int, temperature=None, seed=None, step=None, row_id=None,
+                        target=None, recs=None, win=None, workspace=None, stream=None):
+    """Rank-local summaries of one vocabulary shard [B, V_r] starting at token v0: (recs [B, NP, 32] uint8,
+    win [B, 16] uint8), as vsamp_piece_rec / vsamp_shard_win bytes."""
+    B, Vr, ld = _rows(logits_shard, None)
+    dev = logits_shard.device
+    dt = _dtype_code(logits_shard)
+    temperature = _param(temperature, B, torch.float32, dev, "temperature")
+    seed = _param(seed, B, torch.int64, dev, "seed")
+    step = _param(step, B, torch.int64, dev, "step")
+    row_id = _param(row_id, B, torch.int32, dev, "row_id")
+    target = _param(target, B, torch.int32, dev, "target")
+    lib = load()
+    recs = torch.empty((B, int(NP), PIECE_REC_BYTES), dtype=torch.uint8, device=dev) if recs is None else recs
+    win = torch.empty((B, SHARD_WIN_BYTES), dtype=torch.uint8, device=dev) if win is None else win
+    need = int(lib.vsamp_shard_workspace_size(dt, B, Vr))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    st = lib.vsamp_shard_partial(
+        logits_shard.data_ptr(), dt, B, Vr, ld, int(v0), int(NP), _ptr(temperature, torch.float32, dev, B, "temperature"),
+        _ptr(seed, torch.int64, dev, B, "seed"), _ptr(step, torch.int64, dev, B, "step"),
+        _ptr(row_id, torch.int32, dev, B, "row_id"), _ptr(target, torch.int32, dev, B, "target"),
+        _ptr(recs, torch.uint8, dev, B * int(NP) * PIECE_REC_BYTES, "recs"),
+        _ptr(win, torch.uint8, dev, B * SHARD_WIN_BYTES, "win"), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "vsamp_shard_partial")
+    return recs, win
+
+
+def vsamp_shard_merge(recs, wins, V: int, temperature=None, seed=None, step=None, row_id=None,
+                      want_target=False, stream=None):
+    """The owned merge of rank-ordered records recs [R, B, NP, 32] and wins [R, B, 16] (uint8). Returns
+    (row_max, row_logsum, token, logprob, target_logprob or None, row_status)."""
+    if recs.dim() != 4 or wins.dim() != 3 or recs.shape[:2] != wins.shape[:2]:
+        raise ValueError("recs must be [R, B, NP, 32] and wins [R, B, 16]")
+    R, B, NP = int(recs.shape[0]), int(recs.shape[1]), int(recs.shape[2])
+    dev = recs.device
+    temperature = _param(temperature, B, torch.float32, dev, "temperature")
+    seed = _param(seed, B, torch.int64, dev, "seed")
+    step = _param(step, B, torch.int64, dev, "step")
+    row_id = _param(row_id, B, torch.int32, dev, "row_id")
+    f32 = lambda: torch.empty(B, dtype=torch.float32, device=dev)
+    row_max, row_logsum, logprob = f32(), f32(), f32()
+    target_lp = f32() if want_target else None
+    token = torch.empty(B, dtype=torch.int32, device=dev)
+    row_status = torch.empty(B, dtype=torch.int32, device=dev)
+    st = load().vsamp_shard_merge(
+        _ptr(recs.contiguous(), torch.uint8, dev, None, "recs"), _ptr(wins.contiguous(), torch.uint8, dev, None, "wins"),
+        R, B, NP, int(V), _ptr(temperature, torch.float32, dev, B, "temperature"), _ptr(seed, torch.int64, dev, B, "seed"),
+        _ptr(step, torch.int64, dev, B, "step"), _ptr(row_id, torch.int32, dev, B, "row_id"),
+        row_max.data_ptr(), row_logsum.data_ptr(), token.data_ptr(), logprob.data_ptr(),
+        0 if target_lp is None else target_lp.data_ptr(), row_status.data_ptr(), _stream(stream))
+    _check(st, "vsamp_shard_merge")
+    return row_max, row_logsum, token, logprob, target_lp, row_status
+
+
+def gather_shard_records(recs, win, group=None):
+    """The rank-ordered exchange: all-gather this rank's recs [B, NP, 32] and win [B, 16] into [R, B, NP, 32] and
+    [R, B, 16] in rank order, with no reduction in transit (torch.distributed; any backend)."""
+    import torch.distributed as dist
+
+    R = dist.get_world_size(group)
+    # concatenated along the first dimension (the form every backend accepts), then viewed rank-major
+    out_r = torch.empty((R * recs.shape[0],) + tuple(recs.shape[1:]), dtype=recs.dtype, device=recs.device)
+    out_w = torch.empty((R * win.shape[0],) + tuple(win.shape[1:]), dtype=win.dtype, device=win.device)
+    dist.all_gather_into_tensor(out_r, recs.contiguous(), group=group)
+    dist.all_gather_into_tensor(out_w, win.contiguous(), group=group)
+    return out_r.view((R,) + tuple(recs.shape)), out_w.view((R,) + tuple(win.shape))
+
+
+def vsamp_sample_sharded(logits, R: int, temperature=None, seed=None, step=None, row_id=None, target=None,
+                         align_to_pieces: bool = True, stream=None):
+    """R vocabulary shards of one device's [B, V] logits, each summarised by vsamp_shard_partial into its slice of
+    the rank-ordered record arrays, then vsamp_shard_merge. Returns (row_max, row_logsum, token, logprob,
+    target_logprob or None, row_status)."""
+    B, V, _ = _rows(logits, None)
+    bounds = shard_bounds(V, R, logits.dtype, align_to_pieces)
+    NP = shard_record_slots(bounds, logits.dtype)
+    dev = logits.device
+    recs = torch.empty((R, B, NP, PIECE_REC_BYTES), dtype=torch.uint8, device=dev)
+    wins = torch.empty((R, B, SHARD_WIN_BYTES), dtype=torch.uint8, device=dev)
+    for r, (v0, n) in enumerate(bounds):
+        vsamp_shard_partial(logits[:, v0:v0 + n], v0, NP, temperature=temperature, seed=seed, step=step,
+                            row_id=row_id, target=target, recs=recs[r], win=wins[r], stream=stream)
+    return vsamp_shard_merge(recs, wins, V, temperature=temperature, seed=seed, step=step, row_id=row_id,
+                             want_target=target is not None, stream=stream)

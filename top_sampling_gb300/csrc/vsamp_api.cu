@@ -431,6 +431,55 @@ vsamp_status vsamp_sample_static(const void* logits, vsamp_dtype dt, int64_t B, 
                          logprob, row_status, stats, scratch, (size_t)VSAMP_STATIC_SCRATCH_BYTES, stream);
 }
 
+static_assert(sizeof(vsamp_piece_rec) == sizeof(vsamp::PieceRec) && offsetof(vsamp_piece_rec, s) == 8 &&
+                  offsetof(vsamp_piece_rec, mn) == 16,
+              "vsamp_piece_rec mirrors the piece record the kernels write");
+
+int64_t vsamp_shard_pieces(vsamp_dtype dt, int64_t V_shard) {
+  if ((dt != VSAMP_F32 && dt != VSAMP_BF16) || V_shard <= 0) return 0;
+  return split_nchunks(V_shard, dt == VSAMP_F32 ? 4 : 2);
+}
+
+size_t vsamp_shard_workspace_size(vsamp_dtype dt, int64_t B, int64_t V_shard) {
+  if ((dt != VSAMP_F32 && dt != VSAMP_BF16) || B <= 0 || V_shard <= 0) return 0;
+  return sizeof(StreamHeader) + (size_t)B * (size_t)split_nchunks(V_shard, dt == VSAMP_F32 ? 4 : 2) * 128u;
+}
+
+vsamp_status vsamp_shard_partial(const void* logits, vsamp_dtype dt, int64_t B, int64_t V_shard, int64_t ld,
+                                 int64_t v0, int64_t NP, const float* temperature, const uint64_t* seed,
+                                 const uint64_t* step, const uint32_t* row_id, const int32_t* target,
+                                 vsamp_piece_rec* recs, vsamp_shard_win* win, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  vsamp_status st = check_common(logits, dt, B, V_shard, ld);
+  if (st != VSAMP_OK) return st;
+  const int ve = dt == VSAMP_F32 ? 4 : 8;
+  if (!recs || !win || !workspace || (reinterpret_cast<uintptr_t>(workspace) & 15u) != 0 ||
+      (reinterpret_cast<uintptr_t>(recs) & 15u) != 0)
+    return VSAMP_ERR_INVALID_ARG;
+  if (v0 < 0 || v0 % ve != 0 || v0 + V_shard > 0x7FFEFFFFLL) return VSAMP_ERR_INVALID_ARG;
+  if (NP < vsamp_shard_pieces(dt, V_shard)) return VSAMP_ERR_INVALID_ARG;
+  if (workspace_bytes < vsamp_shard_workspace_size(dt, B, V_shard)) return VSAMP_ERR_INVALID_ARG;
+  Params p = base_params(logits, dt, B, V_shard, ld);
+  p.temperature = temperature;
+  p.seed = seed;
+  p.step = step;
+  p.row_id = row_id;
+  p.v0 = v0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dt == VSAMP_F32) return launch_shard_partial<float>(p, B, 4, NP, target, win, recs, workspace, s);
+  return launch_shard_partial<__nv_bfloat16>(p, B, 2, NP, target, win, recs, workspace, s);
+}
+
+vsamp_status vsamp_shard_merge(const vsamp_piece_rec* recs, const vsamp_shard_win* wins, int32_t R, int64_t B,
+                               int64_t NP, int64_t V, const float* temperature, const uint64_t* seed,
+                               const uint64_t* step, const uint32_t* row_id, float* row_max, float* row_logsum,
+                               int32_t* token, float* logprob, float* target_logprob, int32_t* row_status,
+                               void* stream) {
+  if (!recs || !wins || R <= 0 || B <= 0 || NP <= 0 || V <= 0 || V > 0x7FFEFFFFLL) return VSAMP_ERR_INVALID_ARG;
+  return launch_shard_merge(recs, wins, R, B, NP, V, temperature, seed, step, row_id, row_max, row_logsum, token,
+                            logprob, target_logprob, row_status, static_cast<cudaStream_t>(stream));
+}
+
 vsamp_status vsamp_logprob(const void* logits, vsamp_dtype dt, int64_t B, int64_t V, int64_t ld,
                            const float* temperature, const int32_t* token, const float* row_max,
                            const float* row_logsum, float* out, int32_t* row_status, void* stream) {

@@ -51,6 +51,17 @@ vsamp_status launch_sample(Params p, int64_t B, int esize, cudaStream_t stream);
 template <typename T>
 vsamp_status launch_sample_split(Params p, int64_t B, int esize, void* workspace, cudaStream_t stream);
 
+// vsamp_shard_partial's kernels (piece pass over a vocabulary shard, the shard's winners)
+template <typename T>
+vsamp_status launch_shard_partial(Params p, int64_t B, int esize, int64_t NP, const int32_t* target, void* win,
+                                  void* recs, void* workspace, cudaStream_t stream);
+
+// vsamp_shard_merge's kernel (dtype-free)
+vsamp_status launch_shard_merge(const void* recs, const void* wins, int R, int64_t B, int64_t NP, int64_t V,
+                                const float* temperature, const uint64_t* seed, const uint64_t* step,
+                                const uint32_t* row_id, float* row_max, float* row_logsum, int32_t* token,
+                                float* logprob, float* target_logprob, int32_t* row_status, cudaStream_t stream);
+
 template <typename T, int MODE>
 vsamp_status launch(Params p, int64_t B, int esize, cudaStream_t stream);
 

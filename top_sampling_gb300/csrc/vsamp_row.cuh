@@ -78,6 +78,7 @@ struct Params {
   int32_t drop_loads;       // failure-detection test hook: loads are armed but never issued, so every
                             // load wait runs out and the rows report VSAMP_ERR_TIMEOUT
   int32_t nbuf;             // slice buffers per CTA (vsamp_sample: 2 streams the next row during this one)
+  int64_t v0;               // global index of a row's first element: a vocabulary shard's offset (0 otherwise)
 };
 
 constexpr int32_t kNoIndex = -1;

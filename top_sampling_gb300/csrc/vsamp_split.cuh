@@ -514,7 +514,8 @@ constexpr uint32_t kTimeoutCnt = 0xFFFFFFFFu;
 constexpr int kFlagMax = 1024;                     // flagged vectors a row finish collects before it scans instead
 
 struct StreamWs {
-  PieceRec* recs;                    // [B, np]
+  PieceRec* recs;                    // [B, rec_ld]: the first np records of each row
+  int64_t rec_ld;                    // records per row in `recs` (np, or more for a shard's record slots)
   uint32_t* codes;                   // [B, np, 32]: lane l's word holds the codes of vectors u * 32 + l
 };
 
@@ -618,7 +619,7 @@ __device__ __noinline__ void score_row(const Params& p, int64_t row, const DrawR
   for (int64_t vi = threadIdx.x; vi < nvec; vi += kStreamThreads) {
     uint4 v;
     const int cnt = load_vec<T, false>(p, xr, vi * VE, v);
-    score_vector<T>(v, cnt, vi * VE, d, bscore, bidx, bs);
+    score_vector<T>(v, cnt, p.v0 + vi * VE, d, bscore, bidx, bs);   // global index: counters and the result
   }
 }
 
@@ -707,7 +708,7 @@ static __device__ __forceinline__ void finish_row(const Params& p, const StreamW
   SplitShared& sh = S.sh;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int64_t n = p.V;
-  const PieceRec* recs = ws.recs + row * nchunks;
+  const PieceRec* recs = ws.recs + row * ws.rec_ld;
   const float temp0 = p.temperature ? p.temperature[row] : 1.f;
   const float Teff = temp0 > 0.f ? temp0 : 1.f;   // greedy rows use T = 1 for their statistics
   const float invT = 1.f / Teff;
@@ -1142,7 +1143,8 @@ static __device__ __noinline__ void piece_stats_partial(const unsigned char* xr,
 }
 
 // ------------------------------------------------------------------------------------------------
-// Piece pass of one warp over a full piece in shared memory: the record, and for a coded row the draw codes.
+// Piece pass of one warp over a full piece in shared memory: the record, and for a coded row the draw codes
+// (e_begin: the global index of the piece's first element, for the Philox counters).
 // ------------------------------------------------------------------------------------------------
 template <typename T>
 static __device__ __forceinline__ void piece_pass_full(const uint4* sbuf, int64_t e_begin, float c1,
@@ -1293,7 +1295,7 @@ __global__ void __launch_bounds__(kStreamThreads, 3) piece_kernel(const Params p
     const float Teff = temp0 > 0.f ? temp0 : 1.f;
     const float invT = 1.f / Teff;
     const float c1 = kLog2e * invT;
-    PieceRec* rec = ws.recs + row * np + pc;
+    PieceRec* rec = ws.recs + row * ws.rec_ld + pc;
     const bool coded = row_coded(p, row);
     uint32_t k0 = 0u, k1 = 0u, rid = (uint32_t)row, st_lo = 0u, st_hi = 0u;
     if (coded) {
@@ -1305,12 +1307,13 @@ __global__ void __launch_bounds__(kStreamThreads, 3) piece_kernel(const Params p
       st_hi = (uint32_t)(stp >> 32);
       if (p.row_id) rid = p.row_id[row];
     }
+    // the Philox counters use the token's global index (a vocabulary shard starts at p.v0)
     if (sbuf) {
-      piece_pass_full<T>(sbuf, (int64_t)pc * kPieceElems<T>, c1, timeout, coded, k0, k1, rid, st_lo, st_hi, rec,
-                         ws.codes + (row * np + pc) * 32);
+      piece_pass_full<T>(sbuf, p.v0 + (int64_t)pc * kPieceElems<T>, c1, timeout, coded, k0, k1, rid, st_lo, st_hi,
+                         rec, ws.codes + (row * np + pc) * 32);
     } else {
       piece_stats_partial<T>(p.x + row * p.ld * Tr::ESIZE, p.V, p.tma, (int64_t)pc * kPieceElems<T>, c1, timeout, rec);
-      if (coded && !timeout) piece_codes<T>((int64_t)pc * kPieceElems<T>, k0, k1, rid, st_lo, st_hi,
+      if (coded && !timeout) piece_codes<T>(p.v0 + (int64_t)pc * kPieceElems<T>, k0, k1, rid, st_lo, st_hi,
                                             ws.codes + (row * np + pc) * 32);
     }
   }

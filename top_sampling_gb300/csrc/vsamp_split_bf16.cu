@@ -1,6 +1,8 @@
-// bf16 instantiation of the split-vocabulary sampling kernels and their launcher.
+// bf16 instantiation of the split-vocabulary sampling kernels and their launchers.
 #include "vsamp_split_launch.cuh"
 
 namespace vsamp {
 template vsamp_status launch_sample_split<__nv_bfloat16>(Params, int64_t, int, void*, cudaStream_t);
+template vsamp_status launch_shard_partial<__nv_bfloat16>(Params, int64_t, int, int64_t, const int32_t*, void*, void*,
+                                                          void*, cudaStream_t);
 }  // namespace vsamp

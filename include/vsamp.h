@@ -232,6 +232,25 @@ vsamp_status vsamp_topn_logprobs(const void* logits, vsamp_dtype dt, int64_t B, 
                                  const float* temperature, int32_t N, float* row_max, float* row_logsum,
                                  int32_t* out_idx, float* out_lp, int32_t* row_status, void* stream);
 
+/* The dual-pivot rejection sampler ("Sorting-free top-k/top-p/min-p sampling with dual-pivot rejection
+ * kernels #901", Background and Task): a draw from the same filtered law as vsamp_sample (temperature, then
+ * top-k, top-p on the top-k mass, min-p; the kept set is a prefix of the order value desc / index asc) without
+ * sorting the row or forming the cut. Each round draws a candidate from the fixed-point CDF of a prefix of
+ * that order (pivot_0 = its logit), counts the tokens and mass above pivot_0 and above pivot_1 = (pivot_0 +
+ * high) / 2, accepts the candidate if it lies in the kept prefix, and otherwise shrinks the prefix. Rounds
+ * are capped at 32; a row that reaches the cap takes the exact cut and one draw inside it.
+ *   Random numbers: round r uses word 0 of Philox4x32-10 at counter (2^32 - 1 - r, row_id, step mod 2^32,
+ *   step >> 32) with the row's key (the cap's draw uses r = 32). Tokens therefore differ from vsamp_sample's
+ *   (which draws a Gumbel word per token); the law is the same.
+ *   stats [B, 4] int32 or NULL: {passes over the row, rounds, 0, path flags; 64 = the cap was reached}.
+ * Every other argument, the log-probability and the errors are as for vsamp_sample. One launch, one CTA per
+ * row; the row is read from global memory at every pass. */
+vsamp_status vsamp_sample_rejection(const void* logits, vsamp_dtype dt, int64_t B, int64_t V, int64_t ld,
+                                    const float* temperature, const int32_t* top_k, const float* top_p,
+                                    const float* min_p, const uint64_t* seed, const uint64_t* step,
+                                    const uint32_t* row_id, int32_t* token, float* logprob, int32_t* row_status,
+                                    int32_t* stats, void* stream);
+
 /* ---------------------------------------------------------------------------------------------------
  * Vocabulary-sharded sampling ("[WS2][Logprob] Deterministic SM90 linear_logp ...", Tensor parallelism:
  * rank order + owned merge: each rank computes rank-local tile summaries over its vocabulary shard, the

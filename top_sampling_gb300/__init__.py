@@ -31,6 +31,7 @@ VSAMP_BF16 = 1
 EXPORTED = ("vsamp_softmax_lse", "vsamp_topk_select", "vsamp_topp_minp_mask", "vsamp_sample",
             "vsamp_sample_ws", "vsamp_sample_workspace_size", "vsamp_sample_static", "vsamp_logprob", "vsamp_topn_logprobs", "vsamp_kept_logprob",
             "vsamp_shard_pieces", "vsamp_shard_workspace_size", "vsamp_shard_partial", "vsamp_shard_merge",
+            "vsamp_sample_rejection",
             "vsamp_status_string",
             "vsamp_device_info", "vsamp_version")
 
@@ -82,6 +83,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                                         ctypes.c_size_t, vp]
     lib.vsamp_shard_merge.argtypes = [vp, vp, i32, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.vsamp_shard_partial.restype = st
+    lib.vsamp_sample_rejection.argtypes = [vp, st, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.vsamp_sample_rejection.restype = st
     lib.vsamp_shard_merge.restype = st
     lib.vsamp_kept_logprob.argtypes = [vp, st, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.vsamp_sample_workspace_size.argtypes = [st, i64, i64]
@@ -264,6 +267,38 @@ def vsamp_sample(logits, temperature=None, top_k=None, top_p=None, min_p=None, s
         _ptr(row_status, torch.int32, dev, B, "row_status"), _ptr(stats, torch.int32, dev, 4 * B, "stats"),
         _stream(stream))
     _check(st, "vsamp_sample")
+    return token, logprob, row_status, stats
+
+
+def vsamp_sample_rejection(logits, temperature=None, top_k=None, top_p=None, min_p=None, seed=None, step=None,
+                           row_id=None, V=None, token=None, logprob=None, row_status=None, stats=None,
+                           want_logprob=True, want_stats=False, stream=None):
+    """The dual-pivot rejection sampler: the law of vsamp_sample from other random numbers. Returns (token,
+    logprob or None, row_status, stats or None); stats rows are {passes, rounds, 0, path flags}."""
+    B, V, ld = _rows(logits, V)
+    dev = logits.device
+    temperature = _param(temperature, B, torch.float32, dev, "temperature")
+    top_k = _param(top_k, B, torch.int32, dev, "top_k")
+    top_p = _param(top_p, B, torch.float32, dev, "top_p")
+    min_p = _param(min_p, B, torch.float32, dev, "min_p")
+    seed = _param(seed, B, torch.int64, dev, "seed")
+    step = _param(step, B, torch.int64, dev, "step")
+    row_id = _param(row_id, B, torch.int32, dev, "row_id")
+    token = torch.empty(B, dtype=torch.int32, device=dev) if token is None else token
+    if want_logprob and logprob is None:
+        logprob = torch.empty(B, dtype=torch.float32, device=dev)
+    row_status = torch.empty(B, dtype=torch.int32, device=dev) if row_status is None else row_status
+    if want_stats and stats is None:
+        stats = torch.empty((B, 4), dtype=torch.int32, device=dev)
+    st = load().vsamp_sample_rejection(
+        logits.data_ptr(), _dtype_code(logits), B, V, ld, _ptr(temperature, torch.float32, dev, B, "temperature"),
+        _ptr(top_k, torch.int32, dev, B, "top_k"), _ptr(top_p, torch.float32, dev, B, "top_p"),
+        _ptr(min_p, torch.float32, dev, B, "min_p"), _ptr(seed, torch.int64, dev, B, "seed"),
+        _ptr(step, torch.int64, dev, B, "step"), _ptr(row_id, torch.int32, dev, B, "row_id"),
+        _ptr(token, torch.int32, dev, B, "token"), _ptr(logprob, torch.float32, dev, B, "logprob"),
+        _ptr(row_status, torch.int32, dev, B, "row_status"), _ptr(stats, torch.int32, dev, 4 * B, "stats"),
+        _stream(stream))
+    _check(st, "vsamp_sample_rejection")
     return token, logprob, row_status, stats
 
 

@@ -435,6 +435,31 @@ static_assert(sizeof(vsamp_piece_rec) == sizeof(vsamp::PieceRec) && offsetof(vsa
                   offsetof(vsamp_piece_rec, mn) == 16,
               "vsamp_piece_rec mirrors the piece record the kernels write");
 
+vsamp_status vsamp_sample_rejection(const void* logits, vsamp_dtype dt, int64_t B, int64_t V, int64_t ld,
+                                    const float* temperature, const int32_t* top_k, const float* top_p,
+                                    const float* min_p, const uint64_t* seed, const uint64_t* step,
+                                    const uint32_t* row_id, int32_t* token, float* logprob, int32_t* row_status,
+                                    int32_t* stats, void* stream) {
+  vsamp_status st = check_common(logits, dt, B, V, ld);
+  if (st != VSAMP_OK) return st;
+  if (!token) return VSAMP_ERR_INVALID_ARG;
+  Params p = base_params(logits, dt, B, V, ld);
+  p.temperature = temperature;
+  p.top_k = top_k;
+  p.top_p = top_p;
+  p.min_p = min_p;
+  p.seed = seed;
+  p.step = step;
+  p.row_id = row_id;
+  p.token = token;
+  p.logprob = logprob;
+  p.row_status = row_status;
+  p.stats = stats;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dt == VSAMP_F32) return launch_reject<float>(p, B, s);
+  return launch_reject<__nv_bfloat16>(p, B, s);
+}
+
 int64_t vsamp_shard_pieces(vsamp_dtype dt, int64_t V_shard) {
   if ((dt != VSAMP_F32 && dt != VSAMP_BF16) || V_shard <= 0) return 0;
   return split_nchunks(V_shard, dt == VSAMP_F32 ? 4 : 2);

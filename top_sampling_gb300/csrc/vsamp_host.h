@@ -56,6 +56,10 @@ template <typename T>
 vsamp_status launch_shard_partial(Params p, int64_t B, int esize, int64_t NP, const int32_t* target, void* win,
                                   void* recs, void* workspace, cudaStream_t stream);
 
+// vsamp_sample_rejection's kernel (dual-pivot rejection rounds, one CTA per row)
+template <typename T>
+vsamp_status launch_reject(Params p, int64_t B, cudaStream_t stream);
+
 // vsamp_shard_merge's kernel (dtype-free)
 vsamp_status launch_shard_merge(const void* recs, const void* wins, int R, int64_t B, int64_t NP, int64_t V,
                                 const float* temperature, const uint64_t* seed, const uint64_t* step,

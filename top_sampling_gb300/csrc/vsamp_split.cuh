@@ -696,6 +696,108 @@ __device__ __noinline__ int32_t piece_nth_equal_staged(const PieceView<T>& pv, f
 }
 
 // ------------------------------------------------------------------------------------------------
+// The cut of one row (a CTA): the shortest prefix of the order (value desc, index asc) over top-k, top-p (on
+// the top-k mass) and min-p, at least one token. From the row statistics (maximum P.M, fixed-point mass Sfx,
+// count of maxima cM); radix rounds and the min-p pass re-read the row through the planner only when the cut
+// leaves the maximum's tie group. Sets PATH_* flags in `path` and a row error in `plan_status`.
+// ------------------------------------------------------------------------------------------------
+template <typename T>
+static __device__ __noinline__ Cut plan_cut(RowPlanner<T>& P, bool greedy, float Teff, int32_t topk, float topp,
+                                            float minp, unsigned long long Sfx, uint32_t cM, int& path,
+                                            int& plan_status) {
+  using Tr = Traits<T>;
+  const int64_t n = P.n;
+  const float M = P.M, c1 = P.c1;
+  const unsigned long long one = 1ull << kMassShift;
+  const uint32_t rkM = Tr::rkey_of_value(M);
+  Cut fin{};
+  const bool minp_on = !greedy && minp > 0.f;
+  if (greedy) {
+    fin = Cut{rkM, 0, 1, cM, one, 0};
+    path |= PATH_MAXGROUP;
+  } else {
+    int ck_mode = 0, cp_mode = 0;
+    float goal_p = -1.f;
+    unsigned long long cp_goal = 0ull;
+    Cut ck{}, cp{};
+    const bool topk_on = topk > 0 && (int64_t)topk < n;
+    const bool topp_on = topp < 1.f;
+    const unsigned long long keff = topk_on ? (unsigned long long)topk : (unsigned long long)n;
+    if (topk_on) {
+      if (keff <= cM) { ck = Cut{rkM, 0, keff, cM, keff * one, 0}; ck_mode = 1; }
+      else { ck = Cut{0, 0, keff, 0, 0, 0}; ck_mode = 2; }
+    }
+    if (topp_on) {
+      if (ck_mode != 2) {
+        const unsigned long long Sk = topk_on ? ck.mass : Sfx;
+        const unsigned long long target = ceil_mul_frac(topp, Sk);
+        if (target <= cM * one) {
+          unsigned long long need = (target + one - 1) >> kMassShift;
+          need = need < 1 ? 1 : need;
+          cp = Cut{rkM, 0, need, cM, need * one, 0};
+          cp_mode = 1;
+        } else {
+          cp_mode = 2;
+          if (topk_on) cp_goal = target;
+          else goal_p = topp;
+        }
+      } else if (ceil_mul_frac(topp, Sfx) <= one) {
+        cp = Cut{rkM, 0, 1, cM, one, 0};
+        cp_mode = 1;
+      } else {
+        cp_mode = 2;
+      }
+    }
+    // top-p keeping the first maximum alone is the shortest cut: no radix search for top-k, no min-p pass
+    const bool cp_one = cp_mode == 1 && cp.kept() == 1;
+    if (cp_one && ck_mode == 2) ck_mode = 0;
+    if (ck_mode == 1 || cp_mode == 1) path |= PATH_MAXGROUP;
+    if (minp_on && !cp_one) {
+      // min-p keeps w >= minp <=> x >= x* = M + T ln(minp) (an unevaluated sum; the threshold is the
+      // smallest fp32 value >= x*): the kept group ends with the smallest key at or above it
+      const float L = logf(minp);
+      const float ph = Teff * L, pl_ = fmaf(Teff, L, -ph);
+      const float sh_ = M + ph;
+      const float bb = sh_ - M;
+      const float sl = (M - (sh_ - bb)) + (ph - bb);
+      const float lo = sl + pl_;
+      const float xf = lo > 0.f ? nextafterf(sh_, INFINITY) : sh_;
+      uint32_t cnt_ge, minkey, cnt_minkey;
+      unsigned long long mass_ge;
+      P.minp_stats(key_f32_bits(__float_as_uint(xf)), cnt_ge, mass_ge, minkey, cnt_minkey);
+      const uint32_t rkm = (Tr::KB == 32) ? minkey : (minkey >> 16);
+      fin = Cut{rkm, (unsigned long long)(cnt_ge - cnt_minkey), cnt_minkey, cnt_minkey, mass_ge, 1};
+    } else {
+      fin = Cut{rkM, 0, (unsigned long long)n, 0, Sfx, 1};
+    }
+    if (ck_mode == 2) {
+      const RadixOut r = P.radix(false, ck.need, -1.f, cp_mode == 2);
+      if (!r.ok) plan_status = VSAMP_ERR_INVALID_ARG;
+      const unsigned long long need = ck.need - r.cnt_above;
+      const unsigned long long wP = mass_fx_split(ex2_approx((Tr::value_of_rkey(r.rk) - M) * c1));
+      ck = Cut{r.rk, r.cnt_above, need, r.cnt_eq, r.mass_above + need * wP, 0};
+      path |= PATH_RADIX_K;
+      if (cp_mode == 2) cp_goal = ceil_mul_frac(topp, ck.mass);
+    }
+    if (cp_mode == 2 && plan_status == VSAMP_OK) {
+      const RadixOut r = P.radix(true, cp_goal, goal_p, true);
+      if (!r.ok) plan_status = VSAMP_ERR_INVALID_ARG;
+      const unsigned long long wP = mass_fx_split(ex2_approx((Tr::value_of_rkey(r.rk) - M) * c1));
+      unsigned long long need = wP ? (r.goal + wP - 1) / wP : 1;
+      need = need < 1 ? 1 : (need > r.cnt_eq ? r.cnt_eq : need);
+      cp = Cut{r.rk, r.cnt_above, need, r.cnt_eq, r.mass_above + need * wP, 0};
+      path |= PATH_RADIX_P;
+    }
+    Cut best = fin;
+    if (ck_mode && ck.kept() < best.kept()) best = ck;
+    if (cp_mode && cp.kept() < best.kept()) best = cp;
+    if (minp_on && best.whole) path |= PATH_MINP;
+    fin = best;
+  }
+  return fin;
+}
+
+// ------------------------------------------------------------------------------------------------
 // Row finish: one CTA (all 256 threads) per row. The row's dependent memory accesses are batched: the piece
 // records and the draw codes come in one round of loads, and after the plan the boundary piece and the flagged
 // vectors in another.
@@ -803,90 +905,7 @@ static __device__ __forceinline__ void finish_row(const Params& p, const StreamW
 
   // ---- plan: the shortest prefix over top-k, top-p and min-p ----
   int plan_status = VSAMP_OK;
-  Cut fin{};
-  const bool minp_on = !greedy && minp > 0.f;
-  if (greedy) {
-    fin = Cut{rkM, 0, 1, cM, one, 0};
-    path |= PATH_MAXGROUP;
-  } else {
-    int ck_mode = 0, cp_mode = 0;
-    float goal_p = -1.f;
-    unsigned long long cp_goal = 0ull;
-    Cut ck{}, cp{};
-    const bool topk_on = topk > 0 && (int64_t)topk < n;
-    const bool topp_on = topp < 1.f;
-    const unsigned long long keff = topk_on ? (unsigned long long)topk : (unsigned long long)n;
-    if (topk_on) {
-      if (keff <= cM) { ck = Cut{rkM, 0, keff, cM, keff * one, 0}; ck_mode = 1; }
-      else { ck = Cut{0, 0, keff, 0, 0, 0}; ck_mode = 2; }
-    }
-    if (topp_on) {
-      if (ck_mode != 2) {
-        const unsigned long long Sk = topk_on ? ck.mass : Sfx;
-        const unsigned long long target = ceil_mul_frac(topp, Sk);
-        if (target <= cM * one) {
-          unsigned long long need = (target + one - 1) >> kMassShift;
-          need = need < 1 ? 1 : need;
-          cp = Cut{rkM, 0, need, cM, need * one, 0};
-          cp_mode = 1;
-        } else {
-          cp_mode = 2;
-          if (topk_on) cp_goal = target;
-          else goal_p = topp;
-        }
-      } else if (ceil_mul_frac(topp, Sfx) <= one) {
-        cp = Cut{rkM, 0, 1, cM, one, 0};
-        cp_mode = 1;
-      } else {
-        cp_mode = 2;
-      }
-    }
-    // top-p keeping the first maximum alone is the shortest cut: no radix search for top-k, no min-p pass
-    const bool cp_one = cp_mode == 1 && cp.kept() == 1;
-    if (cp_one && ck_mode == 2) ck_mode = 0;
-    if (ck_mode == 1 || cp_mode == 1) path |= PATH_MAXGROUP;
-    if (minp_on && !cp_one) {
-      // min-p keeps w >= minp <=> x >= x* = M + T ln(minp) (an unevaluated sum; the threshold is the
-      // smallest fp32 value >= x*): the kept group ends with the smallest key at or above it
-      const float L = logf(minp);
-      const float ph = Teff * L, pl_ = fmaf(Teff, L, -ph);
-      const float sh_ = M + ph;
-      const float bb = sh_ - M;
-      const float sl = (M - (sh_ - bb)) + (ph - bb);
-      const float lo = sl + pl_;
-      const float xf = lo > 0.f ? nextafterf(sh_, INFINITY) : sh_;
-      uint32_t cnt_ge, minkey, cnt_minkey;
-      unsigned long long mass_ge;
-      P.minp_stats(key_f32_bits(__float_as_uint(xf)), cnt_ge, mass_ge, minkey, cnt_minkey);
-      const uint32_t rkm = (Tr::KB == 32) ? minkey : (minkey >> 16);
-      fin = Cut{rkm, (unsigned long long)(cnt_ge - cnt_minkey), cnt_minkey, cnt_minkey, mass_ge, 1};
-    } else {
-      fin = Cut{rkM, 0, (unsigned long long)n, 0, Sfx, 1};
-    }
-    if (ck_mode == 2) {
-      const RadixOut r = P.radix(false, ck.need, -1.f, cp_mode == 2);
-      if (!r.ok) plan_status = VSAMP_ERR_INVALID_ARG;
-      const unsigned long long need = ck.need - r.cnt_above;
-      const unsigned long long wP = mass_fx_split(ex2_approx((Tr::value_of_rkey(r.rk) - M) * c1));
-      ck = Cut{r.rk, r.cnt_above, need, r.cnt_eq, r.mass_above + need * wP, 0};
-      path |= PATH_RADIX_K;
-      if (cp_mode == 2) cp_goal = ceil_mul_frac(topp, ck.mass);
-    }
-    if (cp_mode == 2 && plan_status == VSAMP_OK) {
-      const RadixOut r = P.radix(true, cp_goal, goal_p, true);
-      if (!r.ok) plan_status = VSAMP_ERR_INVALID_ARG;
-      const unsigned long long wP = mass_fx_split(ex2_approx((Tr::value_of_rkey(r.rk) - M) * c1));
-      unsigned long long need = wP ? (r.goal + wP - 1) / wP : 1;
-      need = need < 1 ? 1 : (need > r.cnt_eq ? r.cnt_eq : need);
-      cp = Cut{r.rk, r.cnt_above, need, r.cnt_eq, r.mass_above + need * wP, 0};
-      path |= PATH_RADIX_P;
-    }
-    Cut best = fin;
-    if (ck_mode && ck.kept() < best.kept()) best = ck;
-    if (cp_mode && cp.kept() < best.kept()) best = cp;
-    if (minp_on && best.whole) path |= PATH_MINP;
-    fin = best;
-  }
+  const Cut fin = plan_cut<T>(P, greedy, Teff, topk, topp, minp, Sfx, cM, path, plan_status);
   if (plan_status != VSAMP_OK) {
     write_outputs(-1, __int_as_float(0x7FC00000), plan_status, 0u);
     return;

@@ -124,3 +124,76 @@ def test_wide_rows(ts, dev, width, k, dtype):
     rng = np.random.default_rng(width + k)
     x = np.stack([_keys(rng, kind, width) for kind in ("random", "ties", "equal", "random")])
     _run_and_check(ts, dev, x, np.full(4, width, np.int32), k, dtype=dtype)
+
+
+# ------------------------------------------------------------------------------------------------
+# the uncached path: rows longer than a thread-block cluster holds on chip ("[Kernel] Make persistent_topk
+# deterministic", the wide-row fallback runs), and the same path forced on the shapes above
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("width", [1 << 20, 2 << 20])
+def test_rows_beyond_on_chip_capacity(ts, dev, width, dtype):
+    """1 M and 2 M keys per row (past the on-chip capacity for fp32; 2 M also for bf16): random, tie-heavy and
+    all-equal rows, bit-exact, where the on-chip select would refuse the row."""
+    lim = ts.device_info(0)
+    cap = lim.max_row_f32 if dtype == "f32" else lim.max_row_bf16
+    rng = np.random.default_rng(width)
+    x = np.stack([_keys(rng, kind, width) for kind in ("random", "ties", "equal")])
+    for k in (512, 2048):
+        _run_and_check(ts, dev, x, np.full(3, width, np.int32), k, repeats=2, dtype=dtype)
+    if width <= cap:
+        pytest.skip(f"{width} keys fit on chip ({cap}): the on-chip path ran")
+
+
+@pytest.fixture
+def forced_stream():
+    import os
+
+    old = os.environ.get("VSAMP_SELECT_STREAM")
+    os.environ["VSAMP_SELECT_STREAM"] = "1"
+    yield
+    if old is None:
+        os.environ.pop("VSAMP_SELECT_STREAM", None)
+    else:
+        os.environ["VSAMP_SELECT_STREAM"] = old
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("k", [512, 2048])
+@pytest.mark.parametrize("kind", ["random", "ties", "equal", "narrow"])
+def test_uncached_path_on_indexer_shapes(ts, dev, forced_stream, k, kind, dtype):
+    rng = np.random.default_rng(k + len(kind))
+    lens = np.array([256, 1024, 4096, 20480, 40960, 2048], dtype=np.int32)
+    x = np.stack([_keys(rng, kind, 40960) for _ in range(lens.size)])
+    _run_and_check(ts, dev, x, lens, k, dtype=dtype)
+
+
+def test_uncached_path_contract_edges(ts, dev, forced_stream):
+    rng = np.random.default_rng(8)
+    B, L = 6, 5000
+    x = (rng.integers(0, 3, size=(B, L)) * 1.0).astype(np.float32)
+    x[0, :4] = [np.inf, -np.inf, np.inf, -np.inf]
+    x[1, 100:] = np.nan                      # beyond its length: never read
+    x[2, 10] = np.nan                        # inside: a row error
+    lengths = np.array([L, 100, 50, 3000, 0, L + 1], dtype=np.int32)
+    ks = np.array([64, 64, 64, 0, 10, 10], dtype=np.int32)
+    idx, st = ts.vsamp_topk_select(torch.from_numpy(x).to(dev), t(ks, dev), k_max=64, lengths=t(lengths, dev),
+                                   max_len=L)
+    idx, st = idx.cpu().numpy(), st.cpu().numpy()
+    for r in range(B):
+        s_o, want = osm.topk_select_row(x[r], int(lengths[r]), int(ks[r]), 64) if 0 < lengths[r] <= L else \
+            (osm.STATUS_INVALID_ARG, np.full(64, -1, dtype=np.int32))
+        assert st[r] == s_o and np.array_equal(idx[r], want), r
+    idx, st = ts.vsamp_topk_select(torch.from_numpy(x).to(dev), t(np.full(B, 65, np.int32), dev), k_max=64)
+    want_st = [osm.topk_select_row(x[r], L, 65, 64)[0] for r in range(B)]
+    assert list(st.cpu().numpy()) == want_st and np.all(idx.cpu().numpy() == -1)
+
+
+def test_uncached_path_on_the_quantised_workload(ts, dev, forced_stream):
+    b = workloads.c3(B=32)
+    x = torch.from_numpy(b.scores).to(dev)
+    idx, st = ts.vsamp_topk_select(x, t(b.k, dev), k_max=b.k_max, lengths=t(b.lengths, dev))
+    idx, st = idx.cpu().numpy(), st.cpu().numpy()
+    for r in range(b.B):
+        s_o, want = osm.topk_select_row(b.scores[r], int(b.lengths[r]), int(b.k[r]), b.k_max)
+        assert st[r] == s_o and np.array_equal(idx[r], want), r

@@ -333,7 +333,14 @@ vsamp_status vsamp_topk_select(const void* scores, vsamp_dtype dt, int64_t B, in
   p.k_max = k_max;
   p.out_idx = out_idx;
   p.row_status = row_status;
-  return dispatch<MODE_SELECT>(p, dt, B, static_cast<cudaStream_t>(stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // rows that a cluster cannot hold on chip (or VSAMP_SELECT_STREAM=1) take the uncached path
+  if (env_int("VSAMP_SELECT_STREAM", 0) == 0) {
+    st = dispatch<MODE_SELECT>(p, dt, B, s);
+    if (st != VSAMP_ERR_UNSUPPORTED) return st;
+  }
+  if (dt == VSAMP_F32) return launch_select_stream<float>(p, B, s);
+  return launch_select_stream<__nv_bfloat16>(p, B, s);
 }
 
 vsamp_status vsamp_topp_minp_mask(const void* logits, vsamp_dtype dt, int64_t B, int64_t V, int64_t ld,

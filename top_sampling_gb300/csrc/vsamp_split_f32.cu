@@ -1,8 +1,10 @@
 // f32 instantiation of the split-vocabulary sampling kernels and their launchers; the shard merge (dtype-free).
 #include "vsamp_reject.cuh"
+#include "vsamp_select_stream.cuh"
 #include "vsamp_split_launch.cuh"
 
 namespace vsamp {
+template vsamp_status launch_select_stream<float>(Params, int64_t, cudaStream_t);
 template vsamp_status launch_reject<float>(Params, int64_t, cudaStream_t);
 template vsamp_status launch_sample_split<float>(Params, int64_t, int, void*, cudaStream_t);
 template vsamp_status launch_shard_partial<float>(Params, int64_t, int, int64_t, const int32_t*, void*, void*, void*,

@@ -55,7 +55,7 @@ def _peaks():
         return 6800.0, "fallback", 2070.0
 
 
-PROFILE = os.path.join(ROOT, "profiles", "sample_kernel_c4.md")
+PROFILE = os.path.join(ROOT, "profiles", "sample_kernel_c4.json")
 
 
 def _csrc_digest() -> str:
@@ -69,17 +69,14 @@ def _csrc_digest() -> str:
 
 
 def _traffic():
-    """DRAM bytes per launch from the committed ncu summary, or None once the kernel sources changed."""
+    """DRAM bytes per launch from the committed machine-readable ncu record (profiles/sample_kernel_c4.json), or
+    None once the kernel sources changed since the counters were taken."""
     try:
-        fields = {}
         with open(PROFILE) as f:
-            for line in f:
-                k, _, v = line.partition(":")
-                if k in ("source_digest", "dram_bytes_per_launch"):
-                    fields[k] = v.strip()
-        if fields.get("source_digest") != _csrc_digest():
+            rec = json.load(f)
+        if rec.get("source_digest") != _csrc_digest():
             return None
-        return int(fields["dram_bytes_per_launch"])
+        return int(rec["dram_bytes_per_launch"])
     except Exception:
         return None
 
@@ -244,6 +241,42 @@ def c5_passes(ts, dev) -> dict:
         return {"error": f"{type(e).__name__}: {e}"[:200]}
 
 
+def other_entry_points(ts, dev, copies, kw, steps_dev, reps: int = 200) -> dict:
+    """Context, outside the timed region: the same C4 step through the other sampling entry points (the streaming
+    sampler with a workspace, the dual-pivot rejection sampler, the vocabulary-sharded pair with R = 4 shards on
+    this one device), CUDA events over `reps` calls with the rotating input copies. Never raises."""
+    try:
+        import torch
+
+        out = {}
+        stream = torch.cuda.current_stream(dev)
+
+        def timed(fn):
+            for i in range(5):
+                fn(i)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(reps):
+                fn(i)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / reps * 1e3
+
+        n = len(copies)
+        us = timed(lambda i: ts.vsamp_sample_ws(copies[i % n], step=steps_dev[i % n], want_logprob=True, **kw))
+        out["vsamp_sample_ws"] = {"us_per_call": us, "rows_per_s": B_ROWS / (us * 1e-6)}
+        us = timed(lambda i: ts.vsamp_sample_rejection(copies[i % n], step=steps_dev[i % n], **kw))
+        out["vsamp_sample_rejection"] = {"us_per_call": us, "rows_per_s": B_ROWS / (us * 1e-6)}
+        kws = {k: v for k, v in kw.items() if k in ("temperature", "seed", "row_id")}
+        us = timed(lambda i: ts.vsamp_sample_sharded(copies[i % n], 4, step=steps_dev[i % n], **kws))
+        out["vsamp_shard_partial_x4_merge"] = {"us_per_call": us, "rows_per_s": B_ROWS / (us * 1e-6),
+                                               "note": "top-p off (the sharded draw has no filters); 4 shards"}
+        return out
+    except Exception as e:
+        return {"error": f"{type(e).__name__}: {e}"[:200]}
+
+
 def run_gpu(args):
     import torch
 
@@ -299,9 +332,17 @@ def run_gpu(args):
     if int(status.ne(0).sum()) != 0:
         raise RuntimeError("sampling rows reported errors")
 
+    # the clock sampler runs over a loaded stretch: at least 0.6 s of back-to-back calls right before the timed
+    # region, then the timed region itself, so its samples describe the kernel under load
     clocks = ClockSampler(local)
     clocks.start()
-    time.sleep(0.3)
+    t_load = time.perf_counter()
+    i_load = 0
+    while time.perf_counter() - t_load < 0.6:
+        for _ in range(50):
+            call(i_load)
+            i_load += 1
+        torch.cuda.synchronize()
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
@@ -366,6 +407,7 @@ def run_gpu(args):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f32",
+        "dtype_note": "the arithmetic type of the path: fp32 on exactly widened bf16 inputs (config.input_dtype)",
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "B": B_ROWS, "V": V_COLS, "input_dtype": "bf16",
                    "l2": f"rotating {N_COPIES} input copies ({N_COPIES * BYTES_PER_STEP / 1e6:.0f} MB > 2x L2)",
@@ -387,6 +429,9 @@ def run_gpu(args):
         out["cpu_baseline"] = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
     if world == 1 and not args.no_cpu:
         out["c5_pivot_search"] = c5_passes(ts, dev)
+        out["other_entry_points"] = other_entry_points(ts, dev, copies, dict(temperature=temp, top_k=topk, top_p=topp,
+                                                                             min_p=minp, seed=seed, row_id=row_id),
+                                                       steps_dev)
     if dist:
         dist.destroy_process_group()
     if rank == 0:

@@ -1,5 +1,5 @@
 """The benchmark's reporting on CPU: the reference arm's JSON line, and the DRAM traffic that `bench.py` takes
-from the committed ncu summary only while that summary describes the current kernel sources."""
+from the committed machine-readable ncu record only while that record describes the current kernel sources."""
 import json
 import os
 import subprocess
@@ -11,16 +11,23 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def test_traffic_follows_the_profile_digest(tmp_path, monkeypatch):
-    good = tmp_path / "good.md"
-    good.write_text(f"x\nsource_digest: {bench._csrc_digest()}\ndram_bytes_per_launch: 123456\n")
+    good = tmp_path / "good.json"
+    good.write_text(json.dumps({"source_digest": bench._csrc_digest(), "dram_bytes_per_launch": 123456}))
     monkeypatch.setattr(bench, "PROFILE", str(good))
     assert bench._traffic() == 123456
-    stale = tmp_path / "stale.md"
-    stale.write_text("source_digest: 0000000000000000\ndram_bytes_per_launch: 123456\n")
+    stale = tmp_path / "stale.json"
+    stale.write_text(json.dumps({"source_digest": "0000000000000000", "dram_bytes_per_launch": 123456}))
     monkeypatch.setattr(bench, "PROFILE", str(stale))
     assert bench._traffic() is None
-    monkeypatch.setattr(bench, "PROFILE", str(tmp_path / "missing.md"))
+    monkeypatch.setattr(bench, "PROFILE", str(tmp_path / "missing.json"))
     assert bench._traffic() is None
+
+
+def test_committed_profile_record_is_machine_readable():
+    with open(os.path.join(ROOT, "profiles", "sample_kernel_c4.json")) as f:
+        rec = json.load(f)
+    assert len(rec["source_digest"]) == 16 and int(rec["dram_bytes_per_launch"]) > 0
+    assert "ncu" in rec["command"] and "--clock-control none" in rec["command"]
 
 
 def test_digest_covers_every_kernel_source(tmp_path, monkeypatch):

@@ -518,8 +518,10 @@ def run_call(spec: str, repeat: int):
         kw = dict(temperature=T(b.temperature), top_k=T(b.top_k), top_p=T(b.top_p), min_p=T(b.min_p), V=b.V)
         seed, step, token = T(b.seed), T(b.step), torch.zeros(b.B, dtype=torch.int32, device=dev)
         for _ in range(repeat):
-            if fn in ("sample", "sample_ws"):
+            if fn in ("sample", "sample_ws", "sample_rejection"):
                 getattr(ts, "vsamp_" + fn)(x, seed=seed, step=step, **kw)
+            elif fn == "sharded4":
+                ts.vsamp_sample_sharded(x, 4, temperature=kw["temperature"], seed=seed, step=step)
             elif fn == "cut":
                 ts.vsamp_topp_minp_mask(x, want_mask=False, **kw)
             elif fn == "mask":

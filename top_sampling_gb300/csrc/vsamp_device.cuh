@@ -134,6 +134,14 @@ __device__ __forceinline__ void dsmem_store_v4(uint32_t addr, uint32_t a, uint32
   asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                : "memory");
 }
+// 16 bytes into a peer CTA's shared memory (addr mapped by dsmem_map) whose arrival is counted in bytes on the
+// peer's mbarrier `bar` (mapped too): the issuing thread neither waits for the write nor orders its own earlier
+// memory operations before it; the peer's wait on `bar` (acquire, cluster scope) makes the bytes visible.
+__device__ __forceinline__ void dsmem_store_async_v4(uint32_t addr, uint4 v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
+               ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(bar)
+               : "memory");
+}
 __device__ __forceinline__ uint4 dsmem_load_v4(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
@@ -253,6 +261,11 @@ struct PhiloxRow {
 };
 
 __device__ __forceinline__ uint32_t min4_u32(uint4 w) { return min(__vimin3_u32(w.x, w.y, w.z), w.w); }
+
+// 4-bit draw code of a 16-byte vector from the smallest Philox word w of its tokens: min(clz(w), 15).
+// w < bk implies code(w) >= code(bk), so testing codes flags a superset of the vectors the prune bound keeps.
+__device__ __forceinline__ uint32_t draw_code(uint32_t w) { return min((uint32_t)__clz(w), 15u); }
+
 
 // PhiloxRow with few live registers: the round keys from the third round on are formed as the rounds run
 // (one add per key word and round, shared by the counters drawn together), and only the smallest of each

@@ -184,16 +184,17 @@ __global__ void __launch_bounds__(kSplitThreads) reject_sample_kernel(const Para
     // ---- pass 0: maximum and non-finite check, then the mass and the count of maxima ----
     RejectRow<T> R{p, sh, row, n, 0.f, c1};
     const int64_t nvec = (n + VE - 1) / VE;
-    float m = -INFINITY, nf = 0.f;
+    float m = -INFINITY, mn = INFINITY, nf = 0.f;
     for (int64_t vi = t; vi < nvec; vi += kSplitThreads) {
       float x[VE];
       const int cnt = R.load(vi, x);
 #pragma unroll
       for (int i = 0; i < VE; ++i)
-        if (i < cnt) { m = fmaxf(m, x[i]); nf = fmaf(x[i], 0.f, nf); }
+        if (i < cnt) { m = fmaxf(m, x[i]); mn = fminf(mn, x[i]); nf = fmaf(x[i], 0.f, nf); }
     }
     const uint32_t nonfin = __syncthreads_or(nf != 0.f ? 1 : 0);
     const float M = block_max_f(m, sh);
+    const float Mmin = -block_max_f(-mn, sh);
     R.M = M;
     unsigned long long s = 0;
     uint32_t cm = 0;
@@ -233,6 +234,7 @@ __global__ void __launch_bounds__(kSplitThreads) reject_sample_kernel(const Para
       const bool p_on = topp < 1.f;
       const bool m_on = minp > 0.f;
       RowPlanner<T> P{p, sh, row, n, M, c1};
+      P.Mmin = Mmin;
       // S_k: the mass the top-p target is taken on (the top-k mass when both are on)
       unsigned long long Sk = Sfx;
       if (k_on && p_on) {

@@ -228,6 +228,70 @@ struct RadixOut {
   int ok;
 };
 
+// ------------------------------------------------------------------------------------------------
+// Value bins of a radix search's first round: 256 bins linear in the value over [xlo, xhi] (the range of the
+// candidate values), so that rows whose values share their top key bits (one binade, a narrow distribution,
+// a few levels) still spread over many bins and their histogram updates over many addresses. The bin is a
+// monotone function of x (a rounded subtraction, a rounded product, a truncation), so the elements of one bin
+// are exactly the keys of a contiguous range, which bisection on the same function finds; the later rounds
+// refine that range by key bytes, from its highest differing bit down.
+// ------------------------------------------------------------------------------------------------
+struct ValueBins {
+  float xlo, sc;   // bin(x) = min(255, (int)((x - xlo) * sc)); sc == 0: the first round uses key bytes
+};
+
+__device__ __forceinline__ ValueBins make_value_bins(float xlo, float xhi) {
+  ValueBins vb{xlo, 0.f};
+  const float span = __fsub_rn(xhi, xlo);
+  if (span > 0.f && span <= 3.0e38f) {
+    const float sc = __fdiv_rn(256.f, span);
+    if (sc <= 3.0e38f) vb.sc = sc;
+  }
+  return vb;
+}
+
+__device__ __forceinline__ int value_bin(float x, const ValueBins& vb) {
+  const float t = __fmul_rn(__fsub_rn(x, vb.xlo), vb.sc);
+  return t >= 255.f ? 255 : (t > 0.f ? (int)t : 0);
+}
+
+// The smallest radix key k in [a, b] whose value falls in a value bin >= target (b + 1 if there is none).
+template <typename Tr>
+__device__ __forceinline__ uint32_t first_key_of_bin(uint32_t a, uint32_t b, int target, const ValueBins& vb) {
+  unsigned long long lo = a, hi = (unsigned long long)b + 1ull;   // the answer lies in [lo, hi]
+#pragma unroll 1
+  while (lo < hi) {
+    const unsigned long long mid = (lo + hi) >> 1;
+    if (value_bin(Tr::value_of_rkey((uint32_t)mid), vb) >= target) hi = mid;
+    else lo = mid + 1ull;
+  }
+  return (uint32_t)lo;
+}
+
+// The radix rounds after a value-bin round: the key range [klo, khi] of the selected bin, and the first key
+// round (the byte holding the highest bit where klo and khi differ) with its prefix.
+struct KeyRange {
+  uint32_t klo, khi;
+  int shift;         // first key round's shift; -1: the bin holds a single key
+  uint32_t prefix;   // key bits above the first round's byte (shared by every key of the range)
+};
+
+template <typename Tr>
+__device__ __forceinline__ KeyRange key_range_of_bin(int b, uint32_t kxlo, uint32_t kxhi, const ValueBins& vb) {
+  KeyRange r;
+  r.klo = first_key_of_bin<Tr>(kxlo, kxhi, b, vb);
+  r.khi = b >= 255 ? kxhi : first_key_of_bin<Tr>(kxlo, kxhi, b + 1, vb) - 1u;
+  const uint32_t d = r.klo ^ r.khi;
+  if (d == 0u) {
+    r.shift = -1;
+    r.prefix = r.klo;
+  } else {
+    r.shift = (31 - __clz((int)d)) & ~7;
+    r.prefix = r.shift + 8 >= 32 ? 0u : (r.klo & (0xFFFFFFFFu << (r.shift + 8)));
+  }
+  return r;
+}
+
 template <typename T, int NT, int MODE>
 struct RowEngine {
   using Tr = Traits<T>;
@@ -463,10 +527,13 @@ struct RowEngine {
   // want_mass: also histogram masses (mass_above / mass_eq are valid).
   // floor_rk: keys below it are left out of the histograms. The caller passes a floor only when the goal is
   //   reached within the keys at or above it, so the group found and its counts do not change.
+  // xmin: the row's smallest value. When the candidates span a finite range, the first round bins values
+  //   linearly over it (ValueBins) and the key rounds then refine the selected bin's key range; otherwise the
+  //   rounds take the key bytes from the top.
   // Each round visits only the vectors of the thread's chunk that held an element matching the previous
   // round's prefix (chunks of at most 64 vectors; longer chunks visit every vector).
   __device__ RadixOut radix_search(bool mass_mode, unsigned long long goal, float goal_p, bool want_mass, float M,
-                                   float c1, uint32_t floor_rk = 0u) {
+                                   float c1, uint32_t floor_rk, float xmin) {
     RadixOut out{};
     out.ok = 1;
     uint32_t prefix = 0;
@@ -477,7 +544,14 @@ struct RowEngine {
     uint32_t cand[2];
     cand[0] = nvec >= 32 ? 0xFFFFFFFFu : ((1u << nvec) - 1u);
     cand[1] = nvec >= 64 ? 0xFFFFFFFFu : (nvec > 32 ? ((1u << (nvec - 32)) - 1u) : 0u);
-    for (int shift = Tr::KB - 8; shift >= 0; shift -= 8) {
+    // the candidates' value range: [max(xmin, value of floor_rk), M]
+    const float xlo = floor_rk ? fmaxf(xmin, Tr::value_of_rkey(floor_rk)) : xmin;
+    const ValueBins vb = make_value_bins(xlo, M);
+    bool vround = vb.sc > 0.f;          // this round bins values
+    bool first = true;
+    uint32_t klo = 0u, khi = 0xFFFFFFFFu;
+    int shift = vround ? 0 : Tr::KB - 8;
+    for (;;) {
       const int par = xc & 1;
       uint32_t* hc = sh.hcnt[par];
       uint32_t* hl = sh.hlo[par];
@@ -501,9 +575,10 @@ struct RowEngine {
       };
       auto visit = [&](int64_t, float x) -> bool {
         const uint32_t rk = Tr::rkey_of_value(x);
-        const bool match = (rk & hmask) == (prefix & hmask) && rk >= floor_rk;
+        const bool match = vround ? rk >= floor_rk
+                                  : ((rk & hmask) == (prefix & hmask) && rk >= floor_rk && rk >= klo && rk <= khi);
         if (match) {
-          const uint32_t bin = (rk >> shift) & 255u;
+          const uint32_t bin = vround ? (uint32_t)value_bin(x, vb) : ((rk >> shift) & 255u);
           if (bin != run_bin) {
             flush();
             run_bin = bin;
@@ -555,7 +630,7 @@ struct RowEngine {
       }
       exchange_done();
       __syncthreads();
-      if (mass_mode && goal_p >= 0.f && shift == Tr::KB - 8) {
+      if (mass_mode && goal_p >= 0.f && first) {
         if (warp == 0) {
           unsigned long long tot = 0;
           for (int b = lane; b < 256; b += 32) tot += sh.gmass[b];
@@ -565,6 +640,7 @@ struct RowEngine {
         __syncthreads();
         goal = sh.bq[3];
       }
+      first = false;
       // warp 0: suffix scan from the top bin; lane l covers bins 255-8l .. 248-8l
       if (warp == 0) {
         uint32_t lc = 0;
@@ -616,10 +692,23 @@ struct RowEngine {
       out.cnt_eq = sh.gcnt[sel];
       out.mass_eq = sh.gmass[sel];
       __syncthreads();
-      prefix |= sel << shift;
       cnt_above += ac;
       mass_above += am;
       if (mass_mode) goal -= am; else goal -= ac;
+      if (vround) {
+        // the selected bin's key range (every thread bisects the same monotone function)
+        const KeyRange kr = key_range_of_bin<Tr>((int)sel, Tr::rkey_of_value(xlo), Tr::rkey_of_value(M), vb);
+        vround = false;
+        klo = kr.klo;
+        khi = kr.khi;
+        prefix = kr.prefix;
+        if (kr.shift < 0) break;   // one key: the group
+        shift = kr.shift;
+        continue;
+      }
+      prefix |= sel << shift;
+      if (shift == 0) break;
+      shift -= 8;
     }
     out.rk = prefix;
     out.cnt_above = cnt_above;
@@ -957,7 +1046,8 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
       pending = true;
     };
 
-  // ---------------- P1: maximum (minimum for cut descriptors), non-finite check ----------------
+  // ---------------- P1: maximum (minimum for cut descriptors and radix searches), non-finite check --------
+  constexpr bool kMin = (MODE & (MODE_CUT | MODE_SELECT | MODE_SAMPLE | MODE_TOPN | MODE_KEPT)) != 0;
   float mx = -INFINITY, mn = INFINITY, nf = 0.f;
   {
     const int nfull = E.thr_n / VE;
@@ -972,7 +1062,7 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
         for (int h = 0; h < 4; ++h) {
           const __nv_bfloat162 a = Tr::pair(w[h]);
           mx2 = __hmax2(mx2, a);
-          if (MODE & MODE_CUT) mn2 = __hmin2(mn2, a);
+          if (kMin) mn2 = __hmin2(mn2, a);
           nf2 = kSel ? __hmax2(nf2, __hneu2(a, a)) : __hfma2(a, zero2, nf2);
         }
       }
@@ -987,7 +1077,7 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
 #pragma unroll
         for (int i = 0; i < VE; ++i) {
           mx = fmaxf(mx, x[i]);
-          if (MODE & MODE_CUT) mn = fminf(mn, x[i]);
+          if (kMin) mn = fminf(mn, x[i]);
           // x * 0 is NaN for +-inf and NaN; the top-k select only rejects NaN
           nf = kSel ? (x[i] != x[i] ? 1.f : nf) : fmaf(x[i], 0.f, nf);
         }
@@ -1001,7 +1091,7 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
       for (int i = 0; i < VE; ++i) {
         if (i < tail) {
           mx = fmaxf(mx, x[i]);
-          if (MODE & MODE_CUT) mn = fminf(mn, x[i]);
+          if (kMin) mn = fminf(mn, x[i]);
           nf = kSel ? (x[i] != x[i] ? 1.f : nf) : fmaf(x[i], 0.f, nf);
         }
       }
@@ -1209,7 +1299,7 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
         // ---------------- radix rounds where the cut leaves the maximum's group ----------------
         if (plan.ck_mode == 2) {
           // a count search; the kept mass, where the top-p goal needs it, in one pass after it
-          const RadixOut r = E.radix_search(false, plan.ck.need, -1.f, false, M, c1);
+          const RadixOut r = E.radix_search(false, plan.ck.need, -1.f, false, M, c1, 0u, Mmin);
           {
             if (!r.ok) plan.status = VSAMP_ERR_INVALID_ARG;
             const unsigned long long need = plan.ck.need - r.cnt_above;
@@ -1224,7 +1314,7 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
         if (plan.cp_mode == 2 && plan.status == VSAMP_OK) {
           // after a top-k cut the goal lies within the keys at or above its pivot
           const uint32_t floor_rk = plan.ck_mode == 2 ? plan.ck.rk : 0u;
-          const RadixOut r = E.radix_search(true, plan.cp_goal, plan.goal_p, true, M, c1, floor_rk);
+          const RadixOut r = E.radix_search(true, plan.cp_goal, plan.goal_p, true, M, c1, floor_rk, Mmin);
           {
             if (!r.ok) plan.status = VSAMP_ERR_INVALID_ARG;
             const unsigned long long wP = mass_fx(ex2_approx((Tr::value_of_rkey(r.rk) - M) * c1));
@@ -1254,7 +1344,7 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
       } else if (ksel >= n) {
         fin = Cut{0u, 0, (unsigned long long)n, 0, 0, 1};
       } else {
-        const RadixOut r = E.radix_search(false, (unsigned long long)ksel, -1.f, false, M, c1);
+        const RadixOut r = E.radix_search(false, (unsigned long long)ksel, -1.f, false, M, c1, 0u, Mmin);
         if (!r.ok) status = VSAMP_ERR_INVALID_ARG;
         fin = Cut{r.rk, r.cnt_above, (unsigned long long)ksel - r.cnt_above, r.cnt_eq, 0, 0};
       }

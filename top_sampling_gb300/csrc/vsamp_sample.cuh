@@ -60,6 +60,10 @@ struct SampleCtl {
   int32_t shift;            // REQ_HIST: bin = (key >> shift) & 255 for keys matching prefix above shift + 8
   uint32_t prefix;           // REQ_HIST: the prefix; REQ_MASS: keys above it are summed
   uint32_t floor_rk;        // REQ_HIST: keys below it are left out
+  int32_t hfirst;           // REQ_HIST: the first round of a search (every vector is visited)
+  int32_t vround;           // REQ_HIST: bins are value bins (vxlo, vsc) instead of key bytes
+  float vxlo, vsc;
+  uint32_t klo, khi;        // REQ_HIST key rounds: only keys in [klo, khi] (the selected value bin)
   uint32_t kmin32;          // min-p threshold (fp32 key space)
   uint32_t bk;              // prune bound on the Philox word
   uint32_t rid, st_lo, st_hi, k0, k1;
@@ -70,7 +74,7 @@ struct SampleCtl {
 
 struct SampleSmem {
   unsigned long long lbar[2][kMaxDataWarps];   // per slice buffer and data warp: its region has landed
-  unsigned long long xbar[2];            // cluster exchange: one arrival per CTA, per exchange parity
+  unsigned long long xbar[2];            // cluster exchange: the local arrival and the C messages' bytes, per parity
   uint4 xm[2][16][2];                    // cluster exchange mailboxes: each CTA's 32-byte message
   uint4 dp[kMaxDataWarps][2];            // data -> control partials (P1, P2, tie counts)
   uint4 ap[kMaxDataWarps];               // P4 partials: score, index, scaled logit, boundary index
@@ -91,11 +95,15 @@ __host__ __device__ constexpr int sample_slice_offset() {
 }
 
 // ------------------------------------------------------------------------------------------------
-// Control warp: cluster exchange of one 32-byte message per CTA. Lane r < C writes this CTA's message
-// into CTA r's mailbox and arrives on CTA r's mbarrier; lane 0 then waits for the C arrivals on this
-// CTA's own (bounded). Afterwards every lane may read xm[par][0 .. C-1]. Returns false on timeout.
+// Control warp: cluster exchange of one 32-byte message per CTA. Lane 0 arms this CTA's mbarrier for the
+// C messages (C * 32 bytes, its own arrival the only one); lane r < C writes this CTA's message into CTA r's
+// mailbox with two asynchronous 16-byte stores that count their bytes on CTA r's mbarrier, so the sender
+// waits neither for the writes nor for its own earlier memory operations; lane 0 then waits (bounded) for
+// this CTA's barrier. Afterwards every lane may read xm[par][0 .. C-1]. Returns false on timeout.
 // Mailboxes are double-buffered by exchange parity: a CTA cannot reach exchange n + 2 before every peer
-// has sent exchange n + 1, which each does only after reading exchange n.
+// has sent exchange n + 1, which each does only after reading exchange n. A peer's bytes may land before
+// the local arming; the barrier's transaction count then runs below zero and the phase still cannot
+// complete before the local arrival.
 // ------------------------------------------------------------------------------------------------
 struct ClusterXchg {
   int n = 0;   // exchanges so far
@@ -110,11 +118,12 @@ struct ClusterXchg {
       __syncwarp();
       return true;
     }
+    if (lane == 0) mbar_arrive_expect_tx(&sh.xbar[pb], (uint32_t)(C * 32));
     if (lane < C) {
       const uint32_t dst = dsmem_map(&sh.xm[pb][crank][0], (uint32_t)lane);
-      dsmem_store_v4(dst, m0.x, m0.y, m0.z, m0.w);
-      dsmem_store_v4(dst + 16u, m1.x, m1.y, m1.z, m1.w);
-      mbar_arrive_remote(dsmem_map(&sh.xbar[pb], (uint32_t)lane));
+      const uint32_t bar = dsmem_map(&sh.xbar[pb], (uint32_t)lane);
+      dsmem_store_async_v4(dst, m0, bar);
+      dsmem_store_async_v4(dst + 16u, m1, bar);
     }
     uint32_t ok = 1u;
     if (lane == 0) ok = mbar_wait_cluster_bounded(&sh.xbar[pb], ph, wait_cycles) ? 1u : 0u;
@@ -129,40 +138,75 @@ __device__ __forceinline__ unsigned long long u64_of(uint32_t lo, uint32_t hi) {
 }
 
 // ------------------------------------------------------------------------------------------------
-// P1 over one thread's vectors: the maximum, and nf != 0 when a value is NaN or +-inf (x * 0 is NaN
-// exactly for those). bf16 pairs are handled packed.
+// Control warp: the draw over every kept token of a row (x > xP, or x == xP and index <= It), read from
+// global memory, when the prune bound did not certify the cluster's winner. Out of line: it runs with
+// probability ~1e-9 per row and would otherwise hold registers in the control warp's common path.
 // ------------------------------------------------------------------------------------------------
 template <typename T>
-static __device__ __noinline__ float max_pass(const uint4* mine, int thr_n, float& nf_out) {
+static __device__ __noinline__ ArgMax control_fallback_draw(const unsigned char* xrow, int64_t n, float xP, int32_t It,
+                                                            float M, float invT, uint32_t rid, uint64_t st, uint64_t sd) {
+  using Tr = Traits<T>;
+  const int lane = threadIdx.x & 31;
+  const PhiloxKey key{(uint32_t)sd, (uint32_t)(sd >> 32)};
+  const uint32_t st_lo = (uint32_t)st, st_hi = (uint32_t)(st >> 32);
+  float fs = -INFINITY, fsv = 0.f;
+  int32_t fi = 0x7FFFFFFF;
+  for (int64_t e = lane; e < n; e += 32) {
+    const float xv = Tr::load_global(xrow, e);
+    if (!(xv > xP || (xv == xP && e <= (int64_t)It))) continue;
+    const uint4 w4 = philox4x32_10(make_uint4((uint32_t)(e >> 2), rid, st_lo, st_hi), key);
+    const uint32_t bw = philox_word(w4, (int)(e & 3));
+    const float sv = (xv - M) * invT;
+    const float score = gumbel_score(sv, bw);
+    if (argmax_better(score, (int32_t)e, fs, fi)) { fs = score; fi = (int32_t)e; fsv = sv; }
+  }
+  return warp_argmax(ArgMax{fs, fi, fsv});
+}
+
+// ------------------------------------------------------------------------------------------------
+// P1 over one thread's vectors: the maximum, the minimum (mn_out; the first radix round bins values over
+// the row's range), and nf != 0 when a value is NaN or +-inf (x * 0 is NaN exactly for those). bf16 pairs
+// are handled packed.
+// ------------------------------------------------------------------------------------------------
+template <typename T>
+static __device__ __noinline__ float max_pass(const uint4* mine, int thr_n, float& nf_out, float& mn_out) {
   using Tr = Traits<T>;
   constexpr int VE = Tr::VE;
   const int nfull = thr_n / VE;
-  float mx = -INFINITY, nf = 0.f;
+  float mx = -INFINITY, mn = INFINITY, nf = 0.f;
   if constexpr (VE == 8) {
     const __nv_bfloat162 zero2 = __float2bfloat162_rn(0.f);
-    __nv_bfloat162 mxa = __float2bfloat162_rn(-INFINITY), mxb = mxa, nfa = zero2, nfb = zero2;
+    __nv_bfloat162 mxa = __float2bfloat162_rn(-INFINITY), mxb = mxa, mna = __float2bfloat162_rn(INFINITY),
+                   mnb = mna, nfa = zero2, nfb = zero2;
     for (int j = 0; j < nfull; ++j) {
       const uint4 v = mine[j];
       mxa = __hmax2(mxa, __hmax2(Tr::pair(v.x), Tr::pair(v.y)));
       mxb = __hmax2(mxb, __hmax2(Tr::pair(v.z), Tr::pair(v.w)));
+      mna = __hmin2(mna, __hmin2(Tr::pair(v.x), Tr::pair(v.y)));
+      mnb = __hmin2(mnb, __hmin2(Tr::pair(v.z), Tr::pair(v.w)));
       nfa = __hfma2(Tr::pair(v.x), zero2, __hfma2(Tr::pair(v.y), zero2, nfa));
       nfb = __hfma2(Tr::pair(v.z), zero2, __hfma2(Tr::pair(v.w), zero2, nfb));
     }
     mxa = __hmax2(mxa, mxb);
+    mna = __hmin2(mna, mnb);
     nfa = __hadd2(nfa, nfb);
     mx = fmaxf(__low2float(mxa), __high2float(mxa));
+    mn = fminf(__low2float(mna), __high2float(mna));
     nf = (__low2float(nfa) != 0.f || __high2float(nfa) != 0.f) ? 1.f : 0.f;
   } else {
-    float mb = -INFINITY, nb = 0.f;
+    float mb = -INFINITY, nb = 0.f, lb = INFINITY;
     for (int j = 0; j < nfull; ++j) {
       float x[VE];
       Tr::values(mine[j], x);
       mx = fmaxf(mx, fmaxf(x[0], x[1]));
       mb = fmaxf(mb, fmaxf(x[2], x[3]));
+      mn = fminf(mn, fminf(x[0], x[1]));
+      lb = fminf(lb, fminf(x[2], x[3]));
       nf = fmaf(x[0], 0.f, fmaf(x[1], 0.f, nf));
       nb = fmaf(x[2], 0.f, fmaf(x[3], 0.f, nb));
     }
     mx = fmaxf(mx, mb);
+    mn = fminf(mn, lb);
     nf += nb;
   }
   const int tail = thr_n - nfull * VE;
@@ -171,9 +215,10 @@ static __device__ __noinline__ float max_pass(const uint4* mine, int thr_n, floa
     Tr::values(mine[nfull], x);
 #pragma unroll
     for (int i = 0; i < VE; ++i)
-      if (i < tail) { mx = fmaxf(mx, x[i]); nf = fmaf(x[i], 0.f, nf); }
+      if (i < tail) { mx = fmaxf(mx, x[i]); mn = fminf(mn, x[i]); nf = fmaf(x[i], 0.f, nf); }
   }
   nf_out = nf;
+  mn_out = mn;
   return mx;
 }
 
@@ -271,8 +316,8 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
       mbar_init(&sh.lbar[0][w], 1);
       mbar_init(&sh.lbar[1][w], 1);
     }
-    mbar_init(&sh.xbar[0], (uint32_t)C);
-    mbar_init(&sh.xbar[1], (uint32_t)C);
+    mbar_init(&sh.xbar[0], 1u);
+    mbar_init(&sh.xbar[1], 1u);
     sh.acnt[0] = 0u;
     sh.acnt[1] = 0u;
     fence_mbar_init();
@@ -383,10 +428,12 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
       // ---- P1: maximum and non-finite check ----
       {
         float nf;
-        float mx = max_pass<T>(mine, thr_n, nf);
+        float mn;
+        float mx = max_pass<T>(mine, thr_n, nf, mn);
         const uint32_t flags = __reduce_or_sync(kFullMask, ((nf != 0.f) ? 1u : 0u) | (timeout ? 2u : 0u));
         mx = warp_max_f(mx);
-        if (lane == 0) sh.dp[warp][0] = make_uint4(__float_as_uint(mx), flags, 0u, 0u);
+        mn = -warp_max_f(-mn);
+        if (lane == 0) sh.dp[warp][0] = make_uint4(__float_as_uint(mx), flags, __float_as_uint(mn), 0u);
         nb_arrive(SB_P1, kSampleThreads);
       }
       nb_sync(SB_CTL, kSampleThreads);
@@ -447,6 +494,9 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
           const uint32_t prefix = sh.ctl.prefix;
           const uint32_t floor_rk = sh.ctl.floor_rk;
           const float c1 = sh.ctl.c1;
+          const bool vround = sh.ctl.vround != 0;
+          const ValueBins vb{sh.ctl.vxlo, sh.ctl.vsc};
+          const uint32_t klo = sh.ctl.klo, khi = sh.ctl.khi;
           const int hi_shift = shift + 8;
           const uint32_t hmask = hi_shift >= 32 ? 0u : (0xFFFFFFFFu << hi_shift);
           uint32_t* hc = sh.hcnt[hp];
@@ -474,9 +524,11 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
             for (int i = 0; i < VE; ++i) {
               if (j * VE + i >= thr_n) break;
               const uint32_t rk = Tr::rkey_of_value(x[i]);
-              if ((rk & hmask) == (prefix & hmask) && rk >= floor_rk) {
+              const bool match = vround ? rk >= floor_rk
+                                        : ((rk & hmask) == (prefix & hmask) && rk >= floor_rk && rk >= klo && rk <= khi);
+              if (match) {
                 any = true;
-                const uint32_t bin = (rk >> shift) & 255u;
+                const uint32_t bin = vround ? (uint32_t)value_bin(x[i], vb) : ((rk >> shift) & 255u);
                 if (bin != run_bin) {
                   flush();
                   run_bin = bin;
@@ -490,7 +542,7 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
             return any;
           };
           if (masked) {
-            if (shift == Tr::KB - 8) {   // the first round of a search visits every vector
+            if (sh.ctl.hfirst) {   // the first round of a search visits every vector
               cand0 = nvec_thr >= 32 ? 0xFFFFFFFFu : ((1u << nvec_thr) - 1u);
               cand1 = nvec_thr >= 64 ? 0xFFFFFFFFu : (nvec_thr > 32 ? ((1u << (nvec_thr - 32)) - 1u) : 0u);
             }
@@ -708,33 +760,38 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
       if (p.row_id) rid = p.row_id[row];
       int passes = 1, rounds = 0, path = p.tma ? 0 : PATH_NOTMA;
 
-      // ---- P1 partials -> cluster maximum ----
+      // ---- P1 partials -> cluster maximum and minimum ----
       nb_sync(SB_P1, kSampleThreads);
-      float M;
+      float M, Mmin;
       uint32_t flags;
       {
-        float m = -INFINITY;
+        float m = -INFINITY, m2 = INFINITY;
         uint32_t fl = 0u;
         if (lane < kDataWarps) {
           const uint4 v = sh.dp[lane][0];
           m = __uint_as_float(v.x);
           fl = v.y;
+          m2 = __uint_as_float(v.z);
         }
         m = warp_max_f(m);
+        m2 = -warp_max_f(-m2);
         fl = __reduce_or_sync(kFullMask, fl);
         if (!dead) {
-          if (!X.run(sh, C, crank, make_uint4(__float_as_uint(m), fl, 0u, 0u), make_uint4(0u, 0u, 0u, 0u),
-                     p.wait_cycles))
+          if (!X.run(sh, C, crank, make_uint4(__float_as_uint(m), fl, __float_as_uint(m2), 0u),
+                     make_uint4(0u, 0u, 0u, 0u), p.wait_cycles))
             dead = true;
         }
         m = -INFINITY;
+        m2 = INFINITY;
         fl = dead ? 2u : 0u;
         if (!dead && lane < C) {
           const uint4 v = sh.xm[X.par() ^ 1][lane][0];
           m = __uint_as_float(v.x);
           fl |= v.y;
+          m2 = __uint_as_float(v.z);
         }
         M = warp_max_f(m);
+        Mmin = -warp_max_f(-m2);
         flags = __reduce_or_sync(kFullMask, fl);
         if (flags & 2u) dead = true;
       }
@@ -886,7 +943,13 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
         uint32_t prefix = 0;
         unsigned long long cnt_above = 0, mass_above = 0;
         const bool hist_mass = want_mass || mass_mode;
-        for (int shift = Tr::KB - 8; shift >= 0; shift -= 8) {
+        // the first round bins values linearly over the candidates' range when it is finite (ValueBins)
+        const float xlo = floor_rk ? fmaxf(Mmin, Tr::value_of_rkey(floor_rk)) : Mmin;
+        const ValueBins vb = make_value_bins(xlo, M);
+        bool vround = vb.sc > 0.f, first = true;
+        uint32_t klo = 0u, khi = 0xFFFFFFFFu;
+        int shift = vround ? 0 : Tr::KB - 8;
+        for (;;) {
           const int hp = hround & 1;
           ++hround;
           for (int b = lane; b < 256; b += 32) {
@@ -901,6 +964,12 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
             sh.ctl.hist_mass = hist_mass ? 1 : 0;
             sh.ctl.prefix = prefix;
             sh.ctl.floor_rk = floor_rk;
+            sh.ctl.hfirst = first ? 1 : 0;
+            sh.ctl.vround = vround ? 1 : 0;
+            sh.ctl.vxlo = vb.xlo;
+            sh.ctl.vsc = vb.sc;
+            sh.ctl.klo = klo;
+            sh.ctl.khi = khi;
           }
           __syncwarp();
           nb_arrive(SB_CTL, kSampleThreads);
@@ -948,7 +1017,7 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
               if (hist_mass) bm[i] += u64_of(ll[i], hh[i]);
             }
           }
-          if (mass_mode && gp >= 0.f && shift == Tr::KB - 8) {
+          if (mass_mode && gp >= 0.f && first) {
             unsigned long long tot = 0;
 #pragma unroll
             for (int i = 0; i < 8; ++i) tot += bm[i];
@@ -993,10 +1062,24 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
           meq = __shfl_sync(kFullMask, meq, src);
           out.cnt_eq = ceq;
           out.mass_eq = meq;
-          prefix |= sel << shift;
           cnt_above += ac;
           mass_above += am;
           if (mass_mode) goal -= am; else goal -= ac;
+          first = false;
+          if (vround) {
+            // the selected value bin's key range, then key rounds inside it
+            const KeyRange kr = key_range_of_bin<Tr>((int)sel, Tr::rkey_of_value(xlo), Tr::rkey_of_value(M), vb);
+            vround = false;
+            klo = kr.klo;
+            khi = kr.khi;
+            prefix = kr.prefix;
+            if (kr.shift < 0) break;   // one key: the group
+            shift = kr.shift;
+            continue;
+          }
+          prefix |= sel << shift;
+          if (shift == 0) break;
+          shift -= 8;
         }
         out.rk = prefix;
         out.cnt_above = cnt_above;
@@ -1251,21 +1334,8 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
         // the prune bound did not certify the draw (probability ~1e-9): this warp evaluates every kept
         // token of the row from global memory
         path |= PATH_FALLBACK;
-        const int32_t Ig = cut < 0 ? kAllIndex : cut;
-        const PhiloxKey key{(uint32_t)sd, (uint32_t)(sd >> 32)};
-        const uint32_t st_lo = (uint32_t)st, st_hi = (uint32_t)(st >> 32);
-        float fs = -INFINITY, fsv = 0.f;
-        int32_t fi = 0x7FFFFFFF;
-        for (int64_t e = lane; e < n; e += 32) {
-          const float xv = Tr::load_global(p.x, (int64_t)row * p.ld + e);
-          if (!(xv > xP || (xv == xP && e <= (int64_t)Ig))) continue;
-          const uint4 w4 = philox4x32_10(make_uint4((uint32_t)(e >> 2), rid, st_lo, st_hi), key);
-          const uint32_t bw = philox_word(w4, (int)(e & 3));
-          const float sv = (xv - M) * invT;
-          const float score = gumbel_score(sv, bw);
-          if (argmax_better(score, (int32_t)e, fs, fi)) { fs = score; fi = (int32_t)e; fsv = sv; }
-        }
-        const ArgMax fb = warp_argmax(ArgMax{fs, fi, fsv});
+        const ArgMax fb = control_fallback_draw<T>(p.x + (int64_t)row * p.ld * ES, n, xP, cut < 0 ? kAllIndex : cut, M,
+                                                   invT, rid, st, sd);
         out_token = fb.idx;
         out_s = fb.s;
       }

@@ -27,8 +27,9 @@ __global__ void __launch_bounds__(kSplitThreads) select_stream_kernel(const Para
     const int32_t k = p.k_sel ? p.k_sel[row] : p.k_max;
     const unsigned char* xr = p.x + row * p.ld * Tr::ESIZE;
     const int64_t nvec = (n + VE - 1) / VE;
-    // ---- NaN inside the length ----
+    // ---- NaN inside the length; the range of the values (the radix search's first round) ----
     uint32_t nan = 0;
+    float mx = -INFINITY, mn = INFINITY;
     for (int64_t vi = t; vi < nvec; vi += kSplitThreads) {
       uint4 v;
       int cnt = load_vec<T, false>(p, xr, vi * VE, v);
@@ -36,9 +37,17 @@ __global__ void __launch_bounds__(kSplitThreads) select_stream_kernel(const Para
       float x[VE];
       Tr::values(v, x);
 #pragma unroll
-      for (int i = 0; i < VE; ++i) nan |= (i < cnt && x[i] != x[i]) ? 1u : 0u;
+      for (int i = 0; i < VE; ++i) {
+        if (i < cnt) {
+          nan |= x[i] != x[i] ? 1u : 0u;
+          mx = fmaxf(mx, x[i]);
+          mn = fminf(mn, x[i]);
+        }
+      }
     }
     nan = __syncthreads_or(nan);
+    const float Mrow = block_max_f(mx, sh);
+    const float Mmin = -block_max_f(-mn, sh);
     int status = VSAMP_OK;
     if (bad_len) status = VSAMP_ERR_INVALID_ARG;
     else if (nan) status = VSAMP_ERR_NONFINITE;
@@ -49,7 +58,8 @@ __global__ void __launch_bounds__(kSplitThreads) select_stream_kernel(const Para
       unsigned long long need = 0;
       bool all = (int64_t)k >= n;
       if (!all) {
-        RowPlanner<T> P{p, sh, row, n, 0.f, 0.f};
+        RowPlanner<T> P{p, sh, row, n, Mrow, 0.f};
+        P.Mmin = Mmin;
         const RadixOut r = P.radix(false, (unsigned long long)k, -1.f, false);
         if (!r.ok) {
           status = VSAMP_ERR_INVALID_ARG;   // cannot happen with consistent counts

@@ -182,6 +182,7 @@ struct RowPlanner {
   int64_t row, n;
   float M, c1;
   int passes = 0, rounds = 0;
+  float Mmin = -INFINITY;   // the row's minimum (-inf when unknown: the first round then takes key bytes)
 
   // visits every element of the row in tiles of 256 vectors: f(index, value, valid); tile order is index order
   template <typename F>
@@ -209,7 +210,8 @@ struct RowPlanner {
     }
   }
 
-  // radix search over the whole row (as the row engine's, with the row read from L2 by this CTA)
+  // radix search over the whole row (as the row engine's, with the row read from L2 by this CTA): a first
+  // round of value bins over [Mmin, M] when that range is finite, then key rounds inside the selected bin
   __device__ __noinline__ RadixOut radix(bool mass_mode, unsigned long long goal, float goal_p, bool want_mass) {
     RadixOut out{};
     out.ok = 1;
@@ -217,7 +219,11 @@ struct RowPlanner {
     unsigned long long cnt_above = 0, mass_above = 0;
     const bool hist_mass = want_mass || mass_mode;
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    for (int shift = Tr::KB - 8; shift >= 0; shift -= 8) {
+    const ValueBins vb = make_value_bins(Mmin, M);
+    bool vround = vb.sc > 0.f, first = true;
+    uint32_t klo = 0u, khi = 0xFFFFFFFFu;
+    int shift = vround ? 0 : Tr::KB - 8;
+    for (;;) {
       __syncthreads();
       for (int b = t; b < 256; b += kSplitThreads) { sh.hcnt[b] = 0; sh.hlo[b] = 0; sh.hhi[b] = 0; }
       __syncthreads();
@@ -241,8 +247,8 @@ struct RowPlanner {
         for (int i = 0; i < VE; ++i) {
           if (i >= cnt) break;
           const uint32_t rk = Tr::rkey_of_value(x[i]);
-          if ((rk & hmask) == (prefix & hmask)) {
-            const uint32_t bin = (rk >> shift) & 255u;
+          if (vround || ((rk & hmask) == (prefix & hmask) && rk >= klo && rk <= khi)) {
+            const uint32_t bin = vround ? (uint32_t)value_bin(x[i], vb) : ((rk >> shift) & 255u);
             if (bin != run_bin) { flush(); run_bin = bin; run_cnt = 0; run_mass = 0; }
             ++run_cnt;
             if (hist_mass) run_mass += mass_fx_split(ex2_approx((x[i] - M) * c1));
@@ -254,7 +260,7 @@ struct RowPlanner {
       ++passes;
       ++rounds;
       __syncthreads();
-      if (mass_mode && goal_p >= 0.f && shift == Tr::KB - 8) {
+      if (mass_mode && goal_p >= 0.f && first) {
         unsigned long long tot = 0;
         for (int b = lane; b < 256; b += 32) tot += ((unsigned long long)sh.hhi[b] << 32) + sh.hlo[b];
         tot = warp_sum_u64(tot);
@@ -307,10 +313,24 @@ struct RowPlanner {
       const unsigned long long ac = sh.bq[0], am = sh.bq[1];
       out.cnt_eq = sh.hcnt[sel];
       out.mass_eq = ((unsigned long long)sh.hhi[sel] << 32) + sh.hlo[sel];
-      prefix |= sel << shift;
       cnt_above += ac;
       mass_above += am;
       if (mass_mode) goal -= am; else goal -= ac;
+      first = false;
+      if (vround) {
+        // the selected value bin's key range, then key rounds inside it
+        const KeyRange kr = key_range_of_bin<Tr>((int)sel, Tr::rkey_of_value(Mmin), Tr::rkey_of_value(M), vb);
+        vround = false;
+        klo = kr.klo;
+        khi = kr.khi;
+        prefix = kr.prefix;
+        if (kr.shift < 0) break;   // one key: the group
+        shift = kr.shift;
+        continue;
+      }
+      prefix |= sel << shift;
+      if (shift == 0) break;
+      shift -= 8;
     }
     __syncthreads();
     out.rk = prefix;
@@ -536,10 +556,6 @@ __device__ __forceinline__ PieceRec load_rec(const PieceRec* a) {
   r.mn = __uint_as_float(v1.x);
   return r;
 }
-
-// 4-bit draw code of a 16-byte vector from the smallest Philox word w of its tokens: min(clz(w), 15).
-// w < bk implies code(w) >= code(bk), so testing codes flags a superset of the vectors the prune bound keeps.
-__device__ __forceinline__ uint32_t draw_code(uint32_t w) { return min((uint32_t)__clz(w), 15u); }
 
 // Shared memory of a piece_kernel CTA: per warp, two 4 KB piece buffers and their mbarriers.
 struct PieceSmem {
@@ -831,21 +847,26 @@ static __device__ __forceinline__ void finish_row(const Params& p, const StreamW
     return k == t ? r0 : (k == t + kStreamThreads ? r1 : load_rec(recs + k));
   };
   // ---- combine the pieces: M and the flags, then S rescaled to M and the count of maxima ----
-  float m = -INFINITY;
+  float m = -INFINITY, mn = INFINITY;
   uint32_t flags = 0;   // 1: a non-finite value, 2: a load timed out
   for (int k = t; k < nchunks; k += kStreamThreads) {
     const PieceRec r = rec_at(k);
     if (r.m != r.m) flags |= r.cnt == kTimeoutCnt ? 3u : 1u;
-    else m = fmaxf(m, r.m);
+    else { m = fmaxf(m, r.m); mn = fminf(mn, r.mn); }
   }
   m = warp_max_f(m);
+  mn = -warp_max_f(-mn);
   flags = __reduce_or_sync(kFullMask, flags);
-  if (lane == 0) { sh.f[warp] = m; sh.u[warp][0] = flags; }
+  if (lane == 0) { sh.f[warp] = m; sh.u[warp][0] = flags; sh.u[warp][2] = __float_as_uint(mn); }
   __syncthreads();
-  float M = sh.f[0];
+  float M = sh.f[0], Mmin = __uint_as_float(sh.u[0][2]);
   flags = sh.u[0][0];
 #pragma unroll
-  for (int w = 1; w < kItemPieces; ++w) { M = fmaxf(M, sh.f[w]); flags |= sh.u[w][0]; }
+  for (int w = 1; w < kItemPieces; ++w) {
+    M = fmaxf(M, sh.f[w]);
+    Mmin = fminf(Mmin, __uint_as_float(sh.u[w][2]));
+    flags |= sh.u[w][0];
+  }
   const bool nonfin = flags != 0u;
   unsigned long long Sp = 0;
   uint32_t cMp = 0;
@@ -881,6 +902,7 @@ static __device__ __forceinline__ void finish_row(const Params& p, const StreamW
   const bool greedy = !(temp0 > 0.f);
   int path = p.tma ? 0 : PATH_NOTMA;
   RowPlanner<T> P{p, sh, row, n, M, c1};
+  P.Mmin = Mmin;
   P.passes = 1;
   auto write_outputs = [&](int32_t tok, float lp, int st, uint32_t kept) {
     if (t == 0) {

@@ -169,6 +169,19 @@ static vsamp_status dispatch(Params p, vsamp_dtype dt, int64_t B, cudaStream_t s
   return VSAMP_ERR_INVALID_ARG;
 }
 
+// Row statistics (MODE_LSE, MODE_LOGPROB): the streaming piece kernel, or the cluster row kernel for rows longer
+// than it takes (VSAMP_STATS_ROW=1 forces the row kernel)
+template <int MODE>
+static vsamp_status dispatch_stats(Params p, vsamp_dtype dt, int64_t B, cudaStream_t s) {
+  if (env_int("VSAMP_STATS_ROW", 0) == 0) {
+    vsamp_status st = VSAMP_ERR_UNSUPPORTED;
+    if (dt == VSAMP_F32) st = launch_stats<float, MODE>(p, B, 4, s);
+    else if (dt == VSAMP_BF16) st = launch_stats<__nv_bfloat16, MODE>(p, B, 2, s);
+    if (st != VSAMP_ERR_UNSUPPORTED) return st;
+  }
+  return dispatch<MODE>(p, dt, B, s);
+}
+
 static bool aligned16(const void* ptr, int64_t ld, int esize) {
   return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0 && ((ld * esize) & 15) == 0;
 }
@@ -318,7 +331,7 @@ vsamp_status vsamp_softmax_lse(const void* logits, vsamp_dtype dt, int64_t B, in
   p.row_max = row_max;
   p.row_logsum = row_logsum;
   p.row_status = row_status;
-  return dispatch<MODE_LSE>(p, dt, B, static_cast<cudaStream_t>(stream));
+  return dispatch_stats<MODE_LSE>(p, dt, B, static_cast<cudaStream_t>(stream));
 }
 
 vsamp_status vsamp_topk_select(const void* scores, vsamp_dtype dt, int64_t B, int64_t max_len, int64_t ld,
@@ -538,7 +551,7 @@ vsamp_status vsamp_logprob(const void* logits, vsamp_dtype dt, int64_t B, int64_
   p.token_in = token;
   p.logprob = out;
   p.row_status = row_status;
-  return dispatch<MODE_LOGPROB>(p, dt, B, s);
+  return dispatch_stats<MODE_LOGPROB>(p, dt, B, s);
 }
 
 vsamp_status vsamp_topn_logprobs(const void* logits, vsamp_dtype dt, int64_t B, int64_t V, int64_t ld,

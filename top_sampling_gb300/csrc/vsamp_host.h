@@ -63,6 +63,10 @@ vsamp_status launch_reject(Params p, int64_t B, cudaStream_t stream);
 // vsamp_topk_select's uncached path (rows longer than a cluster holds on chip)
 template <typename T>
 vsamp_status launch_select_stream(Params p, int64_t B, cudaStream_t stream);
+// vsamp_stats.cuh: row statistics by streaming pieces (MODE_LSE or MODE_LOGPROB); VSAMP_ERR_UNSUPPORTED for rows
+// longer than it takes
+template <typename T, int MODE>
+vsamp_status launch_stats(Params p, int64_t B, int esize, cudaStream_t stream);
 
 // vsamp_shard_merge's kernel (dtype-free)
 vsamp_status launch_shard_merge(const void* recs, const void* wins, int R, int64_t B, int64_t NP, int64_t V,

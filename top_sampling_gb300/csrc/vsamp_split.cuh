@@ -1110,8 +1110,9 @@ static __device__ __forceinline__ void piece_codes(int64_t e_begin, uint32_t k0,
 // ------------------------------------------------------------------------------------------------
 // Statistics of a partial piece, or of a piece of an unaligned row: the lanes' vectors from global memory, with
 // element counts per vector (out of line: the full-piece path keeps its registers). No winner, no codes.
+// kHeadOnly: only the record's first 16 bytes {m, cnt, s} are written (the piece minimum is left out).
 // ------------------------------------------------------------------------------------------------
-template <typename T>
+template <typename T, bool kHeadOnly = false>
 static __device__ __noinline__ void piece_stats_partial(const unsigned char* xr, int64_t V, int32_t tma,
                                                         int64_t e_begin, float c1, bool timeout, PieceRec* rec_out) {
   using Tr = Traits<T>;
@@ -1179,15 +1180,16 @@ static __device__ __noinline__ void piece_stats_partial(const unsigned char* xr,
   if (lane == 0) {
     uint4* o = reinterpret_cast<uint4*>(rec_out);
     o[0] = make_uint4(bad ? 0x7FC00000u : __float_as_uint(mc), timeout ? kTimeoutCnt : cm, (uint32_t)s, (uint32_t)(s >> 32));
-    o[1] = make_uint4(__float_as_uint(mn), 0u, 0u, 0u);
+    if (!kHeadOnly) o[1] = make_uint4(__float_as_uint(mn), 0u, 0u, 0u);
   }
 }
 
 // ------------------------------------------------------------------------------------------------
 // Piece pass of one warp over a full piece in shared memory: the record, and for a coded row the draw codes
-// (e_begin: the global index of the piece's first element, for the Philox counters).
+// (e_begin: the global index of the piece's first element, for the Philox counters). kHeadOnly: only the
+// record's head {m, 0, s}, without the piece minimum and the count of maxima (the row statistics alone).
 // ------------------------------------------------------------------------------------------------
-template <typename T>
+template <typename T, bool kHeadOnly = false>
 static __device__ __forceinline__ void piece_pass_full(const uint4* sbuf, int64_t e_begin, float c1,
                                                        bool timeout, bool coded, uint32_t k0, uint32_t k1,
                                                        uint32_t rid, uint32_t st_lo, uint32_t st_hi,
@@ -1207,7 +1209,7 @@ static __device__ __forceinline__ void piece_pass_full(const uint4* sbuf, int64_
       const uint4 v = sbuf[u * 32 + lane];
       const __nv_bfloat162 a = Tr::pair(v.x), b = Tr::pair(v.y), c = Tr::pair(v.z), d = Tr::pair(v.w);
       mx2 = __hmax2(mx2, __hmax2(__hmax2(a, b), __hmax2(c, d)));
-      mn2 = __hmin2(mn2, __hmin2(__hmin2(a, b), __hmin2(c, d)));
+      if (!kHeadOnly) mn2 = __hmin2(mn2, __hmin2(__hmin2(a, b), __hmin2(c, d)));
       nf2 = __hfma2(a, zero2, __hfma2(b, zero2, __hfma2(c, zero2, __hfma2(d, zero2, nf2))));
     }
     mt = fmaxf(__low2float(mx2), __high2float(mx2));
@@ -1222,12 +1224,12 @@ static __device__ __forceinline__ void piece_pass_full(const uint4* sbuf, int64_
       float x[VE];
       Tr::values(sbuf[u * 32 + lane], x);
       mt = fmaxf(mt, fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])));
-      mn = fminf(mn, fminf(fminf(x[0], x[1]), fminf(x[2], x[3])));
+      if (!kHeadOnly) mn = fminf(mn, fminf(fminf(x[0], x[1]), fminf(x[2], x[3])));
       nf = fmaf(x[0], 0.f, fmaf(x[1], 0.f, fmaf(x[2], 0.f, fmaf(x[3], 0.f, nf))));
     }
   }
   const float mc = warp_max_f(mt);
-  mn = -warp_max_f(-mn);
+  if (!kHeadOnly) mn = -warp_max_f(-mn);
   const bool bad = timeout || __any_sync(kFullMask, nf != 0.f);
   // ---- mass relative to the piece maximum (2^-40 fixed point per vector) and the count of maxima ----
   unsigned long long s = 0ull;
@@ -1250,7 +1252,8 @@ static __device__ __forceinline__ void piece_pass_full(const uint4* sbuf, int64_
       if constexpr (VE == 8) a = __fadd2_rn(__fadd2_rn(w2[0], w2[2]), __fadd2_rn(w2[1], w2[3]));
       else a = __fadd2_rn(w2[0], w2[1]);
       s += mass_fx_split(a.x + a.y);
-      if constexpr (VE == 8) {
+      if constexpr (kHeadOnly) {
+      } else if constexpr (VE == 8) {
         const __nv_bfloat162 M2 = __float2bfloat162_rn(mc);   // a bf16 value: exact
         cm2 += __heq2_mask(Tr::pair(v.x), M2) & 0x00010001u;
         cm2 += __heq2_mask(Tr::pair(v.y), M2) & 0x00010001u;
@@ -1264,12 +1267,12 @@ static __device__ __forceinline__ void piece_pass_full(const uint4* sbuf, int64_
     cm += (cm2 & 0xFFFFu) + (cm2 >> 16);
   }
   s = warp_sum_u64(s);
-  cm = warp_sum_u32(cm);
+  if (!kHeadOnly) cm = warp_sum_u32(cm);
   if (coded && !bad) piece_codes<T>(e_begin, k0, k1, rid, st_lo, st_hi, code_out);
   if (lane == 0) {
     uint4* o = reinterpret_cast<uint4*>(rec_out);
     o[0] = make_uint4(bad ? 0x7FC00000u : __float_as_uint(mc), timeout ? kTimeoutCnt : cm, (uint32_t)s, (uint32_t)(s >> 32));
-    o[1] = make_uint4(__float_as_uint(mn), 0u, 0u, 0u);
+    if (!kHeadOnly) o[1] = make_uint4(__float_as_uint(mn), 0u, 0u, 0u);
   }
 }
 

@@ -394,8 +394,14 @@ vsamp_status vsamp_sample(const void* logits, vsamp_dtype dt, int64_t B, int64_t
   p.logprob = logprob;
   p.row_status = row_status;
   p.stats = stats;
-  if (dt == VSAMP_F32) return launch_sample<float>(p, B, 4, static_cast<cudaStream_t>(stream));
-  return launch_sample<__nv_bfloat16>(p, B, 2, static_cast<cudaStream_t>(stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (env_int("VSAMP_SAMPLE_STREAM", 0) != 0) {
+    const vsamp_status ss = dt == VSAMP_F32 ? launch_sample_stream<float>(p, B, 4, s)
+                                            : launch_sample_stream<__nv_bfloat16>(p, B, 2, s);
+    if (ss != VSAMP_ERR_UNSUPPORTED) return ss;
+  }
+  if (dt == VSAMP_F32) return launch_sample<float>(p, B, 4, s);
+  return launch_sample<__nv_bfloat16>(p, B, 2, s);
 }
 
 size_t vsamp_sample_workspace_size(vsamp_dtype dt, int64_t B, int64_t V) {

@@ -67,6 +67,10 @@ vsamp_status launch_select_stream(Params p, int64_t B, cudaStream_t stream);
 // longer than it takes
 template <typename T, int MODE>
 vsamp_status launch_stats(Params p, int64_t B, int esize, cudaStream_t stream);
+// vsamp_sample_stream.cuh: the streaming sampler without a workspace; VSAMP_ERR_UNSUPPORTED for rows longer than
+// it takes
+template <typename T>
+vsamp_status launch_sample_stream(Params p, int64_t B, int esize, cudaStream_t stream);
 
 // vsamp_shard_merge's kernel (dtype-free)
 vsamp_status launch_shard_merge(const void* recs, const void* wins, int R, int64_t B, int64_t NP, int64_t V,

@@ -545,10 +545,11 @@ inline size_t split_workspace_bytes(int64_t B, int64_t V, int esize) {
   return sizeof(StreamHeader) + (size_t)B * np * sizeof(PieceRec) + (size_t)B * np * 32u * sizeof(uint32_t);
 }
 
-// A piece record written by the other launch: read through L2.
+// A piece record written by the other launch: read through L2 (kLocal: a record in this CTA's shared memory).
+template <bool kLocal = false>
 __device__ __forceinline__ PieceRec load_rec(const PieceRec* a) {
-  const uint4 v0 = __ldcg(reinterpret_cast<const uint4*>(a));
-  const uint4 v1 = __ldcg(reinterpret_cast<const uint4*>(a) + 1);
+  const uint4 v0 = kLocal ? reinterpret_cast<const uint4*>(a)[0] : __ldcg(reinterpret_cast<const uint4*>(a));
+  const uint4 v1 = kLocal ? reinterpret_cast<const uint4*>(a)[1] : __ldcg(reinterpret_cast<const uint4*>(a) + 1);
   PieceRec r;
   r.m = __uint_as_float(v0.x);
   r.cnt = v0.y;
@@ -816,9 +817,10 @@ static __device__ __noinline__ Cut plan_cut(RowPlanner<T>& P, bool greedy, float
 // ------------------------------------------------------------------------------------------------
 // Row finish: one CTA (all 256 threads) per row. The row's dependent memory accesses are batched: the piece
 // records and the draw codes come in one round of loads, and after the plan the boundary piece and the flagged
-// vectors in another.
+// vectors in another. kLocal: the records (ws.recs, rec_ld 0) and the codes (S.codes) are already in this
+// CTA's shared memory.
 // ------------------------------------------------------------------------------------------------
-template <typename T>
+template <typename T, bool kLocal = false>
 static __device__ __forceinline__ void finish_row(const Params& p, const StreamWs& ws, int64_t row, int nchunks,
                                                   FinishSmem& S) {
   using Tr = Traits<T>;
@@ -836,15 +838,15 @@ static __device__ __forceinline__ void finish_row(const Params& p, const StreamW
   const bool codes_staged = coded && nwords <= (int64_t)kCodeSmem;
   // ---- one round of loads: the thread's first two piece records and the row's codes into shared memory ----
   PieceRec r0{}, r1{};
-  if (t < nchunks) r0 = load_rec(recs + t);
-  if (t + kStreamThreads < nchunks) r1 = load_rec(recs + t + kStreamThreads);
-  if (codes_staged) {
+  if (t < nchunks) r0 = load_rec<kLocal>(recs + t);
+  if (t + kStreamThreads < nchunks) r1 = load_rec<kLocal>(recs + t + kStreamThreads);
+  if (codes_staged && !kLocal) {
     const uint32_t* src = ws.codes + row * nwords;
 #pragma unroll 4
     for (int w = t; w < (int)nwords; w += kStreamThreads) S.codes[w] = __ldcg(src + w);
   }
   auto rec_at = [&](int k) -> PieceRec {
-    return k == t ? r0 : (k == t + kStreamThreads ? r1 : load_rec(recs + k));
+    return k == t ? r0 : (k == t + kStreamThreads ? r1 : load_rec<kLocal>(recs + k));
   };
   // ---- combine the pieces: M and the flags, then S rescaled to M and the count of maxima ----
   float m = -INFINITY, mn = INFINITY;

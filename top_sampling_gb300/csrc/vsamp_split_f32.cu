@@ -2,9 +2,11 @@
 #include "vsamp_reject.cuh"
 #include "vsamp_select_stream.cuh"
 #include "vsamp_split_launch.cuh"
+#include "vsamp_sample_stream.cuh"
 #include "vsamp_stats.cuh"
 
 namespace vsamp {
+template vsamp_status launch_sample_stream<float>(Params, int64_t, int, cudaStream_t);
 template vsamp_status launch_stats<float, MODE_LSE>(Params, int64_t, int, cudaStream_t);
 template vsamp_status launch_stats<float, MODE_LOGPROB>(Params, int64_t, int, cudaStream_t);
 template vsamp_status launch_select_stream<float>(Params, int64_t, cudaStream_t);

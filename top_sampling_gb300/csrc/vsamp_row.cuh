@@ -1144,7 +1144,7 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
   const float Teff = temp > 0.f ? temp : 1.f;
   const float invT = 1.f / Teff;
   const float c1 = kLog2e * invT;
-  const bool minp_on = kCutLike && !greedy && minp > 0.f;
+  bool minp_on = kCutLike && !greedy && minp > 0.f;
   const unsigned long long one = 1ull << kMassShift;     // fixed-point mass of a maximum token
 
   // min-p keeps w >= minp  <=>  x >= x* = M + T ln(minp). x* is formed as an unevaluated sum hi + lo
@@ -1158,6 +1158,8 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
     const float lo = sl + pl;
     const float xf = lo > 0.f ? nextafterf(sh_, INFINITY) : sh_;
     plan.kmin32 = key_f32_bits(__float_as_uint(xf));
+    // a threshold at or below the row's minimum keeps every token: the filter is off
+    if (plan.kmin32 <= key_f32_bits(__float_as_uint(Mmin))) minp_on = false;
   }
 
   unsigned long long Sfx = 0, cM = 0;

@@ -804,7 +804,7 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
       const float Teff = greedy ? 1.f : temp;
       const float invT = 1.f / Teff;
       const float c1 = kLog2e * invT;
-      const bool minp_on = !greedy && minp > 0.f;
+      bool minp_on = !greedy && minp > 0.f;
       uint32_t kmin32 = 0u;
       if (minp_on && status == VSAMP_OK) {
         // min-p keeps w >= minp <=> x >= x* = M + T ln(minp), formed as an unevaluated sum; the threshold
@@ -817,6 +817,8 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
         const float lo = sl + pl;
         const float xf = lo > 0.f ? nextafterf(sh_, INFINITY) : sh_;
         kmin32 = key_f32_bits(__float_as_uint(xf));
+        // a threshold at or below the row's minimum keeps every token: the filter is off
+        if (kmin32 <= key_f32_bits(__float_as_uint(Mmin))) minp_on = false;
       }
       if (lane == 0) {
         sh.ctl.status = status;

@@ -728,7 +728,7 @@ static __device__ __noinline__ Cut plan_cut(RowPlanner<T>& P, bool greedy, float
   const unsigned long long one = 1ull << kMassShift;
   const uint32_t rkM = Tr::rkey_of_value(M);
   Cut fin{};
-  const bool minp_on = !greedy && minp > 0.f;
+  bool minp_on = !greedy && minp > 0.f;
   if (greedy) {
     fin = Cut{rkM, 0, 1, cM, one, 0};
     path |= PATH_MAXGROUP;
@@ -779,12 +779,18 @@ static __device__ __noinline__ Cut plan_cut(RowPlanner<T>& P, bool greedy, float
       const float sl = (M - (sh_ - bb)) + (ph - bb);
       const float lo = sl + pl_;
       const float xf = lo > 0.f ? nextafterf(sh_, INFINITY) : sh_;
-      uint32_t cnt_ge, minkey, cnt_minkey;
-      unsigned long long mass_ge;
-      P.minp_stats(key_f32_bits(__float_as_uint(xf)), cnt_ge, mass_ge, minkey, cnt_minkey);
-      const uint32_t rkm = (Tr::KB == 32) ? minkey : (minkey >> 16);
-      fin = Cut{rkm, (unsigned long long)(cnt_ge - cnt_minkey), cnt_minkey, cnt_minkey, mass_ge, 1};
-    } else {
+      const uint32_t kmin32 = key_f32_bits(__float_as_uint(xf));
+      // a threshold at or below the row's minimum keeps every token: the filter is off (no pass)
+      if (kmin32 <= key_f32_bits(__float_as_uint(P.Mmin))) minp_on = false;
+      if (minp_on) {
+        uint32_t cnt_ge, minkey, cnt_minkey;
+        unsigned long long mass_ge;
+        P.minp_stats(kmin32, cnt_ge, mass_ge, minkey, cnt_minkey);
+        const uint32_t rkm = (Tr::KB == 32) ? minkey : (minkey >> 16);
+        fin = Cut{rkm, (unsigned long long)(cnt_ge - cnt_minkey), cnt_minkey, cnt_minkey, mass_ge, 1};
+      }
+    }
+    if (!(minp_on && !cp_one)) {
       fin = Cut{rkM, 0, (unsigned long long)n, 0, Sfx, 1};
     }
     if (ck_mode == 2) {

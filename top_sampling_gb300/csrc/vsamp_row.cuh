@@ -323,7 +323,11 @@ struct RowEngine {
     passes = 0;
     rounds = 0;
   }
-  __device__ void set_slice(const unsigned char* slice) { mine = reinterpret_cast<const uint4*>(slice) + (size_t)t * q; }
+  // this thread's vectors: warp w's region of the slice starts at vector w * 32 * qmax (the launch's q); a row
+  // spread over fewer vectors per thread (qr <= qmax) fills the first 32 * qr vectors of it, qr per lane
+  __device__ void set_slice(const unsigned char* slice, int qmax) {
+    mine = reinterpret_cast<const uint4*>(slice) + (size_t)warp * 32 * qmax + (size_t)lane * q;
+  }
 
   // ---------------- cluster exchange primitives ----------------
   __device__ __forceinline__ Mail& my_mail() { return sh.mail[xc & 1]; }
@@ -917,29 +921,38 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
   const int t = E.t, lane = E.lane, warp = E.warp, q = E.q, C = E.C, crank = E.crank;
   const int64_t G = gridDim.y;
   const int64_t first = blockIdx.y;
-  const int64_t elems_cta = (int64_t)NT * q * VE;
-  const int64_t cta_e0 = (int64_t)crank * elems_cta;
-  const int64_t warp_bytes = (int64_t)32 * q * 16;     // each warp's region of the slice
+  const int64_t warp_region = (int64_t)32 * q * 16;    // each warp's region of the slice (bytes)
 
   auto row_len = [&](int64_t r) -> int64_t {
     int64_t n = p.V;
     if (p.lengths) n = p.lengths[r];
     return (n > 0 && n <= p.V) ? n : 0;
   };
-  auto cta_count = [&](int64_t n) -> int64_t {
-    const int64_t c = n - cta_e0;
-    return c < 0 ? 0 : (c > elems_cta ? elems_cta : c);
+  // vectors per thread for a row of n elements: q, or for rows of their own lengths (a ragged batch) the fewest
+  // (odd, for conflict-free 16-byte loads) that spread the row over every CTA of the cluster
+  auto q_of = [&](int64_t n) -> int {
+    if (!p.lengths) return q;
+    const int64_t nv = (n + VE - 1) / VE;
+    int64_t qq = (nv + (int64_t)C * NT - 1) / ((int64_t)C * NT);
+    if (qq < 1) qq = 1;
+    if ((qq & 1) == 0 && qq < q) ++qq;
+    return (int)(qq < q ? qq : q);
   };
-  // lane 0 of each warp: bulk copy of the warp's region of row r (its 16-byte-aligned part); returns
-  // whether a copy is in flight
+  // lane 0 of each warp: bulk copy of the warp's part of row r (its 16-byte-aligned part) into the warp's
+  // region; returns whether a copy is in flight
   auto issue_warp = [&](int64_t r) -> bool {
-    const int64_t b16 = (cta_count(row_len(r)) * ES) & ~(int64_t)15;
-    const int64_t lo = (int64_t)warp * warp_bytes;
+    const int64_t n = row_len(r);
+    const int qr = q_of(n);
+    const int64_t span = (int64_t)NT * qr * VE, e0 = (int64_t)crank * span;
+    const int64_t c = n - e0 < 0 ? 0 : (n - e0 > span ? span : n - e0);
+    const int64_t b16 = (c * ES) & ~(int64_t)15;
+    const int64_t wb = (int64_t)32 * qr * 16, lo = (int64_t)warp * wb;
     int64_t nb = b16 - lo;
-    nb = nb < 0 ? 0 : (nb > warp_bytes ? warp_bytes : nb);
+    nb = nb < 0 ? 0 : (nb > wb ? wb : nb);
     mbar_arrive_expect_tx(&sh.bar[warp], (uint32_t)nb);
     if (nb && !p.drop_loads) {
-      bulk_copy_g2s(slice + lo, p.x + ((int64_t)r * p.ld + cta_e0) * ES + lo, (uint32_t)nb, &sh.bar[warp]);
+      bulk_copy_g2s(slice + (int64_t)warp * warp_region, p.x + ((int64_t)r * p.ld + e0) * ES + lo, (uint32_t)nb,
+                    &sh.bar[warp]);
       return true;
     }
     return false;
@@ -964,7 +977,6 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
   for (int64_t k = 0;; ++k) {
     const int64_t row = first + k * G;
     if (row >= p.B) break;
-    E.set_slice(slice);
     E.row = (int)row;
     E.passes = 0;
     E.rounds = 0;
@@ -975,13 +987,23 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
   const bool bad_len = !(n > 0 && n <= p.V);
   if (bad_len) n = 0;
   E.n = n;
+  const int qr = q_of(n);
+  E.q = qr;
+  E.set_slice(slice, q);
+  const int64_t elems_cta = (int64_t)NT * qr * VE;
+  const int64_t cta_e0 = (int64_t)crank * elems_cta;
   const int64_t cta_n = n - cta_e0 < 0 ? 0 : (n - cta_e0 > elems_cta ? elems_cta : n - cta_e0);
-  E.thr_e0 = cta_e0 + (int64_t)t * q * VE;
+  E.thr_e0 = cta_e0 + (int64_t)t * qr * VE;
   {
     const int64_t r = n - E.thr_e0;
-    E.thr_n = r < 0 ? 0 : (r > (int64_t)q * VE ? q * VE : (int)r);
+    E.thr_n = r < 0 ? 0 : (r > (int64_t)qr * VE ? qr * VE : (int)r);
   }
   const unsigned char* grow = p.x + ((int64_t)row * p.ld + cta_e0) * ES;
+  // slice element of the CTA's element e: thread e / (qr VE), in its warp's region
+  auto slice_elem = [&](int64_t e) -> int64_t {
+    const int64_t th = e / ((int64_t)qr * VE);
+    return ((th >> 5) * 32 * q + (th & 31) * qr) * VE + (e - th * qr * VE);
+  };
 
   // ---------------- the row's parameters (loads issued before the wait, so their latency overlaps it) ----
   float temp = 1.f, topp = 1.f, minp = 0.f;
@@ -1016,17 +1038,19 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
       // the (< 16 byte) tail of the slice, by its owner thread with plain loads
       const int64_t b16 = (cta_n * ES) & ~(int64_t)15;
       const int64_t tail_e0 = b16 / ES;
-      if (!timeout && tail_e0 < cta_n && t == (int)(tail_e0 / ((int64_t)q * VE))) {
+      if (!timeout && tail_e0 < cta_n && t == (int)(tail_e0 / ((int64_t)qr * VE))) {
         for (int64_t e = tail_e0; e < cta_n; ++e) {
-          if (ES == 4) reinterpret_cast<uint32_t*>(slice)[e] = reinterpret_cast<const uint32_t*>(grow)[e];
-          else reinterpret_cast<uint16_t*>(slice)[e] = reinterpret_cast<const uint16_t*>(grow)[e];
+          const int64_t se = slice_elem(e);
+          if (ES == 4) reinterpret_cast<uint32_t*>(slice)[se] = reinterpret_cast<const uint32_t*>(grow)[e];
+          else reinterpret_cast<uint16_t*>(slice)[se] = reinterpret_cast<const uint16_t*>(grow)[e];
         }
       }
     } else {
       for (int64_t e = 0; e < E.thr_n; ++e) {
-        const int64_t le = (int64_t)t * q * VE + e;
-        if (ES == 4) reinterpret_cast<uint32_t*>(slice)[le] = reinterpret_cast<const uint32_t*>(grow)[le];
-        else reinterpret_cast<uint16_t*>(slice)[le] = reinterpret_cast<const uint16_t*>(grow)[le];
+        const int64_t le = (int64_t)t * qr * VE + e;
+        const int64_t se = slice_elem(le);
+        if (ES == 4) reinterpret_cast<uint32_t*>(slice)[se] = reinterpret_cast<const uint32_t*>(grow)[le];
+        else reinterpret_cast<uint16_t*>(slice)[se] = reinterpret_cast<const uint16_t*>(grow)[le];
       }
     }
     __syncthreads();

@@ -1073,6 +1073,15 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
   // ---------------- P1: maximum (minimum for cut descriptors and radix searches), non-finite check --------
   constexpr bool kMin = (MODE & (MODE_CUT | MODE_SELECT | MODE_SAMPLE | MODE_TOPN | MODE_KEPT)) != 0;
   float mx = -INFINITY, mn = INFINITY, nf = 0.f;
+  // the top-k select also counts the elements equal to the thread's running maximum (a select whose k lies
+  // inside the row maximum's tie group then needs no radix search)
+  float cmx = -INFINITY;
+  uint32_t ccount = 0u;
+  auto count_max = [&](float x) {
+    const bool gt = x > cmx;
+    ccount = gt ? 1u : ccount + (x == cmx ? 1u : 0u);
+    cmx = gt ? x : cmx;
+  };
   {
     const int nfull = E.thr_n / VE;
     if constexpr (VE == 8) {
@@ -1089,6 +1098,12 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
           if (kMin) mn2 = __hmin2(mn2, a);
           nf2 = kSel ? __hmax2(nf2, __hneu2(a, a)) : __hfma2(a, zero2, nf2);
         }
+        if (kSel) {
+          float x[VE];
+          Tr::values(v, x);
+#pragma unroll
+          for (int i = 0; i < VE; ++i) count_max(x[i]);
+        }
       }
       mx = fmaxf(__low2float(mx2), __high2float(mx2));
       mn = fminf(__low2float(mn2), __high2float(mn2));
@@ -1104,6 +1119,7 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
           if (kMin) mn = fminf(mn, x[i]);
           // x * 0 is NaN for +-inf and NaN; the top-k select only rejects NaN
           nf = kSel ? (x[i] != x[i] ? 1.f : nf) : fmaf(x[i], 0.f, nf);
+          if (kSel) count_max(x[i]);
         }
       }
     }
@@ -1117,6 +1133,7 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
           mx = fmaxf(mx, x[i]);
           if (kMin) mn = fminf(mn, x[i]);
           nf = kSel ? (x[i] != x[i] ? 1.f : nf) : fmaf(x[i], 0.f, nf);
+          if (kSel) count_max(x[i]);
         }
       }
     }
@@ -1125,12 +1142,14 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
   E.passes = 1;
   float M, Mmin;
   uint32_t gflags;
+  uint32_t cMax = 0u;   // the top-k select: elements equal to the row maximum
   {
     const uint32_t bad = (nf != 0.f) ? 1u : 0u;    // NaN compares unequal as well
     mx = warp_max_f(mx);
     mn = -warp_max_f(-mn);
     const uint32_t flags = __reduce_or_sync(kFullMask, bad | (timeout ? 2u : 0u));
-    if (lane == 0) sh.ws[E.xc & 1][warp][0] = make_uint4(__float_as_uint(mx), __float_as_uint(mn), flags, 0u);
+    const uint32_t wcount = kSel ? warp_sum_u32(cmx == mx ? ccount : 0u) : 0u;
+    if (lane == 0) sh.ws[E.xc & 1][warp][0] = make_uint4(__float_as_uint(mx), __float_as_uint(mn), flags, wcount);
     E.exchange();
     // every warp reduces every warp's slot (no broadcast barrier)
     float m = -INFINITY, m2 = INFINITY;
@@ -1144,6 +1163,14 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
     M = warp_max_f(m);
     Mmin = -warp_max_f(-m2);
     gflags = __reduce_or_sync(kFullMask, fl);
+    if (kSel) {
+      uint32_t c = 0u;
+      for (int i = lane; i < C * Eng::NW; i += 32) {
+        const uint4 v = E.wslot(i / Eng::NW, i % Eng::NW, 0);
+        c += __uint_as_float(v.x) == M ? v.w : 0u;
+      }
+      cMax = warp_sum_u32(c);
+    }
     E.exchange_done();
   }
   if (gflags & 2u) dead = true;
@@ -1369,6 +1396,9 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
         fin = Cut{0u, 0, 0, 0, 0, 0};
       } else if (ksel >= n) {
         fin = Cut{0u, 0, (unsigned long long)n, 0, 0, 1};
+      } else if ((int64_t)cMax >= (int64_t)ksel) {
+        // k inside the maximum's tie group: the first k maxima by index, no radix search
+        fin = Cut{Tr::rkey_of_value(M), 0, (unsigned long long)ksel, cMax, 0, 0};
       } else {
         const RadixOut r = E.radix_search(false, (unsigned long long)ksel, -1.f, false, M, c1, 0u, Mmin);
         if (!r.ok) status = VSAMP_ERR_INVALID_ARG;

@@ -581,7 +581,11 @@ struct RowEngine {
         const uint32_t rk = Tr::rkey_of_value(x);
         const bool match = vround ? rk >= floor_rk
                                   : ((rk & hmask) == (prefix & hmask) && rk >= floor_rk && rk >= klo && rk <= khi);
-        if (match) {
+        if (match && !hist_mass) {
+          // a count-only round: one atomic per element, no dependency from one element to the next
+          atomicAdd(&hc[vround ? (uint32_t)value_bin(x, vb) : ((rk >> shift) & 255u)], 1u);
+        } else if (match) {
+          // a mass round: runs of equal bins merged before the (carry-propagating) 64-bit adds
           const uint32_t bin = vround ? (uint32_t)value_bin(x, vb) : ((rk >> shift) & 255u);
           if (bin != run_bin) {
             flush();

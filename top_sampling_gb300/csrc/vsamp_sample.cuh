@@ -526,7 +526,11 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
               const uint32_t rk = Tr::rkey_of_value(x[i]);
               const bool match = vround ? rk >= floor_rk
                                         : ((rk & hmask) == (prefix & hmask) && rk >= floor_rk && rk >= klo && rk <= khi);
-              if (match) {
+              if (match && !hist_mass) {
+                // a count-only round: one atomic per element, no dependency from one element to the next
+                any = true;
+                atomicAdd(&hc[vround ? (uint32_t)value_bin(x[i], vb) : ((rk >> shift) & 255u)], 1u);
+              } else if (match) {
                 any = true;
                 const uint32_t bin = vround ? (uint32_t)value_bin(x[i], vb) : ((rk >> shift) & 255u);
                 if (bin != run_bin) {

@@ -249,6 +249,10 @@ struct RowPlanner {
           const uint32_t rk = Tr::rkey_of_value(x[i]);
           if (vround || ((rk & hmask) == (prefix & hmask) && rk >= klo && rk <= khi)) {
             const uint32_t bin = vround ? (uint32_t)value_bin(x[i], vb) : ((rk >> shift) & 255u);
+            if (!hist_mass) {   // a count-only round: one atomic per element
+              atomicAdd(&sh.hcnt[bin], 1u);
+              continue;
+            }
             if (bin != run_bin) { flush(); run_bin = bin; run_cnt = 0; run_mass = 0; }
             ++run_cnt;
             if (hist_mass) run_mass += mass_fx_split(ex2_approx((x[i] - M) * c1));

@@ -551,13 +551,51 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
               cand1 = nvec_thr >= 64 ? 0xFFFFFFFFu : (nvec_thr > 32 ? ((1u << (nvec_thr - 32)) - 1u) : 0u);
             }
             uint32_t next0 = 0u, next1 = 0u;
-            for (uint32_t bits = cand0; bits; bits &= bits - 1u) {
-              const int b = __ffs(bits) - 1;
-              if (visit(b)) next0 |= 1u << b;
-            }
-            for (uint32_t bits = cand1; bits; bits &= bits - 1u) {
-              const int b = __ffs(bits) - 1;
-              if (visit(32 + b)) next1 |= 1u << b;
+            if (!hist_mass) {
+              // count-only rounds: two vectors per step (both loads issued before either is used), elements
+              // predicated, one atomic per matching element
+              auto count_vec = [&](const uint4 v, int j) -> bool {
+                float x[VE];
+                Tr::values(v, x);
+                bool any = false;
+#pragma unroll
+                for (int i = 0; i < VE; ++i) {
+                  const uint32_t rk = Tr::rkey_of_value(x[i]);
+                  const bool match = j * VE + i < thr_n &&
+                      (vround ? rk >= floor_rk
+                              : ((rk & hmask) == (prefix & hmask) && rk >= floor_rk && rk >= klo && rk <= khi));
+                  if (match) {
+                    any = true;
+                    atomicAdd(&hc[vround ? (uint32_t)value_bin(x[i], vb) : ((rk >> shift) & 255u)], 1u);
+                  }
+                }
+                return any;
+              };
+#pragma unroll
+              for (int w = 0; w < 2; ++w) {
+                uint32_t bits = w ? cand1 : cand0, hit = 0u;
+                while (bits) {
+                  const int b0 = __ffs(bits) - 1;
+                  bits &= bits - 1u;
+                  const int b1 = bits ? __ffs(bits) - 1 : b0;
+                  const bool two = bits != 0u;
+                  if (two) bits &= bits - 1u;
+                  const uint4 v0 = mine[w * 32 + b0];
+                  const uint4 v1 = mine[w * 32 + b1];
+                  if (count_vec(v0, w * 32 + b0)) hit |= 1u << b0;
+                  if (two && count_vec(v1, w * 32 + b1)) hit |= 1u << b1;
+                }
+                if (w) next1 = hit; else next0 = hit;
+              }
+            } else {
+              for (uint32_t bits = cand0; bits; bits &= bits - 1u) {
+                const int b = __ffs(bits) - 1;
+                if (visit(b)) next0 |= 1u << b;
+              }
+              for (uint32_t bits = cand1; bits; bits &= bits - 1u) {
+                const int b = __ffs(bits) - 1;
+                if (visit(32 + b)) next1 |= 1u << b;
+              }
             }
             cand0 = next0;
             cand1 = next1;

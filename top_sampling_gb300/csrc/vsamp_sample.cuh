@@ -61,6 +61,8 @@ struct SampleCtl {
   uint32_t prefix;           // REQ_HIST: the prefix; REQ_MASS: keys above it are summed
   uint32_t floor_rk;        // REQ_HIST: keys below it are left out
   int32_t hfirst;           // REQ_HIST: the first round of a search (every vector is visited)
+  int32_t kfloor;           // REQ_HIST, REQ_COUNT: only keys at or above the top-k pivot of the last REQ_MASS
+                            // matter (the first round, or the count, visits only the vectors holding one)
   int32_t vround;           // REQ_HIST: bins are value bins (vxlo, vsc) instead of key bytes
   float vxlo, vsc;
   uint32_t klo, khi;        // REQ_HIST key rounds: only keys in [klo, khi] (the selected value bin)
@@ -483,6 +485,8 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
       const int nvec_thr = (thr_n + VE - 1) / VE;
       const bool masked = nvec_thr <= 64;
       uint32_t cand0 = 0u, cand1 = 0u;
+      uint32_t km0 = 0u, km1 = 0u;   // vectors holding a key at or above the last REQ_MASS pivot
+      bool km_ok = false;
       int req;
       for (;;) {
         nb_sync(SB_CTL, kSampleThreads);
@@ -546,9 +550,14 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
             return any;
           };
           if (masked) {
-            if (sh.ctl.hfirst) {   // the first round of a search visits every vector
-              cand0 = nvec_thr >= 32 ? 0xFFFFFFFFu : ((1u << nvec_thr) - 1u);
-              cand1 = nvec_thr >= 64 ? 0xFFFFFFFFu : (nvec_thr > 32 ? ((1u << (nvec_thr - 32)) - 1u) : 0u);
+            if (sh.ctl.hfirst) {   // the first round of a search visits every vector (with a floor: those above it)
+              if (sh.ctl.kfloor && km_ok) {
+                cand0 = km0;
+                cand1 = km1;
+              } else {
+                cand0 = nvec_thr >= 32 ? 0xFFFFFFFFu : ((1u << nvec_thr) - 1u);
+                cand1 = nvec_thr >= 64 ? 0xFFFFFFFFu : (nvec_thr > 32 ? ((1u << (nvec_thr - 32)) - 1u) : 0u);
+              }
             }
             uint32_t next0 = 0u, next1 = 0u;
             if (!hist_mass) {
@@ -607,23 +616,40 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
           const uint32_t rk0 = sh.ctl.prefix;
           const float c1 = sh.ctl.c1;
           unsigned long long sm = 0ull;
+          km0 = 0u;
+          km1 = 0u;
           for (int j = 0; j * VE < thr_n; ++j) {
             float x[VE];
             Tr::values(mine[j], x);
+            bool ge = false;
 #pragma unroll
-            for (int i = 0; i < VE; ++i)
-              if (j * VE + i < thr_n && Tr::rkey_of_value(x[i]) > rk0) sm += mass_fx(ex2_approx((x[i] - M) * c1));
+            for (int i = 0; i < VE; ++i) {
+              const uint32_t rk = Tr::rkey_of_value(x[i]);
+              if (j * VE + i < thr_n && rk > rk0) sm += mass_fx(ex2_approx((x[i] - M) * c1));
+              ge = ge || (j * VE + i < thr_n && rk >= rk0);
+            }
+            if (ge && j < 64) {
+              if (j < 32) km0 |= 1u << j;
+              else km1 |= 1u << (j - 32);
+            }
           }
+          km_ok = masked;
           sm = warp_sum_u64(sm);
           if (lane == 0) sh.dp[warp][0] = make_uint4((uint32_t)sm, (uint32_t)(sm >> 32), 0u, 0u);
         } else {   // REQ_COUNT: elements equal to xP, prefixed inside the warp
           const float xv = sh.ctl.xP;
           uint32_t c = 0;
-          for (int j = 0; j * VE < thr_n; ++j) {
+          auto count_vec = [&](int j) {
             float x[VE];
             Tr::values(mine[j], x);
 #pragma unroll
             for (int i = 0; i < VE; ++i) c += (j * VE + i < thr_n && x[i] == xv) ? 1u : 0u;
+          };
+          if (sh.ctl.kfloor && km_ok) {   // xP is at or above the top-k pivot: only the vectors holding such keys
+            for (uint32_t bits = km0; bits; bits &= bits - 1u) count_vec(__ffs(bits) - 1);
+            for (uint32_t bits = km1; bits; bits &= bits - 1u) count_vec(32 + __ffs(bits) - 1);
+          } else {
+            for (int j = 0; j * VE < thr_n; ++j) count_vec(j);
           }
           uint32_t incl = c;
 #pragma unroll
@@ -1009,6 +1035,7 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
             sh.ctl.prefix = prefix;
             sh.ctl.floor_rk = floor_rk;
             sh.ctl.hfirst = first ? 1 : 0;
+            sh.ctl.kfloor = floor_rk != 0u ? 1 : 0;
             sh.ctl.vround = vround ? 1 : 0;
             sh.ctl.vxlo = vb.xlo;
             sh.ctl.vsc = vb.sc;
@@ -1266,6 +1293,7 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
         if (lane == 0) {
           sh.ctl.req = REQ_COUNT;
           sh.ctl.xP = xP;
+          sh.ctl.kfloor = ck_mode == 2 ? 1 : 0;
         }
         __syncwarp();
         nb_arrive(SB_CTL, kSampleThreads);

@@ -383,7 +383,19 @@ __device__ __forceinline__ float ex2_approx(float x) {
 }
 constexpr float kLog2e = 1.4426950408889634f;
 
-__device__ __forceinline__ uint64_t mass_fx(float w) { return __float2ull_rn(w * kMassScale); }
+// round(w * 2^40), ties to even, for 0 <= w < 16, without a 64-bit conversion instruction (those run on the
+// FP64 pipe, a few results per clock per SM on this part): v = w * 2^40 < 2^44 is split into h (v rounded
+// at the granularity 2^21) and l = v - h (exact, |l| <= 2^20); each becomes an integer by adding a power of
+// two that puts the unit in the last mantissa bit. The sum is v rounded to nearest-even because h is even.
+__device__ __forceinline__ uint64_t mass_fx(float w) {
+  const float v = w * kMassScale;
+  const float big = 26388279066624.0f;          // 1.5 * 2^44: unit in the last place 2^21
+  const float h = (v + big) - big;
+  const float l = v - h;
+  const uint32_t hi = __float_as_uint(fmaf(h, 4.76837158203125e-07f, 8388608.0f)) - 0x4B000000u;   // h / 2^21
+  const int32_t lo = (int32_t)(__float_as_uint(l + 12582912.0f) - 0x4B400000u);                   // round(l)
+  return ((uint64_t)hi << 21) + (uint64_t)(int64_t)lo;
+}
 
 // ceil(p * S) for an fp32 p in [0, 1] and a fixed-point mass S < 2^63, exactly, in integer arithmetic:
 // p = m * 2^(e - 150) with a 24-bit m, and the 88-bit product m * S is shifted right with rounding up.

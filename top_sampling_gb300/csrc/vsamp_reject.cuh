@@ -30,7 +30,7 @@ enum : int { PATH_REJECT_CAP = 64 };   // stats[r][3]: the rejection rounds hit 
 constexpr int kRejectRounds = 32;
 
 __device__ __forceinline__ unsigned long long elem_mass(float x, float M, float c1) {
-  return mass_fx_split(ex2_approx((x - M) * c1));
+  return mass_fx(ex2_approx((x - M) * c1));
 }
 // inside the proposal set {x > lx} u {x == lx, i < li}
 __device__ __forceinline__ bool in_set(float x, int64_t i, float lx, int64_t li) {
@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(kSplitThreads) reject_sample_kernel(const Para
         } else {
           const RadixOut r = P.radix(false, (unsigned long long)topk, -1.f, true);
           const unsigned long long need = (unsigned long long)topk - r.cnt_above;
-          Sk = r.mass_above + need * mass_fx_split(ex2_approx((Tr::value_of_rkey(r.rk) - M) * c1));
+          Sk = r.mass_above + need * mass_fx(ex2_approx((Tr::value_of_rkey(r.rk) - M) * c1));
           path |= PATH_RADIX_K;
         }
       }

@@ -78,6 +78,7 @@ struct Params {
   int32_t drop_loads;       // failure-detection test hook: loads are armed but never issued, so every
                             // load wait runs out and the rows report VSAMP_ERR_TIMEOUT
   int32_t nbuf;             // slice buffers per CTA (vsamp_sample: 2 streams the next row during this one)
+  int32_t vbytes;           // vsamp_sample: a byte per vector after the slices (the largest value bin it holds)
   int64_t v0;               // global index of a row's first element: a vocabulary shard's offset (0 otherwise)
 };
 
@@ -226,6 +227,7 @@ struct RadixOut {
   unsigned long long mass_eq;
   unsigned long long goal;      // the goal left inside the group (top-p: target mass minus mass above)
   int ok;
+  int vsel;                     // sampling kernel: the value bin its first round selected (-1: no value round)
 };
 
 // ------------------------------------------------------------------------------------------------
@@ -250,20 +252,34 @@ __device__ __forceinline__ ValueBins make_value_bins(float xlo, float xhi) {
   return vb;
 }
 
+// The integer part of t in (0, 255) comes from adding 2^23 with rounding toward zero (the sum's unit is 1)
+// instead of a float-to-integer conversion, which this part executes at a few results per clock per SM.
 __device__ __forceinline__ int value_bin(float x, const ValueBins& vb) {
   const float t = __fmul_rn(__fsub_rn(x, vb.xlo), vb.sc);
-  return t >= 255.f ? 255 : (t > 0.f ? (int)t : 0);
+  const int ti = (int)(__float_as_uint(__fadd_rz(t, 8388608.0f)) - 0x4B000000u);
+  return t >= 255.f ? 255 : (t > 0.f ? ti : 0);
 }
 
 // The smallest radix key k in [a, b] whose value falls in a value bin >= target (b + 1 if there is none).
+// Called by a full warp: every step tests 32 evenly spaced keys of the interval at once (value_bin is
+// monotone in the key), so a 32-bit range takes at most 7 steps.
 template <typename Tr>
 __device__ __forceinline__ uint32_t first_key_of_bin(uint32_t a, uint32_t b, int target, const ValueBins& vb) {
+  const unsigned long long lane = threadIdx.x & 31;
   unsigned long long lo = a, hi = (unsigned long long)b + 1ull;   // the answer lies in [lo, hi]
 #pragma unroll 1
   while (lo < hi) {
-    const unsigned long long mid = (lo + hi) >> 1;
-    if (value_bin(Tr::value_of_rkey((uint32_t)mid), vb) >= target) hi = mid;
-    else lo = mid + 1ull;
+    const unsigned long long span = hi - lo;   // keys lo .. hi - 1 are untested
+    const unsigned long long k = lo + ((span * lane) >> 5);
+    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, value_bin(Tr::value_of_rkey((uint32_t)k), vb) >= target);
+    if (bal & 1u) return (uint32_t)lo;         // lane 0 tested lo itself
+    if (bal == 0u) {                           // every tested key is below the bin: past the last one
+      lo += ((span * 31ull) >> 5) + 1ull;
+      continue;
+    }
+    const unsigned long long f = (unsigned long long)(__ffs(bal) - 1);   // >= 1
+    hi = lo + ((span * f) >> 5);               // passes
+    lo = lo + ((span * (f - 1ull)) >> 5) + 1ull;   // the key before it fails
   }
   return (uint32_t)lo;
 }

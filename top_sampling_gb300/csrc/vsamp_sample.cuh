@@ -30,7 +30,7 @@ constexpr int kMaxDataWarps = 8;
 // named barriers (0 is __syncthreads)
 enum SampleBarrier : int { SB_P1 = 1, SB_CTL = 2, SB_P2 = 3, SB_HIST = 4, SB_P4 = 5 };
 // control -> data requests after P2
-enum SampleRequest : int { REQ_DONE = 0, REQ_HIST = 1, REQ_COUNT = 2, REQ_ABORT = 3, REQ_MASS = 4 };
+enum SampleRequest : int { REQ_DONE = 0, REQ_HIST = 1, REQ_COUNT = 2, REQ_ABORT = 3, REQ_MASS = 4, REQ_GATHER = 5 };
 // how the data warps find the cut's last kept element
 enum CutGroup : int {
   GROUP_MAX = 0,     // inside the maxima: counts and prefixes from P2
@@ -64,6 +64,10 @@ struct SampleCtl {
   int32_t kfloor;           // REQ_HIST, REQ_COUNT: only keys at or above the top-k pivot of the last REQ_MASS
                             // matter (the first round, or the count, visits only the vectors holding one)
   int32_t vround;           // REQ_HIST: bins are value bins (vxlo, vsc) instead of key bytes
+  int32_t vsel;             // REQ_HIST key round after a value round, REQ_MASS after a count search: the value
+                            // bin the search's value round selected (only vectors whose largest bin is at or
+                            // above it are visited); -1: none
+  int32_t p4km;             // the draw visits only the vectors holding a key at or above the top-k pivot
   float vxlo, vsc;
   uint32_t klo, khi;        // REQ_HIST key rounds: only keys in [klo, khi] (the selected value bin)
   uint32_t kmin32;          // min-p threshold (fp32 key space)
@@ -165,6 +169,61 @@ static __device__ __noinline__ ArgMax control_fallback_draw(const unsigned char*
   return warp_argmax(ArgMax{fs, fi, fsv});
 }
 
+// A radix search's first round over every vector of a thread's chunk, in value bins with no floor, counts
+// only: one shared-memory atomic per element, and each vector's largest bin into vbyte (when given).
+template <typename T, int NTD>
+static __device__ __noinline__ void value_round_full(const uint4* mine, int thr_n, ValueBins vb, uint32_t* hc,
+                                                     unsigned char* vbyte, int td) {
+  using Tr = Traits<T>;
+  constexpr int VE = Tr::VE;
+  const int nfull = thr_n / VE;
+  auto bins = [&](const uint4 v, int j, int cnt) {
+    float x[VE];
+    Tr::values(v, x);
+    uint32_t vmax = 0u;
+#pragma unroll
+    for (int i = 0; i < VE; ++i) {
+      if (i < cnt) {
+        const uint32_t b = (uint32_t)value_bin(x[i], vb);
+        vmax = max(vmax, b);
+        atomicAdd(&hc[b], 1u);
+      }
+    }
+    if (vbyte) vbyte[j * NTD + td] = (unsigned char)vmax;
+  };
+  int j = 0;
+  for (; j + 2 <= nfull; j += 2) {
+    const uint4 v0 = mine[j], v1 = mine[j + 1];
+    bins(v0, j, VE);
+    bins(v1, j + 1, VE);
+  }
+  for (; j < nfull; ++j) bins(mine[j], j, VE);
+  if (nfull * VE < thr_n) bins(mine[nfull], nfull, thr_n - nfull * VE);
+}
+
+// The vectors of a thread's chunk that hold a kept token, among the vectors vis (~0: every vector).
+template <typename T>
+static __device__ __noinline__ unsigned long long kept_vectors_in(const uint4* mine, int thr_n, int64_t thr_e0,
+                                                                 float xP, int32_t It, unsigned long long vis) {
+  if (vis == ~0ull) return kept_vectors<T>(mine, thr_n, thr_e0, xP, It);
+  using Tr = Traits<T>;
+  constexpr int VE = Tr::VE;
+  const int nfull = thr_n / VE;
+  unsigned long long m = 0ull;
+  for (; vis; vis &= vis - 1ull) {
+    const int j = __ffsll((long long)vis) - 1;
+    float x[VE];
+    Tr::values(mine[j], x);
+    const int cnt = j < nfull ? VE : thr_n - nfull * VE;
+    const int64_t e0 = thr_e0 + (int64_t)j * VE;
+    bool any = false;
+#pragma unroll
+    for (int i = 0; i < VE; ++i) any |= i < cnt && (x[i] > xP || (x[i] == xP && e0 + i <= (int64_t)It));
+    if (any) m |= 1ull << j;
+  }
+  return m;
+}
+
 // ------------------------------------------------------------------------------------------------
 // P1 over one thread's vectors: the maximum, the minimum (mn_out; the first radix round bins values over
 // the row's range), and nf != 0 when a value is NaN or +-inf (x * 0 is NaN exactly for those). bf16 pairs
@@ -234,7 +293,7 @@ template <typename T>
 static __device__ __noinline__ unsigned long long draw_scan(const uint4* mine, int thr_n, int64_t thr_e0, int jfull,
                                                            float xP, int32_t It, uint32_t g0, uint32_t rid,
                                                            uint32_t st_lo, uint32_t st_hi, uint32_t k0, uint32_t k1,
-                                                           uint32_t bk) {
+                                                           uint32_t bk, unsigned long long vis) {
   using Tr = Traits<T>;
   constexpr int VE = Tr::VE;
   constexpr int G = VE / 4;            // counters per vector
@@ -260,6 +319,10 @@ static __device__ __noinline__ unsigned long long draw_scan(const uint4* mine, i
       if ((gmask >> g) & 1u) bmin = min(bmin, min4_u32(ph(g0 + (uint32_t)(j * G + g))));
     if (bmin < bk) flagged |= 1ull << j;
   };
+  if (vis != ~0ull) {   // only the given vectors hold kept tokens
+    for (; vis; vis &= vis - 1ull) one(__ffsll((long long)vis) - 1);
+    return flagged;
+  }
   int j = 0;
   for (; j + U <= jfull; j += U) {
     uint4 v[U];
@@ -337,6 +400,8 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
     const int td = t;
     const int nbuf = p.nbuf > 1 ? 2 : 1;
     const int64_t slice_bytes = (int64_t)kDataThreads * q * 16;
+    // byte j * kDataThreads + td: the largest value bin of vector j of thread td in the last value round
+    unsigned char* vbyte = p.vbytes ? slices + nbuf * slice_bytes : nullptr;
     auto cta_count = [&](int64_t n) -> int64_t {
       const int64_t c = n - cta_e0;
       return c < 0 ? 0 : (c > elems_cta ? elems_cta : c);
@@ -487,6 +552,21 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
       uint32_t cand0 = 0u, cand1 = 0u;
       uint32_t km0 = 0u, km1 = 0u;   // vectors holding a key at or above the last REQ_MASS pivot
       bool km_ok = false;
+      uint32_t vm0 = 0u, vm1 = 0u;   // vectors with a byte from the last value round (those that matched it)
+      // cand* reduced to the vectors whose largest bin in the last value round is at or above vsel
+      auto by_bin = [&](uint32_t& m0, uint32_t& m1, int vsel) {
+        uint32_t o0 = 0u, o1 = 0u;
+        for (uint32_t bits = m0; bits; bits &= bits - 1u) {
+          const int j = __ffs(bits) - 1;
+          if ((int)vbyte[j * kDataThreads + td] >= vsel) o0 |= 1u << j;
+        }
+        for (uint32_t bits = m1; bits; bits &= bits - 1u) {
+          const int j = __ffs(bits) - 1;
+          if ((int)vbyte[(32 + j) * kDataThreads + td] >= vsel) o1 |= 1u << j;
+        }
+        m0 = o0;
+        m1 = o1;
+      };
       int req;
       for (;;) {
         nb_sync(SB_CTL, kSampleThreads);
@@ -524,6 +604,7 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
             float x[VE];
             Tr::values(mine[j], x);
             bool any = false;
+            uint32_t vmax = 0u;
 #pragma unroll
             for (int i = 0; i < VE; ++i) {
               if (j * VE + i >= thr_n) break;
@@ -533,10 +614,13 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
               if (match && !hist_mass) {
                 // a count-only round: one atomic per element, no dependency from one element to the next
                 any = true;
-                atomicAdd(&hc[vround ? (uint32_t)value_bin(x[i], vb) : ((rk >> shift) & 255u)], 1u);
+                const uint32_t bin = vround ? (uint32_t)value_bin(x[i], vb) : ((rk >> shift) & 255u);
+                vmax = max(vmax, bin);
+                atomicAdd(&hc[bin], 1u);
               } else if (match) {
                 any = true;
                 const uint32_t bin = vround ? (uint32_t)value_bin(x[i], vb) : ((rk >> shift) & 255u);
+                vmax = max(vmax, bin);
                 if (bin != run_bin) {
                   flush();
                   run_bin = bin;
@@ -547,9 +631,15 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
                 if (hist_mass) run_mass += mass_fx(ex2_approx((x[i] - M) * c1));
               }
             }
+            if (vround && vbyte && j < 64) vbyte[j * kDataThreads + td] = (unsigned char)vmax;
             return any;
           };
-          if (masked) {
+          if (masked && sh.ctl.hfirst && vround && floor_rk == 0u && !hist_mass && !(sh.ctl.kfloor && km_ok)) {
+            // the first round of a count search over the whole row
+            value_round_full<T, kDataThreads>(mine, thr_n, vb, hc, vbyte, td);
+            cand0 = vm0 = nvec_thr >= 32 ? 0xFFFFFFFFu : ((1u << nvec_thr) - 1u);
+            cand1 = vm1 = nvec_thr >= 64 ? 0xFFFFFFFFu : (nvec_thr > 32 ? ((1u << (nvec_thr - 32)) - 1u) : 0u);
+          } else if (masked) {
             if (sh.ctl.hfirst) {   // the first round of a search visits every vector (with a floor: those above it)
               if (sh.ctl.kfloor && km_ok) {
                 cand0 = km0;
@@ -558,6 +648,9 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
                 cand0 = nvec_thr >= 32 ? 0xFFFFFFFFu : ((1u << nvec_thr) - 1u);
                 cand1 = nvec_thr >= 64 ? 0xFFFFFFFFu : (nvec_thr > 32 ? ((1u << (nvec_thr - 32)) - 1u) : 0u);
               }
+            } else if (sh.ctl.vsel >= 0 && vbyte) {
+              // the first key round after a value round: the vectors holding a value in the selected bin or above
+              by_bin(cand0, cand1, sh.ctl.vsel);
             }
             uint32_t next0 = 0u, next1 = 0u;
             if (!hist_mass) {
@@ -567,6 +660,7 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
                 float x[VE];
                 Tr::values(v, x);
                 bool any = false;
+                uint32_t vmax = 0u;
 #pragma unroll
                 for (int i = 0; i < VE; ++i) {
                   const uint32_t rk = Tr::rkey_of_value(x[i]);
@@ -575,9 +669,12 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
                               : ((rk & hmask) == (prefix & hmask) && rk >= floor_rk && rk >= klo && rk <= khi));
                   if (match) {
                     any = true;
-                    atomicAdd(&hc[vround ? (uint32_t)value_bin(x[i], vb) : ((rk >> shift) & 255u)], 1u);
+                    const uint32_t bin = vround ? (uint32_t)value_bin(x[i], vb) : ((rk >> shift) & 255u);
+                    vmax = max(vmax, bin);
+                    atomicAdd(&hc[bin], 1u);
                   }
                 }
+                if (vround && vbyte) vbyte[j * kDataThreads + td] = (unsigned char)vmax;
                 return any;
               };
 #pragma unroll
@@ -608,6 +705,10 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
             }
             cand0 = next0;
             cand1 = next1;
+            if (vround) {
+              vm0 = next0;
+              vm1 = next1;
+            }
           } else {
             for (int j = 0; j * VE < thr_n; ++j) (void)visit(j);
           }
@@ -618,7 +719,7 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
           unsigned long long sm = 0ull;
           km0 = 0u;
           km1 = 0u;
-          for (int j = 0; j * VE < thr_n; ++j) {
+          auto mass_vec = [&](int j) {
             float x[VE];
             Tr::values(mine[j], x);
             bool ge = false;
@@ -632,10 +733,52 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
               if (j < 32) km0 |= 1u << j;
               else km1 |= 1u << (j - 32);
             }
+          };
+          if (masked && vbyte && sh.ctl.vsel >= 0) {
+            // keys at or above the pivot lie in its value bin or above: only the vectors reaching that bin
+            uint32_t v0 = vm0, v1 = vm1;
+            by_bin(v0, v1, sh.ctl.vsel);
+            for (uint32_t bits = v0; bits; bits &= bits - 1u) mass_vec(__ffs(bits) - 1);
+            for (uint32_t bits = v1; bits; bits &= bits - 1u) mass_vec(32 + __ffs(bits) - 1);
+          } else {
+            for (int j = 0; j * VE < thr_n; ++j) mass_vec(j);
           }
           km_ok = masked;
           sm = warp_sum_u64(sm);
           if (lane == 0) sh.dp[warp][0] = make_uint4((uint32_t)sm, (uint32_t)(sm >> 32), 0u, 0u);
+        } else if (req == REQ_GATHER) {
+          // the cluster's totals of this round's histograms, a bin per thread, into the other parity's arrays
+          // (no peer reads those any more: every CTA has gathered the previous round before this exchange)
+          const int hp = sh.ctl.hpar;
+          const bool hm = sh.ctl.hist_mass != 0;
+          for (int b = td; b < 256; b += kDataThreads) {
+            uint32_t ct = 0u;
+            unsigned long long mt = 0ull;
+            for (int r0 = 0; r0 < C; r0 += 8) {
+              uint32_t c[8], lo[8], hi[8];
+#pragma unroll
+              for (int r = 0; r < 8; ++r) {   // every load issued before any is used: one round trip
+                c[r] = lo[r] = hi[r] = 0u;
+                if (r0 + r < C) {
+                  c[r] = dsmem_load_u32(dsmem_map(&sh.hcnt[hp][b], (uint32_t)(r0 + r)));
+                  if (hm) {
+                    lo[r] = dsmem_load_u32(dsmem_map(&sh.hlo[hp][b], (uint32_t)(r0 + r)));
+                    hi[r] = dsmem_load_u32(dsmem_map(&sh.hhi[hp][b], (uint32_t)(r0 + r)));
+                  }
+                }
+              }
+#pragma unroll
+              for (int r = 0; r < 8; ++r) {
+                ct += c[r];
+                mt += u64_of(lo[r], hi[r]);
+              }
+            }
+            sh.hcnt[hp ^ 1][b] = ct;
+            if (hm) {
+              sh.hlo[hp ^ 1][b] = (uint32_t)mt;
+              sh.hhi[hp ^ 1][b] = (uint32_t)(mt >> 32);
+            }
+          }
         } else {   // REQ_COUNT: elements equal to xP, prefixed inside the warp
           const float xv = sh.ctl.xP;
           uint32_t c = 0;
@@ -754,9 +897,11 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
           if (lim >= 0) jfull = (int)(lim / VE + 1 < (int64_t)nfull ? lim / VE + 1 : (int64_t)nfull);
         }
         const uint32_t g0 = (uint32_t)(thr_e0 >> 2);
+        // after a top-k search every kept token lies in a vector holding a key at or above its pivot
+        const unsigned long long vis = (sh.ctl.p4km && km_ok) ? (((unsigned long long)km1 << 32) | km0) : ~0ull;
         unsigned long long flagged =
-            all_cand ? kept_vectors<T>(mine, thr_n, thr_e0, xP, It)
-                     : draw_scan<T>(mine, thr_n, thr_e0, jfull, xP, It, g0, rid, st_lo, st_hi, key.k0, key.k1, bk);
+            all_cand ? kept_vectors_in<T>(mine, thr_n, thr_e0, xP, It, vis)
+                     : draw_scan<T>(mine, thr_n, thr_e0, jfull, xP, It, g0, rid, st_lo, st_hi, key.k0, key.k1, bk, vis);
         // flagged vectors: the kept tokens whose word passes the bound get the exact perturbed score
         float bscore = -INFINITY, bs = 0.f;
         int32_t bidx = 0x7FFFFFFF;
@@ -1010,6 +1155,8 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
                        RadixOut& out) -> bool {
         out = RadixOut{};
         out.ok = 1;
+        out.vsel = -1;
+        int vsel_next = -1;   // the next request is the first key round after the value round
         uint32_t prefix = 0;
         unsigned long long cnt_above = 0, mass_above = 0;
         const bool hist_mass = want_mass || mass_mode;
@@ -1041,7 +1188,9 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
             sh.ctl.vsc = vb.sc;
             sh.ctl.klo = klo;
             sh.ctl.khi = khi;
+            sh.ctl.vsel = vsel_next;
           }
+          vsel_next = -1;
           __syncwarp();
           nb_arrive(SB_CTL, kSampleThreads);
           nb_sync(SB_HIST, kSampleThreads);
@@ -1049,34 +1198,27 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
           ++rounds;
           // every CTA's histogram is complete once every CTA has passed this exchange
           if (!X.run(sh, C, crank, make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u), p.wait_cycles)) return false;
-          // lane l: bins 255 - 8l .. 248 - 8l, summed over the cluster
+          int sp = hp;   // the arrays holding the cluster's totals
+          if (C > 1) {   // the data warps sum the peers' histograms, a bin per thread, into the other parity
+            if (lane == 0) sh.ctl.req = REQ_GATHER;
+            __syncwarp();
+            nb_arrive(SB_CTL, kSampleThreads);
+            nb_sync(SB_HIST, kSampleThreads);
+            sp = hp ^ 1;
+          }
+          // lane l: bins 255 - 8l .. 248 - 8l (32-byte aligned: two 16-byte loads per array)
           uint32_t bc[8];
           unsigned long long bm[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) { bc[i] = 0u; bm[i] = 0ull; }
-          // bins 248 - 8l .. 255 - 8l are 32-byte aligned: two 16-byte loads per array and rank, all of a rank's
-          // loads issued before any is used, so a rank costs one round trip
-          const int b0 = 248 - 8 * lane;
-          for (int r = 0; r < C; ++r) {
-            uint4 c0, c1, l0 = make_uint4(0u, 0u, 0u, 0u), l1 = l0, h0 = l0, h1 = l0;
-            if (C == 1) {
-              c0 = *reinterpret_cast<const uint4*>(&sh.hcnt[hp][b0]);
-              c1 = *reinterpret_cast<const uint4*>(&sh.hcnt[hp][b0 + 4]);
-              if (hist_mass) {
-                l0 = *reinterpret_cast<const uint4*>(&sh.hlo[hp][b0]);
-                l1 = *reinterpret_cast<const uint4*>(&sh.hlo[hp][b0 + 4]);
-                h0 = *reinterpret_cast<const uint4*>(&sh.hhi[hp][b0]);
-                h1 = *reinterpret_cast<const uint4*>(&sh.hhi[hp][b0 + 4]);
-              }
-            } else {
-              c0 = dsmem_load_v4(dsmem_map(&sh.hcnt[hp][b0], (uint32_t)r));
-              c1 = dsmem_load_v4(dsmem_map(&sh.hcnt[hp][b0 + 4], (uint32_t)r));
-              if (hist_mass) {
-                l0 = dsmem_load_v4(dsmem_map(&sh.hlo[hp][b0], (uint32_t)r));
-                l1 = dsmem_load_v4(dsmem_map(&sh.hlo[hp][b0 + 4], (uint32_t)r));
-                h0 = dsmem_load_v4(dsmem_map(&sh.hhi[hp][b0], (uint32_t)r));
-                h1 = dsmem_load_v4(dsmem_map(&sh.hhi[hp][b0 + 4], (uint32_t)r));
-              }
+          {
+            const int b0 = 248 - 8 * lane;
+            const uint4 c0 = *reinterpret_cast<const uint4*>(&sh.hcnt[sp][b0]);
+            const uint4 c1 = *reinterpret_cast<const uint4*>(&sh.hcnt[sp][b0 + 4]);
+            uint4 l0 = make_uint4(0u, 0u, 0u, 0u), l1 = l0, h0 = l0, h1 = l0;
+            if (hist_mass) {
+              l0 = *reinterpret_cast<const uint4*>(&sh.hlo[sp][b0]);
+              l1 = *reinterpret_cast<const uint4*>(&sh.hlo[sp][b0 + 4]);
+              h0 = *reinterpret_cast<const uint4*>(&sh.hhi[sp][b0]);
+              h1 = *reinterpret_cast<const uint4*>(&sh.hhi[sp][b0 + 4]);
             }
             // bc[i] / bm[i] hold bin 255 - 8l - i = b0 + 7 - i
             const uint32_t cc[8] = {c1.w, c1.z, c1.y, c1.x, c0.w, c0.z, c0.y, c0.x};
@@ -1084,8 +1226,8 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
             const uint32_t hh[8] = {h1.w, h1.z, h1.y, h1.x, h0.w, h0.z, h0.y, h0.x};
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              bc[i] += cc[i];
-              if (hist_mass) bm[i] += u64_of(ll[i], hh[i]);
+              bc[i] = cc[i];
+              bm[i] = hist_mass ? u64_of(ll[i], hh[i]) : 0ull;
             }
           }
           if (mass_mode && gp >= 0.f && first) {
@@ -1144,6 +1286,8 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
             klo = kr.klo;
             khi = kr.khi;
             prefix = kr.prefix;
+            out.vsel = (int)sel;
+            vsel_next = (int)sel;
             if (kr.shift < 0) break;   // one key: the group
             shift = kr.shift;
             continue;
@@ -1216,6 +1360,7 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
             if (lane == 0) {
               sh.ctl.req = REQ_MASS;
               sh.ctl.prefix = r.rk;
+              sh.ctl.vsel = r.vsel;
             }
             __syncwarp();
             nb_arrive(SB_CTL, kSampleThreads);
@@ -1341,6 +1486,7 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
       if (lane < kDataWarps) sh.ctl.wstart[lane] = wstart;
       if (lane == 0) {
         sh.ctl.req = REQ_DONE;
+        sh.ctl.p4km = ck_mode == 2 ? 1 : 0;   // the cut lies at or above the top-k pivot
         sh.ctl.group = group;
         sh.ctl.xP = xP;
         sh.ctl.need = need;

@@ -24,9 +24,31 @@ static vsamp_status launch_sample_cfg(Params p, int64_t B, int esize, const Devi
   p.wait_cycles = wc > 0 ? wc : 4000000000LL;   // ~2 s at the maximum SM clock
   p.drop_loads = env_int("VSAMP_TEST_DROP_LOADS", 0) != 0 ? 1 : 0;
   auto kern = sample_kernel<T, NDW, PER_SM>;
+  const int smem_sm = d.smem_per_sm > 0 ? d.smem_per_sm : d.optin;
+  int per_sm = PER_SM;
+  // a slice that leaves no room for a second CTA on an SM: the instantiation without a register cap (the
+  // capped one spills its row state, and with the shared-memory carve-out at its largest the spills miss L1)
+  if constexpr (NDW == 8 && PER_SM > 1) {
+    if (2 * (g.smem + 1024) > smem_sm) {
+      kern = sample_kernel<T, NDW, 1>;
+      per_sm = 1;
+    }
+  }
+  // a byte per vector after the slices (each vector's largest value bin in a radix search's first round),
+  // where it costs no CTA per SM
+  int smem = g.smem;
+  p.vbytes = 0;
+  if (g.q <= 64) {
+    const int vb = (kDataThreads * g.q + 15) / 16 * 16;
+    auto fit = [&](int s) { const int f = smem_sm / (s + 1024); return f < per_sm ? f : per_sm; };
+    if (g.smem + vb <= d.optin && fit(g.smem + vb) >= fit(g.smem)) {
+      smem = g.smem + vb;
+      p.vbytes = 1;
+    }
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kSampleThreads, 1, 1);
-  cfg.dynamicSmemBytes = (size_t)g.smem;
+  cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -36,7 +58,7 @@ static vsamp_status launch_sample_cfg(Params p, int64_t B, int esize, const Devi
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cfg.gridDim = dim3((unsigned)g.C, 1, 1);
-  const int nclusters = cached_max_clusters(reinterpret_cast<const void*>(kern), kSampleThreads, g.smem, g.C);
+  const int nclusters = cached_max_clusters(reinterpret_cast<const void*>(kern), kSampleThreads, smem, g.C);
   if (nclusters < 1) return VSAMP_ERR_UNSUPPORTED;
   const int fit = env_int("VSAMP_GRID_CLUSTERS", 0) > 0 ? env_int("VSAMP_GRID_CLUSTERS", 0) : nclusters;
   int64_t G = B < fit ? B : fit;

@@ -31,20 +31,6 @@ __host__ __device__ inline int64_t split_nchunks(int64_t V, int esize) {
   return (V + k - 1) / k;
 }
 
-// round(w * 2^40) for 0 <= w < 8 without a 64-bit conversion instruction: v = w * 2^40 < 2^43 is split into
-// h (a multiple of 2^21, by rounding at that granularity) and l = v - h (exact, |l| <= 2^20); both are
-// turned into integers by adding a power of two that places the unit in the last mantissa bit. The sum is
-// round-to-nearest-even of v because h is even.
-__device__ __forceinline__ unsigned long long mass_fx_split(float w) {
-  const float v = w * kMassScale;
-  const float big = 26388279066624.0f;          // 1.5 * 2^44: unit in the last place 2^21
-  const float h = (v + big) - big;
-  const float l = v - h;
-  const uint32_t hi = __float_as_uint(fmaf(h, 4.76837158203125e-07f, 8388608.0f)) - 0x4B000000u;   // h / 2^21
-  const int32_t lo = (int32_t)(__float_as_uint(l + 12582912.0f) - 0x4B400000u);                   // round(l)
-  return ((unsigned long long)hi << 21) + (unsigned long long)(long long)lo;
-}
-
 // orderable 32-bit key of a non-NaN float (larger float, larger key)
 __device__ __forceinline__ uint32_t score_key(float s) {
   const uint32_t f = __float_as_uint(s);
@@ -255,7 +241,7 @@ struct RowPlanner {
             }
             if (bin != run_bin) { flush(); run_bin = bin; run_cnt = 0; run_mass = 0; }
             ++run_cnt;
-            if (hist_mass) run_mass += mass_fx_split(ex2_approx((x[i] - M) * c1));
+            if (hist_mass) run_mass += mass_fx(ex2_approx((x[i] - M) * c1));
           }
         }
         flush();
@@ -356,7 +342,7 @@ struct RowPlanner {
         const uint32_t k32 = key_f32_bits(__float_as_uint(x[i]));
         if (i < cnt && k32 >= kmin32) {
           ++c;
-          m += mass_fx_split(ex2_approx((x[i] - M) * c1));
+          m += mass_fx(ex2_approx((x[i] - M) * c1));
           if (k32 < mk) { mk = k32; cmk = 1; }
           else if (k32 == mk) ++cmk;
         }
@@ -801,7 +787,7 @@ static __device__ __noinline__ Cut plan_cut(RowPlanner<T>& P, bool greedy, float
       const RadixOut r = P.radix(false, ck.need, -1.f, cp_mode == 2);
       if (!r.ok) plan_status = VSAMP_ERR_INVALID_ARG;
       const unsigned long long need = ck.need - r.cnt_above;
-      const unsigned long long wP = mass_fx_split(ex2_approx((Tr::value_of_rkey(r.rk) - M) * c1));
+      const unsigned long long wP = mass_fx(ex2_approx((Tr::value_of_rkey(r.rk) - M) * c1));
       ck = Cut{r.rk, r.cnt_above, need, r.cnt_eq, r.mass_above + need * wP, 0};
       path |= PATH_RADIX_K;
       if (cp_mode == 2) cp_goal = ceil_mul_frac(topp, ck.mass);
@@ -809,7 +795,7 @@ static __device__ __noinline__ Cut plan_cut(RowPlanner<T>& P, bool greedy, float
     if (cp_mode == 2 && plan_status == VSAMP_OK) {
       const RadixOut r = P.radix(true, cp_goal, goal_p, true);
       if (!r.ok) plan_status = VSAMP_ERR_INVALID_ARG;
-      const unsigned long long wP = mass_fx_split(ex2_approx((Tr::value_of_rkey(r.rk) - M) * c1));
+      const unsigned long long wP = mass_fx(ex2_approx((Tr::value_of_rkey(r.rk) - M) * c1));
       unsigned long long need = wP ? (r.goal + wP - 1) / wP : 1;
       need = need < 1 ? 1 : (need > r.cnt_eq ? r.cnt_eq : need);
       cp = Cut{r.rk, r.cnt_above, need, r.cnt_eq, r.mass_above + need * wP, 0};
@@ -1168,7 +1154,7 @@ static __device__ __noinline__ void piece_stats_partial(const unsigned char* xr,
         float2 a;
         if constexpr (VE == 8) a = __fadd2_rn(__fadd2_rn(w2[0], w2[2]), __fadd2_rn(w2[1], w2[3]));
         else a = __fadd2_rn(w2[0], w2[1]);
-        s += mass_fx_split(a.x + a.y);
+        s += mass_fx(a.x + a.y);
 #pragma unroll
         for (int i = 0; i < VE; ++i) cm += x[i] == mc ? 1u : 0u;
       } else {
@@ -1183,7 +1169,7 @@ static __device__ __noinline__ void piece_stats_partial(const unsigned char* xr,
         for (int h = VE / 2; h >= 1; h >>= 1)
 #pragma unroll
           for (int i = 0; i < h; ++i) w[i] += w[i + h];
-        s += mass_fx_split(w[0]);
+        s += mass_fx(w[0]);
       }
     }
   }
@@ -1263,7 +1249,7 @@ static __device__ __forceinline__ void piece_pass_full(const uint4* sbuf, int64_
       float2 a;
       if constexpr (VE == 8) a = __fadd2_rn(__fadd2_rn(w2[0], w2[2]), __fadd2_rn(w2[1], w2[3]));
       else a = __fadd2_rn(w2[0], w2[1]);
-      s += mass_fx_split(a.x + a.y);
+      s += mass_fx(a.x + a.y);
       if constexpr (kHeadOnly) {
       } else if constexpr (VE == 8) {
         const __nv_bfloat162 M2 = __float2bfloat162_rn(mc);   // a bf16 value: exact

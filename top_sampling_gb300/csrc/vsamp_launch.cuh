@@ -8,9 +8,29 @@ namespace vsamp {
 template <typename T, int NT, int MODE>
 static vsamp_status launch_nt(Params p, int64_t B, const Geometry& g, cudaStream_t stream) {
   auto kern = row_kernel<T, NT, MODE>;
+  // a byte per vector after the slice (each vector's largest value bin in a radix search's first round),
+  // where it costs no CTA per SM
+  int smem = g.smem;
+  p.vbytes = 0;
+  if (g.q <= 64) {
+    int dev = 0;
+    DeviceInfo d;
+    if (cudaGetDevice(&dev) == cudaSuccess && device_info(dev, d) == VSAMP_OK) {
+      const int smem_sm = d.smem_per_sm > 0 ? d.smem_per_sm : d.optin;
+      const int per_sm = NT <= 128 ? 6 : 3;   // the kernel's launch bound
+      const int vb = (NT * g.q + 15) / 16 * 16;
+      auto fit = [&](int s) { const int f = smem_sm / (s + 1024); return f < per_sm ? f : per_sm; };
+      if (g.smem + vb <= d.optin && fit(g.smem + vb) >= fit(g.smem)) {
+        smem = g.smem + vb;
+        p.vbytes = 1;
+      }
+    } else {
+      cudaGetLastError();
+    }
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(NT, 1, 1);
-  cfg.dynamicSmemBytes = (size_t)g.smem;
+  cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -22,7 +42,7 @@ static vsamp_status launch_nt(Params p, int64_t B, const Geometry& g, cudaStream
   // persistent clusters: as many as fit at once, then evened out so every cluster has the same number
   // of rows (+-1)
   cfg.gridDim = dim3((unsigned)g.C, 1, 1);
-  const int nclusters = cached_max_clusters(reinterpret_cast<const void*>(kern), NT, g.smem, g.C);
+  const int nclusters = cached_max_clusters(reinterpret_cast<const void*>(kern), NT, smem, g.C);
   if (nclusters < 1) return VSAMP_ERR_UNSUPPORTED;
   const int fit = env_int("VSAMP_GRID_CLUSTERS", 0) > 0 ? env_int("VSAMP_GRID_CLUSTERS", 0) : nclusters;
   int64_t G = B < fit ? B : fit;

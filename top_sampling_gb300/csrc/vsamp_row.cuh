@@ -308,6 +308,38 @@ __device__ __forceinline__ KeyRange key_range_of_bin(int b, uint32_t kxlo, uint3
   return r;
 }
 
+// A radix search's first round over every vector of a thread's chunk, in value bins with no floor, counts
+// only: one shared-memory atomic per element, and each vector's largest bin into vbyte (when given).
+template <typename T, int NTD>
+static __device__ __noinline__ void value_round_full(const uint4* mine, int thr_n, ValueBins vb, uint32_t* hc,
+                                                     unsigned char* vbyte, int td) {
+  using Tr = Traits<T>;
+  constexpr int VE = Tr::VE;
+  const int nfull = thr_n / VE;
+  auto bins = [&](const uint4 v, int j, int cnt) {
+    float x[VE];
+    Tr::values(v, x);
+    uint32_t vmax = 0u;
+#pragma unroll
+    for (int i = 0; i < VE; ++i) {
+      if (i < cnt) {
+        const uint32_t b = (uint32_t)value_bin(x[i], vb);
+        vmax = max(vmax, b);
+        atomicAdd(&hc[b], 1u);
+      }
+    }
+    if (vbyte) vbyte[j * NTD + td] = (unsigned char)vmax;
+  };
+  int j = 0;
+  for (; j + 2 <= nfull; j += 2) {
+    const uint4 v0 = mine[j], v1 = mine[j + 1];
+    bins(v0, j, VE);
+    bins(v1, j + 1, VE);
+  }
+  for (; j < nfull; ++j) bins(mine[j], j, VE);
+  if (nfull * VE < thr_n) bins(mine[nfull], nfull, thr_n - nfull * VE);
+}
+
 template <typename T, int NT, int MODE>
 struct RowEngine {
   using Tr = Traits<T>;
@@ -324,6 +356,14 @@ struct RowEngine {
   int thr_n;               // valid elements in this thread's chunk
   int xc;                  // cluster exchange counter (ping-pong parity)
   int passes, rounds;
+  // byte j * NT + t: the largest value bin of vector j of this thread's chunk in the last value round (null when
+  // the launch has no room for them); vm: the vectors with such a byte (those that matched that round)
+  unsigned char* vbyte;
+  uint32_t vm[2];
+  // km: the vectors holding a key at or above km_rk (set by mass_above_key for chunks of at most 64 vectors)
+  uint32_t km[2];
+  bool km_ok;
+  uint32_t km_rk;
 
   __device__ RowEngine(const Params& p_, Smem<NT>& sh_)
       : p(p_), sh(sh_), cluster(cg::this_cluster()) {
@@ -338,6 +378,24 @@ struct RowEngine {
     xc = 0;
     passes = 0;
     rounds = 0;
+    vbyte = nullptr;
+    vm[0] = vm[1] = 0u;
+    km[0] = km[1] = 0u;
+    km_ok = false;
+    km_rk = 0u;
+  }
+  __device__ __forceinline__ bool masked() const { return (thr_n + VE - 1) / VE <= 64; }
+  // m reduced to the vectors whose largest bin in the last value round is at or above vsel
+  __device__ void by_bin(uint32_t (&m)[2], int vsel) const {
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+      uint32_t o = 0u;
+      for (uint32_t bits = m[w]; bits; bits &= bits - 1u) {
+        const int b = __ffs(bits) - 1;
+        if ((int)vbyte[(w * 32 + b) * NT + t] >= vsel) o |= 1u << b;
+      }
+      m[w] = o;
+    }
   }
   // this thread's vectors: warp w's region of the slice starts at vector w * 32 * qmax (the launch's q); a row
   // spread over fewer vectors per thread (qr <= qmax) fills the first 32 * qr vectors of it, qr per lane
@@ -413,6 +471,11 @@ struct RowEngine {
   // where f returned true for some element.
   template <class F>
   __device__ __forceinline__ void for_each_cand(const uint32_t (&cand)[2], uint32_t (&out)[2], F&& f) {
+    for_each_cand(cand, out, f, [](int) {});
+  }
+  // the same, with g(vector) called after each vector
+  template <class F, class Gv>
+  __device__ __forceinline__ void for_each_cand(const uint32_t (&cand)[2], uint32_t (&out)[2], F&& f, Gv&& g) {
 #pragma unroll
     for (int w = 0; w < 2; ++w) {
       uint32_t bits = cand[w], hit = 0u;
@@ -427,6 +490,7 @@ struct RowEngine {
 #pragma unroll
         for (int i = 0; i < VE; ++i)
           if (i < cnt && f(thr_e0 + (int64_t)j * VE + i, x[i])) any = true;
+        g(j);
         if (any) hit |= 1u << b;
       }
       out[w] = hit;
@@ -451,12 +515,35 @@ struct RowEngine {
   }
 
   // Fixed-point mass (as the radix histograms sum it) of the row's keys above rk0, summed over the cluster.
-  // Collective over the cluster; one exchange.
-  __device__ unsigned long long mass_above_key(uint32_t rk0, float M, float c1) {
+  // Collective over the cluster; one exchange. vsel >= 0: the value bin of rk0 in the last value round, whose
+  // bytes limit the pass to the vectors reaching it. Records km (the vectors holding a key >= rk0).
+  __device__ unsigned long long mass_above_key(uint32_t rk0, float M, float c1, int vsel) {
     unsigned long long s = 0ull;
-    for_each([&](int64_t, float x) {
-      if (Tr::rkey_of_value(x) > rk0) s += mass_fx(ex2_approx((x - M) * c1));
-    });
+    if (masked()) {
+      const int nvec = (thr_n + VE - 1) / VE;
+      uint32_t v[2];
+      v[0] = nvec >= 32 ? 0xFFFFFFFFu : ((1u << nvec) - 1u);
+      v[1] = nvec >= 64 ? 0xFFFFFFFFu : (nvec > 32 ? ((1u << (nvec - 32)) - 1u) : 0u);
+      if (vbyte && vsel >= 0) {
+        v[0] = vm[0];
+        v[1] = vm[1];
+        by_bin(v, vsel);
+      }
+      uint32_t o[2];
+      for_each_cand(v, o, [&](int64_t, float x) -> bool {
+        const uint32_t rk = Tr::rkey_of_value(x);
+        if (rk > rk0) s += mass_fx(ex2_approx((x - M) * c1));
+        return rk >= rk0;
+      });
+      km[0] = o[0];
+      km[1] = o[1];
+      km_ok = true;
+      km_rk = rk0;
+    } else {
+      for_each([&](int64_t, float x) {
+        if (Tr::rkey_of_value(x) > rk0) s += mass_fx(ex2_approx((x - M) * c1));
+      });
+    }
     ++passes;
     s = warp_sum_u64(s);
     if (lane == 0) sh.ws[xc & 1][warp][0] = make_uint4((uint32_t)s, (uint32_t)(s >> 32), 0u, 0u);
@@ -474,7 +561,15 @@ struct RowEngine {
   // Per-thread count of elements equal to xv, into tcount[].
   __device__ void count_equal_pass(float xv) {
     uint32_t c = 0;
-    for_each([&](int64_t, float x) { c += (x == xv) ? 1u : 0u; });
+    if (km_ok && Tr::rkey_of_value(xv) >= km_rk) {   // only the vectors holding a key at or above km_rk
+      uint32_t o[2];
+      for_each_cand(km, o, [&](int64_t, float x) -> bool {
+        c += (x == xv) ? 1u : 0u;
+        return false;
+      });
+    } else {
+      for_each([&](int64_t, float x) { c += (x == xv) ? 1u : 0u; });
+    }
     sh.tcount[t] = c;
     ++passes;
   }
@@ -556,6 +651,7 @@ struct RowEngine {
                                    float c1, uint32_t floor_rk, float xmin) {
     RadixOut out{};
     out.ok = 1;
+    out.vsel = -1;
     uint32_t prefix = 0;
     unsigned long long cnt_above = 0, mass_above = 0;
     const bool hist_mass = want_mass || mass_mode;
@@ -564,6 +660,13 @@ struct RowEngine {
     uint32_t cand[2];
     cand[0] = nvec >= 32 ? 0xFFFFFFFFu : ((1u << nvec) - 1u);
     cand[1] = nvec >= 64 ? 0xFFFFFFFFu : (nvec > 32 ? ((1u << (nvec - 32)) - 1u) : 0u);
+    bool all = true;   // cand holds every vector
+    if (masked && floor_rk && km_ok && floor_rk >= km_rk) {   // keys at or above the floor lie in the km vectors
+      cand[0] = km[0];
+      cand[1] = km[1];
+      all = false;
+    }
+    int vsel_next = -1;   // the round after a value round: the vectors reaching the selected bin
     // the candidates' value range: [max(xmin, value of floor_rk), M]
     const float xlo = floor_rk ? fmaxf(xmin, Tr::value_of_rkey(floor_rk)) : xmin;
     const ValueBins vb = make_value_bins(xlo, M);
@@ -578,6 +681,11 @@ struct RowEngine {
       uint32_t* hh = sh.hhi[par];
       for (int b = t; b < 256; b += NT) { hc[b] = 0; hl[b] = 0; hh[b] = 0; }
       __syncthreads();
+      if (vsel_next >= 0 && masked && vbyte) {
+        by_bin(cand, vsel_next);
+        all = false;
+      }
+      vsel_next = -1;
       const int hi_shift = shift + 8;
       const uint32_t hmask = hi_shift >= 32 ? 0u : (0xFFFFFFFFu << hi_shift);
       uint32_t run_bin = 0xFFFFFFFFu, run_cnt = 0;
@@ -593,16 +701,20 @@ struct RowEngine {
           }
         }
       };
+      uint32_t vmax = 0u;   // a value round: the largest bin of the vector being visited
       auto visit = [&](int64_t, float x) -> bool {
         const uint32_t rk = Tr::rkey_of_value(x);
         const bool match = vround ? rk >= floor_rk
                                   : ((rk & hmask) == (prefix & hmask) && rk >= floor_rk && rk >= klo && rk <= khi);
         if (match && !hist_mass) {
           // a count-only round: one atomic per element, no dependency from one element to the next
-          atomicAdd(&hc[vround ? (uint32_t)value_bin(x, vb) : ((rk >> shift) & 255u)], 1u);
+          const uint32_t bin = vround ? (uint32_t)value_bin(x, vb) : ((rk >> shift) & 255u);
+          vmax = max(vmax, bin);
+          atomicAdd(&hc[bin], 1u);
         } else if (match) {
           // a mass round: runs of equal bins merged before the (carry-propagating) 64-bit adds
           const uint32_t bin = vround ? (uint32_t)value_bin(x, vb) : ((rk >> shift) & 255u);
+          vmax = max(vmax, bin);
           if (bin != run_bin) {
             flush();
             run_bin = bin;
@@ -614,11 +726,24 @@ struct RowEngine {
         }
         return match;
       };
-      if (masked) {
+      if (masked && all && vround && !hist_mass && floor_rk == 0u) {
+        // the first round of a count search over the whole chunk
+        value_round_full<T, NT>(mine, thr_n, vb, hc, vbyte, t);
+        vm[0] = cand[0];
+        vm[1] = cand[1];
+      } else if (masked) {
         uint32_t next[2];
-        for_each_cand(cand, next, visit);
+        const bool rec = vround && vbyte != nullptr;
+        for_each_cand(cand, next, visit, [&](int j) {
+          if (rec) vbyte[j * NT + t] = (unsigned char)vmax;
+          vmax = 0u;
+        });
         cand[0] = next[0];
         cand[1] = next[1];
+        if (vround) {
+          vm[0] = next[0];
+          vm[1] = next[1];
+        }
       } else {
         for_each([&](int64_t e, float x) { (void)visit(e, x); });
       }
@@ -726,6 +851,8 @@ struct RowEngine {
         klo = kr.klo;
         khi = kr.khi;
         prefix = kr.prefix;
+        out.vsel = (int)sel;
+        vsel_next = (int)sel;
         if (kr.shift < 0) break;   // one key: the group
         shift = kr.shift;
         continue;
@@ -823,7 +950,10 @@ __device__ __forceinline__ MassPart mass_pass_body(const uint4* mine, int thr_n,
     float2 a;
     if constexpr (VE == 8) a = __fadd2_rn(__fadd2_rn(w2[0], w2[2]), __fadd2_rn(w2[1], w2[3]));
     else a = __fadd2_rn(w2[0], w2[1]);
-    o.s += mass_fx(a.x + a.y);
+    // bf16: one conversion per eight exponentials leaves the FP64 pipe idle most of the time, so the conversion
+    // instruction is cheaper there than mass_fx's arithmetic (both round to nearest-even: the same value)
+    if constexpr (VE == 8) o.s += __float2ull_rn((a.x + a.y) * kMassScale);
+    else o.s += mass_fx(a.x + a.y);
   }
   const int cnt = thr_n - nfull * VE;
   if (cnt > 0) {
@@ -937,6 +1067,7 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
   Smem<NT>& sh = *reinterpret_cast<Smem<NT>*>(dyn);
   unsigned char* slice = dyn + slice_offset<NT>();
   Eng E(p, sh);
+  if (p.vbytes) E.vbyte = slice + (int64_t)NT * p.q * 16;   // after the slice
   Plan plan{};          // per-row decisions, computed identically by every thread
   const int t = E.t, lane = E.lane, warp = E.warp, q = E.q, C = E.C, crank = E.crank;
   const int64_t G = gridDim.y;
@@ -1000,6 +1131,7 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
     E.row = (int)row;
     E.passes = 0;
     E.rounds = 0;
+    E.km_ok = false;
 
   // ---------------- row geometry ----------------
   int64_t n = p.V;
@@ -1378,7 +1510,7 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
             const unsigned long long need = plan.ck.need - r.cnt_above;
             const unsigned long long wP = mass_fx(ex2_approx((Tr::value_of_rkey(r.rk) - M) * c1));
             const bool want_mass = plan.cp_mode == 2 || (MODE & MODE_KEPT) != 0;
-            const unsigned long long above = want_mass ? E.mass_above_key(r.rk, M, c1) : 0ull;
+            const unsigned long long above = want_mass ? E.mass_above_key(r.rk, M, c1, r.vsel) : 0ull;
             plan.ck = Cut{r.rk, r.cnt_above, need, r.cnt_eq, above + need * wP, 0};
             plan.path |= PATH_RADIX_K;
             if (plan.cp_mode == 2) plan.cp_goal = ceil_mul_frac(topp, plan.ck.mass);

@@ -169,38 +169,6 @@ static __device__ __noinline__ ArgMax control_fallback_draw(const unsigned char*
   return warp_argmax(ArgMax{fs, fi, fsv});
 }
 
-// A radix search's first round over every vector of a thread's chunk, in value bins with no floor, counts
-// only: one shared-memory atomic per element, and each vector's largest bin into vbyte (when given).
-template <typename T, int NTD>
-static __device__ __noinline__ void value_round_full(const uint4* mine, int thr_n, ValueBins vb, uint32_t* hc,
-                                                     unsigned char* vbyte, int td) {
-  using Tr = Traits<T>;
-  constexpr int VE = Tr::VE;
-  const int nfull = thr_n / VE;
-  auto bins = [&](const uint4 v, int j, int cnt) {
-    float x[VE];
-    Tr::values(v, x);
-    uint32_t vmax = 0u;
-#pragma unroll
-    for (int i = 0; i < VE; ++i) {
-      if (i < cnt) {
-        const uint32_t b = (uint32_t)value_bin(x[i], vb);
-        vmax = max(vmax, b);
-        atomicAdd(&hc[b], 1u);
-      }
-    }
-    if (vbyte) vbyte[j * NTD + td] = (unsigned char)vmax;
-  };
-  int j = 0;
-  for (; j + 2 <= nfull; j += 2) {
-    const uint4 v0 = mine[j], v1 = mine[j + 1];
-    bins(v0, j, VE);
-    bins(v1, j + 1, VE);
-  }
-  for (; j < nfull; ++j) bins(mine[j], j, VE);
-  if (nfull * VE < thr_n) bins(mine[nfull], nfull, thr_n - nfull * VE);
-}
-
 // The vectors of a thread's chunk that hold a kept token, among the vectors vis (~0: every vector).
 template <typename T>
 static __device__ __noinline__ unsigned long long kept_vectors_in(const uint4* mine, int thr_n, int64_t thr_e0,
@@ -293,7 +261,7 @@ template <typename T>
 static __device__ __noinline__ unsigned long long draw_scan(const uint4* mine, int thr_n, int64_t thr_e0, int jfull,
                                                            float xP, int32_t It, uint32_t g0, uint32_t rid,
                                                            uint32_t st_lo, uint32_t st_hi, uint32_t k0, uint32_t k1,
-                                                           uint32_t bk, unsigned long long vis) {
+                                                           uint32_t bk) {
   using Tr = Traits<T>;
   constexpr int VE = Tr::VE;
   constexpr int G = VE / 4;            // counters per vector
@@ -319,10 +287,6 @@ static __device__ __noinline__ unsigned long long draw_scan(const uint4* mine, i
       if ((gmask >> g) & 1u) bmin = min(bmin, min4_u32(ph(g0 + (uint32_t)(j * G + g))));
     if (bmin < bk) flagged |= 1ull << j;
   };
-  if (vis != ~0ull) {   // only the given vectors hold kept tokens
-    for (; vis; vis &= vis - 1ull) one(__ffsll((long long)vis) - 1);
-    return flagged;
-  }
   int j = 0;
   for (; j + U <= jfull; j += U) {
     uint4 v[U];
@@ -349,6 +313,39 @@ static __device__ __noinline__ unsigned long long draw_scan(const uint4* mine, i
     }
   }
   for (; j < nvec; ++j) one(j);
+  return flagged;
+}
+
+// The same over the vectors vis only (they hold every kept token).
+template <typename T>
+static __device__ __noinline__ unsigned long long draw_scan_in(const uint4* mine, int thr_n, int64_t thr_e0,
+                                                           float xP, int32_t It, uint32_t g0, uint32_t rid,
+                                                           uint32_t st_lo, uint32_t st_hi, uint32_t k0, uint32_t k1,
+                                                           uint32_t bk, unsigned long long vis) {
+  using Tr = Traits<T>;
+  constexpr int VE = Tr::VE;
+  constexpr int G = VE / 4;            // counters per vector
+  const PhiloxRow ph(PhiloxKey{k0, k1}, rid, st_lo, st_hi);
+  const int nfull = thr_n / VE;
+  unsigned long long flagged = 0ull;
+  // one vector, any position: the groups of four tokens holding a kept token
+  auto one = [&](int j) {
+    float x[VE];
+    Tr::values(mine[j], x);
+    const int cnt = j < nfull ? VE : thr_n - nfull * VE;
+    const int64_t e0 = thr_e0 + (int64_t)j * VE;
+    uint32_t gmask = 0u;
+#pragma unroll
+    for (int i = 0; i < VE; ++i)
+      if (i < cnt && (x[i] > xP || (x[i] == xP && e0 + i <= (int64_t)It))) gmask |= 1u << (i >> 2);
+    if (!gmask) return;
+    uint32_t bmin = 0xFFFFFFFFu;
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+      if ((gmask >> g) & 1u) bmin = min(bmin, min4_u32(ph(g0 + (uint32_t)(j * G + g))));
+    if (bmin < bk) flagged |= 1ull << j;
+  };
+  for (; vis; vis &= vis - 1ull) one(__ffsll((long long)vis) - 1);
   return flagged;
 }
 
@@ -901,7 +898,9 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
         const unsigned long long vis = (sh.ctl.p4km && km_ok) ? (((unsigned long long)km1 << 32) | km0) : ~0ull;
         unsigned long long flagged =
             all_cand ? kept_vectors_in<T>(mine, thr_n, thr_e0, xP, It, vis)
-                     : draw_scan<T>(mine, thr_n, thr_e0, jfull, xP, It, g0, rid, st_lo, st_hi, key.k0, key.k1, bk, vis);
+            : vis != ~0ull
+                ? draw_scan_in<T>(mine, thr_n, thr_e0, xP, It, g0, rid, st_lo, st_hi, key.k0, key.k1, bk, vis)
+                : draw_scan<T>(mine, thr_n, thr_e0, jfull, xP, It, g0, rid, st_lo, st_hi, key.k0, key.k1, bk);
         // flagged vectors: the kept tokens whose word passes the bound get the exact perturbed score
         float bscore = -INFINITY, bs = 0.f;
         int32_t bidx = 0x7FFFFFFF;

@@ -201,6 +201,8 @@ struct Smem {
   uint32_t hhi[2][256];
   uint32_t gcnt[256];
   unsigned long long gmass[256];
+  uint32_t kmm[2][2];   // radix key rounds: smallest and largest matching key of this CTA, per round parity
+  uint32_t gkm[2];      // ... and of the cluster
   uint32_t tcount[NT];
   uint32_t tpre[NT];
   float wf[NW][3];
@@ -680,7 +682,11 @@ struct RowEngine {
       uint32_t* hl = sh.hlo[par];
       uint32_t* hh = sh.hhi[par];
       for (int b = t; b < 256; b += NT) { hc[b] = 0; hl[b] = 0; hh[b] = 0; }
+      if (t == 0) { sh.kmm[par][0] = 0xFFFFFFFFu; sh.kmm[par][1] = 0u; }
       __syncthreads();
+      // the first key round after a value round also finds the smallest and largest matching key: when they
+      // are equal (a bin holding one distinct value) the search ends there
+      const bool track = vsel_next >= 0;
       if (vsel_next >= 0 && masked && vbyte) {
         by_bin(cand, vsel_next);
         all = false;
@@ -702,10 +708,15 @@ struct RowEngine {
         }
       };
       uint32_t vmax = 0u;   // a value round: the largest bin of the vector being visited
+      uint32_t kmn = 0xFFFFFFFFu, kmx = 0u;   // a key round: the smallest and largest matching key
       auto visit = [&](int64_t, float x) -> bool {
         const uint32_t rk = Tr::rkey_of_value(x);
         const bool match = vround ? rk >= floor_rk
                                   : ((rk & hmask) == (prefix & hmask) && rk >= floor_rk && rk >= klo && rk <= khi);
+        if (match && track) {
+          kmn = min(kmn, rk);
+          kmx = max(kmx, rk);
+        }
         if (match && !hist_mass) {
           // a count-only round: one atomic per element, no dependency from one element to the next
           const uint32_t bin = vround ? (uint32_t)value_bin(x, vb) : ((rk >> shift) & 255u);
@@ -748,6 +759,14 @@ struct RowEngine {
         for_each([&](int64_t e, float x) { (void)visit(e, x); });
       }
       flush();
+      if (track) {
+        kmn = __reduce_min_sync(kFullMask, kmn);
+        kmx = __reduce_max_sync(kFullMask, kmx);
+        if (lane == 0) {
+          atomicMin(&sh.kmm[par][0], kmn);
+          atomicMax(&sh.kmm[par][1], kmx);
+        }
+      }
       ++passes;
       ++rounds;
       exchange();
@@ -776,6 +795,26 @@ struct RowEngine {
         }
         sh.gcnt[b] = cs;
         sh.gmass[b] = ms;
+      }
+      if (t == 0 && track) {   // the cluster's smallest and largest matching key
+        uint32_t mn[16], mx[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          mn[r] = 0xFFFFFFFFu;
+          mx[r] = 0u;
+          if (r < C) {
+            mn[r] = C == 1 ? sh.kmm[par][0] : dsmem_load_u32(dsmem_map(&sh.kmm[par][0], (uint32_t)r));
+            mx[r] = C == 1 ? sh.kmm[par][1] : dsmem_load_u32(dsmem_map(&sh.kmm[par][1], (uint32_t)r));
+          }
+        }
+        uint32_t a = 0xFFFFFFFFu, z = 0u;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          a = min(a, mn[r]);
+          z = max(z, mx[r]);
+        }
+        sh.gkm[0] = a;
+        sh.gkm[1] = z;
       }
       exchange_done();
       __syncthreads();
@@ -856,6 +895,10 @@ struct RowEngine {
         if (kr.shift < 0) break;   // one key: the group
         shift = kr.shift;
         continue;
+      }
+      if (track && sh.gkm[0] == sh.gkm[1]) {   // every matching element holds the same key: the group
+        prefix = sh.gkm[0];
+        break;
       }
       prefix |= sel << shift;
       if (shift == 0) break;

@@ -585,6 +585,9 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
           uint32_t* hh = sh.hhi[hp];
           uint32_t run_bin = 0xFFFFFFFFu, run_cnt = 0;
           unsigned long long run_mass = 0;
+          // the first key round after a value round: the smallest and largest matching key
+          const bool track = !vround && sh.ctl.vsel >= 0;
+          uint32_t kmn = 0xFFFFFFFFu, kmx = 0u;
           auto flush = [&]() {
             if (run_cnt) {
               atomicAdd(&hc[run_bin], run_cnt);
@@ -608,6 +611,10 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
               const uint32_t rk = Tr::rkey_of_value(x[i]);
               const bool match = vround ? rk >= floor_rk
                                         : ((rk & hmask) == (prefix & hmask) && rk >= floor_rk && rk >= klo && rk <= khi);
+              if (match && track) {
+                kmn = min(kmn, rk);
+                kmx = max(kmx, rk);
+              }
               if (match && !hist_mass) {
                 // a count-only round: one atomic per element, no dependency from one element to the next
                 any = true;
@@ -669,6 +676,10 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
                     const uint32_t bin = vround ? (uint32_t)value_bin(x[i], vb) : ((rk >> shift) & 255u);
                     vmax = max(vmax, bin);
                     atomicAdd(&hc[bin], 1u);
+                    if (track) {
+                      kmn = min(kmn, rk);
+                      kmx = max(kmx, rk);
+                    }
                   }
                 }
                 if (vround && vbyte) vbyte[j * kDataThreads + td] = (unsigned char)vmax;
@@ -710,6 +721,11 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
             for (int j = 0; j * VE < thr_n; ++j) (void)visit(j);
           }
           flush();
+          if (track) {
+            kmn = __reduce_min_sync(kFullMask, kmn);
+            kmx = __reduce_max_sync(kFullMask, kmx);
+            if (lane == 0) sh.dp[warp][1] = make_uint4(kmn, kmx, 0u, 0u);
+          }
         } else if (req == REQ_MASS) {   // fixed-point mass of the keys above a pivot, per warp
           const uint32_t rk0 = sh.ctl.prefix;
           const float c1 = sh.ctl.c1;
@@ -1156,6 +1172,7 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
         out.ok = 1;
         out.vsel = -1;
         int vsel_next = -1;   // the next request is the first key round after the value round
+        int vsel_cur = -1;    // this request is
         uint32_t prefix = 0;
         unsigned long long cnt_above = 0, mass_above = 0;
         const bool hist_mass = want_mass || mass_mode;
@@ -1189,14 +1206,37 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
             sh.ctl.khi = khi;
             sh.ctl.vsel = vsel_next;
           }
+          vsel_cur = vsel_next;
           vsel_next = -1;
           __syncwarp();
           nb_arrive(SB_CTL, kSampleThreads);
           nb_sync(SB_HIST, kSampleThreads);
           ++passes;
           ++rounds;
+          // the first key round after a value round: the CTA's smallest and largest matching key travel with
+          // the exchange; when the cluster's are equal (a bin holding one distinct value) the search ends there
+          const bool track = vsel_cur >= 0;
+          uint32_t kmn = 0xFFFFFFFFu, kmx = 0u;
+          if (track && lane < kDataWarps) {
+            kmn = sh.dp[lane][1].x;
+            kmx = sh.dp[lane][1].y;
+          }
+          if (track) {
+            kmn = __reduce_min_sync(kFullMask, kmn);
+            kmx = __reduce_max_sync(kFullMask, kmx);
+          }
           // every CTA's histogram is complete once every CTA has passed this exchange
-          if (!X.run(sh, C, crank, make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u), p.wait_cycles)) return false;
+          if (!X.run(sh, C, crank, make_uint4(kmn, kmx, 0u, 0u), make_uint4(0u, 0u, 0u, 0u), p.wait_cycles)) return false;
+          if (track) {
+            uint32_t a = 0xFFFFFFFFu, z = 0u;
+            if (lane < C) {
+              const uint4 m = sh.xm[X.par() ^ 1][lane][0];
+              a = m.x;
+              z = m.y;
+            }
+            kmn = __reduce_min_sync(kFullMask, a);
+            kmx = __reduce_max_sync(kFullMask, z);
+          }
           int sp = hp;   // the arrays holding the cluster's totals
           if (C > 1) {   // the data warps sum the peers' histograms, a bin per thread, into the other parity
             if (lane == 0) sh.ctl.req = REQ_GATHER;
@@ -1290,6 +1330,10 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
             if (kr.shift < 0) break;   // one key: the group
             shift = kr.shift;
             continue;
+          }
+          if (track && kmn == kmx) {   // every matching element holds the same key: the group
+            prefix = kmn;
+            break;
           }
           prefix |= sel << shift;
           if (shift == 0) break;

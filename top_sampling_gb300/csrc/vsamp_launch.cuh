@@ -8,8 +8,8 @@ namespace vsamp {
 template <typename T, int NT, int MODE>
 static vsamp_status launch_nt(Params p, int64_t B, const Geometry& g, cudaStream_t stream) {
   auto kern = row_kernel<T, NT, MODE>;
-  // a byte per vector after the slice (each vector's largest value bin in a radix search's first round),
-  // where it costs no CTA per SM
+  // a byte per vector after the slice (each vector's largest value bin in a radix search's first round) and
+  // four mask words per thread, where they cost no CTA per SM
   int smem = g.smem;
   p.vbytes = 0;
   if (g.q <= 64) {
@@ -18,7 +18,7 @@ static vsamp_status launch_nt(Params p, int64_t B, const Geometry& g, cudaStream
     if (cudaGetDevice(&dev) == cudaSuccess && device_info(dev, d) == VSAMP_OK) {
       const int smem_sm = d.smem_per_sm > 0 ? d.smem_per_sm : d.optin;
       const int per_sm = NT <= 128 ? 6 : 3;   // the kernel's launch bound
-      const int vb = (NT * g.q + 15) / 16 * 16;
+      const int vb = (NT * g.q + 15) / 16 * 16 + NT * 16;   // the bytes, then four mask words per thread
       auto fit = [&](int s) { const int f = smem_sm / (s + 1024); return f < per_sm ? f : per_sm; };
       if (g.smem + vb <= d.optin && fit(g.smem + vb) >= fit(g.smem)) {
         smem = g.smem + vb;

@@ -203,6 +203,8 @@ struct Smem {
   unsigned long long gmass[256];
   uint32_t kmm[2][2];   // radix key rounds: smallest and largest matching key of this CTA, per round parity
   uint32_t gkm[2];      // ... and of the cluster
+  uint32_t km_ok;       // this row's km masks are valid, for keys at or above km_rk
+  uint32_t km_rk;
   uint32_t tcount[NT];
   uint32_t tpre[NT];
   float wf[NW][3];
@@ -358,14 +360,6 @@ struct RowEngine {
   int thr_n;               // valid elements in this thread's chunk
   int xc;                  // cluster exchange counter (ping-pong parity)
   int passes, rounds;
-  // byte j * NT + t: the largest value bin of vector j of this thread's chunk in the last value round (null when
-  // the launch has no room for them); vm: the vectors with such a byte (those that matched that round)
-  unsigned char* vbyte;
-  uint32_t vm[2];
-  // km: the vectors holding a key at or above km_rk (set by mass_above_key for chunks of at most 64 vectors)
-  uint32_t km[2];
-  bool km_ok;
-  uint32_t km_rk;
 
   __device__ RowEngine(const Params& p_, Smem<NT>& sh_)
       : p(p_), sh(sh_), cluster(cg::this_cluster()) {
@@ -380,11 +374,17 @@ struct RowEngine {
     xc = 0;
     passes = 0;
     rounds = 0;
-    vbyte = nullptr;
-    vm[0] = vm[1] = 0u;
-    km[0] = km[1] = 0u;
-    km_ok = false;
-    km_rk = 0u;
+  }
+  // After the slice, where the launch has room (p.vbytes): byte j * NT + t, the largest value bin of vector j of
+  // this thread's chunk in the last value round; then four words per thread, word f * NT + t: vm (f = 0, 1: the
+  // vectors with such a byte, those that matched that round) and km (f = 2, 3: the vectors holding a key at or
+  // above sh.km_rk, set by mass_above_key). Kept in shared memory so they hold no registers outside the radix
+  // searches.
+  __device__ __forceinline__ unsigned char* vbyte() const {
+    return p.vbytes ? reinterpret_cast<unsigned char*>(&sh) + slice_offset<NT>() + (size_t)NT * p.q * 16 : nullptr;
+  }
+  __device__ __forceinline__ uint32_t& vmk(int f) const {
+    return reinterpret_cast<uint32_t*>(vbyte() + ((size_t)NT * p.q + 15) / 16 * 16)[f * NT + t];
   }
   __device__ __forceinline__ bool masked() const { return (thr_n + VE - 1) / VE <= 64; }
   // m reduced to the vectors whose largest bin in the last value round is at or above vsel
@@ -394,7 +394,7 @@ struct RowEngine {
       uint32_t o = 0u;
       for (uint32_t bits = m[w]; bits; bits &= bits - 1u) {
         const int b = __ffs(bits) - 1;
-        if ((int)vbyte[(w * 32 + b) * NT + t] >= vsel) o |= 1u << b;
+        if ((int)vbyte()[(w * 32 + b) * NT + t] >= vsel) o |= 1u << b;
       }
       m[w] = o;
     }
@@ -521,14 +521,14 @@ struct RowEngine {
   // bytes limit the pass to the vectors reaching it. Records km (the vectors holding a key >= rk0).
   __device__ unsigned long long mass_above_key(uint32_t rk0, float M, float c1, int vsel) {
     unsigned long long s = 0ull;
-    if (masked()) {
+    if (p.vbytes && masked()) {
       const int nvec = (thr_n + VE - 1) / VE;
       uint32_t v[2];
       v[0] = nvec >= 32 ? 0xFFFFFFFFu : ((1u << nvec) - 1u);
       v[1] = nvec >= 64 ? 0xFFFFFFFFu : (nvec > 32 ? ((1u << (nvec - 32)) - 1u) : 0u);
-      if (vbyte && vsel >= 0) {
-        v[0] = vm[0];
-        v[1] = vm[1];
+      if (vsel >= 0) {
+        v[0] = vmk(0);
+        v[1] = vmk(1);
         by_bin(v, vsel);
       }
       uint32_t o[2];
@@ -537,10 +537,12 @@ struct RowEngine {
         if (rk > rk0) s += mass_fx(ex2_approx((x - M) * c1));
         return rk >= rk0;
       });
-      km[0] = o[0];
-      km[1] = o[1];
-      km_ok = true;
-      km_rk = rk0;
+      vmk(2) = o[0];
+      vmk(3) = o[1];
+      if (t == 0) {
+        sh.km_ok = 1u;   // every thread of every CTA reaches this point (read after the exchange below)
+        sh.km_rk = rk0;
+      }
     } else {
       for_each([&](int64_t, float x) {
         if (Tr::rkey_of_value(x) > rk0) s += mass_fx(ex2_approx((x - M) * c1));
@@ -563,8 +565,9 @@ struct RowEngine {
   // Per-thread count of elements equal to xv, into tcount[].
   __device__ void count_equal_pass(float xv) {
     uint32_t c = 0;
-    if (km_ok && Tr::rkey_of_value(xv) >= km_rk) {   // only the vectors holding a key at or above km_rk
+    if (sh.km_ok && Tr::rkey_of_value(xv) >= sh.km_rk && masked()) {   // only the vectors holding such a key
       uint32_t o[2];
+      const uint32_t km[2] = {vmk(2), vmk(3)};
       for_each_cand(km, o, [&](int64_t, float x) -> bool {
         c += (x == xv) ? 1u : 0u;
         return false;
@@ -663,9 +666,9 @@ struct RowEngine {
     cand[0] = nvec >= 32 ? 0xFFFFFFFFu : ((1u << nvec) - 1u);
     cand[1] = nvec >= 64 ? 0xFFFFFFFFu : (nvec > 32 ? ((1u << (nvec - 32)) - 1u) : 0u);
     bool all = true;   // cand holds every vector
-    if (masked && floor_rk && km_ok && floor_rk >= km_rk) {   // keys at or above the floor lie in the km vectors
-      cand[0] = km[0];
-      cand[1] = km[1];
+    if (masked && floor_rk && sh.km_ok && floor_rk >= sh.km_rk) {   // keys at or above the floor lie in the km vectors
+      cand[0] = vmk(2);
+      cand[1] = vmk(3);
       all = false;
     }
     int vsel_next = -1;   // the round after a value round: the vectors reaching the selected bin
@@ -687,7 +690,7 @@ struct RowEngine {
       // the first key round after a value round also finds the smallest and largest matching key: when they
       // are equal (a bin holding one distinct value) the search ends there
       const bool track = vsel_next >= 0;
-      if (vsel_next >= 0 && masked && vbyte) {
+      if (vsel_next >= 0 && masked && p.vbytes) {
         by_bin(cand, vsel_next);
         all = false;
       }
@@ -739,21 +742,23 @@ struct RowEngine {
       };
       if (masked && all && vround && !hist_mass && floor_rk == 0u) {
         // the first round of a count search over the whole chunk
-        value_round_full<T, NT>(mine, thr_n, vb, hc, vbyte, t);
-        vm[0] = cand[0];
-        vm[1] = cand[1];
+        value_round_full<T, NT>(mine, thr_n, vb, hc, vbyte(), t);
+        if (p.vbytes) {
+          vmk(0) = cand[0];
+          vmk(1) = cand[1];
+        }
       } else if (masked) {
         uint32_t next[2];
-        const bool rec = vround && vbyte != nullptr;
+        unsigned char* const vb8 = vround ? vbyte() : nullptr;
         for_each_cand(cand, next, visit, [&](int j) {
-          if (rec) vbyte[j * NT + t] = (unsigned char)vmax;
+          if (vb8) vb8[j * NT + t] = (unsigned char)vmax;
           vmax = 0u;
         });
         cand[0] = next[0];
         cand[1] = next[1];
-        if (vround) {
-          vm[0] = next[0];
-          vm[1] = next[1];
+        if (vround && p.vbytes) {
+          vmk(0) = next[0];
+          vmk(1) = next[1];
         }
       } else {
         for_each([&](int64_t e, float x) { (void)visit(e, x); });
@@ -1110,7 +1115,6 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
   Smem<NT>& sh = *reinterpret_cast<Smem<NT>*>(dyn);
   unsigned char* slice = dyn + slice_offset<NT>();
   Eng E(p, sh);
-  if (p.vbytes) E.vbyte = slice + (int64_t)NT * p.q * 16;   // after the slice
   Plan plan{};          // per-row decisions, computed identically by every thread
   const int t = E.t, lane = E.lane, warp = E.warp, q = E.q, C = E.C, crank = E.crank;
   const int64_t G = gridDim.y;
@@ -1174,7 +1178,7 @@ __global__ void __launch_bounds__(NT, (NT <= 128 ? 6 : 3)) row_kernel(const Para
     E.row = (int)row;
     E.passes = 0;
     E.rounds = 0;
-    E.km_ok = false;
+    if (t == 0) sh.km_ok = 0u;   // read only after this row's first cluster exchange
 
   // ---------------- row geometry ----------------
   int64_t n = p.V;

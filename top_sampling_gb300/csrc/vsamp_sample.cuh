@@ -397,8 +397,13 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
     const int td = t;
     const int nbuf = p.nbuf > 1 ? 2 : 1;
     const int64_t slice_bytes = (int64_t)kDataThreads * q * 16;
-    // byte j * kDataThreads + td: the largest value bin of vector j of thread td in the last value round
+    // After the slices, where the launch has room (p.vbytes): byte j * kDataThreads + td, the largest value bin of
+    // vector j of thread td in the last value round; then four words per thread, word f * kDataThreads + td: vm
+    // (f = 0, 1: the vectors with such a byte, those that matched that round) and km (f = 2, 3: the vectors
+    // holding a key at or above the last REQ_MASS pivot). Kept in shared memory so they hold no registers
+    // outside the radix requests.
     unsigned char* vbyte = p.vbytes ? slices + nbuf * slice_bytes : nullptr;
+    uint32_t* vmw = p.vbytes ? reinterpret_cast<uint32_t*>(vbyte + ((int64_t)kDataThreads * q + 15) / 16 * 16) : nullptr;
     auto cta_count = [&](int64_t n) -> int64_t {
       const int64_t c = n - cta_e0;
       return c < 0 ? 0 : (c > elems_cta ? elems_cta : c);
@@ -547,9 +552,7 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
       const int nvec_thr = (thr_n + VE - 1) / VE;
       const bool masked = nvec_thr <= 64;
       uint32_t cand0 = 0u, cand1 = 0u;
-      uint32_t km0 = 0u, km1 = 0u;   // vectors holding a key at or above the last REQ_MASS pivot
-      bool km_ok = false;
-      uint32_t vm0 = 0u, vm1 = 0u;   // vectors with a byte from the last value round (those that matched it)
+      bool km_ok = false;            // this row's km words are valid
       // cand* reduced to the vectors whose largest bin in the last value round is at or above vsel
       auto by_bin = [&](uint32_t& m0, uint32_t& m1, int vsel) {
         uint32_t o0 = 0u, o1 = 0u;
@@ -641,13 +644,17 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
           if (masked && sh.ctl.hfirst && vround && floor_rk == 0u && !hist_mass && !(sh.ctl.kfloor && km_ok)) {
             // the first round of a count search over the whole row
             value_round_full<T, kDataThreads>(mine, thr_n, vb, hc, vbyte, td);
-            cand0 = vm0 = nvec_thr >= 32 ? 0xFFFFFFFFu : ((1u << nvec_thr) - 1u);
-            cand1 = vm1 = nvec_thr >= 64 ? 0xFFFFFFFFu : (nvec_thr > 32 ? ((1u << (nvec_thr - 32)) - 1u) : 0u);
+            cand0 = nvec_thr >= 32 ? 0xFFFFFFFFu : ((1u << nvec_thr) - 1u);
+            cand1 = nvec_thr >= 64 ? 0xFFFFFFFFu : (nvec_thr > 32 ? ((1u << (nvec_thr - 32)) - 1u) : 0u);
+            if (vmw) {
+              vmw[td] = cand0;
+              vmw[kDataThreads + td] = cand1;
+            }
           } else if (masked) {
             if (sh.ctl.hfirst) {   // the first round of a search visits every vector (with a floor: those above it)
               if (sh.ctl.kfloor && km_ok) {
-                cand0 = km0;
-                cand1 = km1;
+                cand0 = vmw[2 * kDataThreads + td];
+                cand1 = vmw[3 * kDataThreads + td];
               } else {
                 cand0 = nvec_thr >= 32 ? 0xFFFFFFFFu : ((1u << nvec_thr) - 1u);
                 cand1 = nvec_thr >= 64 ? 0xFFFFFFFFu : (nvec_thr > 32 ? ((1u << (nvec_thr - 32)) - 1u) : 0u);
@@ -713,9 +720,9 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
             }
             cand0 = next0;
             cand1 = next1;
-            if (vround) {
-              vm0 = next0;
-              vm1 = next1;
+            if (vround && vmw) {
+              vmw[td] = next0;
+              vmw[kDataThreads + td] = next1;
             }
           } else {
             for (int j = 0; j * VE < thr_n; ++j) (void)visit(j);
@@ -730,8 +737,7 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
           const uint32_t rk0 = sh.ctl.prefix;
           const float c1 = sh.ctl.c1;
           unsigned long long sm = 0ull;
-          km0 = 0u;
-          km1 = 0u;
+          uint32_t km0 = 0u, km1 = 0u;
           auto mass_vec = [&](int j) {
             float x[VE];
             Tr::values(mine[j], x);
@@ -749,14 +755,18 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
           };
           if (masked && vbyte && sh.ctl.vsel >= 0) {
             // keys at or above the pivot lie in its value bin or above: only the vectors reaching that bin
-            uint32_t v0 = vm0, v1 = vm1;
+            uint32_t v0 = vmw[td], v1 = vmw[kDataThreads + td];
             by_bin(v0, v1, sh.ctl.vsel);
             for (uint32_t bits = v0; bits; bits &= bits - 1u) mass_vec(__ffs(bits) - 1);
             for (uint32_t bits = v1; bits; bits &= bits - 1u) mass_vec(32 + __ffs(bits) - 1);
           } else {
             for (int j = 0; j * VE < thr_n; ++j) mass_vec(j);
           }
-          km_ok = masked;
+          km_ok = masked && vmw;
+          if (km_ok) {
+            vmw[2 * kDataThreads + td] = km0;
+            vmw[3 * kDataThreads + td] = km1;
+          }
           sm = warp_sum_u64(sm);
           if (lane == 0) sh.dp[warp][0] = make_uint4((uint32_t)sm, (uint32_t)(sm >> 32), 0u, 0u);
         } else if (req == REQ_GATHER) {
@@ -802,8 +812,8 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
             for (int i = 0; i < VE; ++i) c += (j * VE + i < thr_n && x[i] == xv) ? 1u : 0u;
           };
           if (sh.ctl.kfloor && km_ok) {   // xP is at or above the top-k pivot: only the vectors holding such keys
-            for (uint32_t bits = km0; bits; bits &= bits - 1u) count_vec(__ffs(bits) - 1);
-            for (uint32_t bits = km1; bits; bits &= bits - 1u) count_vec(32 + __ffs(bits) - 1);
+            for (uint32_t bits = vmw[2 * kDataThreads + td]; bits; bits &= bits - 1u) count_vec(__ffs(bits) - 1);
+            for (uint32_t bits = vmw[3 * kDataThreads + td]; bits; bits &= bits - 1u) count_vec(32 + __ffs(bits) - 1);
           } else {
             for (int j = 0; j * VE < thr_n; ++j) count_vec(j);
           }
@@ -911,7 +921,8 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
         }
         const uint32_t g0 = (uint32_t)(thr_e0 >> 2);
         // after a top-k search every kept token lies in a vector holding a key at or above its pivot
-        const unsigned long long vis = (sh.ctl.p4km && km_ok) ? (((unsigned long long)km1 << 32) | km0) : ~0ull;
+        const unsigned long long vis = (sh.ctl.p4km && km_ok)
+            ? (((unsigned long long)vmw[3 * kDataThreads + td] << 32) | vmw[2 * kDataThreads + td]) : ~0ull;
         unsigned long long flagged =
             all_cand ? kept_vectors_in<T>(mine, thr_n, thr_e0, xP, It, vis)
             : vis != ~0ull

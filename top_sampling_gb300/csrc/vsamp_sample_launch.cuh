@@ -34,12 +34,12 @@ static vsamp_status launch_sample_cfg(Params p, int64_t B, int esize, const Devi
       per_sm = 1;
     }
   }
-  // a byte per vector after the slices (each vector's largest value bin in a radix search's first round),
-  // where it costs no CTA per SM
+  // a byte per vector after the slices (each vector's largest value bin in a radix search's first round) and
+  // four mask words per thread, where they cost no CTA per SM
   int smem = g.smem;
   p.vbytes = 0;
   if (g.q <= 64) {
-    const int vb = (kDataThreads * g.q + 15) / 16 * 16;
+    const int vb = (kDataThreads * g.q + 15) / 16 * 16 + kDataThreads * 16;   // the bytes, then four mask words per thread
     auto fit = [&](int s) { const int f = smem_sm / (s + 1024); return f < per_sm ? f : per_sm; };
     if (g.smem + vb <= d.optin && fit(g.smem + vb) >= fit(g.smem)) {
       smem = g.smem + vb;

@@ -148,6 +148,11 @@ __device__ __forceinline__ uint4 dsmem_load_v4(uint32_t addr) {
                : "memory");
   return v;
 }
+__device__ __forceinline__ unsigned long long dsmem_load_u64(uint32_t addr) {
+  unsigned long long v;
+  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
+  return v;
+}
 __device__ __forceinline__ uint32_t dsmem_load_u32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");

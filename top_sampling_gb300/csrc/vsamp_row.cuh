@@ -197,8 +197,7 @@ struct Smem {
   uint32_t lcnt[2];
   uint32_t acnt[2];
   uint32_t hcnt[2][256];
-  uint32_t hlo[2][256];
-  uint32_t hhi[2][256];
+  unsigned long long hm[2][256];   // fixed-point mass histograms (64-bit shared-memory adds)
   uint32_t gcnt[256];
   unsigned long long gmass[256];
   uint32_t kmm[2][2];   // radix key rounds: smallest and largest matching key of this CTA, per round parity
@@ -682,9 +681,8 @@ struct RowEngine {
     for (;;) {
       const int par = xc & 1;
       uint32_t* hc = sh.hcnt[par];
-      uint32_t* hl = sh.hlo[par];
-      uint32_t* hh = sh.hhi[par];
-      for (int b = t; b < 256; b += NT) { hc[b] = 0; hl[b] = 0; hh[b] = 0; }
+      unsigned long long* hm = sh.hm[par];
+      for (int b = t; b < 256; b += NT) { hc[b] = 0; hm[b] = 0ull; }
       if (t == 0) { sh.kmm[par][0] = 0xFFFFFFFFu; sh.kmm[par][1] = 0u; }
       __syncthreads();
       // the first key round after a value round also finds the smallest and largest matching key: when they
@@ -702,12 +700,7 @@ struct RowEngine {
       auto flush = [&]() {
         if (run_cnt) {
           atomicAdd(&hc[run_bin], run_cnt);
-          if (hist_mass) {
-            const uint32_t lo = (uint32_t)run_mass, hi = (uint32_t)(run_mass >> 32);
-            const uint32_t old = atomicAdd(&hl[run_bin], lo);
-            const uint32_t carry = (old + lo < old) ? 1u : 0u;
-            if (hi + carry) atomicAdd(&hh[run_bin], hi + carry);
-          }
+          if (hist_mass) atomicAdd(&hm[run_bin], run_mass);   // one 64-bit shared-memory add, no return
         }
       };
       uint32_t vmax = 0u;   // a value round: the largest bin of the vector being visited
@@ -781,21 +774,19 @@ struct RowEngine {
         uint32_t cs = 0;
         unsigned long long ms = 0;
         for (int r0 = 0; r0 < C; r0 += 4) {
-          uint32_t cv[4] = {0u, 0u, 0u, 0u}, lv[4] = {0u, 0u, 0u, 0u}, hv[4] = {0u, 0u, 0u, 0u};
+          uint32_t cv[4] = {0u, 0u, 0u, 0u};
+          unsigned long long mv[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             if (r0 + k < C) {
               cv[k] = dsmem_load_u32(dsmem_map(&sh.hcnt[par][b], (uint32_t)(r0 + k)));
-              if (hist_mass) {
-                lv[k] = dsmem_load_u32(dsmem_map(&sh.hlo[par][b], (uint32_t)(r0 + k)));
-                hv[k] = dsmem_load_u32(dsmem_map(&sh.hhi[par][b], (uint32_t)(r0 + k)));
-              }
+              if (hist_mass) mv[k] = dsmem_load_u64(dsmem_map(&sh.hm[par][b], (uint32_t)(r0 + k)));
             }
           }
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             cs += cv[k];
-            ms += (unsigned long long)lv[k] + ((unsigned long long)hv[k] << 32);
+            ms += mv[k];
           }
         }
         sh.gcnt[b] = cs;

@@ -88,12 +88,10 @@ struct SampleSmem {
   uint32_t acnt[2];                      // CTA 0's copy: CTAs that have published, per row parity
   SampleCtl ctl;
   __align__(16) uint32_t hcnt[2][256];   // radix histograms (count, mass low / high words), per round parity;
-  __align__(16) uint32_t hlo[2][256];    // 16-byte aligned: the cluster sum reads them as 16-byte vectors
-  __align__(16) uint32_t hhi[2][256];
+  __align__(16) unsigned long long hm[2][256];   // 16-byte aligned: read as 16-byte vectors
 };
 
-static_assert(offsetof(SampleSmem, hcnt) % 16 == 0 && offsetof(SampleSmem, hlo) % 16 == 0 &&
-                  offsetof(SampleSmem, hhi) % 16 == 0,
+static_assert(offsetof(SampleSmem, hcnt) % 16 == 0 && offsetof(SampleSmem, hm) % 16 == 0,
               "the histograms are read as 16-byte vectors");
 
 __host__ __device__ constexpr int sample_slice_offset() {
@@ -584,8 +582,7 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
           const int hi_shift = shift + 8;
           const uint32_t hmask = hi_shift >= 32 ? 0u : (0xFFFFFFFFu << hi_shift);
           uint32_t* hc = sh.hcnt[hp];
-          uint32_t* hl = sh.hlo[hp];
-          uint32_t* hh = sh.hhi[hp];
+          unsigned long long* hm = sh.hm[hp];
           uint32_t run_bin = 0xFFFFFFFFu, run_cnt = 0;
           unsigned long long run_mass = 0;
           // the first key round after a value round: the smallest and largest matching key
@@ -594,12 +591,7 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
           auto flush = [&]() {
             if (run_cnt) {
               atomicAdd(&hc[run_bin], run_cnt);
-              if (hist_mass) {
-                const uint32_t lo = (uint32_t)run_mass, hi = (uint32_t)(run_mass >> 32);
-                const uint32_t old = atomicAdd(&hl[run_bin], lo);
-                const uint32_t carry = (old + lo < old) ? 1u : 0u;
-                if (hi + carry) atomicAdd(&hh[run_bin], hi + carry);
-              }
+              if (hist_mass) atomicAdd(&hm[run_bin], run_mass);   // one 64-bit shared-memory add, no return
             }
           };
           // the vector's elements into the running bin; true if one matched
@@ -778,29 +770,25 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
             uint32_t ct = 0u;
             unsigned long long mt = 0ull;
             for (int r0 = 0; r0 < C; r0 += 8) {
-              uint32_t c[8], lo[8], hi[8];
+              uint32_t c[8];
+              unsigned long long m[8];
 #pragma unroll
               for (int r = 0; r < 8; ++r) {   // every load issued before any is used: one round trip
-                c[r] = lo[r] = hi[r] = 0u;
+                c[r] = 0u;
+                m[r] = 0ull;
                 if (r0 + r < C) {
                   c[r] = dsmem_load_u32(dsmem_map(&sh.hcnt[hp][b], (uint32_t)(r0 + r)));
-                  if (hm) {
-                    lo[r] = dsmem_load_u32(dsmem_map(&sh.hlo[hp][b], (uint32_t)(r0 + r)));
-                    hi[r] = dsmem_load_u32(dsmem_map(&sh.hhi[hp][b], (uint32_t)(r0 + r)));
-                  }
+                  if (hm) m[r] = dsmem_load_u64(dsmem_map(&sh.hm[hp][b], (uint32_t)(r0 + r)));
                 }
               }
 #pragma unroll
               for (int r = 0; r < 8; ++r) {
                 ct += c[r];
-                mt += u64_of(lo[r], hi[r]);
+                mt += m[r];
               }
             }
             sh.hcnt[hp ^ 1][b] = ct;
-            if (hm) {
-              sh.hlo[hp ^ 1][b] = (uint32_t)mt;
-              sh.hhi[hp ^ 1][b] = (uint32_t)(mt >> 32);
-            }
+            if (hm) sh.hm[hp ^ 1][b] = mt;
           }
         } else {   // REQ_COUNT: elements equal to xP, prefixed inside the warp
           const float xv = sh.ctl.xP;
@@ -1198,8 +1186,7 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
           ++hround;
           for (int b = lane; b < 256; b += 32) {
             sh.hcnt[hp][b] = 0u;
-            sh.hlo[hp][b] = 0u;
-            sh.hhi[hp][b] = 0u;
+            sh.hm[hp][b] = 0ull;
           }
           if (lane == 0) {
             sh.ctl.req = REQ_HIST;
@@ -1263,21 +1250,20 @@ __global__ void __launch_bounds__((NDW + 1) * 32, PER_SM) sample_kernel(const Pa
             const int b0 = 248 - 8 * lane;
             const uint4 c0 = *reinterpret_cast<const uint4*>(&sh.hcnt[sp][b0]);
             const uint4 c1 = *reinterpret_cast<const uint4*>(&sh.hcnt[sp][b0 + 4]);
-            uint4 l0 = make_uint4(0u, 0u, 0u, 0u), l1 = l0, h0 = l0, h1 = l0;
+            ulonglong2 m01 = make_ulonglong2(0ull, 0ull), m23 = m01, m45 = m01, m67 = m01;
             if (hist_mass) {
-              l0 = *reinterpret_cast<const uint4*>(&sh.hlo[sp][b0]);
-              l1 = *reinterpret_cast<const uint4*>(&sh.hlo[sp][b0 + 4]);
-              h0 = *reinterpret_cast<const uint4*>(&sh.hhi[sp][b0]);
-              h1 = *reinterpret_cast<const uint4*>(&sh.hhi[sp][b0 + 4]);
+              m01 = *reinterpret_cast<const ulonglong2*>(&sh.hm[sp][b0]);
+              m23 = *reinterpret_cast<const ulonglong2*>(&sh.hm[sp][b0 + 2]);
+              m45 = *reinterpret_cast<const ulonglong2*>(&sh.hm[sp][b0 + 4]);
+              m67 = *reinterpret_cast<const ulonglong2*>(&sh.hm[sp][b0 + 6]);
             }
             // bc[i] / bm[i] hold bin 255 - 8l - i = b0 + 7 - i
             const uint32_t cc[8] = {c1.w, c1.z, c1.y, c1.x, c0.w, c0.z, c0.y, c0.x};
-            const uint32_t ll[8] = {l1.w, l1.z, l1.y, l1.x, l0.w, l0.z, l0.y, l0.x};
-            const uint32_t hh[8] = {h1.w, h1.z, h1.y, h1.x, h0.w, h0.z, h0.y, h0.x};
+            const unsigned long long mm[8] = {m67.y, m67.x, m45.y, m45.x, m23.y, m23.x, m01.y, m01.x};
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               bc[i] = cc[i];
-              bm[i] = hist_mass ? u64_of(ll[i], hh[i]) : 0ull;
+              bm[i] = mm[i];
             }
           }
           if (mass_mode && gp >= 0.f && first) {
